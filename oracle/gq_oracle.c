@@ -1,0 +1,342 @@
+/*
+ * gq_oracle.c -- the plain, slow CPU oracle for the quantized skinny MUL_MAT.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is used by the test-suite, by the smoke
+ * check and by the benchmark's CPU-baseline leg; the product library never
+ * links, loads or calls it, and it shares no code, header or table with the
+ * CUDA sources.  It is scalar C with no SIMD, no threads and no blocking: every
+ * function follows the definition it cites so that it can be checked by eye.
+ *
+ * What is computed (the llama.cpp MUL_MAT of the q_f32 and f16_f32 kinds):
+ *     dst[m][n] = sum_k src0[n][k] * src1[m][k]
+ * with src0 either Q4_0 block-quantized weights or F16 weights, and src1 F32
+ * activations.  For the Q4_0 kind, src1 is first quantized row by row into
+ * Q8_0 blocks (the "wdata" buffer) and the product is taken as integer block
+ * dot products scaled by the two block scales:
+ *   - llama.cpp pull request #1632, "Introduction": the three MUL_MAT kinds
+ *     (f32, f16_f32, q_f32 with src0 in Q4_0/Q4_1/...), each with an INIT stage
+ *     that prepares the operands and a COMPUTE stage.
+ *   - Arm China article on the NUMA patch for llama.cpp (PR #14232), section
+ *     "MulMat 算子優化": src1 is quantized into a buffer named wdata and the
+ *     operator computes dst = src0 * wdata; every worker reads all of wdata.
+ *
+ * The block formats are the common ggml ones; the pages name them (Q4_0, Q8_0)
+ * without defining them, so this library reads them as follows:
+ *   Q4_0 block (18 bytes): fp16 scale d, then 16 bytes of 4-bit codes.  For a
+ *     block x[0..31]: m = the element of largest magnitude (first one wins on a
+ *     tie), d = m / -8, q_j = clamp(round(x_j / d) + 8, 0, 15) (q_j = 8 when
+ *     d == 0); byte i holds q_i in its low nibble and q_{i+16} in its high
+ *     nibble; the weight is w_j = (q_j - 8) * fp16(d).
+ *   Q8_0 block (34 bytes): fp16 scale d = amax / 127, then 32 int8 codes
+ *     q_j = round(x_j / d) (0 when d == 0); the value is q_j * fp16(d).
+ *   round() is C roundf (ties away from zero); x / d is an IEEE f32 division
+ *   with the f32 d; fp16(d) is IEEE round-to-nearest-even and is the scale
+ *   that is stored and used to de-quantize.
+ *
+ * Floating point: the quantizers decide integer codes, so they work in f32 as
+ * the kernels do (the operands are F32).  Everything that is a sum is formed
+ * in f64: each term d4 * d8 * sumi is exact in f64 (11 + 11 + 16 bits), so the
+ * Q4_0 result differs from the exact value of the de-quantized product only by
+ * the f64 rounding of the running sum.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+
+#define QK 32            /* values per block */
+#define Q4_0_BYTES 18    /* 2-byte scale + 16 bytes of nibbles */
+#define Q8_0_BYTES 34    /* 2-byte scale + 32 int8 */
+
+/* ---------------------------------------------------------------------------
+ * IEEE 754 binary16, written from the format's definition.
+ * binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ *   E in 1..30: value = (1024 + F) * 2^(E - 25);  E == 0: value = F * 2^-24.
+ * Conversion from binary32 rounds to nearest, ties to even, with gradual
+ * underflow; magnitudes that round beyond 65504 become infinity.
+ * ------------------------------------------------------------------------- */
+uint16_t oracle_f32_to_f16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    uint32_t exp = (u >> 23) & 0xffu;
+    uint32_t frac = u & 0x7fffffu;
+
+    if (exp == 0xffu)                       /* infinity or NaN */
+        return frac ? (uint16_t)(sign | 0x7e00u) : (uint16_t)(sign | 0x7c00u);
+    if (exp == 0 && frac == 0)              /* signed zero */
+        return sign;
+
+    /* value = sig * 2^e exactly, sig a 24-bit (or smaller) integer */
+    uint32_t sig;
+    int e;
+    if (exp == 0) { sig = frac;             e = -149; }
+    else          { sig = frac | 0x800000u; e = (int)exp - 150; }
+
+    int lead = 31;                          /* position of the top set bit */
+    while (!((sig >> lead) & 1u)) lead--;
+    int top = lead + e;                     /* floor(log2(value)) */
+
+    /* binary16 spacing at this magnitude: 2^(top-10), never below 2^-24 */
+    int qexp = top - 10;
+    if (qexp < -24) qexp = -24;
+
+    uint32_t q;                             /* value / 2^qexp, rounded */
+    int shift = qexp - e;
+    if (shift <= 0) {
+        q = sig << (-shift);                /* exact */
+    } else if (shift > 30) {
+        q = 0;                              /* below half the smallest step */
+    } else {
+        uint32_t rem = sig & ((1u << shift) - 1u);
+        uint32_t half = 1u << (shift - 1);
+        q = sig >> shift;
+        if (rem > half || (rem == half && (q & 1u))) q++;
+    }
+    if (q == 0) return sign;
+    if (q >= 2048u) { q >>= 1; qexp++; }    /* rounding carried into a new bit */
+
+    /* q in [1, 2047]; with qexp == -24 and q < 1024 this is a subnormal */
+    int E = qexp + 25;                      /* biased exponent if normal */
+    if (q < 1024u) return (uint16_t)(sign | q);
+    if (E >= 31) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | (uint16_t)(((uint32_t)E << 10) | (q - 1024u)));
+}
+
+float oracle_f16_to_f32(uint16_t h)
+{
+    uint32_t E = (h >> 10) & 31u;
+    uint32_t F = h & 1023u;
+    float v;
+    if (E == 0)       v = ldexpf((float)F, -24);
+    else if (E == 31) v = F ? NAN : INFINITY;
+    else              v = ldexpf((float)(1024u + F), (int)E - 25);
+    return (h & 0x8000u) ? -v : v;
+}
+
+static void put_f16(uint8_t *p, uint16_t h) { p[0] = (uint8_t)(h & 0xffu); p[1] = (uint8_t)(h >> 8); }
+static uint16_t get_f16(const uint8_t *p) { return (uint16_t)(p[0] | ((uint16_t)p[1] << 8)); }
+
+/* ---------------------------------------------------------------------------
+ * Q4_0 quantization of one block of 32 weights (the format stated at the top).
+ * ------------------------------------------------------------------------- */
+static void quantize_block_q4_0(const float *x, uint8_t *out)
+{
+    float amax = 0.0f, vmax = 0.0f;
+    for (int j = 0; j < QK; j++) {
+        float a = fabsf(x[j]);
+        if (a > amax) { amax = a; vmax = x[j]; }   /* strict: the first wins */
+    }
+    float d = vmax / -8.0f;
+    int q[QK];
+    for (int j = 0; j < QK; j++) {
+        if (d != 0.0f) {
+            int v = (int)roundf(x[j] / d) + 8;
+            q[j] = v < 0 ? 0 : (v > 15 ? 15 : v);
+        } else {
+            q[j] = 8;
+        }
+    }
+    put_f16(out, oracle_f32_to_f16(d));
+    for (int i = 0; i < QK / 2; i++)
+        out[2 + i] = (uint8_t)(q[i] | (q[i + QK / 2] << 4));
+}
+
+/* w: f32 [N][K] row-major; out: canonical Q4_0 blocks [N][K/32] x 18 bytes. */
+void oracle_quantize_q4_0(const float *w, uint8_t *out, int64_t N, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < nb; b++)
+            quantize_block_q4_0(w + n * K + b * QK, out + (n * nb + b) * Q4_0_BYTES);
+}
+
+/* ---------------------------------------------------------------------------
+ * Q8_0 quantization of one block of 32 activations: the INIT stage that turns
+ * an F32 row of src1 into wdata.
+ * ------------------------------------------------------------------------- */
+static void quantize_block_q8_0(const float *x, uint8_t *out)
+{
+    float amax = 0.0f;
+    for (int j = 0; j < QK; j++) {
+        float a = fabsf(x[j]);
+        if (a > amax) amax = a;
+    }
+    float d = amax / 127.0f;
+    put_f16(out, oracle_f32_to_f16(d));
+    for (int j = 0; j < QK; j++) {
+        int v = 0;
+        if (d != 0.0f) {
+            v = (int)roundf(x[j] / d);
+            v = v < -127 ? -127 : (v > 127 ? 127 : v);
+        }
+        out[2 + j] = (uint8_t)(int8_t)v;
+    }
+}
+
+/* x: f32 [M][K]; out: Q8_0 blocks [M][K/32] x 34 bytes. */
+void oracle_quantize_q8_0(const float *x, uint8_t *out, int64_t M, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t b = 0; b < nb; b++)
+            quantize_block_q8_0(x + m * K + b * QK, out + (m * nb + b) * Q8_0_BYTES);
+}
+
+/* ---------------------------------------------------------------------------
+ * De-quantization (for the invariant checks): value = (q - 8) * d  (Q4_0),
+ * value = q * d (Q8_0), in f64 (both products are exact).
+ * ------------------------------------------------------------------------- */
+static int q4_code(const uint8_t *blk, int j)
+{
+    uint8_t byte = blk[2 + (j % (QK / 2))];
+    return j < QK / 2 ? (byte & 0x0f) : (byte >> 4);
+}
+
+static int q8_code(const uint8_t *blk, int j) { return (int)(int8_t)blk[2 + j]; }
+
+void oracle_dequantize_q4_0(const uint8_t *q4, double *out, int64_t N, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = q4 + (n * nb + b) * Q4_0_BYTES;
+            double d = (double)oracle_f16_to_f32(get_f16(blk));
+            for (int j = 0; j < QK; j++)
+                out[n * K + b * QK + j] = (double)(q4_code(blk, j) - 8) * d;
+        }
+}
+
+void oracle_dequantize_q8_0(const uint8_t *q8, double *out, int64_t M, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = q8 + (m * nb + b) * Q8_0_BYTES;
+            double d = (double)oracle_f16_to_f32(get_f16(blk));
+            for (int j = 0; j < QK; j++)
+                out[m * K + b * QK + j] = (double)q8_code(blk, j) * d;
+        }
+}
+
+/* ---------------------------------------------------------------------------
+ * The integer block dot of the COMPUTE stage:
+ *     sumi = sum_{j<32} (q4_j - 8) * q8_j           (|sumi| <= 32*8*127)
+ * ------------------------------------------------------------------------- */
+static int32_t block_dot(const uint8_t *b4, const uint8_t *b8)
+{
+    int32_t s = 0;
+    for (int j = 0; j < QK; j++)
+        s += (int32_t)(q4_code(b4, j) - 8) * (int32_t)q8_code(b8, j);
+    return s;
+}
+
+/* sumi: int32 [M][N][K/32] */
+void oracle_block_dots(const uint8_t *q4, const uint8_t *q8, int32_t *sumi,
+                       int64_t M, int64_t N, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = 0; n < N; n++)
+            for (int64_t b = 0; b < nb; b++)
+                sumi[(m * N + n) * nb + b] =
+                    block_dot(q4 + (n * nb + b) * Q4_0_BYTES, q8 + (m * nb + b) * Q8_0_BYTES);
+}
+
+/* One output of the q_f32 kind from the quantized operands:
+ *     dst = sum_b d4_b * d8_b * sumi_b               (f64)
+ * and the error denominator of the de-quantized terms:
+ *     T   = sum_b |d4_b| |d8_b| sum_j |q4_j - 8| |q8_j|
+ */
+static void dot_row_q4_0_q8_0(const uint8_t *row4, const uint8_t *row8, int64_t nb,
+                              double *dst, double *T)
+{
+    double acc = 0.0, tacc = 0.0;
+    for (int64_t b = 0; b < nb; b++) {
+        const uint8_t *b4 = row4 + b * Q4_0_BYTES;
+        const uint8_t *b8 = row8 + b * Q8_0_BYTES;
+        double d4 = (double)oracle_f16_to_f32(get_f16(b4));
+        double d8 = (double)oracle_f16_to_f32(get_f16(b8));
+        acc += d4 * d8 * (double)block_dot(b4, b8);
+        int64_t sabs = 0;
+        for (int j = 0; j < QK; j++)
+            sabs += (int64_t)abs(q4_code(b4, j) - 8) * (int64_t)abs(q8_code(b8, j));
+        tacc += fabs(d4) * fabs(d8) * (double)sabs;
+    }
+    *dst = acc;
+    *T = tacc;
+}
+
+/* Full q_f32 MUL_MAT for the output columns n in [n_begin, n_end):
+ * INIT quantizes every row of src1 to Q8_0, COMPUTE forms the block dots.
+ * q4: canonical Q4_0 [N][K/32]; src1: f32 [M][K]; dst, T: f64 [M][N]. */
+int oracle_mul_mat_q4_0_f32(const uint8_t *q4, const float *src1, double *dst, double *T,
+                            int64_t M, int64_t N, int64_t K, int64_t n_begin, int64_t n_end)
+{
+    int64_t nb = K / QK;
+    uint8_t *wdata = (uint8_t *)malloc((size_t)(M * nb * Q8_0_BYTES) + 1);
+    if (!wdata) return 1;
+    oracle_quantize_q8_0(src1, wdata, M, K);
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = n_begin; n < n_end; n++)
+            dot_row_q4_0_q8_0(q4 + n * nb * Q4_0_BYTES, wdata + m * nb * Q8_0_BYTES, nb,
+                              &dst[m * N + n], &T[m * N + n]);
+    free(wdata);
+    return 0;
+}
+
+/* Selected outputs (ms[i], ns[i]) of the q_f32 kind from already quantized
+ * operands (q8 from oracle_quantize_q8_0).  out, T: f64 [count]. */
+void oracle_mul_mat_q4_0_q8_0_at(const uint8_t *q4, const uint8_t *q8, const int64_t *ms,
+                                 const int64_t *ns, int64_t count, int64_t K,
+                                 double *out, double *T)
+{
+    int64_t nb = K / QK;
+    for (int64_t i = 0; i < count; i++)
+        dot_row_q4_0_q8_0(q4 + ns[i] * nb * Q4_0_BYTES, q8 + ms[i] * nb * Q8_0_BYTES, nb,
+                          &out[i], &T[i]);
+}
+
+/* ---------------------------------------------------------------------------
+ * The f16_f32 kind: dst[m][n] = sum_k w16[n][k] * src1[m][k] in f64 with the
+ * F32 activations taken as they are; T[m][n] = sum_k |w16[n][k] * src1[m][k]|.
+ * ------------------------------------------------------------------------- */
+static void dot_row_f16_f32(const uint16_t *w, const float *x, int64_t K, double *dst, double *T)
+{
+    double acc = 0.0, tacc = 0.0;
+    for (int64_t k = 0; k < K; k++) {
+        double p = (double)oracle_f16_to_f32(w[k]) * (double)x[k];
+        acc += p;
+        tacc += fabs(p);
+    }
+    *dst = acc;
+    *T = tacc;
+}
+
+void oracle_mul_mat_f16_f32(const uint16_t *w16, const float *src1, double *dst, double *T,
+                            int64_t M, int64_t N, int64_t K, int64_t n_begin, int64_t n_end)
+{
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = n_begin; n < n_end; n++)
+            dot_row_f16_f32(w16 + n * K, src1 + m * K, K, &dst[m * N + n], &T[m * N + n]);
+}
+
+void oracle_mul_mat_f16_f32_at(const uint16_t *w16, const float *src1, const int64_t *ms,
+                               const int64_t *ns, int64_t count, int64_t K,
+                               double *out, double *T)
+{
+    for (int64_t i = 0; i < count; i++)
+        dot_row_f16_f32(w16 + ns[i] * K, src1 + ms[i] * K, K, &out[i], &T[i]);
+}
+
+/* Element-wise conversions, exported for the binary16 pins. */
+void oracle_f32_to_f16_array(const float *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_f32_to_f16(x[i]);
+}
+
+void oracle_f16_to_f32_array(const uint16_t *h, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_f16_to_f32(h[i]);
+}

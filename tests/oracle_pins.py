@@ -1,0 +1,306 @@
+"""Pins for the CPU oracle: checks against facts fixed outside the oracle.
+
+Every function takes an ``oracle.Oracle`` and raises AssertionError on a
+mismatch.  ``test_oracle_pins.py`` runs them on the oracle as built; the
+mutation test runs them on copies of the oracle with a mistake planted in the
+C source and requires that at least one of them fails for every mistake.
+
+What pins what:
+  * binary16 conversion        -> numpy's IEEE float16 conversion (library routine)
+  * the block byte layouts      -> the hand-derived worked examples in golden/
+  * the quantizer's arithmetic  -> exact round trips of representable blocks, the
+                                   range and de-quantization error bounds
+  * the integer block dot       -> brute force over every (q4, q8) pair per lane
+  * the f64 products            -> float64 dense matmul of the de-quantized
+                                   operands (textbook special case), structured
+                                   weights with closed-form results, and the
+                                   row independence of the batched product
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+
+from quantized_skinny_matmul_gb300 import synth
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+GOLDEN = os.path.join(HERE, "golden", "worked_examples.txt")
+
+
+# ---------------------------------------------------------------------------
+# helpers that decode the documented byte layout independently of the oracle
+# ---------------------------------------------------------------------------
+def decode_q4_0(q4: np.ndarray):
+    """(codes uint8 [..., 32], fp16 scale as f64 [...]) from canonical Q4_0 bytes."""
+    d = q4[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    qs = q4[..., 2:18]
+    codes = np.concatenate([qs & 0x0F, qs >> 4], axis=-1)
+    return codes, d
+
+
+def decode_q8_0(q8: np.ndarray):
+    d = q8[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    codes = q8[..., 2:34].view(np.int8)
+    return codes, d
+
+
+def round_half_away(v: np.ndarray) -> np.ndarray:
+    v = np.asarray(v, np.float64)
+    return np.trunc(v + np.copysign(0.5, v))
+
+
+def parse_golden(path: str = GOLDEN):
+    cases = []
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, expr, hexbytes = (s.strip() for s in line.split("|"))
+            name, kind = head.split()
+            j = np.arange(32)
+            env = {"j": j}
+            if expr.startswith("["):
+                x = np.array(eval(expr, {}, env), dtype=np.float64)  # closed-form list
+            else:
+                x = np.broadcast_to(np.asarray(eval(expr, {}, env), np.float64), (32,))
+            cases.append((name, kind, x.astype(np.float32),
+                          bytes.fromhex(hexbytes.replace(" ", ""))))
+    return cases
+
+
+# ---------------------------------------------------------------------------
+# pins
+# ---------------------------------------------------------------------------
+def pin_f16_conversion(o) -> None:
+    rng = np.random.default_rng(11)
+    vals = [rng.standard_normal(4000).astype(np.float32) * np.float32(s)
+            for s in (1e-8, 1e-6, 3e-5, 1e-3, 1.0, 1e3, 6e4)]
+    # exact binary16 values, the half-way points between neighbours, and one
+    # f32 ulp either side of those half-way points
+    h = np.arange(0, 0x7C00, dtype=np.uint16)
+    f = h.view(np.float16).astype(np.float64)
+    mids = ((f[:-1] + f[1:]) / 2).astype(np.float32)
+    vals += [f.astype(np.float32), mids, np.nextafter(mids, np.float32(np.inf)),
+             np.nextafter(mids, np.float32(0))]
+    vals += [np.array([0.0, 65504.0, 65519.99, 65520.0, 1e6, 2.0 ** -25, 2.0 ** -24,
+                       1.5 * 2.0 ** -25, 2.0 ** -26, 1e-30], np.float32)]
+    x = np.concatenate(vals)
+    x = np.concatenate([x, -x])
+    got = o.f32_to_f16_bits(x)
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"f32->f16 mismatch at {x[bad[:5]]}: {got[bad[:5]]} vs {want[bad[:5]]}"
+    # every non-NaN binary16 pattern back to f32
+    allh = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite_or_inf = (allh & 0x7C00) != 0x7C00
+    finite_or_inf |= (allh & 0x03FF) == 0
+    allh = allh[finite_or_inf]
+    back = o.f16_bits_to_f32(allh)
+    want_back = allh.view(np.float16).astype(np.float32)
+    assert np.array_equal(back.view(np.uint32), want_back.view(np.uint32)), "f16->f32 mismatch"
+
+
+def pin_worked_examples(o) -> None:
+    for name, kind, x, want in parse_golden():
+        if kind == "q4_0":
+            got = o.quantize_q4_0(x.reshape(1, 32)).tobytes()
+        else:
+            got = o.quantize_q8_0(x.reshape(1, 32)).tobytes()
+        assert got == want, f"{name}: {got.hex(' ')} != {want.hex(' ')}"
+    # the worked example W1 de-quantizes back to its input exactly
+    x = ((np.arange(32) % 16) - 8).astype(np.float32).reshape(1, 32)
+    assert np.array_equal(o.dequantize_q4_0(o.quantize_q4_0(x)), x.astype(np.float64))
+
+
+def pin_roundtrip_q4_0(o) -> None:
+    """Blocks whose values are codes times a power of two with a -8 code present
+    quantize to exactly those codes and that scale."""
+    rng = np.random.default_rng(5)
+    N, nb = 64, 8
+    c = rng.integers(-8, 8, size=(N, nb, 32))
+    c[:, :, 0] = -8                                   # the signed max: d = scale
+    e = rng.integers(-12, 4, size=(N, nb, 1))
+    x = (c * np.exp2(e)).astype(np.float32).reshape(N, nb * 32)
+    codes, d = decode_q4_0(o.quantize_q4_0(x))
+    assert np.array_equal(codes.astype(np.int64) - 8, c)
+    assert np.array_equal(d, np.exp2(e[..., 0]).astype(np.float64))
+    # a positive signed max flips the sign of d and every code
+    codes, d = decode_q4_0(o.quantize_q4_0(-x))
+    assert np.array_equal(d, -np.exp2(e[..., 0]).astype(np.float64))
+    assert np.array_equal(codes.astype(np.int64) - 8, c)
+
+
+def pin_roundtrip_q8_0(o) -> None:
+    rng = np.random.default_rng(6)
+    M, nb = 16, 8
+    c = rng.integers(-127, 128, size=(M, nb, 32))
+    c[:, :, 3] = 127 * np.where(rng.random((M, nb)) < 0.5, 1, -1)
+    e = rng.integers(-12, 4, size=(M, nb, 1))
+    x = (c * np.exp2(e)).astype(np.float32).reshape(M, nb * 32)
+    codes, d = decode_q8_0(o.quantize_q8_0(x))
+    assert np.array_equal(codes.astype(np.int64), c)
+    assert np.array_equal(d, np.exp2(e[..., 0]).astype(np.float64))
+
+
+def pin_ranges_and_error_bounds(o) -> None:
+    w = synth.edge_weights(21, 48, 512)
+    x = synth.edge_activations(22, 24, 512)
+    codes4, d4 = decode_q4_0(o.quantize_q4_0(w))
+    codes8, d8 = decode_q8_0(o.quantize_q8_0(x))
+    assert codes4.min() >= 0 and codes4.max() <= 15
+    assert codes8.min() >= -127 and codes8.max() <= 127
+    wb = w.reshape(codes4.shape).astype(np.float64)
+    xb = x.reshape(codes8.shape).astype(np.float64)
+    # the f32 scales the quantizers divide by, recomputed from the inputs
+    am4 = np.abs(wb).max(-1)
+    first = np.argmax(np.abs(wb) == am4[..., None], axis=-1)
+    vmax = np.take_along_axis(wb, first[..., None], -1)[..., 0]
+    dq4 = (vmax.astype(np.float32) / np.float32(-8.0)).astype(np.float64)
+    dq8 = np.abs(xb).max(-1).astype(np.float32) / np.float32(127.0)
+    dq8 = dq8.astype(np.float64)
+    assert np.array_equal(d4, dq4.astype(np.float16).astype(np.float64))
+    assert np.array_equal(d8, dq8.astype(np.float16).astype(np.float64))
+    slack = 1.0 + 1e-6
+    err4 = np.abs(wb - (codes4.astype(np.float64) - 8) * d4[..., None])
+    with np.errstate(divide="ignore", invalid="ignore"):
+        clamp = np.abs(wb / dq4[..., None]) > 7.5
+    bound4 = np.where(clamp, np.abs(dq4)[..., None], np.abs(dq4)[..., None] / 2) * slack \
+        + 8 * np.abs(dq4 - d4)[..., None]
+    assert np.all(err4 <= bound4 + 1e-30), "Q4_0 de-quantization error above its bound"
+    err8 = np.abs(xb - codes8.astype(np.float64) * d8[..., None])
+    bound8 = np.abs(dq8)[..., None] / 2 * slack + 127 * np.abs(dq8 - d8)[..., None]
+    assert np.all(err8 <= bound8 + 1e-30), "Q8_0 de-quantization error above its bound"
+    # zero blocks are zero scales with neutral codes
+    z4 = np.all(wb == 0, axis=-1)
+    assert np.all(d4[z4] == 0) and np.all(codes4[z4] == 8)
+    z8 = np.all(xb == 0, axis=-1)
+    assert np.all(d8[z8] == 0) and np.all(codes8[z8] == 0)
+
+
+def _q4_block(codes, d16_bits=0x3C00) -> np.ndarray:
+    codes = np.asarray(codes, np.uint8)
+    out = np.empty(18, np.uint8)
+    out[0], out[1] = d16_bits & 0xFF, d16_bits >> 8
+    out[2:] = codes[:16] | (codes[16:] << 4)
+    return out
+
+
+def _q8_block(codes, d16_bits=0x3C00) -> np.ndarray:
+    out = np.empty(34, np.uint8)
+    out[0], out[1] = d16_bits & 0xFF, d16_bits >> 8
+    out[2:] = np.asarray(codes, np.int8).view(np.uint8)
+    return out
+
+
+def pin_block_dot_bruteforce(o) -> None:
+    """One lane at a time: sumi = (q4 - 8) * q8 for every q4 in 0..15 and q8 in -127..127."""
+    q4v = np.arange(16)
+    q8v = np.arange(-127, 128)
+    for lane in (0, 5, 15, 16, 22, 31):
+        blocks4 = []
+        for a in q4v:
+            c = np.full(32, 8)
+            c[lane] = a
+            blocks4.append(_q4_block(c))
+        blocks8 = []
+        for b in q8v:
+            c = np.zeros(32, np.int64)
+            c[lane] = b
+            blocks8.append(_q8_block(c))
+        q4 = np.stack(blocks4)[:, None, :]
+        q8 = np.stack(blocks8)[:, None, :]
+        got = o.block_dots(q4, q8)[:, :, 0]                 # [q8 index, q4 index]
+        want = np.outer(q8v, q4v - 8)
+        assert np.array_equal(got, want), f"block dot wrong at lane {lane}"
+    # the extreme block: every q4 = 0 and every q8 = -127 gives 32 * 8 * 127
+    got = o.block_dots(_q4_block(np.zeros(32))[None, None], _q8_block(np.full(32, -127))[None, None])
+    assert int(got[0, 0, 0]) == 32512
+
+
+def pin_block_dot_random(o) -> None:
+    rng = np.random.default_rng(7)
+    N, M, nb = 24, 5, 6
+    c4 = rng.integers(0, 16, size=(N, nb, 32))
+    c8 = rng.integers(-127, 128, size=(M, nb, 32))
+    q4 = np.stack([np.stack([_q4_block(c4[n, b]) for b in range(nb)]) for n in range(N)])
+    q8 = np.stack([np.stack([_q8_block(c8[m, b]) for b in range(nb)]) for m in range(M)])
+    got = o.block_dots(q4, q8)
+    want = np.einsum("nbj,mbj->mnb", c4.astype(np.int64) - 8, c8.astype(np.int64))
+    assert np.array_equal(got, want)
+
+
+def pin_matmul_vs_dense(o) -> None:
+    """The f64 product equals float64 dequant(src0) @ dequant(wdata)^T to 1e-12 of T."""
+    for (M, N, K, seed, outl) in ((3, 40, 96, 1, False), (7, 33, 256, 2, True), (1, 17, 32, 3, False)):
+        w, x = synth.problem(seed, M, N, K, outliers=outl)
+        q4 = o.quantize_q4_0(w)
+        q8 = o.quantize_q8_0(x)
+        c4, d4 = decode_q4_0(q4)
+        c8, d8 = decode_q8_0(q8)
+        A = ((c4.astype(np.float64) - 8) * d4[..., None]).reshape(N, K)
+        B = (c8.astype(np.float64) * d8[..., None]).reshape(M, K)
+        want = B @ A.T
+        T_want = np.abs(B) @ np.abs(A).T
+        dst, T = o.mul_mat_q4_0_f32(q4, x)
+        assert np.all(np.abs(dst - want) <= 1e-12 * T_want + 1e-300), "Q4_0 product mismatch"
+        assert np.allclose(T, T_want, rtol=1e-12, atol=0)
+        ms = np.array([0, M - 1, M // 2])
+        ns = np.array([N - 1, 0, N // 2])
+        at, T_at = o.mul_mat_q4_0_q8_0_at(q4, q8, ms, ns)
+        assert np.array_equal(at, dst[ms, ns]) and np.array_equal(T_at, T[ms, ns])
+
+
+def pin_row_independence(o) -> None:
+    """Row m of an M-row product equals the product of row m alone (bit for bit)."""
+    M, N, K = 6, 20, 160
+    w, x = synth.problem(9, M, N, K)
+    q4 = o.quantize_q4_0(w)
+    dst, _ = o.mul_mat_q4_0_f32(q4, x)
+    for m in range(M):
+        one, _ = o.mul_mat_q4_0_f32(q4, x[m:m + 1])
+        assert np.array_equal(one[0], dst[m])
+    dst2, _ = o.mul_mat_f16_f32(synth.f16_bits(w), x)
+    for m in range(M):
+        one, _ = o.mul_mat_f16_f32(synth.f16_bits(w), x[m:m + 1])
+        assert np.array_equal(one[0], dst2[m])
+
+
+def pin_f16_matmul(o) -> None:
+    """F16 kind: selection weights give columns of src1 exactly; dense agreement."""
+    rng = np.random.default_rng(13)
+    M, N, K = 5, 37, 64
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    perm = rng.integers(0, K, size=N)
+    sel = np.zeros((N, K), np.float32)
+    sel[np.arange(N), perm] = 1.0
+    sel[::3, :] *= 2.0                      # powers of two stay exact
+    dst, T = o.mul_mat_f16_f32(synth.f16_bits(sel), x)
+    want = x[:, perm].astype(np.float64) * np.where(np.arange(N) % 3 == 0, 2.0, 1.0)
+    assert np.array_equal(dst, want)
+    w, x = synth.problem(14, 4, 29, 96)
+    wb = synth.f16_bits(w)
+    dst, T = o.mul_mat_f16_f32(wb, x)
+    W = wb.view(np.float16).astype(np.float64)
+    X = x.astype(np.float64)
+    assert np.all(np.abs(dst - X @ W.T) <= 1e-12 * (np.abs(X) @ np.abs(W).T))
+    assert np.allclose(T, np.abs(X) @ np.abs(W).T, rtol=1e-12, atol=0)
+    ms, ns = np.array([3, 0, 2]), np.array([0, 28, 11])
+    at, _ = o.mul_mat_f16_f32_at(wb, x, ms, ns)
+    assert np.array_equal(at, dst[ms, ns])
+
+
+ALL_PINS = [
+    pin_f16_conversion,
+    pin_worked_examples,
+    pin_roundtrip_q4_0,
+    pin_roundtrip_q8_0,
+    pin_ranges_and_error_bounds,
+    pin_block_dot_bruteforce,
+    pin_block_dot_random,
+    pin_matmul_vs_dense,
+    pin_row_independence,
+    pin_f16_matmul,
+]
