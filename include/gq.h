@@ -1,0 +1,182 @@
+/*
+ * gq.h -- C ABI of the GB300 quantized skinny MUL_MAT library (libgq.so).
+ *
+ * The operation is llama.cpp's MUL_MAT for decode and small-batch serving:
+ *
+ *     dst[M][N] = src1[M][K] . src0[N][K]^T        dst[m][n] = sum_k src0[n][k] * src1[m][k]
+ *
+ * in the two kinds named in llama.cpp pull request #1632, "Introduction":
+ * mul_mat_q_f32 (src0 block-quantized, here Q4_0) and mul_mat_f16_f32 (src0
+ * F16); src1 is F32 in both.  For the q_f32 kind, src1 is quantized row by row
+ * to Q8_0 (the "wdata" buffer of the Arm China NUMA article, section
+ * "MulMat 算子優化": dst = src0 * wdata) and the product is formed from exact
+ * int32 block dot products scaled by the two fp16 block scales.
+ *
+ * Conventions shared by every entry point
+ *   - All matrices are row-major with the last index contiguous: src0 [N][K],
+ *     src1 [M][K], dst [M][N].  Sizes are element counts (int64_t).
+ *   - Every pointer is a DEVICE pointer on the current CUDA device.  The caller
+ *     owns every buffer; the library keeps no pointer after a call returns.
+ *   - Work is enqueued on `stream` (0 = the legacy default stream) and the call
+ *     returns without waiting for it.  Results are defined once the stream has
+ *     reached that point.
+ *   - K must be a positive multiple of 32 (the block size); M and N positive.
+ *   - Every pointer must be 16-byte aligned.
+ *   - dst is overwritten, never accumulated into.
+ *   - Inputs are assumed finite; NaN or Inf inputs give unspecified outputs.
+ *   - Errors: GQ_ERR_INVALID_ARG (bad size, null pointer) and GQ_ERR_MISALIGNED
+ *     are returned before anything is launched; GQ_ERR_UNSUPPORTED_DEVICE when
+ *     the current device is not compute capability 10.3 (GB300);
+ *     GQ_ERR_CUDA when a CUDA call or launch failed (see gq_last_error_message);
+ *     a kernel-side wait that gave up is reported later by gq_last_error().
+ *     No C++ exception crosses this interface.
+ *   - Thread safety: every entry point may be called from several host threads.
+ *
+ * Block formats (the pages name Q4_0 and Q8_0 without defining them; these are
+ * the ggml layouts as this library reads them):
+ *   Q4_0, 18 bytes per 32 weights: fp16 d (little endian), then 16 bytes whose
+ *     byte i holds code q_i in the low nibble and q_{i+16} in the high nibble.
+ *     Weight j is (q_j - 8) * d.  Quantization of x[0..31]: m = the element of
+ *     largest magnitude (the first on a tie), d = m / -8 (f32),
+ *     q_j = clamp(roundf(x_j / d) + 8, 0, 15), or 8 when d == 0; the stored
+ *     scale is d rounded to fp16 (nearest even).
+ *   Q8_0, 34 bytes per 32 values: fp16 d, then 32 int8 codes.  d = amax / 127
+ *     (f32), q_j = roundf(x_j / d), or 0 when d == 0; stored scale fp16(d).
+ */
+#ifndef GQ_H
+#define GQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQ_ABI_VERSION 1
+
+typedef enum gq_status {
+    GQ_OK = 0,
+    GQ_ERR_INVALID_ARG = 1,        /* size <= 0, K % 32 != 0, null pointer, bad enum */
+    GQ_ERR_MISALIGNED = 2,         /* a pointer is not 16-byte aligned */
+    GQ_ERR_UNSUPPORTED_DEVICE = 3, /* the current device is not sm_103 */
+    GQ_ERR_CUDA = 4,               /* a CUDA runtime call or a launch failed */
+    GQ_ERR_TIMEOUT = 5,            /* a bounded in-kernel wait gave up (gq_last_error) */
+    GQ_ERR_NO_MEMORY = 6           /* the stream-ordered workspace could not be allocated */
+} gq_status;
+
+/* Which kernel family serves a product. */
+typedef enum gq_path {
+    GQ_PATH_AUTO = 0,   /* M <= threshold: the GEMV family, else the tensor-core tiles */
+    GQ_PATH_GEMV = 1,   /* the skinny GEMV kernels (any M; M > 16 runs in 16-row slices) */
+    GQ_PATH_TC = 2      /* the tcgen05 tensor-core tile kernels (any M) */
+} gq_path;
+
+/* ---- library information and errors ------------------------------------ */
+
+int gq_abi_version(void);                      /* GQ_ABI_VERSION of the built library */
+const char *gq_status_string(gq_status status); /* static text, never NULL */
+
+/* Text of the last error returned to this host thread (static storage of the
+ * thread, valid until its next call).  "" when the last call succeeded. */
+const char *gq_last_error_message(void);
+
+/* Sticky device-side status of the current device: GQ_ERR_TIMEOUT if a kernel
+ * gave up a bounded wait since the last call, else GQ_OK; reading clears it.
+ * Synchronizes the current device first. */
+gq_status gq_last_error(void);
+
+/* ---- buffer sizes --------------------------------------------------------- */
+
+size_t gq_q4_0_bytes(int64_t N, int64_t K);          /* N * K / 32 * 18 */
+size_t gq_q8_0_bytes(int64_t M, int64_t K);          /* M * K / 32 * 34 */
+size_t gq_q4_0_repacked_bytes(int64_t N, int64_t K); /* ceil(N/16) * ceil(K/128) * 1152 */
+
+/* ---- load-time preparation of the weights ---------------------------------- */
+
+/* Quantize F32 weights w [N][K] into canonical Q4_0 blocks q4_blocks
+ * [N][K/32] (gq_q4_0_bytes(N, K) bytes), byte-exact to the format above.
+ * llama.cpp PR #1632, "Introduction": src0 of the q_f32 kind is quantized. */
+gq_status gq_quantize_q4_0(const float *w, void *q4_blocks, int64_t N, int64_t K,
+                           cudaStream_t stream);
+
+/* Permute canonical Q4_0 blocks into the layout the product kernels stream
+ * (done once when the weights are loaded).  q4_repacked must hold
+ * gq_q4_0_repacked_bytes(N, K) bytes and must not overlap q4_blocks.
+ *
+ * Repacked layout (a pure byte permutation plus padding): rows are grouped by
+ * 16 (N16 = ceil(N/16) groups) and columns by 128 (NT = ceil(K/128) tiles of 4
+ * blocks).  Tile (g, t) occupies the 1152 bytes at offset (g*NT + t)*1152:
+ *   bytes [h*512 + L*16, +16), h in {0,1}, L in 0..31, r = L/4, c = L%4:
+ *       four 4-byte words: nibble bytes 4c..4c+3 of (row 16g+r,   block 4t+2h),
+ *       (row 16g+r+8, block 4t+2h), (row 16g+r, block 4t+2h+1),
+ *       (row 16g+r+8, block 4t+2h+1);
+ *   bytes [1024 + r*16, +16), r in 0..7: the fp16 scales of rows 16g+r and
+ *       16g+r+8 for blocks 4t+0..3, ordered (r,0),(r+8,0),(r,1),(r+8,1),...
+ * Rows >= N and blocks >= K/32 are padding: nibble bytes 0x88 and scale +0.
+ * (DeepSpeed-Inference notes, section III.C.3: rearrange the weights once at
+ * initialisation so that each thread's loads fill whole cache lines.) */
+gq_status gq_repack_q4_0(const void *q4_blocks, void *q4_repacked, int64_t N, int64_t K,
+                         cudaStream_t stream);
+
+/* ---- the INIT stage on its own ------------------------------------------------- */
+
+/* Quantize F32 activations x [M][K] into Q8_0 blocks q8_blocks [M][K/32]
+ * (gq_q8_0_bytes(M, K) bytes), byte-exact to the format above.  The product
+ * entry points do this themselves (fused); this entry exists for callers that
+ * keep wdata and for verification.  Arm China NUMA article, "MulMat 算子優化". */
+gq_status gq_quantize_rows_q8_0(const float *x, void *q8_blocks, int64_t M, int64_t K,
+                                cudaStream_t stream);
+
+/* ---- the products ---------------------------------------------------------------- */
+
+/* dst[M][N] = Q8_0(src1)[M][K] . Q4_0(src0)[N][K]^T with src0 given in the
+ * repacked layout of gq_repack_q4_0.  src1 is quantized to Q8_0 inside the call;
+ * each output is sum_b fp16(d4_b) * fp16(d8_b) * sumi_b with the exact int32
+ * block dots sumi_b, accumulated in f32 on the GEMV path (M <= threshold) and,
+ * on the tensor-core path, from fp16-rounded de-quantized operands with f32
+ * accumulation (relative error <= 2e-3 of sum |terms|).
+ * The tensor-core path allocates a stream-ordered workspace (cudaMallocAsync on
+ * `stream` from the device's default pool, freed on `stream` after use):
+ * 2 * ceil(M/128)*128 * K bytes. */
+gq_status gq_mul_mat_q4_0_f32(const void *q4_repacked, const float *src1, float *dst,
+                              int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/* dst[M][N] = src1[M][K] . src0[N][K]^T with F16 weights src0 (IEEE binary16,
+ * row-major).  Activations are rounded to fp16 for the tensor instructions and
+ * the sums are accumulated in f32 (relative error <= 2e-3 of sum |terms|).
+ * Workspace as above on the tensor-core path. */
+gq_status gq_mul_mat_f16_f32(const void *src0_f16, const float *src1, float *dst,
+                             int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/* The same two products with the kernel family chosen by the caller. */
+gq_status gq_mul_mat_q4_0_f32_path(const void *q4_repacked, const float *src1, float *dst,
+                                   int64_t M, int64_t N, int64_t K, gq_path path,
+                                   cudaStream_t stream);
+gq_status gq_mul_mat_f16_f32_path(const void *src0_f16, const float *src1, float *dst,
+                                  int64_t M, int64_t N, int64_t K, gq_path path,
+                                  cudaStream_t stream);
+
+/* M threshold of GQ_PATH_AUTO: M <= threshold runs the GEMV family.  Default 16
+ * (Smallem, "Générer à plusieurs", section "La courbe, une première fois": the
+ * narrow kernel serves products of at most 16 rows, the tiles the rest).
+ * Process-wide; GQ_ERR_INVALID_ARG if t < 0. */
+gq_status gq_set_m_threshold(int64_t t);
+int64_t gq_get_m_threshold(void);
+
+/* ---- verification --------------------------------------------------------------- */
+
+/* The integer block dots of the GEMV instruction sequence, for parity tests:
+ * sumi[M][N][K/32] (int32) = sum_j (q4_j - 8) * q8_j for every (row m of the
+ * Q8_0 blocks q8_blocks [M][K/32], row n of the repacked Q4_0 weights, block b).
+ * Not a product entry point: it writes M*N*K/32 int32 values. */
+gq_status gq_debug_block_dots_q4_0(const void *q4_repacked, const void *q8_blocks,
+                                   int32_t *sumi, int64_t M, int64_t N, int64_t K,
+                                   cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQ_H */

@@ -1,0 +1,231 @@
+"""Python binding of libgq, the GB300 quantized skinny MUL_MAT library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``_lib/libgq.so`` (built by ``_build.py``); PyTorch supplies device
+memory and streams.  There is no CPU fallback: when the library is missing or
+the device is not a GB300, the calls raise.
+
+The functions below carry the names of the C entry points in ``include/gq.h``
+and take the same arguments, with torch CUDA tensors (or raw device addresses
+as ints) in place of pointers and an optional stream (default: torch's current
+stream).  They raise ``GQError`` when the C call returns a non-zero status.
+The lower-case helpers at the end allocate the outputs with torch and call them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libgq.so")
+
+GQ_OK = 0
+GQ_ERR_INVALID_ARG = 1
+GQ_ERR_MISALIGNED = 2
+GQ_ERR_UNSUPPORTED_DEVICE = 3
+GQ_ERR_CUDA = 4
+GQ_ERR_TIMEOUT = 5
+GQ_ERR_NO_MEMORY = 6
+
+GQ_PATH_AUTO = 0
+GQ_PATH_GEMV = 1
+GQ_PATH_TC = 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GQError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        self.status = status
+        super().__init__(f"{where}: status {status}: {message}")
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+_S = ctypes.c_int
+
+# name -> (argtypes, restype); the signatures of include/gq.h
+SIGNATURES = {
+    "gq_abi_version": ([], ctypes.c_int),
+    "gq_status_string": ([_S], ctypes.c_char_p),
+    "gq_last_error_message": ([], ctypes.c_char_p),
+    "gq_last_error": ([], _S),
+    "gq_q4_0_bytes": ([_I, _I], ctypes.c_size_t),
+    "gq_q8_0_bytes": ([_I, _I], ctypes.c_size_t),
+    "gq_q4_0_repacked_bytes": ([_I, _I], ctypes.c_size_t),
+    "gq_quantize_q4_0": ([_P, _P, _I, _I, _P], _S),
+    "gq_quantize_rows_q8_0": ([_P, _P, _I, _I, _P], _S),
+    "gq_repack_q4_0": ([_P, _P, _I, _I, _P], _S),
+    "gq_mul_mat_q4_0_f32": ([_P, _P, _P, _I, _I, _I, _P], _S),
+    "gq_mul_mat_f16_f32": ([_P, _P, _P, _I, _I, _I, _P], _S),
+    "gq_mul_mat_q4_0_f32_path": ([_P, _P, _P, _I, _I, _I, _S, _P], _S),
+    "gq_mul_mat_f16_f32_path": ([_P, _P, _P, _I, _I, _I, _S, _P], _S),
+    "gq_set_m_threshold": ([_I], _S),
+    "gq_get_m_threshold": ([], _I),
+    "gq_debug_block_dots_q4_0": ([_P, _P, _P, _I, _I, _I, _P], _S),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgq.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with "
+                        "`python -m quantized_skinny_matmul_gb300._build` (nvcc, sm_103a)")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (args, res) in SIGNATURES.items():
+                    fn = getattr(handle, name)
+                    fn.argtypes = args
+                    fn.restype = res
+                _lib = handle
+    return _lib
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != GQ_OK:
+        msg = lib().gq_last_error_message().decode(errors="replace")
+        raise GQError(status, where, msg or lib().gq_status_string(status).decode())
+
+
+# ---------------------------------------------------------------------------
+# the entry points of include/gq.h
+# ---------------------------------------------------------------------------
+def gq_abi_version() -> int:
+    return lib().gq_abi_version()
+
+
+def gq_last_error() -> int:
+    """Status of the device-side sticky word (synchronizes the device)."""
+    return lib().gq_last_error()
+
+
+def gq_q4_0_bytes(N: int, K: int) -> int:
+    return lib().gq_q4_0_bytes(N, K)
+
+
+def gq_q8_0_bytes(M: int, K: int) -> int:
+    return lib().gq_q8_0_bytes(M, K)
+
+
+def gq_q4_0_repacked_bytes(N: int, K: int) -> int:
+    return lib().gq_q4_0_repacked_bytes(N, K)
+
+
+def gq_quantize_q4_0(w, q4_blocks, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_quantize_q4_0(_ptr(w), _ptr(q4_blocks), N, K, _stream(stream)), "gq_quantize_q4_0")
+
+
+def gq_quantize_rows_q8_0(x, q8_blocks, M: int, K: int, stream=None) -> None:
+    _check(lib().gq_quantize_rows_q8_0(_ptr(x), _ptr(q8_blocks), M, K, _stream(stream)),
+           "gq_quantize_rows_q8_0")
+
+
+def gq_repack_q4_0(q4_blocks, q4_repacked, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_repack_q4_0(_ptr(q4_blocks), _ptr(q4_repacked), N, K, _stream(stream)),
+           "gq_repack_q4_0")
+
+
+def gq_mul_mat_q4_0_f32(q4_repacked, src1, dst, M: int, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_mul_mat_q4_0_f32(_ptr(q4_repacked), _ptr(src1), _ptr(dst), M, N, K, _stream(stream)),
+           "gq_mul_mat_q4_0_f32")
+
+
+def gq_mul_mat_f16_f32(src0_f16, src1, dst, M: int, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_mul_mat_f16_f32(_ptr(src0_f16), _ptr(src1), _ptr(dst), M, N, K, _stream(stream)),
+           "gq_mul_mat_f16_f32")
+
+
+def gq_mul_mat_q4_0_f32_path(q4_repacked, src1, dst, M: int, N: int, K: int, path: int,
+                             stream=None) -> None:
+    _check(lib().gq_mul_mat_q4_0_f32_path(_ptr(q4_repacked), _ptr(src1), _ptr(dst), M, N, K, path,
+                                          _stream(stream)), "gq_mul_mat_q4_0_f32_path")
+
+
+def gq_mul_mat_f16_f32_path(src0_f16, src1, dst, M: int, N: int, K: int, path: int,
+                            stream=None) -> None:
+    _check(lib().gq_mul_mat_f16_f32_path(_ptr(src0_f16), _ptr(src1), _ptr(dst), M, N, K, path,
+                                         _stream(stream)), "gq_mul_mat_f16_f32_path")
+
+
+def gq_set_m_threshold(t: int) -> None:
+    _check(lib().gq_set_m_threshold(t), "gq_set_m_threshold")
+
+
+def gq_get_m_threshold() -> int:
+    return lib().gq_get_m_threshold()
+
+
+def gq_debug_block_dots_q4_0(q4_repacked, q8_blocks, sumi, M: int, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_debug_block_dots_q4_0(_ptr(q4_repacked), _ptr(q8_blocks), _ptr(sumi), M, N, K,
+                                          _stream(stream)), "gq_debug_block_dots_q4_0")
+
+
+# ---------------------------------------------------------------------------
+# allocating helpers (torch tensors in, torch tensors out)
+# ---------------------------------------------------------------------------
+def quantize_q4_0(w):
+    """f32 CUDA tensor [N, K] -> canonical Q4_0 bytes, uint8 [N, K/32, 18]."""
+    import torch
+    N, K = w.shape
+    out = torch.empty((N, K // 32, 18), dtype=torch.uint8, device=w.device)
+    gq_quantize_q4_0(w, out, N, K)
+    return out
+
+
+def quantize_rows_q8_0(x):
+    import torch
+    M, K = x.shape
+    out = torch.empty((M, K // 32, 34), dtype=torch.uint8, device=x.device)
+    gq_quantize_rows_q8_0(x, out, M, K)
+    return out
+
+
+def repack_q4_0(q4, N: int, K: int):
+    import torch
+    out = torch.empty(gq_q4_0_repacked_bytes(N, K), dtype=torch.uint8, device=q4.device)
+    gq_repack_q4_0(q4, out, N, K)
+    return out
+
+
+def mul_mat_q4_0_f32(q4_repacked, src1, N: int, path: int = GQ_PATH_AUTO, out=None):
+    import torch
+    M, K = src1.shape
+    dst = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=src1.device)
+    gq_mul_mat_q4_0_f32_path(q4_repacked, src1, dst, M, N, K, path)
+    return dst
+
+
+def mul_mat_f16_f32(src0_f16, src1, path: int = GQ_PATH_AUTO, out=None):
+    import torch
+    N, K = src0_f16.shape
+    M = src1.shape[0]
+    dst = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=src1.device)
+    gq_mul_mat_f16_f32_path(src0_f16, src1, dst, M, N, K, path)
+    return dst

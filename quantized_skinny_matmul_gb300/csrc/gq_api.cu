@@ -1,0 +1,263 @@
+// gq_api.cu -- the C entry points of libgq: argument checks, device checks,
+// error reporting and the M-threshold dispatch between the kernel families.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "gq_common.cuh"
+#include "gq_internal.h"
+
+namespace gq {
+
+// Sticky device-side status word of each device (bit STATUS_TIMEOUT).
+__device__ unsigned int g_status_word;
+
+namespace {
+
+thread_local char t_message[512];
+
+constexpr int MAX_DEVICES = 64;
+std::atomic<int> g_arch_ok[MAX_DEVICES];      // 0 unknown, 1 sm_103, -1 other
+std::atomic<int> g_sm_count[MAX_DEVICES];
+std::atomic<int64_t> g_m_threshold{16};
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+gq_status current_device(int *dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return check_cuda(e, "cudaGetDevice");
+    if (*dev < 0 || *dev >= MAX_DEVICES) return fail(GQ_ERR_UNSUPPORTED_DEVICE, "device index %d", *dev);
+    return GQ_OK;
+}
+
+// The kernels are built for sm_103a only: refuse other devices up front.
+gq_status check_device() {
+    int dev;
+    gq_status st = current_device(&dev);
+    if (st != GQ_OK) return st;
+    int known = g_arch_ok[dev].load(std::memory_order_relaxed);
+    if (known == 0) {
+        int major = 0, minor = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return check_cuda(e, "cudaDeviceGetAttribute");
+        known = (major == 10 && minor == 3) ? 1 : -1;
+        g_arch_ok[dev].store(known, std::memory_order_relaxed);
+        if (known < 0)
+            return fail(GQ_ERR_UNSUPPORTED_DEVICE, "device %d is sm_%d%d; libgq is built for sm_103a only",
+                        dev, major, minor);
+    }
+    if (known < 0) return fail(GQ_ERR_UNSUPPORTED_DEVICE, "device %d is not sm_103", dev);
+    return GQ_OK;
+}
+
+gq_status check_sizes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0) return fail(GQ_ERR_INVALID_ARG, "sizes must be positive (M=%lld N=%lld K=%lld)",
+                                                (long long)M, (long long)N, (long long)K);
+    if (K % QK != 0) return fail(GQ_ERR_INVALID_ARG, "K=%lld is not a multiple of 32", (long long)K);
+    // 32-bit index arithmetic inside the kernels
+    if (N > (1LL << 30) || K > (1LL << 30) || M > (1LL << 30) || N * K > (1LL << 40))
+        return fail(GQ_ERR_INVALID_ARG, "sizes too large (M=%lld N=%lld K=%lld)", (long long)M, (long long)N,
+                    (long long)K);
+    return GQ_OK;
+}
+
+gq_status check_ptr(const void *p, const char *name) {
+    if (p == nullptr) return fail(GQ_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned16(p)) return fail(GQ_ERR_MISALIGNED, "%s (%p) is not 16-byte aligned", name, p);
+    return GQ_OK;
+}
+
+gq_status ok() {
+    t_message[0] = '\0';
+    return GQ_OK;
+}
+
+#define GQ_TRY(expr)                       \
+    do {                                   \
+        gq_status _st = (expr);            \
+        if (_st != GQ_OK) return _st;      \
+    } while (0)
+
+}  // namespace
+
+gq_status fail(gq_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_message, sizeof(t_message), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+gq_status check_cuda(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return GQ_OK;
+    return fail(GQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return 148;
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+}  // namespace gq
+
+using namespace gq;
+
+extern "C" {
+
+int gq_abi_version(void) { return GQ_ABI_VERSION; }
+
+const char *gq_status_string(gq_status s) {
+    switch (s) {
+        case GQ_OK: return "ok";
+        case GQ_ERR_INVALID_ARG: return "invalid argument";
+        case GQ_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case GQ_ERR_UNSUPPORTED_DEVICE: return "unsupported device (sm_103 required)";
+        case GQ_ERR_CUDA: return "CUDA error";
+        case GQ_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+        case GQ_ERR_NO_MEMORY: return "workspace allocation failed";
+    }
+    return "unknown status";
+}
+
+const char *gq_last_error_message(void) { return t_message; }
+
+gq_status gq_last_error(void) {
+    GQ_TRY(check_device());
+    GQ_TRY(check_cuda(cudaDeviceSynchronize(), "cudaDeviceSynchronize"));
+    unsigned int word = 0, zero = 0;
+    GQ_TRY(check_cuda(cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)), "read device status"));
+    GQ_TRY(check_cuda(cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)), "clear device status"));
+    if (word & STATUS_TIMEOUT) return fail(GQ_ERR_TIMEOUT, "a kernel gave up a bounded wait");
+    return ok();
+}
+
+size_t gq_q4_0_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % QK) return 0;
+    return (size_t)N * (size_t)(K / QK) * Q4_0_BYTES;
+}
+
+size_t gq_q8_0_bytes(int64_t M, int64_t K) {
+    if (M <= 0 || K <= 0 || K % QK) return 0;
+    return (size_t)M * (size_t)(K / QK) * Q8_0_BYTES;
+}
+
+size_t gq_q4_0_repacked_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % QK) return 0;
+    return (size_t)((N + 15) / 16) * (size_t)((K + TILE_COLS - 1) / TILE_COLS) * TILE_BYTES;
+}
+
+gq_status gq_quantize_q4_0(const float *w, void *q4_blocks, int64_t N, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(1, N, K));
+    GQ_TRY(check_ptr(w, "w"));
+    GQ_TRY(check_ptr(q4_blocks, "q4_blocks"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_quantize_q4_0(w, q4_blocks, N, K, stream));
+    return ok();
+}
+
+gq_status gq_quantize_rows_q8_0(const float *x, void *q8_blocks, int64_t M, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(M, 1, K));
+    GQ_TRY(check_ptr(x, "x"));
+    GQ_TRY(check_ptr(q8_blocks, "q8_blocks"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_quantize_rows_q8_0(x, q8_blocks, M, K, stream));
+    return ok();
+}
+
+gq_status gq_repack_q4_0(const void *q4_blocks, void *q4_repacked, int64_t N, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(1, N, K));
+    GQ_TRY(check_ptr(q4_blocks, "q4_blocks"));
+    GQ_TRY(check_ptr(q4_repacked, "q4_repacked"));
+    const uintptr_t a = (uintptr_t)q4_blocks, b = (uintptr_t)q4_repacked;
+    if (a < b + gq_q4_0_repacked_bytes(N, K) && b < a + gq_q4_0_bytes(N, K))
+        return fail(GQ_ERR_INVALID_ARG, "q4_blocks and q4_repacked overlap");
+    GQ_TRY(check_device());
+    GQ_TRY(launch_repack_q4_0(q4_blocks, q4_repacked, N, K, stream));
+    return ok();
+}
+
+gq_status gq_set_m_threshold(int64_t t) {
+    if (t < 0) return fail(GQ_ERR_INVALID_ARG, "threshold %lld < 0", (long long)t);
+    g_m_threshold.store(t);
+    return ok();
+}
+
+int64_t gq_get_m_threshold(void) { return g_m_threshold.load(); }
+
+static gq_status check_path(gq_path path) {
+    if (path != GQ_PATH_AUTO && path != GQ_PATH_GEMV && path != GQ_PATH_TC)
+        return fail(GQ_ERR_INVALID_ARG, "unknown path %d", (int)path);
+    return GQ_OK;
+}
+
+// Which family serves M rows: Smallem, "La courbe, une première fois" (the
+// narrow kernel up to 16 rows, tiles above); llama.cpp PR #1632, "Introduction"
+// (the M >= 32 rule and how sensitive the choice is around it).
+static gq_path resolve(gq_path path, int64_t M) {
+    if (path != GQ_PATH_AUTO) return path;
+    return M <= g_m_threshold.load() ? GQ_PATH_GEMV : GQ_PATH_TC;
+}
+
+gq_status gq_mul_mat_q4_0_f32_path(const void *q4_repacked, const float *src1, float *dst, int64_t M, int64_t N,
+                                   int64_t K, gq_path path, cudaStream_t stream) {
+    GQ_TRY(check_sizes(M, N, K));
+    GQ_TRY(check_path(path));
+    GQ_TRY(check_ptr(q4_repacked, "q4_repacked"));
+    GQ_TRY(check_ptr(src1, "src1"));
+    GQ_TRY(check_ptr(dst, "dst"));
+    GQ_TRY(check_device());
+    switch (resolve(path, M)) {
+        case GQ_PATH_TC:   // the tensor-core tile family is not built yet: GEMV slices
+        case GQ_PATH_GEMV:
+        default: GQ_TRY(launch_gemv_q4_0(q4_repacked, src1, dst, M, N, K, stream)); break;
+    }
+    return ok();
+}
+
+gq_status gq_mul_mat_f16_f32_path(const void *src0_f16, const float *src1, float *dst, int64_t M, int64_t N,
+                                  int64_t K, gq_path path, cudaStream_t stream) {
+    GQ_TRY(check_sizes(M, N, K));
+    GQ_TRY(check_path(path));
+    GQ_TRY(check_ptr(src0_f16, "src0_f16"));
+    GQ_TRY(check_ptr(src1, "src1"));
+    GQ_TRY(check_ptr(dst, "dst"));
+    GQ_TRY(check_device());
+    switch (resolve(path, M)) {
+        case GQ_PATH_TC:
+        case GQ_PATH_GEMV:
+        default: GQ_TRY(launch_gemv_f16(src0_f16, src1, dst, M, N, K, stream)); break;
+    }
+    return ok();
+}
+
+gq_status gq_mul_mat_q4_0_f32(const void *q4_repacked, const float *src1, float *dst, int64_t M, int64_t N,
+                              int64_t K, cudaStream_t stream) {
+    return gq_mul_mat_q4_0_f32_path(q4_repacked, src1, dst, M, N, K, GQ_PATH_AUTO, stream);
+}
+
+gq_status gq_mul_mat_f16_f32(const void *src0_f16, const float *src1, float *dst, int64_t M, int64_t N, int64_t K,
+                             cudaStream_t stream) {
+    return gq_mul_mat_f16_f32_path(src0_f16, src1, dst, M, N, K, GQ_PATH_AUTO, stream);
+}
+
+gq_status gq_debug_block_dots_q4_0(const void *q4_repacked, const void *q8_blocks, int32_t *sumi, int64_t M,
+                                   int64_t N, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(M, N, K));
+    GQ_TRY(check_ptr(q4_repacked, "q4_repacked"));
+    GQ_TRY(check_ptr(q8_blocks, "q8_blocks"));
+    GQ_TRY(check_ptr(sumi, "sumi"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_block_dots_q4_0(q4_repacked, q8_blocks, sumi, M, N, K, stream));
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,31 @@
+// gq_internal.h -- host-side interface between the translation units of libgq.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gq.h"
+
+namespace gq {
+
+// Records the message returned by gq_last_error_message() for this thread.
+gq_status fail(gq_status s, const char *fmt, ...);
+// Maps a CUDA error to GQ_ERR_CUDA (with its text), cudaSuccess to GQ_OK.
+gq_status check_cuda(cudaError_t e, const char *what);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Launchers (arguments already validated by the entry points).
+gq_status launch_quantize_q4_0(const float *w, void *q4, int64_t N, int64_t K, cudaStream_t s);
+gq_status launch_quantize_rows_q8_0(const float *x, void *q8, int64_t M, int64_t K, cudaStream_t s);
+gq_status launch_repack_q4_0(const void *q4, void *rep, int64_t N, int64_t K, cudaStream_t s);
+
+gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N,
+                           int64_t K, cudaStream_t s);
+gq_status launch_gemv_f16(const void *w16, const float *x, float *dst, int64_t M, int64_t N,
+                          int64_t K, cudaStream_t s);
+gq_status launch_block_dots_q4_0(const void *rep, const void *q8, int32_t *sumi, int64_t M,
+                                 int64_t N, int64_t K, cudaStream_t s);
+
+}  // namespace gq

@@ -1,0 +1,143 @@
+// quantize.cu -- load-time weight quantization (Q4_0), the standalone INIT
+// stage (Q8_0 of activation rows) and the load-time repack of Q4_0 weights.
+//
+// One warp per block of 32 values: lane j owns element j, the block's maximum
+// magnitude is a warp reduction, and the codes are decided in f32 exactly as
+// the block formats define them (IEEE division, roundf, fp16 round-to-even).
+#include "gq_common.cuh"
+#include "gq_internal.h"
+
+namespace gq {
+namespace {
+
+// Q4_0 (llama.cpp PR #1632, "Introduction": src0 of the q_f32 kind is quantized).
+__global__ void quantize_q4_0_kernel(const float *__restrict__ w, uint8_t *__restrict__ out,
+                                     int64_t nblocks) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = warp; b < nblocks; b += nwarps) {
+        const float x = w[b * QK + lane];          // K % 32 == 0: block b is 32 contiguous floats
+        // magnitudes are non-negative, so their bit patterns order like the values
+        const unsigned int abits = __float_as_uint(fabsf(x));
+        const unsigned int amax = __reduce_max_sync(0xffffffffu, abits);
+        const unsigned int first = __ffs(__ballot_sync(0xffffffffu, abits == amax)) - 1;
+        float vmax = __shfl_sync(0xffffffffu, x, first);
+        if (amax == 0u) vmax = 0.0f;               // no element exceeded zero: the signed max stays +0
+        const float d = vmax / -8.0f;
+        int q = 8;
+        if (d != 0.0f) {
+            const int v = (int)roundf(x / d) + 8;
+            q = v < 0 ? 0 : (v > 15 ? 15 : v);
+        }
+        const int qhi = __shfl_down_sync(0xffffffffu, q, 16);
+        uint8_t *o = out + b * Q4_0_BYTES;
+        if (lane < 16) o[2 + lane] = (uint8_t)(q | (qhi << 4));
+        if (lane == 0) {
+            const unsigned short h = __half_as_ushort(__float2half_rn(d));
+            o[0] = (uint8_t)(h & 0xffu);
+            o[1] = (uint8_t)(h >> 8);
+        }
+    }
+}
+
+// Q8_0 of activation rows: the INIT stage that produces wdata (Arm China NUMA
+// article, "MulMat 算子優化").
+__global__ void quantize_rows_q8_0_kernel(const float *__restrict__ x, uint8_t *__restrict__ out,
+                                          int64_t nblocks) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = warp; b < nblocks; b += nwarps) {
+        const float v = x[b * QK + lane];
+        const unsigned int amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
+        const float d = __uint_as_float(amax) / 127.0f;
+        uint8_t *o = out + b * Q8_0_BYTES;
+        o[2 + lane] = (uint8_t)(q8_code(v, d) & 0xff);
+        if (lane == 0) {
+            const unsigned short h = __half_as_ushort(__float2half_rn(d));
+            o[0] = (uint8_t)(h & 0xffu);
+            o[1] = (uint8_t)(h >> 8);
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t load_u32_bytes(const uint8_t *p) {
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+
+// Load-time repack into the tiled layout documented with gq_repack_q4_0
+// (DeepSpeed-Inference notes, III.C.3: weights rearranged once at
+// initialisation so that every load fills whole cache lines).  One thread per
+// (tile, lane): two 16-byte code words, and lanes 0..7 also the tile's scales.
+__global__ void repack_q4_0_kernel(const uint8_t *__restrict__ q4, uint8_t *__restrict__ rep,
+                                   int64_t N, int64_t nb, int64_t NT, int64_t ntiles) {
+    pdl_wait();
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t tile = tid >> 5;
+    if (tile >= ntiles) return;
+    const int L = (int)(tid & 31);
+    const int64_t g = tile / NT, t = tile % NT;
+    const int r = L >> 2, c = L & 3;
+    uint8_t *dst = rep + tile * TILE_BYTES;
+
+    auto code_word = [&](int64_t n, int64_t b) -> uint32_t {
+        if (n >= N || b >= nb) return 0x88888888u;
+        return load_u32_bytes(q4 + (n * nb + b) * Q4_0_BYTES + 2 + 4 * c);
+    };
+    for (int h = 0; h < 2; h++) {
+        const int64_t b0 = 4 * t + 2 * h;
+        uint4 v;
+        v.x = code_word(16 * g + r, b0);
+        v.y = code_word(16 * g + r + 8, b0);
+        v.z = code_word(16 * g + r, b0 + 1);
+        v.w = code_word(16 * g + r + 8, b0 + 1);
+        *reinterpret_cast<uint4 *>(dst + h * 512 + L * 16) = v;
+    }
+    if (L < 8) {
+        auto scale = [&](int64_t n, int64_t b) -> uint32_t {
+            if (n >= N || b >= nb) return 0u;
+            const uint8_t *p = q4 + (n * nb + b) * Q4_0_BYTES;
+            return (uint32_t)p[0] | ((uint32_t)p[1] << 8);
+        };
+        uint32_t s[4];
+        for (int j = 0; j < 4; j++)
+            s[j] = scale(16 * g + L, 4 * t + j) | (scale(16 * g + L + 8, 4 * t + j) << 16);
+        *reinterpret_cast<uint4 *>(dst + TILE_SCALE_OFFSET + L * 16) = make_uint4(s[0], s[1], s[2], s[3]);
+    }
+}
+
+int grid_for(int64_t work_items, int threads) {
+    int64_t blocks = (work_items + threads - 1) / threads;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    return (int)(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+gq_status launch_quantize_q4_0(const float *w, void *q4, int64_t N, int64_t K, cudaStream_t s) {
+    const int64_t nblocks = N * (K / QK);
+    quantize_q4_0_kernel<<<grid_for(nblocks * 32, 256), 256, 0, s>>>(w, (uint8_t *)q4, nblocks);
+    return check_cuda(cudaGetLastError(), "quantize_q4_0 launch");
+}
+
+gq_status launch_quantize_rows_q8_0(const float *x, void *q8, int64_t M, int64_t K, cudaStream_t s) {
+    const int64_t nblocks = M * (K / QK);
+    quantize_rows_q8_0_kernel<<<grid_for(nblocks * 32, 256), 256, 0, s>>>(x, (uint8_t *)q8, nblocks);
+    return check_cuda(cudaGetLastError(), "quantize_rows_q8_0 launch");
+}
+
+gq_status launch_repack_q4_0(const void *q4, void *rep, int64_t N, int64_t K, cudaStream_t s) {
+    const int64_t nb = K / QK;
+    const int64_t N16 = (N + 15) / 16, NT = (K + TILE_COLS - 1) / TILE_COLS;
+    const int64_t ntiles = N16 * NT;
+    const int64_t threads = ntiles * 32;
+    const int64_t blocks = (threads + 255) / 256;
+    repack_q4_0_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint8_t *)q4, (uint8_t *)rep, N, nb, NT, ntiles);
+    return check_cuda(cudaGetLastError(), "repack_q4_0 launch");
+}
+
+}  // namespace gq

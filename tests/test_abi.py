@@ -1,0 +1,97 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/gq.h declares, and rejects bad arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_skinny_matmul_gb300 as gq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gq.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gq_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__  # noqa: F401  (build() is what the driver runs)
+    from quantized_skinny_matmul_gb300 import _build
+    _build.build()
+    return gq.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("gq_quantize_q4_0", "gq_quantize_rows_q8_0", "gq_repack_q4_0",
+                     "gq_mul_mat_q4_0_f32", "gq_mul_mat_f16_f32", "gq_last_error",
+                     "gq_debug_block_dots_q4_0"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(gq.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+    # and the binding declares a signature for each of them
+    assert set(declared_functions()) <= set(gq.SIGNATURES)
+
+
+def test_version_and_strings(lib):
+    assert gq.gq_abi_version() == 1
+    for s in range(7):
+        assert lib.gq_status_string(s)
+    assert lib.gq_status_string(99) == b"unknown status"
+
+
+def test_sizes(lib):
+    assert gq.gq_q4_0_bytes(4096, 4096) == 4096 * 128 * 18
+    assert gq.gq_q8_0_bytes(3, 64) == 3 * 2 * 34
+    assert gq.gq_q4_0_repacked_bytes(4096, 4096) == 256 * 32 * 1152 == 4096 * 128 * 18
+    assert gq.gq_q4_0_repacked_bytes(11008, 4096) == 11008 * 128 * 18
+    assert gq.gq_q4_0_repacked_bytes(4096, 11008) == 4096 * 344 * 18
+    assert gq.gq_q4_0_repacked_bytes(17, 96) == 2 * 1 * 1152
+    assert gq.gq_q4_0_bytes(4, 33) == 0 and gq.gq_q4_0_repacked_bytes(0, 32) == 0
+
+
+FAKE = 0x10000            # 16-byte aligned, never dereferenced: checks fail first
+ODD = 0x10008
+
+
+@pytest.mark.parametrize("args, status", [
+    ((FAKE, FAKE, FAKE, 1, 64, 48), gq.GQ_ERR_INVALID_ARG),     # K % 32
+    ((FAKE, FAKE, FAKE, 0, 64, 64), gq.GQ_ERR_INVALID_ARG),     # M == 0
+    ((FAKE, FAKE, FAKE, 1, -1, 64), gq.GQ_ERR_INVALID_ARG),     # N < 0
+    ((0, FAKE, FAKE, 1, 64, 64), gq.GQ_ERR_INVALID_ARG),        # null weights
+    ((FAKE, 0, FAKE, 1, 64, 64), gq.GQ_ERR_INVALID_ARG),        # null src1
+    ((FAKE, FAKE, 0, 1, 64, 64), gq.GQ_ERR_INVALID_ARG),        # null dst
+    ((ODD, FAKE, FAKE, 1, 64, 64), gq.GQ_ERR_MISALIGNED),
+    ((FAKE, ODD, FAKE, 1, 64, 64), gq.GQ_ERR_MISALIGNED),
+    ((FAKE, FAKE, ODD, 1, 64, 64), gq.GQ_ERR_MISALIGNED),
+])
+def test_argument_checks_mul_mat(lib, args, status):
+    for fn in (lib.gq_mul_mat_q4_0_f32, lib.gq_mul_mat_f16_f32):
+        assert fn(*args, None) == status
+        assert lib.gq_last_error_message()
+
+
+def test_argument_checks_other_entries(lib):
+    assert lib.gq_quantize_q4_0(FAKE, FAKE, 4, 40, None) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_quantize_q4_0(ODD, FAKE, 4, 64, None) == gq.GQ_ERR_MISALIGNED
+    assert lib.gq_quantize_rows_q8_0(FAKE, 0, 4, 64, None) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_repack_q4_0(FAKE, FAKE, 4, 64, None) == gq.GQ_ERR_INVALID_ARG   # overlap
+    assert lib.gq_debug_block_dots_q4_0(FAKE, FAKE, ODD, 1, 16, 64, None) == gq.GQ_ERR_MISALIGNED
+    assert lib.gq_mul_mat_q4_0_f32_path(FAKE, FAKE, FAKE, 1, 64, 64, 7, None) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_set_m_threshold(-1) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_set_m_threshold(16) == gq.GQ_OK and lib.gq_get_m_threshold() == 16
+
+
+def test_binding_raises(lib):
+    with pytest.raises(gq.GQError) as e:
+        gq.gq_mul_mat_q4_0_f32(FAKE, FAKE, FAKE, 1, 64, 48, stream=0)
+    assert e.value.status == gq.GQ_ERR_INVALID_ARG and "multiple of 32" in str(e.value)
