@@ -32,13 +32,9 @@ __global__ void quantize_q4_0_kernel(const float *__restrict__ w, uint8_t *__res
             q = v < 0 ? 0 : (v > 15 ? 15 : v);
         }
         const int qhi = __shfl_down_sync(0xffffffffu, q, 16);
-        uint8_t *o = out + b * Q4_0_BYTES;
+        uint8_t *o = out + b * Q4_0_BYTES;            // 2-byte aligned: 18 * b is even
         if (lane < 16) o[2 + lane] = (uint8_t)(q | (qhi << 4));
-        if (lane == 0) {
-            const unsigned short h = __half_as_ushort(__float2half_rn(d));
-            o[0] = (uint8_t)(h & 0xffu);
-            o[1] = (uint8_t)(h >> 8);
-        }
+        if (lane == 0) *reinterpret_cast<unsigned short *>(o) = __half_as_ushort(__float2half_rn(d));
     }
 }
 
@@ -54,13 +50,9 @@ __global__ void quantize_rows_q8_0_kernel(const float *__restrict__ x, uint8_t *
         const float v = x[b * QK + lane];
         const unsigned int amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
         const float d = __uint_as_float(amax) / 127.0f;
-        uint8_t *o = out + b * Q8_0_BYTES;
+        uint8_t *o = out + b * Q8_0_BYTES;            // 2-byte aligned: 34 * b is even
         o[2 + lane] = (uint8_t)(q8_code(v, d) & 0xff);
-        if (lane == 0) {
-            const unsigned short h = __half_as_ushort(__float2half_rn(d));
-            o[0] = (uint8_t)(h & 0xffu);
-            o[1] = (uint8_t)(h >> 8);
-        }
+        if (lane == 0) *reinterpret_cast<unsigned short *>(o) = __half_as_ushort(__float2half_rn(d));
     }
 }
 

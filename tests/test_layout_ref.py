@@ -1,0 +1,13 @@
+"""The two numpy statements of the repacked layout agree (CPU): the vectorized
+one used by the GPU tests and a byte-by-byte transcription of the header text."""
+import numpy as np
+import pytest
+
+from layout_ref import repack_ref, repack_loops
+
+
+@pytest.mark.parametrize("N,nb", [(16, 4), (37, 3), (33, 9), (1, 1), (64, 16)])
+def test_layout_statements_agree(N, nb):
+    rng = np.random.default_rng(N * 100 + nb)
+    q4 = rng.integers(0, 256, size=(N, nb, 18), dtype=np.uint8)
+    assert np.array_equal(repack_ref(q4), repack_loops(q4))
