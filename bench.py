@@ -142,6 +142,8 @@ class GpuBench:
         self.props = torch.cuda.get_device_properties(self.dev)
         self.l2 = int(getattr(self.props, "L2_cache_size", 126 * 2 ** 20))
         self.stream = torch.cuda.Stream(self.dev)
+        # size the stream's workspace for every shape before any graph capture
+        gq.gq_reserve_workspace(16, 11008, 11008, stream=self.stream)
 
     def smi_id(self):
         p = self.props

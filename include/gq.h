@@ -83,7 +83,8 @@ const char *gq_status_string(gq_status status); /* static text, never NULL */
 const char *gq_last_error_message(void);
 
 /* Sticky device-side status of the current device: GQ_ERR_TIMEOUT if a kernel
- * gave up a bounded wait since the last call, else GQ_OK; reading clears it.
+ * gave up a bounded wait since the last call, else GQ_OK; reading clears it and,
+ * after a timeout, re-zeroes the workspace counters of the device.
  * Synchronizes the current device first. */
 gq_status gq_last_error(void);
 
@@ -108,15 +109,13 @@ gq_status gq_quantize_q4_0(const float *w, void *q4_blocks, int64_t N, int64_t K
  * Repacked layout (a pure byte permutation plus padding): rows are grouped by
  * 16 (N16 = ceil(N/16) groups) and columns by 128 (NT = ceil(K/128) tiles of 4
  * blocks).  Tile (g, t) occupies the 1152 bytes at offset (g*NT + t)*1152:
- *   bytes [h*512 + L*16, +16), h in {0,1}, L in 0..31, r = L/4, c = L%4:
- *       four 4-byte words: nibble bytes 4c..4c+3 of (row 16g+r,   block 4t+2h),
- *       (row 16g+r+8, block 4t+2h), (row 16g+r, block 4t+2h+1),
- *       (row 16g+r+8, block 4t+2h+1);
- *   bytes [1024 + r*16, +16), r in 0..7: the fp16 scales of rows 16g+r and
- *       16g+r+8 for blocks 4t+0..3, ordered (r,0),(r+8,0),(r,1),(r+8,1),...
+ *   bytes [(j*16 + r)*16, +16), j in 0..3, r in 0..15: the 16 code bytes of
+ *       (row 16g+r, block 4t+j), in their canonical order;
+ *   bytes [1024 + (r*4 + j)*2, +2): the fp16 scale of (row 16g+r, block 4t+j).
  * Rows >= N and blocks >= K/32 are padding: nibble bytes 0x88 and scale +0.
- * (DeepSpeed-Inference notes, section III.C.3: rearrange the weights once at
- * initialisation so that each thread's loads fill whole cache lines.) */
+ * Each row group's tiles are contiguous, so a slice of K streams as one block
+ * of bytes (DeepSpeed-Inference notes, section III.C.3: rearrange the weights
+ * once at initialisation so that loads fill whole cache lines). */
 gq_status gq_repack_q4_0(const void *q4_blocks, void *q4_repacked, int64_t N, int64_t K,
                          cudaStream_t stream);
 
@@ -136,19 +135,28 @@ gq_status gq_quantize_rows_q8_0(const float *x, void *q8_blocks, int64_t M, int6
  * each output is sum_b fp16(d4_b) * fp16(d8_b) * sumi_b with the exact int32
  * block dots sumi_b, accumulated in f32 on the GEMV path (M <= threshold) and,
  * on the tensor-core path, from fp16-rounded de-quantized operands with f32
- * accumulation (relative error <= 2e-3 of sum |terms|).
- * The tensor-core path allocates a stream-ordered workspace (cudaMallocAsync on
- * `stream` from the device's default pool, freed on `stream` after use):
- * 2 * ceil(M/128)*128 * K bytes. */
+ * accumulation (relative error <= 2e-3 of sum |terms|).  Uses the stream's
+ * workspace (see gq_reserve_workspace); results do not depend on timing. */
 gq_status gq_mul_mat_q4_0_f32(const void *q4_repacked, const float *src1, float *dst,
                               int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /* dst[M][N] = src1[M][K] . src0[N][K]^T with F16 weights src0 (IEEE binary16,
  * row-major).  Activations are rounded to fp16 for the tensor instructions and
- * the sums are accumulated in f32 (relative error <= 2e-3 of sum |terms|).
- * Workspace as above on the tensor-core path. */
+ * the sums are accumulated in f32 (relative error <= 2e-3 of sum |terms|). */
 gq_status gq_mul_mat_f16_f32(const void *src0_f16, const float *src1, float *dst,
                              int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/* Workspace.  The products keep a small device workspace per (device, stream):
+ * partial sums of weight rows that several CTAs share, with per-row counters
+ * that every launch leaves at zero, and (tensor-core path) the quantized
+ * activations.  It is allocated with cudaMalloc the first time a stream needs it
+ * and grows when a larger problem comes; growth synchronizes that stream.  A
+ * call that would grow it while the stream is being captured into a CUDA graph
+ * returns GQ_ERR_NO_MEMORY: reserve it first with this call, on the stream that
+ * will be captured, for the largest M, N, K it will run.  Graphs captured on a
+ * stream use that stream's workspace: do not replay them concurrently with
+ * other work on that stream's workspace. */
+gq_status gq_reserve_workspace(int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /* The same two products with the kernel family chosen by the caller. */
 gq_status gq_mul_mat_q4_0_f32_path(const void *q4_repacked, const float *src1, float *dst,

@@ -62,6 +62,7 @@ SIGNATURES = {
     "gq_mul_mat_f16_f32": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_path": ([_P, _P, _P, _I, _I, _I, _S, _P], _S),
     "gq_mul_mat_f16_f32_path": ([_P, _P, _P, _I, _I, _I, _S, _P], _S),
+    "gq_reserve_workspace": ([_I, _I, _I, _P], _S),
     "gq_set_m_threshold": ([_I], _S),
     "gq_get_m_threshold": ([], _I),
     "gq_debug_block_dots_q4_0": ([_P, _P, _P, _I, _I, _I, _P], _S),
@@ -172,6 +173,10 @@ def gq_mul_mat_f16_f32_path(src0_f16, src1, dst, M: int, N: int, K: int, path: i
                             stream=None) -> None:
     _check(lib().gq_mul_mat_f16_f32_path(_ptr(src0_f16), _ptr(src1), _ptr(dst), M, N, K, path,
                                          _stream(stream)), "gq_mul_mat_f16_f32_path")
+
+
+def gq_reserve_workspace(M: int, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_reserve_workspace(M, N, K, _stream(stream)), "gq_reserve_workspace")
 
 
 def gq_set_m_threshold(t: int) -> None:

@@ -1,0 +1,573 @@
+// gemv_q4_0.cu -- the persistent Q4_0 x Q8_0 GEMV (up to 16 activation rows
+// per launch), the hot path of single-token and small-batch decode.
+//
+// In this regime every weight byte is read once and the product is bound by
+// HBM (Smallem, "Générer à plusieurs", introduction and "Où la courbe
+// s'aplatit": with B sequences each weight read serves B products; DeepSpeed-
+// Inference notes, III.A: small batches are limited by the bandwidth of reading
+// the weights).  One call is two launches on the caller's stream:
+//
+//  1. INIT (llama.cpp PR #1632, "Introduction": the q_f32 kind quantizes src1
+//     in its INIT stage; Arm China NUMA article, "MulMat 算子優化": src1 goes to
+//     the wdata buffer that every worker reads).  For M > 4 a small kernel
+//     quantizes the M activation rows to Q8_0 once and writes them to the
+//     workspace as "wdata images", one per K slice, already in the shared-memory
+//     layout the consumers read: codes, then per block the scale and -8 * sum of
+//     codes.  When M times the slice width is small (at most eight 16-byte loads
+//     per consumer thread) each CTA quantizes its own slice into shared memory
+//     instead (the article's per-node wdata copies, because quantizing is
+//     cheap), which saves a launch.
+//  2. COMPUTE, persistent, one CTA per SM.  K is cut into S slices (S depends
+//     on K and on how many activation rows share the launch); with one slice
+//     each CTA owns a run of whole row groups, balanced to within one row group,
+//     and with several slices the repacked tiles of each slice, in
+//     row-group-major order, are divided evenly between the CTAs of the slice
+//     (split-K for small grids: Smallem, "La courbe, une première fois"; output
+//     tiles plus input-dimension tiles: DeepSpeed-Inference notes, III.C.1).
+//       * Two producer warps stream the CTA's share through a ring of shared-
+//         memory chunks with bulk (TMA) copies.  Behind INIT they start at their
+//         first instruction: the launch is programmatic-dependent on INIT, and
+//         INIT waited for every earlier grid before letting this one start, so
+//         the weights are final.  Without INIT they first wait for the grids
+//         before.
+//       * Sixteen consumer warps wait for INIT, load their slice's wdata image
+//         into shared memory, then take one tile of every chunk each.  A lane
+//         owns whole block-rows (row r, blocks j and j+2 of the tile): each
+//         block dot is eight dp4a on the unpacked nibbles and
+//         the activation codes, exact in int32, and the f32 sum takes
+//         d4 * d8 * sumi block by block.  (The int8 tensor instructions run at a
+//         small fraction of the fp16 rate on this GPU; dp4a keeps the integer
+//         dots on the CUDA cores.)
+//       * At the end of each row group the consumer warps' partials are added in
+//         shared memory (DeepSpeed-Inference notes, III.C.2: make the partials of
+//         one output contiguous and reduce them in one pass).  A row group that
+//         one CTA owns is stored directly.  A row group shared with other CTAs
+//         goes to its slot in the workspace, and a fix-up warp bumps the row
+//         group's counter; the CTA that arrives last adds all partials in a
+//         fixed order and stores the result.  Shared row groups are
+//         processed first, so their fix-ups overlap the stream; no CTA ever
+//         waits for another and the result does not depend on timing.
+#include <algorithm>
+#include <atomic>
+
+#include "gq_common.cuh"
+#include "gq_internal.h"
+
+namespace gq {
+namespace {
+
+constexpr int CW = 16;                             // consumer warps
+constexpr int PRODUCERS = 2;                       // producer warps (bulk-copy issue rate is per warp)
+constexpr int PRODUCER_WARP = CW;                  // CW .. CW + PRODUCERS - 1
+constexpr int FIXUPS = 2;                          // fix-up warps (shared row groups in parallel)
+constexpr int FIXUP_WARP = CW + PRODUCERS;         // .. + FIXUPS - 1
+constexpr int THREADS = (CW + PRODUCERS + FIXUPS) * 32;
+constexpr int FUSED_LOADS = 8;                     // float4 loads per consumer thread when INIT is fused
+constexpr int CONSUMERS = CW * 32;
+constexpr int CHUNK_TILES = CW;                    // one tile per consumer warp
+constexpr int CHUNK_BYTES = CHUNK_TILES * TILE_BYTES;
+constexpr int MAX_SLOTS = 12;
+constexpr int PART_STRIDE = 16 * 16;               // floats of one partial (16 rows x 16 activation rows)
+constexpr size_t ACT_BUDGET = 112 * 1024;          // wdata image of one slice
+constexpr size_t SMEM_LIMIT = 227 * 1024;
+
+__host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// One slice's wdata image: the Q8_0 codes of M activation rows ([M][4*ntmax
+// blocks][32 bytes], element order) and per (row, block) the pair
+// (f32 scale fp16(d), int32 -8 * sum of the codes).
+struct Image {
+    size_t row_bytes, codes, scales, bytes;
+    __host__ __device__ Image(int M, int ntmax) {
+        row_bytes = (size_t)4 * ntmax * 32;
+        codes = 0;
+        scales = (size_t)M * row_bytes;
+        bytes = align_up(scales + (size_t)M * 4 * ntmax * 8, 16);
+    }
+};
+
+struct Params {
+    const uint8_t *w;        // repacked Q4_0
+    const float *x;          // [M][K]
+    float *dst;              // [M][N]
+    unsigned int *status;    // device status word
+    float *part;             // workspace partials [N16][S][2][PART_STRIDE]
+    unsigned int *cnt;       // workspace counters [N16], zero between launches
+    uint8_t *wdata;          // workspace wdata images [S][image bytes]
+    int M, N, K;
+    int nb, N16, NT;
+    int S, Gs;               // slices, CTAs per slice (grid = S * Gs)
+    int slots, ntmax, maxfix;
+    int fused;               // 1: no INIT launch, each CTA quantizes its slice of src1
+};
+
+struct Layout {
+    size_t bars, ring, act, red, total;
+    __host__ __device__ Layout(int MT, int M, int ntmax, int slots, int maxfix) {
+        const Image im(M, ntmax);
+        bars = 0;                                         // full[slots], empty[slots], act, fix[maxfix]
+        ring = align_up((size_t)(2 * slots + 1 + maxfix) * 8, 128);
+        act = ring + (size_t)slots * CHUNK_BYTES;
+        red = act + im.bytes;
+        total = red + (size_t)CW * 16 * MT * 4;
+    }
+};
+
+__host__ __device__ inline void slice_of(int NT, int S, int s, int &ts0, int &nts) {
+    ts0 = (int)((int64_t)NT * s / S);
+    nts = (int)((int64_t)NT * (s + 1) / S) - ts0;
+}
+
+// The CTAs of a slice own the consecutive ranges [T*i/Gs, T*(i+1)/Gs) of its T
+// tiles.  Index of the CTA whose range holds tile x.
+__host__ __device__ inline int owner(int T, int Gs, int x) {
+    const int i = (int)(((int64_t)(x + 1) * Gs + T - 1) / T) - 1;
+    return i < Gs - 1 ? i : Gs - 1;
+}
+
+// Number of CTAs of all slices that hold a part of row group g.
+__device__ inline unsigned int contributors(const Params &p, int g) {
+    unsigned int n = 0;
+    for (int s2 = 0; s2 < p.S; s2++) {
+        int t2, n2;
+        slice_of(p.NT, p.S, s2, t2, n2);
+        const int T2 = p.N16 * n2;
+        n += (unsigned)(owner(T2, p.Gs, (g + 1) * n2 - 1) - owner(T2, p.Gs, g * n2) + 1);
+    }
+    return n;
+}
+
+// The row-group segments of a CTA's range [a, b) of slice tiles, in the order
+// the CTA processes them: segments shared with another CTA first (all of them
+// when S > 1), then the CTA's own row groups in increasing order.
+struct Segments {
+    int a, b;
+    int nts, g0, n;          // first row group, number of segments
+    bool head, tail, all_shared;
+    int nshared;
+    __host__ __device__ Segments(int a_, int b_, int nts_, int S) : a(a_), b(b_), nts(nts_) {
+        g0 = (int)(a / nts);
+        n = (int)((b - 1) / nts) - g0 + 1;
+        head = (a % nts) != 0;
+        tail = (b % nts) != 0;
+        all_shared = S > 1;
+        nshared = all_shared ? n : (int)head + (int)(tail && !(head && n == 1));
+    }
+    // natural index (0 = first row group of the range) of the j-th processed segment
+    __host__ __device__ int natural(int j) const {
+        if (all_shared) return j;
+        int k = 0;
+        if (tail && !(head && n == 1)) {
+            if (j == k) return n - 1;
+            k++;
+        }
+        if (head) {
+            if (j == k) return 0;
+            k++;
+        }
+        return j - k + (head ? 1 : 0);   // the unshared row groups, ascending
+    }
+    __host__ __device__ void get(int j, int &g, int &u0, int &u1) const {
+        const int nat = natural(j);
+        g = g0 + nat;
+        const int lo = g * nts, hi = lo + nts;
+        u0 = (a > lo ? a : lo) - lo;
+        u1 = (b < hi ? b : hi) - lo;
+    }
+};
+
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Release of this thread's (and, through a preceding barrier, its CTA's or
+// warp's) earlier writes and acquire of the other arrivals' writes.
+__device__ __forceinline__ unsigned int atomic_add_acq_rel_gpu(unsigned int *p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// ---------------------------------------------------------------------------
+// INIT: Q8_0 of the activation rows into the wdata images.  One warp per
+// (row, block): lane j holds element j; the block goes to the image of the
+// slice that holds it.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
+    pdl_wait();                 // src1 and the workspace are final: every earlier grid has completed
+    pdl_launch_dependents();    // the GEMV may start streaming weights now
+    const Image im(p.M, p.ntmax);
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int nblk = 4 * p.NT;                   // blocks including the padding of the last tile
+    for (int64_t task = warp; task < (int64_t)p.M * nblk; task += nwarps) {
+        const int m = (int)(task / nblk), b = (int)(task % nblk);
+        const int t = b / 4;
+        int s = 0, ts0 = 0, nts = 0;
+        for (; s < p.S; s++) {
+            slice_of(p.NT, p.S, s, ts0, nts);
+            if (t < ts0 + nts) break;
+        }
+        const int bl = b - 4 * ts0;
+        const float v = b < p.nb ? p.x[(size_t)m * p.K + (size_t)b * QK + lane] : 0.0f;
+        const unsigned int amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
+        const float d = __uint_as_float(amax) / 127.0f;
+        const int q = q8_code(v, d);
+        const int qsum = __reduce_add_sync(0xffffffffu, q);
+        uint8_t *img = p.wdata + (size_t)s * im.bytes;
+        img[im.codes + (size_t)m * im.row_bytes + (size_t)bl * 32 + lane] = (uint8_t)(q & 0xff);
+        if (lane == 0)
+            reinterpret_cast<float2 *>(img + im.scales)[(size_t)m * 4 * p.ntmax + bl] =
+                make_float2(__half2float(__float2half_rn(d)), __int_as_float(-8 * qsum));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// COMPUTE
+// ---------------------------------------------------------------------------
+template <int MT>
+__global__ void __launch_bounds__(THREADS, 1) gemv_q4_0_kernel(const Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int s = blockIdx.x / p.Gs, ci = blockIdx.x % p.Gs;
+    int ts0, nts;
+    slice_of(p.NT, p.S, s, ts0, nts);
+    const int T = p.N16 * nts;   // tiles of the slice (< 2^31: N * K <= 2^40)
+    // S == 1: whole row groups per CTA (no shared row group); S > 1: equal tile ranges
+    const Segments seg = p.S == 1 ? Segments((int)((int64_t)p.N16 * ci / p.Gs) * nts,
+                                             (int)((int64_t)p.N16 * (ci + 1) / p.Gs) * nts, nts, 1)
+                                  : Segments((int)((int64_t)T * ci / p.Gs), (int)((int64_t)T * (ci + 1) / p.Gs), nts,
+                                             p.S);
+    const Layout L(MT, p.M, p.ntmax, p.slots, p.maxfix);
+    const Image im(p.M, p.ntmax);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + p.slots;
+    uint64_t *actbar = empty + p.slots;
+    uint64_t *fixbar = actbar + 1;
+    uint8_t *ring = smem + L.ring;
+    const int outs = 16 * MT;                        // outputs of a row group: t = m * 16 + row
+
+    // barriers in parallel: full[slots] (1 arrival), empty[slots] (CW), act (1), fix[maxfix] (1)
+    for (int i = threadIdx.x; i < 2 * p.slots + 1 + p.maxfix; i += THREADS)
+        mbar_init(smem_addr(full + i), (i >= p.slots && i < 2 * p.slots) ? CW : 1);
+    fence_barrier_init();
+    __syncthreads();
+    pdl_launch_dependents();
+
+    // ---------------------------------------------------------------- producers
+    // Producer warp pw issues the chunks k = pw (mod PRODUCERS); the ring has an
+    // even number of slots, so each producer refills only its own slots.
+    if (warp >= PRODUCER_WARP && warp < PRODUCER_WARP + PRODUCERS) {
+        const int pw = warp - PRODUCER_WARP;
+        if (p.fused) pdl_wait();   // without INIT in front, the weights may come from the grid before
+        if (lane == 0) {
+            int k = 0;
+            bool failed = false;
+            for (int j = 0; j < seg.n && !failed; j++) {
+                int g, u0, u1;
+                seg.get(j, g, u0, u1);
+                for (int u = u0; u < u1; u += CHUNK_TILES, k++) {
+                    if (k % PRODUCERS != pw) continue;
+                    const int slot = k % p.slots;
+                    if (k >= p.slots &&
+                        !mbar_wait(smem_addr(empty + slot), (uint32_t)(((k / p.slots) - 1) & 1), p.status)) {
+                        failed = true;
+                        break;
+                    }
+                    const uint32_t bytes = (uint32_t)(min(CHUNK_TILES, u1 - u) * TILE_BYTES);
+                    mbar_arrive_expect_tx(smem_addr(full + slot), bytes);
+                    bulk_g2s(smem_addr(ring + (size_t)slot * CHUNK_BYTES),
+                             p.w + ((size_t)g * p.NT + ts0 + u) * TILE_BYTES, bytes, smem_addr(full + slot));
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- fix-up
+    if (warp >= FIXUP_WARP) {
+        pdl_wait();
+        for (int f = warp - FIXUP_WARP; f < seg.nshared; f += FIXUPS) {
+            const bool ok = mbar_wait(smem_addr(fixbar + f), 0u, p.status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            int g, u0, u1;
+            seg.get(f, g, u0, u1);
+            unsigned int last = 0;
+            if (lane == 0)   // the consumers' partial is in the workspace: release it, count the arrival
+                last = (atomic_add_acq_rel_gpu(p.cnt + g, 1u) + 1 == contributors(p, g)) ? 1u : 0u;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {                                   // add every partial of row group g in a fixed order
+                for (int t = lane; t < outs; t += 32) {
+                    float sum = 0.0f;
+                    for (int s2 = 0; s2 < p.S; s2++) {
+                        int t2, n2;
+                        slice_of(p.NT, p.S, s2, t2, n2);
+                        const int T2 = p.N16 * n2;
+                        const int nc = owner(T2, p.Gs, (g + 1) * n2 - 1) - owner(T2, p.Gs, g * n2) + 1;
+                        const float *gp = p.part + ((size_t)g * p.S + s2) * 2 * PART_STRIDE + t;
+                        for (int q = 0; q < nc; q++) sum += __ldcg(gp + q * PART_STRIDE);
+                    }
+                    const int m = t / 16, n = 16 * g + t % 16;
+                    if (m < p.M && n < p.N) p.dst[(size_t)m * p.N + n] = sum;
+                }
+                if (lane == 0) atomicExch(p.cnt + g, 0u);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int tid = threadIdx.x;   // 0 .. CONSUMERS-1
+    const int n = lane & 15, jh = lane >> 4;   // this lane's row of the tile and first block (jh, jh + 2)
+    uint8_t *act = smem + L.act;
+    const float2 *act_sc = reinterpret_cast<const float2 *>(act + im.scales);
+    float *red = reinterpret_cast<float *>(smem + L.red);
+    const int nblkmax = 4 * p.ntmax;
+
+    pdl_wait();                                      // src1, or INIT's wdata, is complete
+    if (p.fused) {
+        // INIT in the CTA: Q8_0 of this slice's columns of the M activation rows.
+        // Every load is issued first (one round trip), then eight consecutive
+        // lanes hold the four-value groups of one block.
+        const int per_row = nts * 32;                  // float4 of one row's slice
+        const int nf4 = p.M * per_row;                 // a multiple of 32: whole warps are valid
+        float4 v[FUSED_LOADS];
+#pragma unroll
+        for (int i = 0; i < FUSED_LOADS; i++) {
+            const int f = tid + CONSUMERS * i, m = f / per_row, col = ts0 * TILE_COLS + (f % per_row) * 4;
+            v[i] = (f < nf4 && col < p.K) ? ldg_f4(p.x + (size_t)m * p.K + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < FUSED_LOADS; i++) {
+            const int f = tid + CONSUMERS * i;
+            if (f >= nf4) break;                       // warp-uniform
+            const int m = f / per_row, c4 = f % per_row, bl = c4 >> 3, e = c4 & 7;
+            float am = absmax4(v[i]);
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+            const float d = am / 127.0f;
+            const uint32_t word = pack_q8x4(v[i], d);
+            int qs = (int)(int8_t)(word & 0xff) + (int)(int8_t)((word >> 8) & 0xff) +
+                     (int)(int8_t)((word >> 16) & 0xff) + (int)(int8_t)(word >> 24);
+            qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+            qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+            qs += __shfl_xor_sync(0xffffffffu, qs, 4);
+            *reinterpret_cast<uint32_t *>(act + im.codes + (size_t)m * im.row_bytes + (size_t)bl * 32 + e * 4) = word;
+            if (e == 0)
+                reinterpret_cast<float2 *>(act + im.scales)[m * 4 * p.ntmax + bl] =
+                    make_float2(__half2float(__float2half_rn(d)), __int_as_float(-8 * qs));
+        }
+    } else {   // plain coalesced loads of the slice's wdata image (the bulk-copy queue carries the weights)
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.wdata + (size_t)s * im.bytes);
+        uint4 *dsts = reinterpret_cast<uint4 *>(act);
+        for (int i = tid; i < (int)(im.bytes / 16); i += CONSUMERS) dsts[i] = __ldcg(src + i);
+    }
+    consumers_sync();
+    bool failed = false;
+
+    float acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; m++) acc[m] = 0.0f;
+
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int j = 0; j < seg.n; j++) {
+        int g, u0, u1;
+        seg.get(j, g, u0, u1);
+        for (int u = u0; u < u1; u += CHUNK_TILES) {
+            if (!failed) {
+                const bool ok = mbar_wait(smem_addr(full + slot), phase, p.status);
+                failed = !__all_sync(0xffffffffu, ok);
+            }
+            if (!failed && warp < u1 - u) {
+                const int tl = u + warp;                       // tile index within the slice
+                const uint8_t *tile = ring + (size_t)slot * CHUNK_BYTES + warp * TILE_BYTES;
+                const uint2 d4w = *reinterpret_cast<const uint2 *>(tile + TILE_SCALE_OFFSET + n * 8);
+#pragma unroll
+                for (int jj = 0; jj < 2; jj++) {
+                    const int jb = jh + 2 * jj;                // block of the tile
+                    const Nibbles q = unpack_q4(lds128(tile + (jb * 16 + n) * 16));
+                    const uint32_t dw = jb & 2 ? d4w.y : d4w.x;
+                    const float d4 = (jb & 1) ? half_hi(dw) : half_lo(dw);
+                    const int blk = 4 * tl + jb;
+                    const uint8_t *a = act + im.codes + (size_t)blk * 32;
+#pragma unroll
+                    for (int m = 0; m < MT; m++) {
+                        if (m < p.M) {
+                            const uint4 a0 = lds128(a + m * im.row_bytes);
+                            const uint4 a1 = lds128(a + m * im.row_bytes + 16);
+                            const float2 sc = act_sc[m * nblkmax + blk];
+                            const int sumi = block_dot(q, a0, a1, __float_as_int(sc.y));
+                            acc[m] = fmaf(d4 * sc.x, (float)sumi, acc[m]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(empty + slot));   // this warp is done with the chunk
+            if (++slot == p.slots) {
+                slot = 0;
+                phase ^= 1u;
+            }
+        }
+
+        // ---- row group g of this slice is complete: add the consumer warps' partials
+#pragma unroll
+        for (int m = 0; m < MT; m++) {
+            const float other = __shfl_down_sync(0xffffffffu, acc[m], 16);   // blocks jh+1 of the same row
+            if (lane < 16) red[warp * outs + m * 16 + n] = acc[m] + other;
+            acc[m] = 0.0f;
+        }
+        consumers_sync();
+        if (tid < outs) {
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < CW; w++) v += red[w * outs + tid];
+            if (j < seg.nshared) {                     // this CTA's part of a shared row group
+                const int slot_i = ci == owner(T, p.Gs, g * nts) ? 0 : 1;
+                p.part[(((size_t)g * p.S + s) * 2 + slot_i) * PART_STRIDE + tid] = v;
+            } else {
+                const int m = tid / 16, row = 16 * g + tid % 16;
+                if (m < p.M && row < p.N) p.dst[(size_t)m * p.N + row] = v;
+            }
+        }
+        consumers_sync();                              // red is reused; the partial is written
+        if (j < seg.nshared && tid == 0) mbar_arrive(smem_addr(fixbar + j));
+    }
+}
+
+int slices_for(int NT, int MT) {
+    int S = 1;
+    while (S < 8 && 2 * S <= NT && Image(MT, (NT + S - 1) / S).bytes > ACT_BUDGET) S *= 2;
+    return S;
+}
+
+int env_int(const char *name, int dflt) {
+    const char *v = getenv(name);
+    return v && *v ? atoi(v) : dflt;
+}
+
+// The dynamic shared-memory limit is raised once per (device, kernel).
+constexpr int MAX_DEV = 64;
+std::atomic<bool> g_smem_set[MAX_DEV][5];
+
+template <typename Kernel>
+gq_status allow_smem(Kernel kernel, int which) {
+    int dev = 0;
+    gq_status st = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+    if (st != GQ_OK) return st;
+    if (dev >= 0 && dev < MAX_DEV && g_smem_set[dev][which].load(std::memory_order_acquire)) return GQ_OK;
+    st = check_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT),
+                    "gemv_q4_0 shared-memory attribute");
+    if (st == GQ_OK && dev >= 0 && dev < MAX_DEV) g_smem_set[dev][which].store(true, std::memory_order_release);
+    return st;
+}
+
+struct Plan {
+    int S, ntmax, Gs, maxfix;
+};
+
+Plan plan(int N16, int NT, int MT) {
+    Plan q;
+    q.S = slices_for(NT, MT);
+    q.ntmax = (NT + q.S - 1) / q.S;
+    q.Gs = std::max(1, std::min(sm_count() / q.S, N16));   // S == 1: every CTA gets >= 1 row group
+    // row groups a CTA touches: at most ceil(N16 / Gs) + 2 (one mbarrier each)
+    q.maxfix = q.S > 1 ? (N16 + q.Gs - 1) / q.Gs + 2 : 2;
+    return q;
+}
+
+}  // namespace
+
+void gemv_q4_0_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes) {
+    const int N16 = (int)((N + 15) / 16), NT = (int)((K + TILE_COLS - 1) / TILE_COLS);
+    size_t db = 0;
+    for (int MT = 1; MT <= 16; MT *= 2) {
+        const Plan q = plan(N16, NT, MT);
+        const size_t parts = (size_t)N16 * q.S * 2 * PART_STRIDE * sizeof(float);
+        const size_t images = (size_t)q.S * Image(MT, q.ntmax).bytes;
+        db = std::max(db, align_up(parts, 256) + images);
+    }
+    *counter_bytes = (size_t)N16 * sizeof(unsigned int);
+    *data_bytes = db;
+}
+
+gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t s) {
+    Params p{};
+    p.w = (const uint8_t *)rep;
+    p.status = device_status_word();
+    if (!p.status) return fail(GQ_ERR_CUDA, "device status word unavailable");
+    p.N = (int)N;
+    p.K = (int)K;
+    p.nb = (int)(K / QK);
+    p.N16 = (int)((N + 15) / 16);
+    p.NT = (int)((K + TILE_COLS - 1) / TILE_COLS);
+
+    size_t cb, db;
+    gemv_q4_0_workspace(N, K, &cb, &db);
+    Workspace ws;
+    gq_status st = get_workspace(s, cb, db, &ws);
+    if (st != GQ_OK) return st;
+    p.cnt = reinterpret_cast<unsigned int *>(ws.counters);
+
+    for (int64_t m0 = 0; m0 < M; m0 += 16) {
+        p.M = (int)std::min<int64_t>(16, M - m0);
+        p.x = x + m0 * K;
+        p.dst = dst + m0 * N;
+        const int MT = p.M <= 1 ? 1 : p.M <= 2 ? 2 : p.M <= 4 ? 4 : p.M <= 8 ? 8 : 16;
+        const Plan q = plan(p.N16, p.NT, MT);
+        p.S = q.S;
+        p.ntmax = q.ntmax;
+        p.Gs = q.Gs;
+        p.maxfix = q.maxfix;
+        // fuse INIT when each consumer thread loads at most FUSED_LOADS float4
+        p.fused = (int64_t)p.M * p.ntmax * 32 <= (int64_t)CONSUMERS * FUSED_LOADS ? 1 : 0;
+        p.part = reinterpret_cast<float *>(ws.data);
+        p.wdata = ws.data + align_up((size_t)p.N16 * p.S * 2 * PART_STRIDE * sizeof(float), 256);
+        const size_t fixed = Layout(MT, p.M, p.ntmax, 0, p.maxfix).total;
+        const size_t budget = SMEM_LIMIT - 1024;
+        p.slots = (int)std::min<size_t>(MAX_SLOTS, (budget - std::min(budget, fixed + 256)) / (CHUNK_BYTES + 16));
+        p.slots = std::min(p.slots, env_int("GQ_GEMV_SLOTS", MAX_SLOTS)) & ~(PRODUCERS - 1);
+        if (p.slots < 2)
+            return fail(GQ_ERR_INVALID_ARG, "gemv_q4_0: N=%lld K=%lld leaves no room for the weight ring",
+                        (long long)N, (long long)K);
+        const size_t smem = Layout(MT, p.M, p.ntmax, p.slots, p.maxfix).total;
+        const int which = MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : MT == 8 ? 3 : 4;
+        void (*const kernels[5])(Params) = {gemv_q4_0_kernel<1>, gemv_q4_0_kernel<2>, gemv_q4_0_kernel<4>,
+                                            gemv_q4_0_kernel<8>, gemv_q4_0_kernel<16>};
+        auto kernel = kernels[which];
+        st = allow_smem(kernel, which);
+        if (st != GQ_OK) return st;
+
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const int64_t warps = (int64_t)p.M * 4 * p.NT;
+        cfg.gridDim = dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>((warps + 7) / 8, 2LL * sm_count())), 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        if (!p.fused) {
+            st = check_cuda(cudaLaunchKernelEx(&cfg, wdata_kernel, p), "gemv_q4_0 INIT launch");
+            if (st != GQ_OK) return st;
+        }
+        cfg.gridDim = dim3((unsigned)(p.S * p.Gs), 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        st = check_cuda(cudaLaunchKernelEx(&cfg, kernel, p), "gemv_q4_0 launch");
+        if (st != GQ_OK) return st;
+    }
+    return GQ_OK;
+}
+
+}  // namespace gq

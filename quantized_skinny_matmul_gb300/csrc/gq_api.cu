@@ -21,6 +21,7 @@ thread_local char t_message[512];
 constexpr int MAX_DEVICES = 64;
 std::atomic<int> g_arch_ok[MAX_DEVICES];      // 0 unknown, 1 sm_103, -1 other
 std::atomic<int> g_sm_count[MAX_DEVICES];
+std::atomic<unsigned int *> g_status_ptr[MAX_DEVICES];
 std::atomic<int64_t> g_m_threshold{16};
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -107,6 +108,21 @@ int sm_count() {
     return n;
 }
 
+// Kernels receive this address as an argument: the symbol itself is a host-side
+// stand-in, so it is resolved once per device, with that device current.
+unsigned int *device_status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+    unsigned int *p = g_status_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_status_word) != cudaSuccess) return nullptr;
+        p = static_cast<unsigned int *>(a);
+        g_status_ptr[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
 }  // namespace gq
 
 using namespace gq;
@@ -136,7 +152,10 @@ gq_status gq_last_error(void) {
     unsigned int word = 0, zero = 0;
     GQ_TRY(check_cuda(cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)), "read device status"));
     GQ_TRY(check_cuda(cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)), "clear device status"));
-    if (word & STATUS_TIMEOUT) return fail(GQ_ERR_TIMEOUT, "a kernel gave up a bounded wait");
+    if (word & STATUS_TIMEOUT) {
+        reset_workspace_counters();
+        return fail(GQ_ERR_TIMEOUT, "a kernel gave up a bounded wait");
+    }
     return ok();
 }
 
@@ -182,6 +201,16 @@ gq_status gq_repack_q4_0(const void *q4_blocks, void *q4_repacked, int64_t N, in
         return fail(GQ_ERR_INVALID_ARG, "q4_blocks and q4_repacked overlap");
     GQ_TRY(check_device());
     GQ_TRY(launch_repack_q4_0(q4_blocks, q4_repacked, N, K, stream));
+    return ok();
+}
+
+gq_status gq_reserve_workspace(int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(M, N, K));
+    GQ_TRY(check_device());
+    size_t cb = 0, db = 0;
+    gemv_q4_0_workspace(N, K, &cb, &db);
+    Workspace ws;
+    GQ_TRY(get_workspace(stream, cb, db, &ws));
     return ok();
 }
 

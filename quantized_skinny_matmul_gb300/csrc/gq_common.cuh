@@ -75,22 +75,42 @@ __device__ __forceinline__ float absmax4(float4 v) {
 }
 
 // ---------------------------------------------------------------------------
-// Nibble unpacking for the int8 tensor instruction.  A word holds the codes of
-// four consecutive bytes; the low nibbles are elements 4c..4c+3 of a block and
-// the high nibbles elements 16+4c..16+4c+3.  Each code q in 0..15 becomes the
-// int8 16*(q-8) = (q ^ 8) << 4, so the product is 16 * sumi exactly.
+// The integer block dot of the q_f32 kind with dp4a.  A Q4_0 block's 16 code
+// bytes hold q_i in the low nibble and q_{i+16} in the high nibble of byte i,
+// so masking the four words gives the codes of elements 0..15 (lo) and 16..31
+// (hi) as bytes in element order, each in 0..15.  With the activation codes
+// a[0..31] (int8, element order) and corr = -8 * sum(a):
+//     sum_j (q_j - 8) * a_j = corr + sum_j q_j * a_j        (exact in int32)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t nib_lo_x16(uint32_t w) { return ((w << 4) & 0xF0F0F0F0u) ^ 0x80808080u; }
-__device__ __forceinline__ uint32_t nib_hi_x16(uint32_t w) { return (w & 0xF0F0F0F0u) ^ 0x80808080u; }
+struct Nibbles {
+    uint32_t lo[4], hi[4];
+};
 
-// D(16x8, s32) = A(16x32, s8, row) . B(32x8, s8, col)
-__device__ __forceinline__ void mma_s8_16x8x32(int32_t (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%10, %11, %12, %13};"
-        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0), "r"(0), "r"(0), "r"(0));
+__device__ __forceinline__ Nibbles unpack_q4(uint4 w) {
+    Nibbles n;
+    n.lo[0] = w.x & 0x0F0F0F0Fu;
+    n.lo[1] = w.y & 0x0F0F0F0Fu;
+    n.lo[2] = w.z & 0x0F0F0F0Fu;
+    n.lo[3] = w.w & 0x0F0F0F0Fu;
+    n.hi[0] = (w.x >> 4) & 0x0F0F0F0Fu;
+    n.hi[1] = (w.y >> 4) & 0x0F0F0F0Fu;
+    n.hi[2] = (w.z >> 4) & 0x0F0F0F0Fu;
+    n.hi[3] = (w.w >> 4) & 0x0F0F0F0Fu;
+    return n;
+}
+
+// a0: activation codes 0..15, a1: codes 16..31 (four per word, element order)
+__device__ __forceinline__ int block_dot(const Nibbles &q, uint4 a0, uint4 a1, int corr) {
+    int s = corr;
+    s = __dp4a((int)q.lo[0], (int)a0.x, s);
+    s = __dp4a((int)q.lo[1], (int)a0.y, s);
+    s = __dp4a((int)q.lo[2], (int)a0.z, s);
+    s = __dp4a((int)q.lo[3], (int)a0.w, s);
+    s = __dp4a((int)q.hi[0], (int)a1.x, s);
+    s = __dp4a((int)q.hi[1], (int)a1.y, s);
+    s = __dp4a((int)q.hi[2], (int)a1.z, s);
+    s = __dp4a((int)q.hi[3], (int)a1.w, s);
+    return s;
 }
 
 // D(16x8, f32) += A(16x16, f16, row) . B(16x8, f16, col)
@@ -132,5 +152,56 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
+
+// ---------------------------------------------------------------------------
+// mbarriers and bulk (TMA) copies global -> shared.
+// ---------------------------------------------------------------------------
+constexpr uint32_t WAIT_LIMIT = 1u << 22;   // try_wait polls before a wait gives up
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the asynchronous (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory accesses before later
+// asynchronous-proxy writes (a refill of a buffer that was just read).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// 1-D bulk copy; dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity; gives up after WAIT_LIMIT polls,
+// records the timeout in the device status word and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int *status) {
+    for (uint32_t i = 0; i < WAIT_LIMIT; i++)
+        if (mbar_try_wait(bar, parity)) return true;
+    flag_timeout(status);
+    return false;
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
 }  // namespace gq

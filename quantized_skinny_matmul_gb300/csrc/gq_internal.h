@@ -15,6 +15,16 @@ gq_status check_cuda(cudaError_t e, const char *what);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+// Device address of the current device's sticky status word (nullptr on error).
+unsigned int *device_status_word();
+
+// Per-(device, stream) workspace: a zeroed counter region and a data region.
+struct Workspace {
+    uint8_t *counters;
+    uint8_t *data;
+};
+gq_status get_workspace(cudaStream_t s, size_t counter_bytes, size_t data_bytes, Workspace *out);
+gq_status reset_workspace_counters();
 
 // Launchers (arguments already validated by the entry points).
 gq_status launch_quantize_q4_0(const float *w, void *q4, int64_t N, int64_t K, cudaStream_t s);
@@ -23,6 +33,8 @@ gq_status launch_repack_q4_0(const void *q4, void *rep, int64_t N, int64_t K, cu
 
 gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N,
                            int64_t K, cudaStream_t s);
+// Workspace bytes (counters, data) the Q4_0 GEMV needs for an [N][K] weight.
+void gemv_q4_0_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes);
 gq_status launch_gemv_f16(const void *w16, const float *x, float *dst, int64_t M, int64_t N,
                           int64_t K, cudaStream_t s);
 gq_status launch_block_dots_q4_0(const void *rep, const void *q8, int32_t *sumi, int64_t M,

@@ -56,48 +56,42 @@ __global__ void quantize_rows_q8_0_kernel(const float *__restrict__ x, uint8_t *
     }
 }
 
-__device__ __forceinline__ uint32_t load_u32_bytes(const uint8_t *p) {
-    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
-}
-
-// Load-time repack into the tiled layout documented with gq_repack_q4_0
-// (DeepSpeed-Inference notes, III.C.3: weights rearranged once at
-// initialisation so that every load fills whole cache lines).  One thread per
-// (tile, lane): two 16-byte code words, and lanes 0..7 also the tile's scales.
+// Load-time repack into the tiled layout documented with gq_repack_q4_0.  One
+// thread per 16-byte piece of a tile: 64 pieces of codes (one block-row each)
+// and 8 pieces of scales.
 __global__ void repack_q4_0_kernel(const uint8_t *__restrict__ q4, uint8_t *__restrict__ rep,
                                    int64_t N, int64_t nb, int64_t NT, int64_t ntiles) {
     pdl_wait();
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t tile = tid >> 5;
+    const int64_t tile = tid / 72;
     if (tile >= ntiles) return;
-    const int L = (int)(tid & 31);
+    const int piece = (int)(tid % 72);
     const int64_t g = tile / NT, t = tile % NT;
-    const int r = L >> 2, c = L & 3;
     uint8_t *dst = rep + tile * TILE_BYTES;
-
-    auto code_word = [&](int64_t n, int64_t b) -> uint32_t {
-        if (n >= N || b >= nb) return 0x88888888u;
-        return load_u32_bytes(q4 + (n * nb + b) * Q4_0_BYTES + 2 + 4 * c);
-    };
-    for (int h = 0; h < 2; h++) {
-        const int64_t b0 = 4 * t + 2 * h;
-        uint4 v;
-        v.x = code_word(16 * g + r, b0);
-        v.y = code_word(16 * g + r + 8, b0);
-        v.z = code_word(16 * g + r, b0 + 1);
-        v.w = code_word(16 * g + r + 8, b0 + 1);
-        *reinterpret_cast<uint4 *>(dst + h * 512 + L * 16) = v;
-    }
-    if (L < 8) {
-        auto scale = [&](int64_t n, int64_t b) -> uint32_t {
-            if (n >= N || b >= nb) return 0u;
-            const uint8_t *p = q4 + (n * nb + b) * Q4_0_BYTES;
-            return (uint32_t)p[0] | ((uint32_t)p[1] << 8);
-        };
-        uint32_t s[4];
-        for (int j = 0; j < 4; j++)
-            s[j] = scale(16 * g + L, 4 * t + j) | (scale(16 * g + L + 8, 4 * t + j) << 16);
-        *reinterpret_cast<uint4 *>(dst + TILE_SCALE_OFFSET + L * 16) = make_uint4(s[0], s[1], s[2], s[3]);
+    if (piece < 64) {
+        const int j = piece / 16, r = piece % 16;
+        const int64_t n = 16 * g + r, b = 4 * t + j;
+        uint32_t wv[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};
+        if (n < N && b < nb) {
+            const uint16_t *src = reinterpret_cast<const uint16_t *>(q4 + (n * nb + b) * Q4_0_BYTES + 2);
+            for (int k = 0; k < 4; k++) wv[k] = (uint32_t)src[2 * k] | ((uint32_t)src[2 * k + 1] << 16);
+        }
+        *reinterpret_cast<uint4 *>(dst + piece * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    } else {
+        const int q = piece - 64;                 // scales 8q .. 8q+7, index r*4 + j
+        uint32_t hv[4];
+        for (int k = 0; k < 4; k++) {
+            uint32_t two = 0;
+            for (int e = 0; e < 2; e++) {
+                const int idx = 8 * q + 2 * k + e, r = idx / 4, j = idx % 4;
+                const int64_t n = 16 * g + r, b = 4 * t + j;
+                const uint32_t h = (n < N && b < nb) ? *reinterpret_cast<const uint16_t *>(q4 + (n * nb + b) * Q4_0_BYTES)
+                                                     : 0u;
+                two |= h << (16 * e);
+            }
+            hv[k] = two;
+        }
+        *reinterpret_cast<uint4 *>(dst + TILE_SCALE_OFFSET + q * 16) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
     }
 }
 
@@ -126,7 +120,7 @@ gq_status launch_repack_q4_0(const void *q4, void *rep, int64_t N, int64_t K, cu
     const int64_t nb = K / QK;
     const int64_t N16 = (N + 15) / 16, NT = (K + TILE_COLS - 1) / TILE_COLS;
     const int64_t ntiles = N16 * NT;
-    const int64_t threads = ntiles * 32;
+    const int64_t threads = ntiles * 72;
     const int64_t blocks = (threads + 255) / 256;
     repack_q4_0_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint8_t *)q4, (uint8_t *)rep, N, nb, NT, ntiles);
     return check_cuda(cudaGetLastError(), "repack_q4_0 launch");
