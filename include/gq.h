@@ -173,6 +173,23 @@ gq_status gq_mul_mat_f16_f32_path(const void *src0_f16, const float *src1, float
 gq_status gq_set_m_threshold(int64_t t);
 int64_t gq_get_m_threshold(void);
 
+/* The Q4_0 product of gq_mul_mat_q4_0_f32, for callers that cannot allocate
+ * device memory: code recording into a CUDA graph while the stream is captured
+ * (allocation is refused during global-mode capture) and applications whose
+ * device memory belongs to a pooling allocator that must see every byte.
+ * (The pages have no counterpart: this is an interface of this library.)
+ * All scratch space comes from one static device array of 4 MiB that every
+ * device loading the library holds until the process exits; nothing is ever
+ * allocated or freed.  It always runs the GEMV family (any M, 16 rows per
+ * launch).  GQ_ERR_INVALID_ARG when [N][K] needs more scratch than 4 MiB (for
+ * example N = 11008 with K up to 11008 fits).  The first call on a device
+ * resolves the array's device address (cudaGetSymbolAddress): make it before
+ * any stream capture.  Each call re-zeroes the array's counters on `stream`
+ * (cudaMemsetAsync) and then uses the whole array: calls that overlap on the
+ * GPU, from any streams, race on it and give wrong results. */
+gq_status gq_mul_mat_q4_0_f32_noalloc(const void *q4_repacked, const float *src1, float *dst,
+                                      int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* ---- verification --------------------------------------------------------------- */
 
 /* The integer block dots of the GEMV instruction sequence, for parity tests:

@@ -66,6 +66,7 @@ SIGNATURES = {
     "gq_set_m_threshold": ([_I], _S),
     "gq_get_m_threshold": ([], _I),
     "gq_debug_block_dots_q4_0": ([_P, _P, _P, _I, _I, _I, _P], _S),
+    "gq_mul_mat_q4_0_f32_noalloc": ([_P, _P, _P, _I, _I, _I, _P], _S),
 }
 
 
@@ -185,6 +186,12 @@ def gq_set_m_threshold(t: int) -> None:
 
 def gq_get_m_threshold() -> int:
     return lib().gq_get_m_threshold()
+
+
+def gq_mul_mat_q4_0_f32_noalloc(q4_repacked, src1, dst, M: int, N: int, K: int, stream=None) -> None:
+    """The Q4_0 product with no device allocation (static scratch in the library)."""
+    _check(lib().gq_mul_mat_q4_0_f32_noalloc(_ptr(q4_repacked), _ptr(src1), _ptr(dst), M, N, K,
+                                             _stream(stream)), "gq_mul_mat_q4_0_f32_noalloc")
 
 
 def gq_debug_block_dots_q4_0(q4_repacked, q8_blocks, sumi, M: int, N: int, K: int, stream=None) -> None:

@@ -498,8 +498,8 @@ void gemv_q4_0_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *da
     *data_bytes = db;
 }
 
-gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
-                           cudaStream_t s) {
+gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                                const Workspace &ws, cudaStream_t s) {
     Params p{};
     p.w = (const uint8_t *)rep;
     p.status = device_status_word();
@@ -510,11 +510,7 @@ gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t 
     p.N16 = (int)((N + 15) / 16);
     p.NT = (int)((K + TILE_COLS - 1) / TILE_COLS);
 
-    size_t cb, db;
-    gemv_q4_0_workspace(N, K, &cb, &db);
-    Workspace ws;
-    gq_status st = get_workspace(s, cb, db, &ws);
-    if (st != GQ_OK) return st;
+    gq_status st = GQ_OK;
     p.cnt = reinterpret_cast<unsigned int *>(ws.counters);
 
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
@@ -568,6 +564,16 @@ gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t 
         if (st != GQ_OK) return st;
     }
     return GQ_OK;
+}
+
+gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t s) {
+    size_t cb, db;
+    gemv_q4_0_workspace(N, K, &cb, &db);
+    Workspace ws;
+    gq_status st = get_workspace(s, cb, db, &ws);
+    if (st != GQ_OK) return st;
+    return launch_gemv_q4_0_with(rep, x, dst, M, N, K, ws, s);
 }
 
 }  // namespace gq

@@ -33,6 +33,14 @@ gq_status current_device(int *dev) {
     return GQ_OK;
 }
 
+#define GQ_TRY(expr)                       \
+    do {                                   \
+        gq_status _st = (expr);            \
+        if (_st != GQ_OK) return _st;      \
+    } while (0)
+
+}  // namespace
+
 // The kernels are built for sm_103a only: refuse other devices up front.
 gq_status check_device() {
     int dev;
@@ -75,14 +83,6 @@ gq_status ok() {
     t_message[0] = '\0';
     return GQ_OK;
 }
-
-#define GQ_TRY(expr)                       \
-    do {                                   \
-        gq_status _st = (expr);            \
-        if (_st != GQ_OK) return _st;      \
-    } while (0)
-
-}  // namespace
 
 gq_status fail(gq_status s, const char *fmt, ...) {
     va_list ap;

@@ -10,6 +10,13 @@ namespace gq {
 
 // Records the message returned by gq_last_error_message() for this thread.
 gq_status fail(gq_status s, const char *fmt, ...);
+// Clears that message and returns GQ_OK.
+gq_status ok();
+// Argument checks shared by the entry points (they never touch the GPU).
+gq_status check_sizes(int64_t M, int64_t N, int64_t K);
+gq_status check_ptr(const void *p, const char *name);
+// GQ_ERR_UNSUPPORTED_DEVICE unless the current device is sm_103.
+gq_status check_device();
 // Maps a CUDA error to GQ_ERR_CUDA (with its text), cudaSuccess to GQ_OK.
 gq_status check_cuda(cudaError_t e, const char *what);
 
@@ -35,6 +42,9 @@ gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t 
                            int64_t K, cudaStream_t s);
 // Workspace bytes (counters, data) the Q4_0 GEMV needs for an [N][K] weight.
 void gemv_q4_0_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes);
+// The Q4_0 GEMV on a given workspace (counters zero on entry, left at zero).
+gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                                const Workspace &ws, cudaStream_t s);
 gq_status launch_gemv_f16(const void *w16, const float *x, float *dst, int64_t M, int64_t N,
                           int64_t K, cudaStream_t s);
 gq_status launch_block_dots_q4_0(const void *rep, const void *q8, int32_t *sumi, int64_t M,
