@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "gq_common.cuh"
@@ -209,6 +210,7 @@ gq_status gq_reserve_workspace(int64_t M, int64_t N, int64_t K, cudaStream_t str
     GQ_TRY(check_device());
     size_t cb = 0, db = 0;
     gemv_q4_0_workspace(N, K, &cb, &db);
+    if (M > gq_get_m_threshold()) db = std::max(db, tc_workspace_bytes(M, K));
     Workspace ws;
     GQ_TRY(get_workspace(stream, cb, db, &ws));
     return ok();
@@ -244,11 +246,10 @@ gq_status gq_mul_mat_q4_0_f32_path(const void *q4_repacked, const float *src1, f
     GQ_TRY(check_ptr(src1, "src1"));
     GQ_TRY(check_ptr(dst, "dst"));
     GQ_TRY(check_device());
-    switch (resolve(path, M)) {
-        case GQ_PATH_TC:   // the tensor-core tile family is not built yet: GEMV slices
-        case GQ_PATH_GEMV:
-        default: GQ_TRY(launch_gemv_q4_0(q4_repacked, src1, dst, M, N, K, stream)); break;
-    }
+    if (resolve(path, M) == GQ_PATH_TC)
+        GQ_TRY(launch_tc_q4_0(q4_repacked, src1, dst, M, N, K, stream));
+    else
+        GQ_TRY(launch_gemv_q4_0(q4_repacked, src1, dst, M, N, K, stream));
     return ok();
 }
 
@@ -260,11 +261,10 @@ gq_status gq_mul_mat_f16_f32_path(const void *src0_f16, const float *src1, float
     GQ_TRY(check_ptr(src1, "src1"));
     GQ_TRY(check_ptr(dst, "dst"));
     GQ_TRY(check_device());
-    switch (resolve(path, M)) {
-        case GQ_PATH_TC:
-        case GQ_PATH_GEMV:
-        default: GQ_TRY(launch_gemv_f16(src0_f16, src1, dst, M, N, K, stream)); break;
-    }
+    if (resolve(path, M) == GQ_PATH_TC)
+        GQ_TRY(launch_tc_f16(src0_f16, src1, dst, M, N, K, stream));
+    else
+        GQ_TRY(launch_gemv_f16(src0_f16, src1, dst, M, N, K, stream));
     return ok();
 }
 

@@ -47,6 +47,12 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
                                 const Workspace &ws, cudaStream_t s);
 gq_status launch_gemv_f16(const void *w16, const float *x, float *dst, int64_t M, int64_t N,
                           int64_t K, cudaStream_t s);
+// Tensor-core tiles (tcgen05) for M >= 32; workspace: the fp16 activations.
+size_t tc_workspace_bytes(int64_t M, int64_t K);
+gq_status launch_tc_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                         cudaStream_t s);
+gq_status launch_tc_f16(const void *w16, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t s);
 gq_status launch_block_dots_q4_0(const void *rep, const void *q8, int32_t *sumi, int64_t M,
                                  int64_t N, int64_t K, cudaStream_t s);
 

@@ -1,0 +1,507 @@
+// tc_gemm.cu -- the tensor-core tile kernels for M >= 32 activation rows, where
+// the product is a dense contraction (Smallem, "Générer à plusieurs", "Où la
+// courbe s'aplatit": past B ~ the ridge point the card computes instead of
+// waiting on memory; llama.cpp PR #1632, "Introduction": de-quantization time
+// is significant up to M ~ 128, so it is fused into the tile pipeline here
+// instead of being a separate pass; Smallem, "La courbe, une première fois":
+// converting operands to bf16 cost more than the tensor cores saved there,
+// which is why the conversion happens in shared memory on the way in).
+//
+// One CTA computes a 128 (weight rows) x BN (activation rows) tile of
+// dst^T = W . X^T over all of K with tcgen05.mma kind::f16 and an f32
+// accumulator in tensor memory:
+//   warp 0      producer: bulk copies of the repacked Q4_0 tiles (or TMA loads
+//               of the F16 weights) and TMA loads of the fp16 activations;
+//   warp 1      allocates tensor memory; one thread issues the MMAs and commits
+//               them to mbarriers;
+//   warps 2..5  (Q4_0) de-quantize each 128 x 128 weight tile into fp16,
+//               (q - 8) * d rounded once, in the 128-byte-swizzled K-major
+//               layout the MMA reads; then all four read the accumulator back
+//               (tcgen05.ld) and store dst.
+// The activations are quantized first by a small kernel into a workspace copy
+// B[m][k] = fp16(q8 * d8) (Q4_0), or rounded to fp16 (F16): the same Q8_0
+// values as the GEMV path, each rounded once to fp16, so the result is within
+// 2e-3 of sum |terms| of the exact block-dot result.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "gq_common.cuh"
+#include "gq_internal.h"
+
+namespace gq {
+namespace {
+
+constexpr int BM = 128;                          // weight rows per CTA = MMA M = TMEM lanes
+constexpr int BK = 128;                          // K per pipeline stage (one repacked tile column)
+constexpr int ATOM_BYTES = BM * 128;             // one 128-row x 64-half swizzle atom: 16 KB
+constexpr int A_STAGE = BM * BK * 2;             // 32 KB
+constexpr int RAW_STAGE = 8 * TILE_BYTES;        // 8 row groups of 16 rows x one tile
+constexpr int STAGES = 2;
+constexpr int RAW_STAGES = 4;
+constexpr int THREADS = 192;
+constexpr int CONVERTERS = 128;
+
+template <int BN>
+struct TcLayout {
+    static constexpr int B_STAGE = BN * BK * 2;
+    static constexpr int a = 0;
+    static constexpr int b = a + STAGES * A_STAGE;
+    static constexpr int raw = b + STAGES * B_STAGE;
+    static constexpr int bars = raw + RAW_STAGES * RAW_STAGE;
+    static constexpr int total = bars + 256;     // from a 1024-aligned base
+};
+
+struct TcParams {
+    const uint8_t *w;        // Q4_0: repacked weights
+    float *dst;
+    unsigned int *status;
+    int M, N, K;
+    int NT, N16;             // tiles of 128 columns, row groups of 16
+};
+
+// barrier indices
+enum : int {
+    RAW_FULL = 0,
+    RAW_EMPTY = RAW_FULL + RAW_STAGES,
+    B_FULL = RAW_EMPTY + RAW_STAGES,
+    A_FULL = B_FULL + STAGES,
+    AB_EMPTY = A_FULL + STAGES,
+    ACC_FULL = AB_EMPTY + STAGES,
+    NUM_BARS = ACC_FULL + 1
+};
+
+// ---------------------------------------------------------------------------
+// tcgen05 / TMA wrappers
+// ---------------------------------------------------------------------------
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+    d |= (uint64_t)1 << 16;                             // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;                   // stride byte offset
+    d |= (uint64_t)1 << 46;                             // version
+    d |= (uint64_t)2 << 61;                             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16: f16 A and B, f32 D, both K-major.
+__host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_plain(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive f32 columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// Waits on a barrier phase unless an earlier wait of this thread gave up.
+__device__ __forceinline__ void wait_or_fail(uint32_t bar, uint32_t parity, bool &failed, unsigned int *status) {
+    if (!failed && !mbar_wait(bar, parity, status)) failed = true;
+}
+
+// Eight Q4_0 codes of bytes [b0..b3] of a word -> two half2 of (q - 8) * d.
+__device__ __forceinline__ uint4 dequant8(uint32_t lo_word, uint32_t hi_word, bool high_nibbles, __half2 d2) {
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+    uint32_t out[4];
+    const uint32_t words[2] = {lo_word, hi_word};
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            uint32_t t = __byte_perm(words[i], 0u, h ? 0x4342u : 0x4140u);   // bytes (2h, 2h+1) -> halves
+            if (high_nibbles) t >>= 4;
+            t = (t & 0x000F000Fu) | 0x64006400u;                             // 1024 + q
+            __half2 v = *reinterpret_cast<__half2 *>(&t);
+            v = __hmul2(__hsub2(v, bias), d2);                               // (q - 8) * d, rounded once
+            out[2 * i + h] = *reinterpret_cast<uint32_t *>(&v);
+        }
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int BN, bool QUANT>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_a,
+                   const TcParams p) {
+    using L = TcLayout<BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * BN, n0 = blockIdx.y * BM;
+    const int NT = p.NT;
+    auto bar = [&](int i) { return smem_addr(bars + i); };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RAW_STAGES; i++) {
+            mbar_init(bar(RAW_FULL + i), 1);
+            mbar_init(bar(RAW_EMPTY + i), CONVERTERS / 32);
+        }
+        for (int i = 0; i < STAGES; i++) {
+            mbar_init(bar(B_FULL + i), 1);
+            mbar_init(bar(A_FULL + i), QUANT ? CONVERTERS / 32 : 1);
+            mbar_init(bar(AB_EMPTY + i), 1);
+        }
+        mbar_init(bar(ACC_FULL), 1);
+    }
+    fence_barrier_init();
+    if (warp == 1) {   // tensor memory: BN f32 columns x 128 lanes
+        constexpr uint32_t cols = BN < 32 ? 32 : BN;
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    pdl_wait();   // weights, activations and dst follow every earlier grid in the stream
+    bool failed = false;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            for (int kt = 0; kt < NT && !failed; kt++) {
+                if (QUANT) {
+                    const int rs = kt % RAW_STAGES;
+                    if (kt >= RAW_STAGES) wait_or_fail(bar(RAW_EMPTY + rs), (uint32_t)((kt / RAW_STAGES - 1) & 1),
+                                                       failed, p.status);
+                    if (failed) break;
+                    const int g0 = n0 / 16;
+                    const int ng = min(8, p.N16 - g0);
+                    mbar_arrive_expect_tx(bar(RAW_FULL + rs), (uint32_t)(ng * TILE_BYTES));
+                    for (int gi = 0; gi < ng; gi++)
+                        bulk_g2s(smem_addr(smem + L::raw + rs * RAW_STAGE + gi * TILE_BYTES),
+                                 p.w + ((size_t)(g0 + gi) * NT + kt) * TILE_BYTES, TILE_BYTES, bar(RAW_FULL + rs));
+                }
+                const int s = kt % STAGES;
+                if (kt >= STAGES)
+                    wait_or_fail(bar(AB_EMPTY + s), (uint32_t)((kt / STAGES - 1) & 1), failed, p.status);
+                if (failed) break;
+                mbar_arrive_expect_tx(bar(B_FULL + s), (uint32_t)L::B_STAGE);
+                tma_load_2d(smem_addr(smem + L::b + s * L::B_STAGE), &map_b, kt * BK, m0, bar(B_FULL + s));
+                tma_load_2d(smem_addr(smem + L::b + s * L::B_STAGE + BN * 128), &map_b, kt * BK + 64, m0,
+                            bar(B_FULL + s));
+                if (!QUANT) {
+                    mbar_arrive_expect_tx(bar(A_FULL + s), (uint32_t)A_STAGE);
+                    tma_load_2d(smem_addr(smem + L::a + s * A_STAGE), &map_a, kt * BK, n0, bar(A_FULL + s));
+                    tma_load_2d(smem_addr(smem + L::a + s * A_STAGE + ATOM_BYTES), &map_a, kt * BK + 64, n0,
+                                bar(A_FULL + s));
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = f16_idesc(BM, BN);
+            for (int kt = 0; kt < NT && !failed; kt++) {
+                const int s = kt % STAGES;
+                const uint32_t par = (uint32_t)((kt / STAGES) & 1);
+                wait_or_fail(bar(A_FULL + s), par, failed, p.status);
+                wait_or_fail(bar(B_FULL + s), par, failed, p.status);
+                if (failed) break;
+                tc_fence_after();
+                const uint32_t a_base = smem_addr(smem + L::a + s * A_STAGE);
+                const uint32_t b_base = smem_addr(smem + L::b + s * L::B_STAGE);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; kk++) {
+                    const uint32_t koff = (uint32_t)((kk & 3) * 32);
+                    const uint64_t ad = sw128_desc(a_base + (kk >> 2) * ATOM_BYTES + koff);
+                    const uint64_t bd = sw128_desc(b_base + (kk >> 2) * (BN * 128) + koff);
+                    mma_f16(tmem, ad, bd, idesc, (kt | kk) != 0 ? 1u : 0u);
+                }
+                mma_commit(bar(AB_EMPTY + s));   // stage s may be refilled once these MMAs completed
+            }
+            if (!failed) mma_commit(bar(ACC_FULL));
+        }
+    } else {
+        // ---------------------------------------------------------- converters, then epilogue
+        const int t = threadIdx.x - 64;            // weight row of the tile, 0..127
+        if (QUANT) {
+            const int gi = t >> 4, rr = t & 15;
+            const bool row_ok = n0 + t < p.N;
+            for (int kt = 0; kt < NT; kt++) {
+                const int rs = kt % RAW_STAGES, s = kt % STAGES;
+                wait_or_fail(bar(RAW_FULL + rs), (uint32_t)((kt / RAW_STAGES) & 1), failed, p.status);
+                if (kt >= STAGES) wait_or_fail(bar(AB_EMPTY + s), (uint32_t)((kt / STAGES - 1) & 1), failed, p.status);
+                if (!failed) {
+                    const uint8_t *tile = smem + L::raw + rs * RAW_STAGE + gi * TILE_BYTES;
+                    uint8_t *a_stage = smem + L::a + s * A_STAGE;
+                    const uint2 sw = row_ok ? *reinterpret_cast<const uint2 *>(tile + TILE_SCALE_OFFSET + rr * 8)
+                                            : make_uint2(0u, 0u);
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const uint4 w = row_ok ? lds128(tile + (j * 16 + rr) * 16) : make_uint4(0x88888888u, 0x88888888u,
+                                                                                              0x88888888u, 0x88888888u);
+                        const uint32_t dw = (j & 2) ? sw.y : sw.x;
+                        const __half d = __ushort_as_half((unsigned short)((j & 1) ? (dw >> 16) : (dw & 0xffffu)));
+                        const __half2 d2 = __halves2half2(d, d);
+                        // chunk u of 8 values: u=0 low nibbles of bytes 0..7, u=1 bytes 8..15, u=2,3 high nibbles
+#pragma unroll
+                        for (int u = 0; u < 4; u++) {
+                            const uint4 v = dequant8((u & 1) ? w.z : w.x, (u & 1) ? w.w : w.y, u >= 2, d2);
+                            const int col = 32 * j + 8 * u;              // K position in the stage
+                            const int c = (col & 63) >> 3;               // 16-byte chunk in the 128-byte row
+                            *reinterpret_cast<uint4 *>(a_stage + (col >> 6) * ATOM_BYTES + (t >> 3) * 1024 +
+                                                       (t & 7) * 128 + ((c ^ (t & 7)) << 4)) = v;
+                        }
+                    }
+                }
+                fence_proxy_async_shared();   // the MMA (async proxy) reads what these threads wrote
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_plain(bar(RAW_EMPTY + rs));
+                    mbar_arrive_plain(bar(A_FULL + s));
+                }
+            }
+        }
+        // epilogue: this warp reads tensor-memory lanes 32 * (warp % 4) .. + 31
+        wait_or_fail(bar(ACC_FULL), 0u, failed, p.status);
+        tc_fence_after();
+        const int q = warp & 3;
+        const int row = n0 + 32 * q + lane;
+        if (!failed) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+                if (row < p.N) {
+#pragma unroll
+                    for (int i = 0; i < 32; i++) {
+                        const int m = m0 + c0 + i;
+                        if (m < p.M) p.dst[(size_t)m * p.N + row] = v[i];
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        constexpr uint32_t cols = BN < 32 ? 32 : BN;
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// activation pre-pass: B[m][k] in fp16
+// ---------------------------------------------------------------------------
+// Q4_0: the Q8_0 value q8 * fp16(d8) of every activation (one warp per block).
+__global__ void __launch_bounds__(256) act_q8_f16_kernel(const float *__restrict__ x, __half *__restrict__ b,
+                                                          int M, int K) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t nblocks = (int64_t)M * (K / QK);
+    for (int64_t blk = warp; blk < nblocks; blk += nwarps) {
+        const float v = x[blk * QK + lane];
+        const unsigned int amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
+        const float d = __uint_as_float(amax) / 127.0f;
+        const float d16 = __half2float(__float2half_rn(d));
+        b[blk * QK + lane] = __float2half_rn((float)q8_code(v, d) * d16);   // the product is exact in f32
+    }
+}
+
+// F16: the activations rounded to fp16.
+__global__ void __launch_bounds__(256) act_f16_kernel(const float *__restrict__ x, __half *__restrict__ b,
+                                                      int64_t n) {
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        b[i] = __float2half_rn(x[i]);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+gq_status encoder(PFN_cuTensorMapEncodeTiled_v12000 *out) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return fail(GQ_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    *out = g_encode;
+    return GQ_OK;
+}
+
+// fp16 matrix [rows][K], K contiguous; box of 64 K x box_rows with 128-byte swizzle
+gq_status f16_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    gq_status st = encoder(&enc);
+    if (st != GQ_OK) return st;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return GQ_OK;
+}
+
+constexpr int MAX_DEV = 64;
+std::atomic<bool> g_tc_smem_set[MAX_DEV][6];
+
+template <typename Kernel>
+gq_status allow_tc_smem(Kernel kernel, int which, int bytes) {
+    int dev = 0;
+    gq_status st = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+    if (st != GQ_OK) return st;
+    if (dev >= 0 && dev < MAX_DEV && g_tc_smem_set[dev][which].load(std::memory_order_acquire)) return GQ_OK;
+    st = check_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+                    "tc shared-memory attribute");
+    if (st == GQ_OK && dev >= 0 && dev < MAX_DEV) g_tc_smem_set[dev][which].store(true, std::memory_order_release);
+    return st;
+}
+
+template <int BN, bool QUANT>
+gq_status launch_tc(const CUtensorMap &mb, const CUtensorMap &ma, const TcParams &p, cudaStream_t s, int which) {
+    constexpr int smem = TcLayout<BN>::total + 1024;
+    auto kernel = tc_gemm_kernel<BN, QUANT>;
+    gq_status st = allow_tc_smem(kernel, which, smem);
+    if (st != GQ_OK) return st;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((p.M + BN - 1) / BN), (unsigned)((p.N + BM - 1) / BM), 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return check_cuda(cudaLaunchKernelEx(&cfg, kernel, mb, ma, p), "tc_gemm launch");
+}
+
+int tile_n(int64_t M) { return M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+
+gq_status launch_tc_common(bool quant, const void *w, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t s) {
+    TcParams p{};
+    p.status = device_status_word();
+    if (!p.status) return fail(GQ_ERR_CUDA, "device status word unavailable");
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.NT = (int)((K + BK - 1) / BK);
+    p.N16 = (int)((N + 15) / 16);
+    p.dst = dst;
+    p.w = (const uint8_t *)w;
+
+    Workspace ws;
+    gq_status st = get_workspace(s, 0, tc_workspace_bytes(M, K), &ws);
+    if (st != GQ_OK) return st;
+    __half *b = reinterpret_cast<__half *>(ws.data);
+
+    // the activations in fp16
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int64_t n = M * K;
+    cfg.gridDim = dim3((unsigned)std::min<int64_t>((n + 255) / 256, 8LL * sm_count()), 1, 1);
+    if (quant)
+        st = check_cuda(cudaLaunchKernelEx(&cfg, act_q8_f16_kernel, x, b, (int)M, (int)K), "activation pre-pass");
+    else
+        st = check_cuda(cudaLaunchKernelEx(&cfg, act_f16_kernel, x, b, n), "activation pre-pass");
+    if (st != GQ_OK) return st;
+
+    const int bn = tile_n(M);
+    CUtensorMap mb, ma;
+    memset(&ma, 0, sizeof(ma));
+    st = f16_map(&mb, b, M, K, bn);
+    if (st != GQ_OK) return st;
+    if (!quant) {
+        st = f16_map(&ma, w, N, K, BM);
+        if (st != GQ_OK) return st;
+    }
+    if (quant) {
+        if (bn == 32) return launch_tc<32, true>(mb, ma, p, s, 0);
+        if (bn == 64) return launch_tc<64, true>(mb, ma, p, s, 1);
+        return launch_tc<128, true>(mb, ma, p, s, 2);
+    }
+    if (bn == 32) return launch_tc<32, false>(mb, ma, p, s, 3);
+    if (bn == 64) return launch_tc<64, false>(mb, ma, p, s, 4);
+    return launch_tc<128, false>(mb, ma, p, s, 5);
+}
+
+}  // namespace
+
+size_t tc_workspace_bytes(int64_t M, int64_t K) { return (size_t)M * (size_t)K * sizeof(__half); }
+
+gq_status launch_tc_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                         cudaStream_t s) {
+    return launch_tc_common(true, rep, x, dst, M, N, K, s);
+}
+
+gq_status launch_tc_f16(const void *w16, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t s) {
+    return launch_tc_common(false, w16, x, dst, M, N, K, s);
+}
+
+}  // namespace gq
