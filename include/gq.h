@@ -190,6 +190,17 @@ int64_t gq_get_m_threshold(void);
 gq_status gq_mul_mat_q4_0_f32_noalloc(const void *q4_repacked, const float *src1, float *dst,
                                       int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
+/* Static weights.  A product launch may start before the kernel in front of it
+ * in the stream has finished (programmatic dependent launch), so that its
+ * weight stream overlaps the tail of that kernel; it waits for it before it
+ * reads src1 or writes dst.  With enable = 1 the caller declares that the work
+ * enqueued right before a product never writes that product's weights (true in
+ * a decode loop, where weights are written once at load time); the GEMV then
+ * reads the weights before that wait.  Default 0: weights are read only after
+ * every earlier kernel in the stream has finished.  Process-wide. */
+gq_status gq_set_static_weights(int enable);
+int gq_get_static_weights(void);
+
 /* ---- verification --------------------------------------------------------------- */
 
 /* The integer block dots of the GEMV instruction sequence, for parity tests:

@@ -64,6 +64,8 @@ SIGNATURES = {
     "gq_mul_mat_f16_f32_path": ([_P, _P, _P, _I, _I, _I, _S, _P], _S),
     "gq_reserve_workspace": ([_I, _I, _I, _P], _S),
     "gq_set_m_threshold": ([_I], _S),
+    "gq_set_static_weights": ([ctypes.c_int], _S),
+    "gq_get_static_weights": ([], ctypes.c_int),
     "gq_get_m_threshold": ([], _I),
     "gq_debug_block_dots_q4_0": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_noalloc": ([_P, _P, _P, _I, _I, _I, _P], _S),
@@ -186,6 +188,14 @@ def gq_set_m_threshold(t: int) -> None:
 
 def gq_get_m_threshold() -> int:
     return lib().gq_get_m_threshold()
+
+
+def gq_set_static_weights(enable: bool) -> None:
+    _check(lib().gq_set_static_weights(1 if enable else 0), "gq_set_static_weights")
+
+
+def gq_get_static_weights() -> bool:
+    return bool(lib().gq_get_static_weights())
 
 
 def gq_mul_mat_q4_0_f32_noalloc(q4_repacked, src1, dst, M: int, N: int, K: int, stream=None) -> None:

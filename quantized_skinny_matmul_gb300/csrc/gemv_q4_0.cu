@@ -56,20 +56,34 @@
 namespace gq {
 namespace {
 
-constexpr int CW = 16;                             // consumer warps
+constexpr int CHUNK_TILES = 16;                    // tiles per chunk = tile positions
 constexpr int PRODUCERS = 2;                       // producer warps (bulk-copy issue rate is per warp)
-constexpr int PRODUCER_WARP = CW;                  // CW .. CW + PRODUCERS - 1
-constexpr int FIXUPS = 2;                          // fix-up warps (shared row groups in parallel)
-constexpr int FIXUP_WARP = CW + PRODUCERS;         // .. + FIXUPS - 1
-constexpr int THREADS = (CW + PRODUCERS + FIXUPS) * 32;
-constexpr int FUSED_LOADS = 8;                     // float4 loads per consumer thread when INIT is fused
-constexpr int CONSUMERS = CW * 32;
-constexpr int CHUNK_TILES = CW;                    // one tile per consumer warp
+constexpr int FIXUPS = 1;                          // fix-up warps
+
+// CTA shapes: 8 consumer warps (two CTAs per SM, so the next product's CTA can
+// stream its weights beside this one) or 16 (one CTA per SM, for the ALU work
+// of several activation rows).  A consumer warp keeps one accumulator per tile
+// position of a chunk, and the row-group sum adds the 16 positions in order:
+// every output is the same sum, in the same order, for both shapes.
+template <int CWT>
+struct Shape {
+    static constexpr int CW = CWT;                          // consumer warps
+    static constexpr int TPW = CHUNK_TILES / CWT;           // tile positions per consumer warp
+    static constexpr int PRODUCER_WARP = CWT;               // .. + PRODUCERS - 1
+    static constexpr int FIXUP_WARP = CWT + PRODUCERS;      // .. + FIXUPS - 1
+    static constexpr int THREADS = (CWT + PRODUCERS + FIXUPS) * 32;
+    static constexpr int CONSUMERS = CWT * 32;
+    static constexpr int MIN_BLOCKS = CWT == 8 ? 2 : 1;
+    static constexpr int FUSED_LOADS = 8;                   // float4 per consumer thread when INIT is fused
+};
 constexpr int CHUNK_BYTES = CHUNK_TILES * TILE_BYTES;
 constexpr int MAX_SLOTS = 12;
 constexpr int PART_STRIDE = 16 * 16;               // floats of one partial (16 rows x 16 activation rows)
+constexpr int FIX_BATCH = 8;                      // partials one fix-up lane loads before adding them
 constexpr size_t ACT_BUDGET = 112 * 1024;          // wdata image of one slice
 constexpr size_t SMEM_LIMIT = 227 * 1024;
+constexpr size_t SMEM_HALF = 113 * 1024;           // two CTAs per SM: the next product's CTA fits beside
+constexpr int MIN_SLOTS_HALF = 4;
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -99,6 +113,7 @@ struct Params {
     int S, Gs;               // slices, CTAs per slice (grid = S * Gs)
     int slots, ntmax, maxfix;
     int fused;               // 1: no INIT launch, each CTA quantizes its slice of src1
+    int early;               // 1: the producers may read the weights before the grids in front finished
 };
 
 struct Layout {
@@ -109,7 +124,7 @@ struct Layout {
         ring = align_up((size_t)(2 * slots + 1 + maxfix) * 8, 128);
         act = ring + (size_t)slots * CHUNK_BYTES;
         red = act + im.bytes;
-        total = red + (size_t)CW * 16 * MT * 4;
+        total = red + (size_t)CHUNK_TILES * 16 * MT * 4;
     }
 };
 
@@ -176,6 +191,7 @@ struct Segments {
     }
 };
 
+template <int CONSUMERS>
 __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS) : "memory");
 }
@@ -198,8 +214,9 @@ __device__ __forceinline__ unsigned int atomic_add_acq_rel_gpu(unsigned int *p, 
 // slice that holds it.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
+    if (p.early) pdl_launch_dependents();   // weights are static: the GEMV may stream them at once
     pdl_wait();                 // src1 and the workspace are final: every earlier grid has completed
-    pdl_launch_dependents();    // the GEMV may start streaming weights now
+    pdl_launch_dependents();    // (no-op if already triggered) every grid before INIT is complete
     const Image im(p.M, p.ntmax);
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -230,8 +247,11 @@ __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
 // ---------------------------------------------------------------------------
 // COMPUTE
 // ---------------------------------------------------------------------------
-template <int MT>
-__global__ void __launch_bounds__(THREADS, 1) gemv_q4_0_kernel(const Params p) {
+template <int MT, int CWT>
+__global__ void __launch_bounds__(Shape<CWT>::THREADS, Shape<CWT>::MIN_BLOCKS) gemv_q4_0_kernel(const Params p) {
+    using SH = Shape<CWT>;
+    constexpr int CW = SH::CW, TPW = SH::TPW, CONSUMERS = SH::CONSUMERS, THREADS = SH::THREADS;
+    constexpr int PRODUCER_WARP = SH::PRODUCER_WARP, FIXUP_WARP = SH::FIXUP_WARP, FUSED_LOADS = SH::FUSED_LOADS;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int s = blockIdx.x / p.Gs, ci = blockIdx.x % p.Gs;
@@ -264,7 +284,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_q4_0_kernel(const Params p) {
     // even number of slots, so each producer refills only its own slots.
     if (warp >= PRODUCER_WARP && warp < PRODUCER_WARP + PRODUCERS) {
         const int pw = warp - PRODUCER_WARP;
-        if (p.fused) pdl_wait();   // without INIT in front, the weights may come from the grid before
+        if (!p.early) pdl_wait();   // the weights may still be written by the grid in front
         if (lane == 0) {
             int k = 0;
             bool failed = false;
@@ -301,19 +321,44 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_q4_0_kernel(const Params p) {
             if (lane == 0)   // the consumers' partial is in the workspace: release it, count the arrival
                 last = (atomic_add_acq_rel_gpu(p.cnt + g, 1u) + 1 == contributors(p, g)) ? 1u : 0u;
             last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {                                   // add every partial of row group g in a fixed order
-                for (int t = lane; t < outs; t += 32) {
-                    float sum = 0.0f;
-                    for (int s2 = 0; s2 < p.S; s2++) {
-                        int t2, n2;
-                        slice_of(p.NT, p.S, s2, t2, n2);
-                        const int T2 = p.N16 * n2;
-                        const int nc = owner(T2, p.Gs, (g + 1) * n2 - 1) - owner(T2, p.Gs, g * n2) + 1;
-                        const float *gp = p.part + ((size_t)g * p.S + s2) * 2 * PART_STRIDE + t;
-                        for (int q = 0; q < nc; q++) sum += __ldcg(gp + q * PART_STRIDE);
+            if (last) {   // add every partial of row group g in a fixed order: slice, then contributor
+                // a lane takes four consecutive outputs and has up to FIX_BATCH partials in flight
+                for (int tq = lane; tq < outs / 4; tq += 32) {
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int i0 = 0; i0 < 2 * p.S; i0 += FIX_BATCH) {
+                        float4 v[FIX_BATCH];
+                        bool have[FIX_BATCH];
+#pragma unroll
+                        for (int b = 0; b < FIX_BATCH; b++) {
+                            const int s2 = (i0 + b) >> 1, q = (i0 + b) & 1;
+                            have[b] = false;
+                            if (s2 < p.S) {
+                                int t2, n2;
+                                slice_of(p.NT, p.S, s2, t2, n2);
+                                const int T2 = p.N16 * n2;
+                                have[b] = q <= owner(T2, p.Gs, (g + 1) * n2 - 1) - owner(T2, p.Gs, g * n2);
+                            }
+                            v[b] = have[b] ? __ldcg(reinterpret_cast<const float4 *>(
+                                                 p.part + (((size_t)g * p.S + s2) * 2 + q) * PART_STRIDE) + tq)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int b = 0; b < FIX_BATCH; b++)
+                            if (have[b]) {
+                                sum.x += v[b].x;
+                                sum.y += v[b].y;
+                                sum.z += v[b].z;
+                                sum.w += v[b].w;
+                            }
                     }
-                    const int m = t / 16, n = 16 * g + t % 16;
-                    if (m < p.M && n < p.N) p.dst[(size_t)m * p.N + n] = sum;
+                    const int m = (4 * tq) / 16, n0 = 16 * g + (4 * tq) % 16;
+                    if (m < p.M) {
+                        float *o = p.dst + (size_t)m * p.N + n0;
+                        if (n0 + 0 < p.N) o[0] = sum.x;
+                        if (n0 + 1 < p.N) o[1] = sum.y;
+                        if (n0 + 2 < p.N) o[2] = sum.z;
+                        if (n0 + 3 < p.N) o[3] = sum.w;
+                    }
                 }
                 if (lane == 0) atomicExch(p.cnt + g, 0u);
             }
@@ -368,12 +413,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_q4_0_kernel(const Params p) {
         uint4 *dsts = reinterpret_cast<uint4 *>(act);
         for (int i = tid; i < (int)(im.bytes / 16); i += CONSUMERS) dsts[i] = __ldcg(src + i);
     }
-    consumers_sync();
+    consumers_sync<CONSUMERS>();
     bool failed = false;
 
-    float acc[MT];
+    float acc[TPW][MT];   // one accumulator per tile position this warp owns
 #pragma unroll
-    for (int m = 0; m < MT; m++) acc[m] = 0.0f;
+    for (int tw = 0; tw < TPW; tw++)
+#pragma unroll
+        for (int m = 0; m < MT; m++) acc[tw][m] = 0.0f;
 
     int slot = 0;
     uint32_t phase = 0;
@@ -385,9 +432,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_q4_0_kernel(const Params p) {
                 const bool ok = mbar_wait(smem_addr(full + slot), phase, p.status);
                 failed = !__all_sync(0xffffffffu, ok);
             }
-            if (!failed && warp < u1 - u) {
-                const int tl = u + warp;                       // tile index within the slice
-                const uint8_t *tile = ring + (size_t)slot * CHUNK_BYTES + warp * TILE_BYTES;
+#pragma unroll
+            for (int tw = 0; tw < TPW; tw++) {
+              const int ti = warp + CW * tw;                   // tile of the chunk
+              if (!failed && ti < u1 - u) {
+                const int tl = u + ti;                         // tile index within the slice
+                const uint8_t *tile = ring + (size_t)slot * CHUNK_BYTES + ti * TILE_BYTES;
                 const uint2 d4w = *reinterpret_cast<const uint2 *>(tile + TILE_SCALE_OFFSET + n * 8);
 #pragma unroll
                 for (int jj = 0; jj < 2; jj++) {
@@ -404,10 +454,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_q4_0_kernel(const Params p) {
                             const uint4 a1 = lds128(a + m * im.row_bytes + 16);
                             const float2 sc = act_sc[m * nblkmax + blk];
                             const int sumi = block_dot(q, a0, a1, __float_as_int(sc.y));
-                            acc[m] = fmaf(d4 * sc.x, (float)sumi, acc[m]);
+                            acc[tw][m] = fmaf(d4 * sc.x, (float)sumi, acc[tw][m]);
                         }
                     }
                 }
+              }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(empty + slot));   // this warp is done with the chunk
@@ -417,18 +468,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_q4_0_kernel(const Params p) {
             }
         }
 
-        // ---- row group g of this slice is complete: add the consumer warps' partials
+        // ---- row group g of this slice is complete: add the partials of the 16 tile positions
 #pragma unroll
-        for (int m = 0; m < MT; m++) {
-            const float other = __shfl_down_sync(0xffffffffu, acc[m], 16);   // blocks jh+1 of the same row
-            if (lane < 16) red[warp * outs + m * 16 + n] = acc[m] + other;
-            acc[m] = 0.0f;
-        }
-        consumers_sync();
+        for (int tw = 0; tw < TPW; tw++)
+#pragma unroll
+            for (int m = 0; m < MT; m++) {
+                const float other = __shfl_down_sync(0xffffffffu, acc[tw][m], 16);   // blocks jh+1 of the row
+                if (lane < 16) red[(warp + CW * tw) * outs + m * 16 + n] = acc[tw][m] + other;
+                acc[tw][m] = 0.0f;
+            }
+        consumers_sync<CONSUMERS>();
         if (tid < outs) {
             float v = 0.0f;
 #pragma unroll
-            for (int w = 0; w < CW; w++) v += red[w * outs + tid];
+            for (int pos = 0; pos < CHUNK_TILES; pos++) v += red[pos * outs + tid];
             if (j < seg.nshared) {                     // this CTA's part of a shared row group
                 const int slot_i = ci == owner(T, p.Gs, g * nts) ? 0 : 1;
                 p.part[(((size_t)g * p.S + s) * 2 + slot_i) * PART_STRIDE + tid] = v;
@@ -437,7 +490,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_q4_0_kernel(const Params p) {
                 if (m < p.M && row < p.N) p.dst[(size_t)m * p.N + row] = v;
             }
         }
-        consumers_sync();                              // red is reused; the partial is written
+        consumers_sync<CONSUMERS>();                   // red is reused; the partial is written
         if (j < seg.nshared && tid == 0) mbar_arrive(smem_addr(fixbar + j));
     }
 }
@@ -463,7 +516,7 @@ gq_status allow_smem(Kernel kernel, int which) {
     gq_status st = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
     if (st != GQ_OK) return st;
     if (dev >= 0 && dev < MAX_DEV && g_smem_set[dev][which].load(std::memory_order_acquire)) return GQ_OK;
-    st = check_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT),
+    st = check_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(SMEM_LIMIT - 1024)),
                     "gemv_q4_0 shared-memory attribute");
     if (st == GQ_OK && dev >= 0 && dev < MAX_DEV) g_smem_set[dev][which].store(true, std::memory_order_release);
     return st;
@@ -523,24 +576,36 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
         p.ntmax = q.ntmax;
         p.Gs = q.Gs;
         p.maxfix = q.maxfix;
-        // fuse INIT when each consumer thread loads at most FUSED_LOADS float4
-        p.fused = (int64_t)p.M * p.ntmax * 32 <= (int64_t)CONSUMERS * FUSED_LOADS ? 1 : 0;
+        // one activation row: 8 consumer warps, two CTAs per SM; more rows: 16 warps, one CTA per SM
+        const bool narrow = p.M == 1;
+        const int consumers = narrow ? Shape<8>::CONSUMERS : Shape<16>::CONSUMERS;
+        const int fused_loads = narrow ? Shape<8>::FUSED_LOADS : Shape<16>::FUSED_LOADS;
+        // fuse INIT when each consumer thread loads a few float4
+        p.fused = (int64_t)p.M * p.ntmax * 32 <= (int64_t)consumers * fused_loads ? 1 : 0;
+        // behind INIT (which waited for every earlier grid) the weights are final; otherwise only
+        // a caller that declared its weights static lets the producers start before the wait
+        p.early = (!p.fused || static_weights()) ? 1 : 0;
         p.part = reinterpret_cast<float *>(ws.data);
         p.wdata = ws.data + align_up((size_t)p.N16 * p.S * 2 * PART_STRIDE * sizeof(float), 256);
         const size_t fixed = Layout(MT, p.M, p.ntmax, 0, p.maxfix).total;
-        const size_t budget = SMEM_LIMIT - 1024;
-        p.slots = (int)std::min<size_t>(MAX_SLOTS, (budget - std::min(budget, fixed + 256)) / (CHUNK_BYTES + 16));
+        auto slots_for = [&](size_t budget) {
+            return (int)std::min<size_t>(MAX_SLOTS, (budget - std::min(budget, fixed + 256)) / (CHUNK_BYTES + 16));
+        };
+        p.slots = narrow ? slots_for(SMEM_HALF - 1024) : 0;   // two CTAs per SM if the ring keeps 4 chunks
+        if (p.slots < MIN_SLOTS_HALF) p.slots = slots_for(SMEM_LIMIT - 1024);
         p.slots = std::min(p.slots, env_int("GQ_GEMV_SLOTS", MAX_SLOTS)) & ~(PRODUCERS - 1);
         if (p.slots < 2)
             return fail(GQ_ERR_INVALID_ARG, "gemv_q4_0: N=%lld K=%lld leaves no room for the weight ring",
                         (long long)N, (long long)K);
         const size_t smem = Layout(MT, p.M, p.ntmax, p.slots, p.maxfix).total;
-        const int which = MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : MT == 8 ? 3 : 4;
-        void (*const kernels[5])(Params) = {gemv_q4_0_kernel<1>, gemv_q4_0_kernel<2>, gemv_q4_0_kernel<4>,
-                                            gemv_q4_0_kernel<8>, gemv_q4_0_kernel<16>};
+        const int which = narrow ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : MT == 8 ? 3 : 4;
+        void (*const kernels[5])(Params) = {gemv_q4_0_kernel<1, 8>, gemv_q4_0_kernel<2, 16>,
+                                            gemv_q4_0_kernel<4, 16>, gemv_q4_0_kernel<8, 16>,
+                                            gemv_q4_0_kernel<16, 16>};
         auto kernel = kernels[which];
         st = allow_smem(kernel, which);
         if (st != GQ_OK) return st;
+        const int threads = narrow ? Shape<8>::THREADS : Shape<16>::THREADS;
 
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -558,7 +623,7 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
             if (st != GQ_OK) return st;
         }
         cfg.gridDim = dim3((unsigned)(p.S * p.Gs), 1, 1);
-        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.blockDim = dim3((unsigned)threads, 1, 1);
         cfg.dynamicSmemBytes = smem;
         st = check_cuda(cudaLaunchKernelEx(&cfg, kernel, p), "gemv_q4_0 launch");
         if (st != GQ_OK) return st;

@@ -24,6 +24,7 @@ std::atomic<int> g_arch_ok[MAX_DEVICES];      // 0 unknown, 1 sm_103, -1 other
 std::atomic<int> g_sm_count[MAX_DEVICES];
 std::atomic<unsigned int *> g_status_ptr[MAX_DEVICES];
 std::atomic<int64_t> g_m_threshold{16};
+std::atomic<int> g_static_weights{0};
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -97,6 +98,8 @@ gq_status check_cuda(cudaError_t e, const char *what) {
     if (e == cudaSuccess) return GQ_OK;
     return fail(GQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
 }
+
+bool static_weights() { return g_static_weights.load(std::memory_order_relaxed) != 0; }
 
 int sm_count() {
     int dev = 0;
@@ -223,6 +226,13 @@ gq_status gq_set_m_threshold(int64_t t) {
 }
 
 int64_t gq_get_m_threshold(void) { return g_m_threshold.load(); }
+
+gq_status gq_set_static_weights(int enable) {
+    g_static_weights.store(enable ? 1 : 0);
+    return ok();
+}
+
+int gq_get_static_weights(void) { return g_static_weights.load(); }
 
 static gq_status check_path(gq_path path) {
     if (path != GQ_PATH_AUTO && path != GQ_PATH_GEMV && path != GQ_PATH_TC)

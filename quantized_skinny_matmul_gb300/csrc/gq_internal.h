@@ -22,6 +22,8 @@ gq_status check_cuda(cudaError_t e, const char *what);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+// Whether callers declared that work in front of a product never writes its weights.
+bool static_weights();
 // Device address of the current device's sticky status word (nullptr on error).
 unsigned int *device_status_word();
 
