@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
         const float v = b < p.nb ? p.x[(size_t)m * p.K + (size_t)b * QK + lane] : 0.0f;
         const unsigned int amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
         const float d = __uint_as_float(amax) / 127.0f;
-        const int q = q8_code(v, d);
+        const int q = q8_code_s(v, q8_scale(d));
         const int qsum = __reduce_add_sync(0xffffffffu, q);
         uint8_t *img = p.wdata + (size_t)s * im.bytes;
         img[im.codes + (size_t)m * im.row_bytes + (size_t)bl * 32 + lane] = (uint8_t)(q & 0xff);
@@ -377,36 +377,42 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS, Shape<CWT>::MIN_BLOCKS) g
     pdl_wait();                                      // src1, or INIT's wdata, is complete
     if (p.fused) {
         // INIT in the CTA: Q8_0 of this slice's columns of the M activation rows.
-        // Every load is issued first (one round trip), then eight consecutive
-        // lanes hold the four-value groups of one block.
-        const int per_row = nts * 32;                  // float4 of one row's slice
-        const int nf4 = p.M * per_row;                 // a multiple of 32: whole warps are valid
-        float4 v[FUSED_LOADS];
+        // Every load is issued first (one round trip).  A thread holds half a
+        // block (16 values, four float4) and the neighbouring lane the other
+        // half, so a block needs one exchange for its maximum and one for its
+        // code sum.
+        constexpr int HALVES = FUSED_LOADS / 4;          // half blocks per thread
+        const int per_row = nts * 8;                     // half blocks of one row's slice
+        const int nh = p.M * per_row;
+        float4 v[HALVES][4];
 #pragma unroll
-        for (int i = 0; i < FUSED_LOADS; i++) {
-            const int f = tid + CONSUMERS * i, m = f / per_row, col = ts0 * TILE_COLS + (f % per_row) * 4;
-            v[i] = (f < nf4 && col < p.K) ? ldg_f4(p.x + (size_t)m * p.K + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < HALVES; i++) {
+            const int h = tid + CONSUMERS * i, m = h / per_row, col = ts0 * TILE_COLS + (h % per_row) * 16;
+            const bool live = h < nh && col < p.K;       // K is a multiple of 32: halves are whole
+            const float *src = p.x + (size_t)m * p.K + col;
+#pragma unroll
+            for (int k = 0; k < 4; k++) v[i][k] = live ? ldg_f4(src + 4 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int i = 0; i < FUSED_LOADS; i++) {
-            const int f = tid + CONSUMERS * i;
-            if (f >= nf4) break;                       // warp-uniform
-            const int m = f / per_row, c4 = f % per_row, bl = c4 >> 3, e = c4 & 7;
-            float am = absmax4(v[i]);
+        for (int i = 0; i < HALVES; i++) {
+            const int h = tid + CONSUMERS * i;
+            if (CONSUMERS * i >= nh) break;              // no half of this round is live (CTA-uniform)
+            float am = fmaxf(fmaxf(absmax4(v[i][0]), absmax4(v[i][1])), fmaxf(absmax4(v[i][2]), absmax4(v[i][3])));
             am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
             const float d = am / 127.0f;
-            const uint32_t word = pack_q8x4(v[i], d);
-            int qs = (int)(int8_t)(word & 0xff) + (int)(int8_t)((word >> 8) & 0xff) +
-                     (int)(int8_t)((word >> 16) & 0xff) + (int)(int8_t)(word >> 24);
+            const Q8Scale q = q8_scale(d);
+            uint32_t w[4];
+            pack_q8x16(v[i], q, w);
+            int qs = sum_q8x4(w[0]) + sum_q8x4(w[1]) + sum_q8x4(w[2]) + sum_q8x4(w[3]);
             qs += __shfl_xor_sync(0xffffffffu, qs, 1);
-            qs += __shfl_xor_sync(0xffffffffu, qs, 2);
-            qs += __shfl_xor_sync(0xffffffffu, qs, 4);
-            *reinterpret_cast<uint32_t *>(act + im.codes + (size_t)m * im.row_bytes + (size_t)bl * 32 + e * 4) = word;
-            if (e == 0)
-                reinterpret_cast<float2 *>(act + im.scales)[m * 4 * p.ntmax + bl] =
-                    make_float2(__half2float(__float2half_rn(d)), __int_as_float(-8 * qs));
+            if (h < nh) {
+                const int m = h / per_row, hb = h % per_row, bl = hb >> 1;
+                *reinterpret_cast<uint4 *>(act + im.codes + (size_t)m * im.row_bytes + (size_t)hb * 16) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+                if ((hb & 1) == 0)
+                    reinterpret_cast<float2 *>(act + im.scales)[m * 4 * p.ntmax + bl] =
+                        make_float2(__half2float(__float2half_rn(d)), __int_as_float(-8 * qs));
+            }
         }
     } else {   // plain coalesced loads of the slice's wdata image (the bulk-copy queue carries the weights)
         const uint4 *src = reinterpret_cast<const uint4 *>(p.wdata + (size_t)s * im.bytes);
@@ -432,10 +438,8 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS, Shape<CWT>::MIN_BLOCKS) g
                 const bool ok = mbar_wait(smem_addr(full + slot), phase, p.status);
                 failed = !__all_sync(0xffffffffu, ok);
             }
-#pragma unroll
-            for (int tw = 0; tw < TPW; tw++) {
-              const int ti = warp + CW * tw;                   // tile of the chunk
-              if (!failed && ti < u1 - u) {
+            // the tile at position ti of the chunk, into the accumulators of position tw
+            auto tile_dot = [&](const int tw, const int ti) {
                 const int tl = u + ti;                         // tile index within the slice
                 const uint8_t *tile = ring + (size_t)slot * CHUNK_BYTES + ti * TILE_BYTES;
                 const uint2 d4w = *reinterpret_cast<const uint2 *>(tile + TILE_SCALE_OFFSET + n * 8);
@@ -458,7 +462,16 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS, Shape<CWT>::MIN_BLOCKS) g
                         }
                     }
                 }
-              }
+            };
+            if (!failed) {
+                if (u1 - u >= CHUNK_TILES) {                   // a full chunk: no per-tile test
+#pragma unroll
+                    for (int tw = 0; tw < TPW; tw++) tile_dot(tw, warp + CW * tw);
+                } else {
+#pragma unroll
+                    for (int tw = 0; tw < TPW; tw++)
+                        if (warp + CW * tw < u1 - u) tile_dot(tw, warp + CW * tw);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(empty + slot));   // this warp is done with the chunk

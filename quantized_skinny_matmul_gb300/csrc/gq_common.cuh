@@ -61,14 +61,101 @@ __device__ __forceinline__ int q8_code(float x, float d) {
     return v < -127 ? -127 : (v > 127 ? 127 : v);
 }
 
-// Four Q8_0 codes packed into a little-endian word (code of x.x in the low byte).
-__device__ __forceinline__ uint32_t pack_q8x4(float4 x, float d) {
-    uint32_t b0 = (uint32_t)(q8_code(x.x, d) & 0xff);
-    uint32_t b1 = (uint32_t)(q8_code(x.y, d) & 0xff);
-    uint32_t b2 = (uint32_t)(q8_code(x.z, d) & 0xff);
-    uint32_t b3 = (uint32_t)(q8_code(x.w, d) & 0xff);
-    return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+// The same code without a division.  With r within one ulp of 1/d
+// (rcp.approx.f32), y = x * r is within a relative 2^-22 of the quotient, and
+// |x / d| <= 127 (1 + 2^-23) for a normal d (below 191 for a subnormal one,
+// whose rounding is coarser), so the two differ by less than 3.5e-5: they
+// round to the same integer unless y lies within 2^-14 (6.1e-5) of a
+// half-integer.  Away from
+// half-integers every round-to-nearest agrees with roundf, so the nearest
+// integer of y (rintf) is the code.
+//
+// Near the half-integer h = k + 1/2 (k = floor|y|), roundf(x / d) is k + 1 in
+// magnitude iff the IEEE quotient rounds to h or above, i.e. iff |x| / d lies
+// above the midpoint m = h - u/2 between h and its predecessor (u = h minus
+// that predecessor), or on it when h has an even significand.  The sign of
+// |x| - m d decides: e = |x| - h d is exact in f32 (|x| and h d agree to 14
+// bits and both are multiples of ulp(d)/2), and fmaf(u/2, d, e) rounds the
+// exact |x| - m d once, which keeps its sign and its zero.
+//
+// Both codes are formed for every value and one is selected, without a
+// branch.  Scales below 2^-60 are first multiplied, with x, by 2^64: the
+// quotient is unchanged, r stays finite and u/2 * d cannot underflow.
+struct Q8Scale {
+    float d;   // the block scale, multiplied by s
+    float r;   // approximately 1 / d (0 when d = 0)
+    float s;   // 1, or 2^64 for a tiny scale
+};
+
+__device__ __forceinline__ Q8Scale q8_scale(float d) {
+    Q8Scale q;
+    q.s = d < 0x1p-60f ? 0x1p64f : 1.0f;
+    q.d = d * q.s;
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(q.d));
+    q.r = d == 0.0f ? 0.0f : r;
+    return q;
 }
+
+// y is within 2^-14 of a half-integer (the quotient is within 3.5e-5 of y)
+__device__ __forceinline__ bool q8_near_half(float y, float n) { return !(fabsf(y - n) < 0.5f - 0x1p-14f); }
+
+__device__ __forceinline__ int q8_code_s(float x, const Q8Scale &q) {
+    const float xs = x * q.s;
+    const float y = xs * q.r;
+    const float n = rintf(y);
+    const bool away = !q8_near_half(y, n);
+    const float ax = fabsf(xs);
+    const float k = floorf(fabsf(y));
+    const float h = k + 0.5f;
+    const float u = h - __int_as_float(__float_as_int(h) - 1);
+    const float t = fmaf(0.5f * u, q.d, fmaf(-h, q.d, ax));
+    const bool up = t > 0.0f || (t == 0.0f && (__float_as_int(h) & 1) == 0);
+    int c = (int)k + (up ? 1 : 0);
+    c = xs < 0.0f ? -c : c;
+    c = away ? (int)n : c;
+    return c < -127 ? -127 : (c > 127 ? 127 : c);   // |x / d| exceeds 127 only for a subnormal d
+}
+
+// Four Q8_0 codes packed into a little-endian word (code of x.x in the low byte).
+__device__ __forceinline__ uint32_t pack_bytes(int c0, int c1, int c2, int c3) {
+    const uint32_t lo = __byte_perm((uint32_t)c0, (uint32_t)c1, 0x0040);
+    const uint32_t hi = __byte_perm((uint32_t)c2, (uint32_t)c3, 0x0040);
+    return __byte_perm(lo, hi, 0x5410);
+}
+
+__device__ __forceinline__ uint32_t pack_q8x4(float4 x, const Q8Scale &q) {
+    return pack_bytes(q8_code_s(x.x, q), q8_code_s(x.y, q), q8_code_s(x.z, q), q8_code_s(x.w, q));
+}
+
+// The codes of sixteen values (a half block) into four words.  The nearest
+// integers are formed first; only if some lane of the warp has a value near a
+// half-integer (a few percent of warps) does the warp form the full codes.
+__device__ __forceinline__ int q8_nearest(float x, const Q8Scale &q, bool &near) {
+    const float y = (x * q.s) * q.r;
+    const float n = rintf(y);
+    near = q8_near_half(y, n);
+    const int c = (int)n;
+    return c < -127 ? -127 : (c > 127 ? 127 : c);
+}
+
+__device__ __forceinline__ void pack_q8x16(const float4 (&x)[4], const Q8Scale &q, uint32_t (&w)[4]) {
+    bool any = false;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        bool n0, n1, n2, n3;
+        const int c0 = q8_nearest(x[k].x, q, n0), c1 = q8_nearest(x[k].y, q, n1);
+        const int c2 = q8_nearest(x[k].z, q, n2), c3 = q8_nearest(x[k].w, q, n3);
+        w[k] = pack_bytes(c0, c1, c2, c3);
+        any |= n0 | n1 | n2 | n3;
+    }
+    if (__any_sync(0xffffffffu, any))   // warp-uniform
+#pragma unroll
+        for (int k = 0; k < 4; k++) w[k] = pack_q8x4(x[k], q);
+}
+
+// Sum of the four signed codes of a packed word.
+__device__ __forceinline__ int sum_q8x4(uint32_t word) { return __dp4a((int)word, 0x01010101, 0); }
 
 __device__ __forceinline__ float absmax4(float4 v) {
     return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
@@ -101,16 +188,16 @@ __device__ __forceinline__ Nibbles unpack_q4(uint4 w) {
 
 // a0: activation codes 0..15, a1: codes 16..31 (four per word, element order)
 __device__ __forceinline__ int block_dot(const Nibbles &q, uint4 a0, uint4 a1, int corr) {
-    int s = corr;
+    int s = corr, t = 0;   // two independent chains; the int32 sum is exact in any order
     s = __dp4a((int)q.lo[0], (int)a0.x, s);
-    s = __dp4a((int)q.lo[1], (int)a0.y, s);
+    t = __dp4a((int)q.lo[1], (int)a0.y, t);
     s = __dp4a((int)q.lo[2], (int)a0.z, s);
-    s = __dp4a((int)q.lo[3], (int)a0.w, s);
+    t = __dp4a((int)q.lo[3], (int)a0.w, t);
     s = __dp4a((int)q.hi[0], (int)a1.x, s);
-    s = __dp4a((int)q.hi[1], (int)a1.y, s);
+    t = __dp4a((int)q.hi[1], (int)a1.y, t);
     s = __dp4a((int)q.hi[2], (int)a1.z, s);
-    s = __dp4a((int)q.hi[3], (int)a1.w, s);
-    return s;
+    t = __dp4a((int)q.hi[3], (int)a1.w, t);
+    return s + t;
 }
 
 // D(16x8, f32) += A(16x16, f16, row) . B(16x8, f16, col)

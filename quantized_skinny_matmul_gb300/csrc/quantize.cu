@@ -51,7 +51,7 @@ __global__ void quantize_rows_q8_0_kernel(const float *__restrict__ x, uint8_t *
         const unsigned int amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
         const float d = __uint_as_float(amax) / 127.0f;
         uint8_t *o = out + b * Q8_0_BYTES;            // 2-byte aligned: 34 * b is even
-        o[2 + lane] = (uint8_t)(q8_code(v, d) & 0xff);
+        o[2 + lane] = (uint8_t)(q8_code_s(v, q8_scale(d)) & 0xff);
         if (lane == 0) *reinterpret_cast<unsigned short *>(o) = __half_as_ushort(__float2half_rn(d));
     }
 }

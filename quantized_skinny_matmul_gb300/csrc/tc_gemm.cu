@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(256) act_q8_f16_kernel(const float *__restrict
         const unsigned int amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
         const float d = __uint_as_float(amax) / 127.0f;
         const float d16 = __half2float(__float2half_rn(d));
-        b[blk * QK + lane] = __float2half_rn((float)q8_code(v, d) * d16);   // the product is exact in f32
+        b[blk * QK + lane] = __float2half_rn((float)q8_code_s(v, q8_scale(d)) * d16);   // the product is exact in f32
     }
 }
 
