@@ -73,13 +73,14 @@ struct Shape {
     static constexpr int FIXUP_WARP = CWT + PRODUCERS;      // .. + FIXUPS - 1
     static constexpr int THREADS = (CWT + PRODUCERS + FIXUPS) * 32;
     static constexpr int CONSUMERS = CWT * 32;
-    static constexpr int MIN_BLOCKS = CWT == 8 ? 2 : 1;
-    static constexpr int FUSED_LOADS = 8;                   // float4 per consumer thread when INIT is fused
+    static constexpr int MAX_REGS = CWT == 8 ? 88 : 96;     // two CTAs of 11 warps, or one of 19
+    static constexpr int FUSED_LOADS = 4;                   // float4 per consumer thread and round of the fused INIT
 };
 constexpr int CHUNK_BYTES = CHUNK_TILES * TILE_BYTES;
 constexpr int MAX_SLOTS = 12;
 constexpr int PART_STRIDE = 16 * 16;               // floats of one partial (16 rows x 16 activation rows)
-constexpr int FIX_BATCH = 8;                      // partials one fix-up lane loads before adding them
+constexpr int FIX_BATCH = 8;                       // partials one fix-up lane loads before adding them
+constexpr int FUSED_ROUNDS = 2;                    // load rounds of the fused INIT (more: a separate INIT is faster)
 constexpr size_t ACT_BUDGET = 112 * 1024;          // wdata image of one slice
 constexpr size_t SMEM_LIMIT = 227 * 1024;
 constexpr size_t SMEM_HALF = 113 * 1024;           // two CTAs per SM: the next product's CTA fits beside
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
 // COMPUTE
 // ---------------------------------------------------------------------------
 template <int MT, int CWT>
-__global__ void __launch_bounds__(Shape<CWT>::THREADS, Shape<CWT>::MIN_BLOCKS) gemv_q4_0_kernel(const Params p) {
+__global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(Shape<CWT>::MAX_REGS) gemv_q4_0_kernel(const Params p) {
     using SH = Shape<CWT>;
     constexpr int CW = SH::CW, TPW = SH::TPW, CONSUMERS = SH::CONSUMERS, THREADS = SH::THREADS;
     constexpr int PRODUCER_WARP = SH::PRODUCER_WARP, FIXUP_WARP = SH::FIXUP_WARP, FUSED_LOADS = SH::FUSED_LOADS;
@@ -377,17 +378,19 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS, Shape<CWT>::MIN_BLOCKS) g
     pdl_wait();                                      // src1, or INIT's wdata, is complete
     if (p.fused) {
         // INIT in the CTA: Q8_0 of this slice's columns of the M activation rows.
-        // Every load is issued first (one round trip).  A thread holds half a
+        // Every load of a round is issued first (one round trip).  A thread holds half a
         // block (16 values, four float4) and the neighbouring lane the other
         // half, so a block needs one exchange for its maximum and one for its
         // code sum.
         constexpr int HALVES = FUSED_LOADS / 4;          // half blocks per thread
         const int per_row = nts * 8;                     // half blocks of one row's slice
         const int nh = p.M * per_row;
+#pragma unroll 1
+        for (int h0 = 0; h0 < nh; h0 += HALVES * CONSUMERS) {   // at most FUSED_ROUNDS rounds
         float4 v[HALVES][4];
 #pragma unroll
         for (int i = 0; i < HALVES; i++) {
-            const int h = tid + CONSUMERS * i, m = h / per_row, col = ts0 * TILE_COLS + (h % per_row) * 16;
+            const int h = h0 + tid + CONSUMERS * i, m = h / per_row, col = ts0 * TILE_COLS + (h % per_row) * 16;
             const bool live = h < nh && col < p.K;       // K is a multiple of 32: halves are whole
             const float *src = p.x + (size_t)m * p.K + col;
 #pragma unroll
@@ -395,8 +398,8 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS, Shape<CWT>::MIN_BLOCKS) g
         }
 #pragma unroll
         for (int i = 0; i < HALVES; i++) {
-            const int h = tid + CONSUMERS * i;
-            if (CONSUMERS * i >= nh) break;              // no half of this round is live (CTA-uniform)
+            const int h = h0 + tid + CONSUMERS * i;
+            if (h0 + CONSUMERS * i >= nh) break;         // no half of this step is live (CTA-uniform)
             float am = fmaxf(fmaxf(absmax4(v[i][0]), absmax4(v[i][1])), fmaxf(absmax4(v[i][2]), absmax4(v[i][3])));
             am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
             const float d = am / 127.0f;
@@ -413,6 +416,7 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS, Shape<CWT>::MIN_BLOCKS) g
                     reinterpret_cast<float2 *>(act + im.scales)[m * 4 * p.ntmax + bl] =
                         make_float2(__half2float(__float2half_rn(d)), __int_as_float(-8 * qs));
             }
+        }
         }
     } else {   // plain coalesced loads of the slice's wdata image (the bulk-copy queue carries the weights)
         const uint4 *src = reinterpret_cast<const uint4 *>(p.wdata + (size_t)s * im.bytes);
@@ -594,7 +598,7 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
         const int consumers = narrow ? Shape<8>::CONSUMERS : Shape<16>::CONSUMERS;
         const int fused_loads = narrow ? Shape<8>::FUSED_LOADS : Shape<16>::FUSED_LOADS;
         // fuse INIT when each consumer thread loads a few float4
-        p.fused = (int64_t)p.M * p.ntmax * 32 <= (int64_t)consumers * fused_loads ? 1 : 0;
+        p.fused = (int64_t)p.M * p.ntmax * 32 <= (int64_t)consumers * fused_loads * FUSED_ROUNDS ? 1 : 0;
         // behind INIT (which waited for every earlier grid) the weights are final; otherwise only
         // a caller that declared its weights static lets the producers start before the wait
         p.early = (!p.fused || static_weights()) ? 1 : 0;
