@@ -60,6 +60,22 @@ def step_bytes_f16(M, N, K):
     return 2 * N * K + 4 * M * K + 4 * M * N
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(t: float, dist) -> float:
+    """The slowest rank's time: the whole job ends with it."""
+    if not dist:
+        return t
+    import torch
+    tt = torch.tensor([t], dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, t: float) -> float:
+    """Replicas: every rank runs the full step, so the job moves world x the bytes in time t."""
+    return bytes_per_step * steps * world / t / 1e9
+
+
 # ----------------------------------------------------------------------------- env
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
@@ -293,12 +309,8 @@ def run_ours(args, rank, world, local):
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    t = start.elapsed_time(end) / 1e3
-    if dist:
-        tt = torch.tensor([t], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
-    value = bytes_per_step * args.steps * world / t / 1e9
+    t = max_over_ranks(start.elapsed_time(end) / 1e3, dist)
+    value = whole_job_gbs(bytes_per_step, args.steps, world, t)
     ms_per_step = t / args.steps * 1e3
     achieved = bytes_per_step * args.steps / t / 1e9          # per GPU, all launches of the one kernel family
 
@@ -325,11 +337,8 @@ def run_ours(args, rank, world, local):
                 ho[i].copy_(outs[i], non_blocking=True)
             b.stream.synchronize()
         t_e2e = time.perf_counter() - t0
-    if dist:
-        tt = torch.tensor([t_e2e], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
-    e2e = {"value": round(bytes_per_step * e2e_steps * world / t_e2e / 1e9, 3), "unit": "GB/s",
+    t_e2e = max_over_ranks(t_e2e, dist)
+    e2e = {"value": round(whole_job_gbs(bytes_per_step, e2e_steps, world, t_e2e), 3), "unit": "GB/s",
            "h2d_bytes_per_step": sum(4 * M * K for N, K in SHAPES),
            "d2h_bytes_per_step": sum(4 * M * N for N, K in SHAPES), "steps": e2e_steps}
 
