@@ -215,7 +215,7 @@ __global__ void block_dots_q4_0_kernel(const uint8_t *__restrict__ w, const uint
     const int64_t rest = idx / nb;
     const int n = (int)(rest % N), m = (int)(rest / N);
     const uint8_t *tile = w + ((size_t)(n / 16) * NT + b / 4) * TILE_BYTES;
-    const Nibbles q = unpack_q4(*reinterpret_cast<const uint4 *>(tile + ((b % 4) * 16 + n % 16) * 16));
+    const uint4 q = *reinterpret_cast<const uint4 *>(tile + ((b % 4) * 16 + n % 16) * 16);
     const uint16_t *codes = reinterpret_cast<const uint16_t *>(q8 + ((size_t)m * nb + b) * Q8_0_BYTES + 2);
     uint32_t a[8];
     int qsum = 0;

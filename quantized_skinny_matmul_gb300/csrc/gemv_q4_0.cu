@@ -438,10 +438,8 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(Shape<CWT>::M
         int g, u0, u1;
         seg.get(j, g, u0, u1);
         for (int u = u0; u < u1; u += CHUNK_TILES) {
-            if (!failed) {
-                const bool ok = mbar_wait(smem_addr(full + slot), phase, p.status);
-                failed = !__all_sync(0xffffffffu, ok);
-            }
+            // a lane whose wait gave up skips the chunks from here on; nothing below needs the whole warp
+            if (!failed) failed = !mbar_wait(smem_addr(full + slot), phase, p.status);
             // the tile at position ti of the chunk, into the accumulators of position tw
             auto tile_dot = [&](const int tw, const int ti) {
                 const int tl = u + ti;                         // tile index within the slice
@@ -450,20 +448,22 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(Shape<CWT>::M
 #pragma unroll
                 for (int jj = 0; jj < 2; jj++) {
                     const int jb = jh + 2 * jj;                // block of the tile
-                    const Nibbles q = unpack_q4(lds128(tile + (jb * 16 + n) * 16));
+                    const uint4 q = lds128(tile + (jb * 16 + n) * 16);
                     const uint32_t dw = jb & 2 ? d4w.y : d4w.x;
                     const float d4 = (jb & 1) ? half_hi(dw) : half_lo(dw);
                     const int blk = 4 * tl + jb;
                     const uint8_t *a = act + im.codes + (size_t)blk * 32;
 #pragma unroll
                     for (int m = 0; m < MT; m++) {
-                        if (m < p.M) {
-                            const uint4 a0 = lds128(a + m * im.row_bytes);
-                            const uint4 a1 = lds128(a + m * im.row_bytes + 16);
-                            const float2 sc = act_sc[m * nblkmax + blk];
-                            const int sumi = block_dot(q, a0, a1, __float_as_int(sc.y));
-                            acc[tw][m] = fmaf(d4 * sc.x, (float)sumi, acc[tw][m]);
-                        }
+                        // up to four rows, rows past M repeat row M-1 (no branch; their sums are
+                        // never stored); with more rows the rows past M are skipped
+                        if (MT > 4 && m >= p.M) continue;
+                        const int mm = MT > 4 ? m : min(m, p.M - 1);
+                        const uint4 a0 = lds128(a + mm * im.row_bytes);
+                        const uint4 a1 = lds128(a + mm * im.row_bytes + 16);
+                        const float2 sc = act_sc[mm * nblkmax + blk];
+                        const int sumi = block_dot(q, a0, a1, __float_as_int(sc.y));
+                        acc[tw][m] = fmaf(d4 * sc.x, (float)sumi, acc[tw][m]);
                     }
                 }
             };
@@ -525,7 +525,7 @@ int env_int(const char *name, int dflt) {
 
 // The dynamic shared-memory limit is raised once per (device, kernel).
 constexpr int MAX_DEV = 64;
-std::atomic<bool> g_smem_set[MAX_DEV][5];
+std::atomic<bool> g_smem_set[MAX_DEV][8];
 
 template <typename Kernel>
 gq_status allow_smem(Kernel kernel, int which) {
@@ -551,6 +551,32 @@ Plan plan(int N16, int NT, int MT) {
     // row groups a CTA touches: at most ceil(N16 / Gs) + 2 (one mbarrier each)
     q.maxfix = q.S > 1 ? (N16 + q.Gs - 1) / q.Gs + 2 : 2;
     return q;
+}
+
+// Instantiated kernels: activation rows per tile (MT) and consumer warps (CW).
+struct Variant {
+    int mt, cw, consumers, threads, fused_loads;
+    void (*kernel)(Params);
+};
+
+template <int MT, int CW>
+constexpr Variant variant() {
+    return {MT, CW, Shape<CW>::CONSUMERS, Shape<CW>::THREADS, Shape<CW>::FUSED_LOADS, gemv_q4_0_kernel<MT, CW>};
+}
+
+const Variant VARIANTS[] = {variant<1, 8>(), variant<1, 16>(), variant<2, 16>(),
+                            variant<4, 16>(), variant<8, 16>(), variant<16, 16>()};
+constexpr int N_VARIANTS = sizeof(VARIANTS) / sizeof(VARIANTS[0]);
+
+// One activation row: 8 consumer warps and two CTAs per SM, so that the next
+// product's CTA streams its weights beside this one.  More rows: 16 warps and
+// one CTA per SM for the ALU work.
+int consumer_warps_for(int M) { return M == 1 ? 8 : 16; }
+
+const Variant *variant_for(int mt, int cw) {
+    for (int i = 0; i < N_VARIANTS; i++)
+        if (VARIANTS[i].mt == mt && VARIANTS[i].cw == cw) return &VARIANTS[i];
+    return nullptr;
 }
 
 }  // namespace
@@ -593,12 +619,11 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
         p.ntmax = q.ntmax;
         p.Gs = q.Gs;
         p.maxfix = q.maxfix;
-        // one activation row: 8 consumer warps, two CTAs per SM; more rows: 16 warps, one CTA per SM
-        const bool narrow = p.M == 1;
-        const int consumers = narrow ? Shape<8>::CONSUMERS : Shape<16>::CONSUMERS;
-        const int fused_loads = narrow ? Shape<8>::FUSED_LOADS : Shape<16>::FUSED_LOADS;
+        const Variant *kvp = variant_for(MT, consumer_warps_for(p.M));
+        if (!kvp) return fail(GQ_ERR_INVALID_ARG, "gemv_q4_0: no kernel for M=%d", p.M);
+        const Variant &kv = *kvp;
         // fuse INIT when each consumer thread loads a few float4
-        p.fused = (int64_t)p.M * p.ntmax * 32 <= (int64_t)consumers * fused_loads * FUSED_ROUNDS ? 1 : 0;
+        p.fused = (int64_t)p.M * p.ntmax * 32 <= (int64_t)kv.consumers * kv.fused_loads * FUSED_ROUNDS ? 1 : 0;
         // behind INIT (which waited for every earlier grid) the weights are final; otherwise only
         // a caller that declared its weights static lets the producers start before the wait
         p.early = (!p.fused || static_weights()) ? 1 : 0;
@@ -608,21 +633,17 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
         auto slots_for = [&](size_t budget) {
             return (int)std::min<size_t>(MAX_SLOTS, (budget - std::min(budget, fixed + 256)) / (CHUNK_BYTES + 16));
         };
-        p.slots = narrow ? slots_for(SMEM_HALF - 1024) : 0;   // two CTAs per SM if the ring keeps 4 chunks
+        // the 8-warp shape runs two CTAs per SM if the ring keeps MIN_SLOTS_HALF chunks
+        p.slots = kv.cw == 8 ? slots_for(SMEM_HALF - 1024) : 0;
         if (p.slots < MIN_SLOTS_HALF) p.slots = slots_for(SMEM_LIMIT - 1024);
         p.slots = std::min(p.slots, env_int("GQ_GEMV_SLOTS", MAX_SLOTS)) & ~(PRODUCERS - 1);
         if (p.slots < 2)
             return fail(GQ_ERR_INVALID_ARG, "gemv_q4_0: N=%lld K=%lld leaves no room for the weight ring",
                         (long long)N, (long long)K);
         const size_t smem = Layout(MT, p.M, p.ntmax, p.slots, p.maxfix).total;
-        const int which = narrow ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : MT == 8 ? 3 : 4;
-        void (*const kernels[5])(Params) = {gemv_q4_0_kernel<1, 8>, gemv_q4_0_kernel<2, 16>,
-                                            gemv_q4_0_kernel<4, 16>, gemv_q4_0_kernel<8, 16>,
-                                            gemv_q4_0_kernel<16, 16>};
-        auto kernel = kernels[which];
-        st = allow_smem(kernel, which);
+        st = allow_smem(kv.kernel, (int)(&kv - VARIANTS));
         if (st != GQ_OK) return st;
-        const int threads = narrow ? Shape<8>::THREADS : Shape<16>::THREADS;
+        const int threads = kv.threads;
 
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -642,7 +663,7 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
         cfg.gridDim = dim3((unsigned)(p.S * p.Gs), 1, 1);
         cfg.blockDim = dim3((unsigned)threads, 1, 1);
         cfg.dynamicSmemBytes = smem;
-        st = check_cuda(cudaLaunchKernelEx(&cfg, kernel, p), "gemv_q4_0 launch");
+        st = check_cuda(cudaLaunchKernelEx(&cfg, kv.kernel, p), "gemv_q4_0 launch");
         if (st != GQ_OK) return st;
     }
     return GQ_OK;

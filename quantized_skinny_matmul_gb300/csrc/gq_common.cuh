@@ -163,41 +163,33 @@ __device__ __forceinline__ float absmax4(float4 v) {
 
 // ---------------------------------------------------------------------------
 // The integer block dot of the q_f32 kind with dp4a.  A Q4_0 block's 16 code
-// bytes hold q_i in the low nibble and q_{i+16} in the high nibble of byte i,
-// so masking the four words gives the codes of elements 0..15 (lo) and 16..31
-// (hi) as bytes in element order, each in 0..15.  With the activation codes
-// a[0..31] (int8, element order) and corr = -8 * sum(a):
+// bytes hold q_i in the low nibble and q_{i+16} in the high nibble of byte i.
+// With the activation codes a[0..31] (int8, element order) and
+// corr = -8 * sum(a):
 //     sum_j (q_j - 8) * a_j = corr + sum_j q_j * a_j        (exact in int32)
+// The low nibbles are masked in place (bytes 0..15); the high nibbles are
+// masked in place too, as 16 q (bytes 0..240, unsigned), so their dot product
+// is 16 times the wanted one and an arithmetic shift by 4 recovers it exactly.
+// Two independent dp4a chains; no shifts of the code words.
 // ---------------------------------------------------------------------------
-struct Nibbles {
-    uint32_t lo[4], hi[4];
-};
-
-__device__ __forceinline__ Nibbles unpack_q4(uint4 w) {
-    Nibbles n;
-    n.lo[0] = w.x & 0x0F0F0F0Fu;
-    n.lo[1] = w.y & 0x0F0F0F0Fu;
-    n.lo[2] = w.z & 0x0F0F0F0Fu;
-    n.lo[3] = w.w & 0x0F0F0F0Fu;
-    n.hi[0] = (w.x >> 4) & 0x0F0F0F0Fu;
-    n.hi[1] = (w.y >> 4) & 0x0F0F0F0Fu;
-    n.hi[2] = (w.z >> 4) & 0x0F0F0F0Fu;
-    n.hi[3] = (w.w >> 4) & 0x0F0F0F0Fu;
-    return n;
+__device__ __forceinline__ int dp4a_u8s8(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
-// a0: activation codes 0..15, a1: codes 16..31 (four per word, element order)
-__device__ __forceinline__ int block_dot(const Nibbles &q, uint4 a0, uint4 a1, int corr) {
-    int s = corr, t = 0;   // two independent chains; the int32 sum is exact in any order
-    s = __dp4a((int)q.lo[0], (int)a0.x, s);
-    t = __dp4a((int)q.lo[1], (int)a0.y, t);
-    s = __dp4a((int)q.lo[2], (int)a0.z, s);
-    t = __dp4a((int)q.lo[3], (int)a0.w, t);
-    s = __dp4a((int)q.hi[0], (int)a1.x, s);
-    t = __dp4a((int)q.hi[1], (int)a1.y, t);
-    s = __dp4a((int)q.hi[2], (int)a1.z, s);
-    t = __dp4a((int)q.hi[3], (int)a1.w, t);
-    return s + t;
+// w: the 16 code bytes of a block; a0: activation codes 0..15, a1: codes 16..31
+__device__ __forceinline__ int block_dot(uint4 w, uint4 a0, uint4 a1, int corr) {
+    int lo = corr, hi = 0;
+    lo = dp4a_u8s8(w.x & 0x0F0F0F0Fu, a0.x, lo);
+    hi = dp4a_u8s8(w.x & 0xF0F0F0F0u, a1.x, hi);
+    lo = dp4a_u8s8(w.y & 0x0F0F0F0Fu, a0.y, lo);
+    hi = dp4a_u8s8(w.y & 0xF0F0F0F0u, a1.y, hi);
+    lo = dp4a_u8s8(w.z & 0x0F0F0F0Fu, a0.z, lo);
+    hi = dp4a_u8s8(w.z & 0xF0F0F0F0u, a1.z, hi);
+    lo = dp4a_u8s8(w.w & 0x0F0F0F0Fu, a0.w, lo);
+    hi = dp4a_u8s8(w.w & 0xF0F0F0F0u, a1.w, hi);
+    return lo + (hi >> 4);
 }
 
 // D(16x8, f32) += A(16x16, f16, row) . B(16x8, f16, col)
