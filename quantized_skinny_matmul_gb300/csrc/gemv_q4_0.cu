@@ -418,19 +418,50 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(Shape<CWT>::M
             }
         }
         }
-    } else {   // plain coalesced loads of the slice's wdata image (the bulk-copy queue carries the weights)
+    } else {   // plain coalesced loads of the slice's wdata image (the bulk-copy queue carries the weights),
+               // eight per thread in flight at a time
         const uint4 *src = reinterpret_cast<const uint4 *>(p.wdata + (size_t)s * im.bytes);
         uint4 *dsts = reinterpret_cast<uint4 *>(act);
-        for (int i = tid; i < (int)(im.bytes / 16); i += CONSUMERS) dsts[i] = __ldcg(src + i);
+        const int n16 = (int)(im.bytes / 16);
+#pragma unroll 1
+        for (int i0 = 0; i0 < n16; i0 += 8 * CONSUMERS) {
+            uint4 v[8];
+#pragma unroll
+            for (int b = 0; b < 8; b++) {
+                const int i = i0 + b * CONSUMERS + tid;
+                if (i < n16) v[b] = __ldcg(src + i);
+            }
+#pragma unroll
+            for (int b = 0; b < 8; b++) {
+                const int i = i0 + b * CONSUMERS + tid;
+                if (i < n16) dsts[i] = v[b];
+            }
+        }
     }
     consumers_sync<CONSUMERS>();
     bool failed = false;
 
-    float acc[TPW][MT];   // one accumulator per tile position this warp owns
+    // dp4a path (up to four rows): one accumulator per tile position this warp owns and row.
+    // MMA path (eight rows and more): per position, block parity (even / odd blocks, the
+    // two halves the dp4a path keeps in lanes jh = 0, 1), activation-row tile and fragment
+    // element; the same sums in the same order.
+    constexpr bool MMA = MT >= 8;
+    constexpr int NTL = MMA ? MT / 8 : 1;
+    float acc[TPW][MMA ? 1 : MT];
+    float hacc[MMA ? TPW : 1][2][NTL][4];
 #pragma unroll
     for (int tw = 0; tw < TPW; tw++)
 #pragma unroll
-        for (int m = 0; m < MT; m++) acc[tw][m] = 0.0f;
+        for (int m = 0; m < (MMA ? 1 : MT); m++) acc[tw][m] = 0.0f;
+#pragma unroll
+    for (int tw = 0; tw < (MMA ? TPW : 1); tw++)
+#pragma unroll
+        for (int e = 0; e < 2; e++)
+#pragma unroll
+            for (int nt = 0; nt < NTL; nt++)
+#pragma unroll
+                for (int i = 0; i < 4; i++) hacc[tw][e][nt][i] = 0.0f;
+    const int fg = lane >> 2, ft = lane & 3;           // m16n8k16 fragment coordinates
 
     int slot = 0;
     uint32_t phase = 0;
@@ -463,18 +494,69 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(Shape<CWT>::M
                         const uint4 a1 = lds128(a + mm * im.row_bytes + 16);
                         const float2 sc = act_sc[mm * nblkmax + blk];
                         const int sumi = block_dot(q, a0, a1, __float_as_int(sc.y));
-                        acc[tw][m] = fmaf(d4 * sc.x, (float)sumi, acc[tw][m]);
+                        acc[tw][MMA ? 0 : m] = fmaf(d4 * sc.x, (float)sumi, acc[tw][MMA ? 0 : m]);
                     }
                 }
+            };
+            // The same tile with tensor-core MMAs (m16n8k16, fp16 in, f32 out).  Weight rows are
+            // the MMA rows, activation rows its columns.  Thread (fg, ft) takes code word ft of
+            // rows fg and fg + 8: its low nibbles are elements 4ft .. 4ft+3 of the block, the
+            // k slots 2ft, 2ft+1, 2ft+8, 2ft+9 of the first MMA; the high nibbles (elements
+            // 16 + 4ft ..) fill the same slots of the second.  The activation fragments take the
+            // matching elements, so the two MMAs add all 32 products.  (q - 8) and the Q8_0
+            // codes are exact in fp16 and every partial sum is an integer below 2^24, so the
+            // f32 result is the exact block dot sumi.
+            auto tile_mma = [&](const int tw, const int ti) {
+                const int tl = u + ti;
+                const uint8_t *tile = ring + (size_t)slot * CHUNK_BYTES + ti * TILE_BYTES;
+                const uint2 s0 = *reinterpret_cast<const uint2 *>(tile + TILE_SCALE_OFFSET + fg * 8);
+                const uint2 s1 = *reinterpret_cast<const uint2 *>(tile + TILE_SCALE_OFFSET + (fg + 8) * 8);
+#pragma unroll
+                for (int jb = 0; jb < 4; jb++) {
+                    const uint32_t w0 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg) * 16 + 4 * ft);
+                    const uint32_t w1 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg + 8) * 16 + 4 * ft);
+                    uint32_t alo[4], ahi[4];
+                    q4_to_f16x2(w0 & 0x0F0F0F0Fu, alo[0], alo[2]);
+                    q4_to_f16x2(w1 & 0x0F0F0F0Fu, alo[1], alo[3]);
+                    q4_to_f16x2((w0 >> 4) & 0x0F0F0F0Fu, ahi[0], ahi[2]);
+                    q4_to_f16x2((w1 >> 4) & 0x0F0F0F0Fu, ahi[1], ahi[3]);
+                    const uint32_t sw0 = jb & 2 ? s0.y : s0.x, sw1 = jb & 2 ? s1.y : s1.x;
+                    const float d4r0 = (jb & 1) ? half_hi(sw0) : half_lo(sw0);   // row fg
+                    const float d4r1 = (jb & 1) ? half_hi(sw1) : half_lo(sw1);   // row fg + 8
+                    const int blk = 4 * tl + jb;
+#pragma unroll
+                    for (int nt = 0; nt < NTL; nt++) {
+                        // rows past M repeat row M-1: no branch, and their sums are never stored
+                        const int mb = min(8 * nt + fg, p.M - 1);
+                        const uint8_t *ab = act + im.codes + (size_t)mb * im.row_bytes + (size_t)blk * 32 + 4 * ft;
+                        uint32_t blo[2], bhi[2];
+                        q8_to_f16x2(*reinterpret_cast<const uint32_t *>(ab), blo[0], blo[1]);
+                        q8_to_f16x2(*reinterpret_cast<const uint32_t *>(ab + 16), bhi[0], bhi[1]);
+                        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        mma_f16_16x8x16(d, alo[0], alo[1], alo[2], alo[3], blo[0], blo[1]);
+                        mma_f16_16x8x16(d, ahi[0], ahi[1], ahi[2], ahi[3], bhi[0], bhi[1]);
+                        const int mc0 = min(8 * nt + 2 * ft, p.M - 1), mc1 = min(8 * nt + 2 * ft + 1, p.M - 1);
+                        const float d8c0 = act_sc[mc0 * nblkmax + blk].x, d8c1 = act_sc[mc1 * nblkmax + blk].x;
+                        float *h = hacc[MMA ? tw : 0][jb & 1][nt];
+                        h[0] = fmaf(d4r0 * d8c0, d[0], h[0]);   // row fg,     activation row 2ft
+                        h[1] = fmaf(d4r0 * d8c1, d[1], h[1]);   // row fg,     activation row 2ft + 1
+                        h[2] = fmaf(d4r1 * d8c0, d[2], h[2]);   // row fg + 8, activation row 2ft
+                        h[3] = fmaf(d4r1 * d8c1, d[3], h[3]);   // row fg + 8, activation row 2ft + 1
+                    }
+                }
+            };
+            auto tile = [&](const int tw, const int ti) {
+                if constexpr (MMA) tile_mma(tw, ti);
+                else tile_dot(tw, ti);
             };
             if (!failed) {
                 if (u1 - u >= CHUNK_TILES) {                   // a full chunk: no per-tile test
 #pragma unroll
-                    for (int tw = 0; tw < TPW; tw++) tile_dot(tw, warp + CW * tw);
+                    for (int tw = 0; tw < TPW; tw++) tile(tw, warp + CW * tw);
                 } else {
 #pragma unroll
                     for (int tw = 0; tw < TPW; tw++)
-                        if (warp + CW * tw < u1 - u) tile_dot(tw, warp + CW * tw);
+                        if (warp + CW * tw < u1 - u) tile(tw, warp + CW * tw);
                 }
             }
             __syncwarp();
@@ -486,14 +568,28 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(Shape<CWT>::M
         }
 
         // ---- row group g of this slice is complete: add the partials of the 16 tile positions
+        if constexpr (MMA) {
 #pragma unroll
-        for (int tw = 0; tw < TPW; tw++)
+            for (int tw = 0; tw < TPW; tw++)
 #pragma unroll
-            for (int m = 0; m < MT; m++) {
-                const float other = __shfl_down_sync(0xffffffffu, acc[tw][m], 16);   // blocks jh+1 of the row
-                if (lane < 16) red[(warp + CW * tw) * outs + m * 16 + n] = acc[tw][m] + other;
-                acc[tw][m] = 0.0f;
-            }
+                for (int nt = 0; nt < NTL; nt++)
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int row = fg + 8 * (i >> 1), m = 8 * nt + 2 * ft + (i & 1);
+                        red[(warp + CW * tw) * outs + m * 16 + row] = hacc[tw][0][nt][i] + hacc[tw][1][nt][i];
+                        hacc[tw][0][nt][i] = 0.0f;
+                        hacc[tw][1][nt][i] = 0.0f;
+                    }
+        } else {
+#pragma unroll
+            for (int tw = 0; tw < TPW; tw++)
+#pragma unroll
+                for (int m = 0; m < MT; m++) {
+                    const float other = __shfl_down_sync(0xffffffffu, acc[tw][m], 16);   // blocks jh+1 of the row
+                    if (lane < 16) red[(warp + CW * tw) * outs + m * 16 + n] = acc[tw][m] + other;
+                    acc[tw][m] = 0.0f;
+                }
+        }
         consumers_sync<CONSUMERS>();
         if (tid < outs) {
             float v = 0.0f;

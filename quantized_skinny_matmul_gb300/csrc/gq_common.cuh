@@ -202,6 +202,26 @@ __device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], uint32_t a0, uint
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Four codes 0..15 (one per byte) -> two half2 of (q - 8), exact: the bytes become the
+// low mantissa bits of 1024 + q, and 1032 is subtracted.
+__device__ __forceinline__ void q4_to_f16x2(uint32_t v, uint32_t &h01, uint32_t &h23) {
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+    uint32_t a = __byte_perm(v, 0x64646464u, 0x4140u), b = __byte_perm(v, 0x64646464u, 0x4342u);
+    __half2 x = __hsub2(*reinterpret_cast<__half2 *>(&a), bias), y = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
+    h01 = *reinterpret_cast<uint32_t *>(&x);
+    h23 = *reinterpret_cast<uint32_t *>(&y);
+}
+
+// Four int8 codes -> two half2, exact: the bytes plus 128 become 1024 + 128 + q, less 1152.
+__device__ __forceinline__ void q8_to_f16x2(uint32_t v, uint32_t &h01, uint32_t &h23) {
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+    v ^= 0x80808080u;
+    uint32_t a = __byte_perm(v, 0x64646464u, 0x4140u), b = __byte_perm(v, 0x64646464u, 0x4342u);
+    __half2 x = __hsub2(*reinterpret_cast<__half2 *>(&a), bias), y = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
+    h01 = *reinterpret_cast<uint32_t *>(&x);
+    h23 = *reinterpret_cast<uint32_t *>(&y);
+}
+
 __device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))); }
 __device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
 
