@@ -92,12 +92,16 @@ __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + 
 // blocks][32 bytes], element order) and per (row, block) the pair
 // (f32 scale fp16(d), int32 -8 * sum of the codes).
 struct Image {
+    // Rows are padded by 16 bytes (codes) and one float2 (scales) so that the eight
+    // activation rows one MMA fragment reads fall in different shared-memory banks.
     size_t row_bytes, codes, scales, bytes;
+    int sc_stride;                                  // float2 per row of scales
     __host__ __device__ Image(int M, int ntmax) {
-        row_bytes = (size_t)4 * ntmax * 32;
+        row_bytes = (size_t)4 * ntmax * 32 + 16;
+        sc_stride = 4 * ntmax + 1;
         codes = 0;
         scales = (size_t)M * row_bytes;
-        bytes = align_up(scales + (size_t)M * 4 * ntmax * 8, 16);
+        bytes = align_up(scales + (size_t)M * sc_stride * 8, 16);
     }
 };
 
@@ -240,7 +244,7 @@ __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
         uint8_t *img = p.wdata + (size_t)s * im.bytes;
         img[im.codes + (size_t)m * im.row_bytes + (size_t)bl * 32 + lane] = (uint8_t)(q & 0xff);
         if (lane == 0)
-            reinterpret_cast<float2 *>(img + im.scales)[(size_t)m * 4 * p.ntmax + bl] =
+            reinterpret_cast<float2 *>(img + im.scales)[(size_t)m * im.sc_stride + bl] =
                 make_float2(__half2float(__float2half_rn(d)), __int_as_float(-8 * qsum));
     }
 }
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(Shape<CWT>::M
     uint8_t *act = smem + L.act;
     const float2 *act_sc = reinterpret_cast<const float2 *>(act + im.scales);
     float *red = reinterpret_cast<float *>(smem + L.red);
-    const int nblkmax = 4 * p.ntmax;
+    const int sc_stride = im.sc_stride;
 
     pdl_wait();                                      // src1, or INIT's wdata, is complete
     if (p.fused) {
@@ -413,7 +417,7 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(Shape<CWT>::M
                 *reinterpret_cast<uint4 *>(act + im.codes + (size_t)m * im.row_bytes + (size_t)hb * 16) =
                     make_uint4(w[0], w[1], w[2], w[3]);
                 if ((hb & 1) == 0)
-                    reinterpret_cast<float2 *>(act + im.scales)[m * 4 * p.ntmax + bl] =
+                    reinterpret_cast<float2 *>(act + im.scales)[m * im.sc_stride + bl] =
                         make_float2(__half2float(__float2half_rn(d)), __int_as_float(-8 * qs));
             }
         }
@@ -492,7 +496,7 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(Shape<CWT>::M
                         const int mm = MT > 4 ? m : min(m, p.M - 1);
                         const uint4 a0 = lds128(a + mm * im.row_bytes);
                         const uint4 a1 = lds128(a + mm * im.row_bytes + 16);
-                        const float2 sc = act_sc[mm * nblkmax + blk];
+                        const float2 sc = act_sc[mm * sc_stride + blk];
                         const int sumi = block_dot(q, a0, a1, __float_as_int(sc.y));
                         acc[tw][MMA ? 0 : m] = fmaf(d4 * sc.x, (float)sumi, acc[tw][MMA ? 0 : m]);
                     }
@@ -536,7 +540,7 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(Shape<CWT>::M
                         mma_f16_16x8x16(d, alo[0], alo[1], alo[2], alo[3], blo[0], blo[1]);
                         mma_f16_16x8x16(d, ahi[0], ahi[1], ahi[2], ahi[3], bhi[0], bhi[1]);
                         const int mc0 = min(8 * nt + 2 * ft, p.M - 1), mc1 = min(8 * nt + 2 * ft + 1, p.M - 1);
-                        const float d8c0 = act_sc[mc0 * nblkmax + blk].x, d8c1 = act_sc[mc1 * nblkmax + blk].x;
+                        const float d8c0 = act_sc[mc0 * sc_stride + blk].x, d8c1 = act_sc[mc1 * sc_stride + blk].x;
                         float *h = hacc[MMA ? tw : 0][jb & 1][nt];
                         h[0] = fmaf(d4r0 * d8c0, d[0], h[0]);   // row fg,     activation row 2ft
                         h[1] = fmaf(d4r0 * d8c1, d[1], h[1]);   // row fg,     activation row 2ft + 1
