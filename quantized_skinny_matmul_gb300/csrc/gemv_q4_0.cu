@@ -58,7 +58,6 @@ namespace {
 
 constexpr int CHUNK_TILES = 16;                    // tiles per chunk = tile positions
 constexpr int PRODUCERS = 2;                       // producer warps (bulk-copy issue rate is per warp)
-constexpr int FIXUPS = 1;                          // fix-up warps
 
 // CTA shapes: 8 consumer warps (two CTAs per SM, so the next product's CTA can
 // stream its weights beside this one) or 16 (one CTA per SM, for the ALU work
@@ -70,10 +69,11 @@ struct Shape {
     static constexpr int CW = CWT;                          // consumer warps
     static constexpr int TPW = CHUNK_TILES / CWT;           // tile positions per consumer warp
     static constexpr int PRODUCER_WARP = CWT;               // .. + PRODUCERS - 1
+    static constexpr int FIXUPS = CWT == 8 ? 1 : 2;         // fix-up warps (registers: at most 5 warps
+                                                            // of 96 per scheduler, 6 of 80 in the pair)
     static constexpr int FIXUP_WARP = CWT + PRODUCERS;      // .. + FIXUPS - 1
     static constexpr int THREADS = (CWT + PRODUCERS + FIXUPS) * 32;
     static constexpr int CONSUMERS = CWT * 32;
-    static constexpr int MAX_REGS = CWT == 8 ? 88 : 96;     // two CTAs of 11 warps, or one of 19
     static constexpr int FUSED_LOADS = 4;                   // float4 per consumer thread and round of the fused INIT
 };
 constexpr int CHUNK_BYTES = CHUNK_TILES * TILE_BYTES;
@@ -83,7 +83,7 @@ constexpr int FIX_BATCH = 8;                       // partials one fix-up lane l
 constexpr int FUSED_ROUNDS = 2;                    // load rounds of the fused INIT (more: a separate INIT is faster)
 constexpr size_t ACT_BUDGET = 112 * 1024;          // wdata image of one slice
 constexpr size_t SMEM_LIMIT = 227 * 1024;
-constexpr size_t SMEM_HALF = 113 * 1024;           // two CTAs per SM: the next product's CTA fits beside
+constexpr size_t SMEM_HALF = 113 * 1024;           // half of the shared memory of an SM
 constexpr int MIN_SLOTS_HALF = 4;
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -252,11 +252,12 @@ __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
 // ---------------------------------------------------------------------------
 // COMPUTE
 // ---------------------------------------------------------------------------
-template <int MT, int CWT>
-__global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(Shape<CWT>::MAX_REGS) gemv_q4_0_kernel(const Params p) {
+template <int MT, int CWT, int REGS>
+__global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4_0_kernel(const Params p) {
     using SH = Shape<CWT>;
     constexpr int CW = SH::CW, TPW = SH::TPW, CONSUMERS = SH::CONSUMERS, THREADS = SH::THREADS;
     constexpr int PRODUCER_WARP = SH::PRODUCER_WARP, FIXUP_WARP = SH::FIXUP_WARP, FUSED_LOADS = SH::FUSED_LOADS;
+    constexpr int FIXUPS = SH::FIXUPS;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int s = blockIdx.x / p.Gs, ci = blockIdx.x % p.Gs;
@@ -635,6 +636,10 @@ gq_status allow_smem(Kernel kernel, int which) {
     if (dev >= 0 && dev < MAX_DEV && g_smem_set[dev][which].load(std::memory_order_acquire)) return GQ_OK;
     st = check_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(SMEM_LIMIT - 1024)),
                     "gemv_q4_0 shared-memory attribute");
+    if (st == GQ_OK)   // all of the unified L1 as shared memory: two CTAs of the 8-warp shape fit
+        st = check_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             (int)cudaSharedmemCarveoutMaxShared),
+                        "gemv_q4_0 carveout attribute");
     if (st == GQ_OK && dev >= 0 && dev < MAX_DEV) g_smem_set[dev][which].store(true, std::memory_order_release);
     return st;
 }
@@ -653,29 +658,35 @@ Plan plan(int N16, int NT, int MT) {
     return q;
 }
 
-// Instantiated kernels: activation rows per tile (MT) and consumer warps (CW).
+// Instantiated kernels: activation rows per tile (MT), consumer warps (CW) and the
+// register cap.  A scheduler holds 16 K registers.  The 8-warp shape (11 warps) would
+// fit two CTAs per SM at 80 registers; at 88 it runs one per SM, which measured
+// faster on sequences of products of different shapes (the INIT grid of a product
+// that needs one, and the next product's CTAs, then find room).  The 16-warp shape
+// (20 warps) fits one CTA per SM at 96.
 struct Variant {
-    int mt, cw, consumers, threads, fused_loads;
+    int mt, cw, regs, consumers, threads, fused_loads;
     void (*kernel)(Params);
 };
 
-template <int MT, int CW>
+template <int MT, int CW, int REGS>
 constexpr Variant variant() {
-    return {MT, CW, Shape<CW>::CONSUMERS, Shape<CW>::THREADS, Shape<CW>::FUSED_LOADS, gemv_q4_0_kernel<MT, CW>};
+    return {MT, CW, REGS, Shape<CW>::CONSUMERS, Shape<CW>::THREADS, Shape<CW>::FUSED_LOADS,
+            gemv_q4_0_kernel<MT, CW, REGS>};
 }
 
-const Variant VARIANTS[] = {variant<1, 8>(), variant<1, 16>(), variant<2, 16>(),
-                            variant<4, 16>(), variant<8, 16>(), variant<16, 16>()};
+const Variant VARIANTS[] = {variant<1, 8, 88>(),  variant<1, 16, 96>(), variant<2, 16, 96>(),
+                            variant<4, 16, 96>(), variant<8, 16, 96>(), variant<16, 16, 96>()};
 constexpr int N_VARIANTS = sizeof(VARIANTS) / sizeof(VARIANTS[0]);
 
-// One activation row: 8 consumer warps and two CTAs per SM, so that the next
-// product's CTA streams its weights beside this one.  More rows: 16 warps and
-// one CTA per SM for the ALU work.
+// One activation row: 8 consumer warps.  More rows: 16 warps for the ALU work.
 int consumer_warps_for(int M) { return M == 1 ? 8 : 16; }
 
-const Variant *variant_for(int mt, int cw) {
+int regs_for(int cw) { return cw == 16 ? 96 : 88; }
+
+const Variant *variant_for(int mt, int cw, int regs) {
     for (int i = 0; i < N_VARIANTS; i++)
-        if (VARIANTS[i].mt == mt && VARIANTS[i].cw == cw) return &VARIANTS[i];
+        if (VARIANTS[i].mt == mt && VARIANTS[i].cw == cw && VARIANTS[i].regs == regs) return &VARIANTS[i];
     return nullptr;
 }
 
@@ -719,11 +730,14 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
         p.ntmax = q.ntmax;
         p.Gs = q.Gs;
         p.maxfix = q.maxfix;
-        const Variant *kvp = variant_for(MT, consumer_warps_for(p.M));
+        const int cw = consumer_warps_for(p.M);
+        const int consumers = cw == 8 ? Shape<8>::CONSUMERS : Shape<16>::CONSUMERS;
+        const int fused_loads = cw == 8 ? Shape<8>::FUSED_LOADS : Shape<16>::FUSED_LOADS;
+        // fuse INIT when each consumer thread loads a few float4
+        p.fused = (int64_t)p.M * p.ntmax * 32 <= (int64_t)consumers * fused_loads * FUSED_ROUNDS ? 1 : 0;
+        const Variant *kvp = variant_for(MT, cw, regs_for(cw));
         if (!kvp) return fail(GQ_ERR_INVALID_ARG, "gemv_q4_0: no kernel for M=%d", p.M);
         const Variant &kv = *kvp;
-        // fuse INIT when each consumer thread loads a few float4
-        p.fused = (int64_t)p.M * p.ntmax * 32 <= (int64_t)kv.consumers * kv.fused_loads * FUSED_ROUNDS ? 1 : 0;
         // behind INIT (which waited for every earlier grid) the weights are final; otherwise only
         // a caller that declared its weights static lets the producers start before the wait
         p.early = (!p.fused || static_weights()) ? 1 : 0;
@@ -733,7 +747,8 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
         auto slots_for = [&](size_t budget) {
             return (int)std::min<size_t>(MAX_SLOTS, (budget - std::min(budget, fixed + 256)) / (CHUNK_BYTES + 16));
         };
-        // the 8-warp shape runs two CTAs per SM if the ring keeps MIN_SLOTS_HALF chunks
+        // the 8-warp shape keeps a ring of half the shared memory (MIN_SLOTS_HALF chunks at
+        // least), which measured faster than a full one
         p.slots = kv.cw == 8 ? slots_for(SMEM_HALF - 1024) : 0;
         if (p.slots < MIN_SLOTS_HALF) p.slots = slots_for(SMEM_LIMIT - 1024);
         p.slots = std::min(p.slots, env_int("GQ_GEMV_SLOTS", MAX_SLOTS)) & ~(PRODUCERS - 1);
