@@ -442,7 +442,36 @@ def extras(b, weights, C, hbm_peak, bf16_peak, bf16_sustained, args):
             st[f"M{M}"] = {"ms_per_token_pass": round(t * 1e3, 4), "tokens_per_s": round(M / t, 1),
                            "GB/s": round(stack_bytes / t / 1e9, 1), "frac_of_hbm": round(stack_bytes / t / 1e9 / hbm_peak, 4)}
         res["stack_32_layers"] = st
+
+        # the same stack with the products that share an input fused by row concatenation:
+        # Q|K|V (12288 x 4096) and gate|up (22016 x 4096): 4 products per layer instead of 7
+        names = [n for n, _, _ in synth.LAYER_SHAPES]
+        groups = [("attn_q", "attn_k", "attn_v"), ("attn_o",), ("ffn_gate", "ffn_up"), ("ffn_down",)]
+        fused = []
+        for l in range(synth.N_LAYERS):
+            fl = []
+            for grp in groups:
+                idx = [names.index(g) for g in grp]
+                Ns = [synth.LAYER_SHAPES[i][1] for i in idx]
+                K = synth.LAYER_SHAPES[idx[0]][2]
+                w = gq.concat_rows_q4_0([layers[l][i] for i in idx], Ns, K) if len(idx) > 1 else layers[l][idx[0]]
+                fl.append((w, sum(Ns), K))
+            fused.append(fl)
         del layers
+        sf = {"weight_bytes": stack_bytes, "products_per_layer": len(groups)}
+        for M in (1, 8):
+            xs = {K: b.acts(M, K, 600 + K + M) for K in (4096, 11008)}
+            outs = {N: torch.empty((M, N), device=b.dev) for _, N, _ in fused[0]}
+            ls = []
+            for l in range(synth.N_LAYERS):
+                for (w, N, K) in fused[l]:
+                    ls.append(lambda w=w, N=N, K=K, M=M, xs=xs, outs=outs:
+                              gq.gq_mul_mat_q4_0_f32(w, xs[K], outs[N], M, N, K))
+            t = b.time_launches(ls, max_graph=len(ls))
+            sf[f"M{M}"] = {"ms_per_token_pass": round(t * 1e3, 4), "tokens_per_s": round(M / t, 1),
+                           "GB/s": round(stack_bytes / t / 1e9, 1), "frac_of_hbm": round(stack_bytes / t / 1e9 / hbm_peak, 4)}
+        res["stack_32_layers_fused_qkv_gate_up"] = sf
+        del fused
     return res
 
 

@@ -236,6 +236,26 @@ def repack_q4_0(q4, N: int, K: int):
     return out
 
 
+def concat_rows_q4_0(repacked, Ns, K: int):
+    """Several repacked weight matrices with the same K as one matrix of sum(Ns) rows.
+
+    The repacked layout stores whole 16-row groups one after the other, so when
+    every N is a multiple of 16 the concatenated buffers are the repacked layout
+    of the stacked matrix: one product then computes [x W1^T | x W2^T | ...]
+    (for example Q, K and V, or gate and up, which share their input) with one
+    weight stream and one quantized copy of the activations.
+    """
+    import torch
+    if len(repacked) != len(Ns):
+        raise ValueError("one N per matrix")
+    for r, n in zip(repacked, Ns):
+        if n % 16:
+            raise ValueError(f"N={n} is not a multiple of 16: row groups would be padded")
+        if r.numel() != gq_q4_0_repacked_bytes(n, K):
+            raise ValueError(f"a buffer of {r.numel()} bytes is not the repacked layout of N={n}, K={K}")
+    return torch.cat([r.reshape(-1) for r in repacked])
+
+
 def mul_mat_q4_0_f32(q4_repacked, src1, N: int, path: int = GQ_PATH_AUTO, out=None):
     import torch
     M, K = src1.shape

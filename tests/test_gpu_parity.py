@@ -200,3 +200,18 @@ def test_full_size_sampled(oracle, M, N, K):
     dst16 = host(gq.mul_mat_f16_f32(dev(wb.view(np.int16)), dev(x)))
     ref16, T16 = oracle.mul_mat_f16_f32_at(wb, x, ms, ns)
     assert_within(dst16[ms, ns], ref16, T16, what="f16 full size")
+
+
+def test_concatenated_rows_equal_separate_products():
+    """Q/K/V-like matrices sharing an input: one product over the concatenated
+    repacked buffers equals the separate products, bit for bit."""
+    K = 768
+    Ns = (64, 48, 112)
+    ws = [synth.weights(60 + i, N, K) for i, N in enumerate(Ns)]
+    reps = [gq.repack_q4_0(gq.quantize_q4_0(dev(w)), N, K) for w, N in zip(ws, Ns)]
+    both = gq.concat_rows_q4_0(reps, Ns, K)
+    for M in (1, 3, 8, 16, 40):
+        x = dev(synth.activations(70 + M, M, K))
+        whole = host(gq.mul_mat_q4_0_f32(both, x, sum(Ns)))
+        parts = [host(gq.mul_mat_q4_0_f32(r, x, N)) for r, N in zip(reps, Ns)]
+        assert np.array_equal(whole, np.concatenate(parts, axis=1)), f"M={M}"
