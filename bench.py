@@ -391,7 +391,19 @@ def extras(b, weights, C, hbm_peak, bf16_peak, bf16_sustained, args):
     t = b.time_launches(ls)
     res["f16_m1"] = {"GB/s": round(sum(step_bytes_f16(1, N, K) for N, K in SHAPES) * C16 / t / 1e9, 1),
                      "frac_of_hbm": round(sum(step_bytes_f16(1, N, K) for N, K in SHAPES) * C16 / t / 1e9 / hbm_peak, 4)}
+    # the same weights in the 16 x 32 tile layout (gq_repack_f16), M = 1 and M = 8
+    r16 = [[gq.repack_f16(w) for w in ws] for ws in w16]
     del w16
+    for M in (1, 8):
+        xm = [b.acts(M, K, 320 + i) for i, (N, K) in enumerate(SHAPES)]
+        om = [torch.empty((M, N), device=b.dev) for N, K in SHAPES]
+        ls = [lambda c=c, i=i, N=N, K=K, M=M: gq.gq_mul_mat_f16r_f32(r16[c][i], xm[i], om[i], M, N, K)
+              for c in range(C16) for i, (N, K) in enumerate(SHAPES)]
+        t = b.time_launches(ls)
+        gbs = sum(step_bytes_f16(M, N, K) for N, K in SHAPES) * C16 / t / 1e9
+        res[f"f16r_m{M}"] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4),
+                             "us_per_step": round(t / C16 * 1e6, 2)}
+    del r16
 
     # M sweep on the two FFN shapes (Q4_0)
     sweep = {}
@@ -533,7 +545,7 @@ def cpu_baseline(seconds: float):
 
 
 def run_profile(spec: str):
-    """A few plain launches of one product, for ncu: KIND:M:N:K with KIND q4_0 | f16 | q4_0_tc | f16_tc."""
+    """A few plain launches of one product, for ncu: KIND:M:N:K with KIND q4_0 | f16 | f16r | q4_0_tc | f16_tc."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -547,6 +559,9 @@ def run_profile(spec: str):
     if kind.startswith("q4_0"):
         w = b.q4_weights(N, K, 2)
         fn = lambda: gq.gq_mul_mat_q4_0_f32_path(w, x, o, M, N, K, path)
+    elif kind == "f16r":
+        w = gq.repack_f16(b.f16_weights(N, K, 2))
+        fn = lambda: gq.gq_mul_mat_f16r_f32(w, x, o, M, N, K)
     else:
         w = b.f16_weights(N, K, 2)
         fn = lambda: gq.gq_mul_mat_f16_f32_path(w, x, o, M, N, K, path)

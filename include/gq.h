@@ -146,6 +146,24 @@ gq_status gq_mul_mat_q4_0_f32(const void *q4_repacked, const float *src1, float 
 gq_status gq_mul_mat_f16_f32(const void *src0_f16, const float *src1, float *dst,
                              int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
+/* F16 weights for decode.  gq_repack_f16 copies row-major F16 weights [N][K]
+ * into tiles of 16 rows x 32 columns (64 bytes per row, tile (g, t) of rows
+ * 16g.. and columns 32t.. at byte (g * K/32 + t) * 1024, rows past N zero):
+ * gq_f16_repacked_bytes(N, K) = ceil(N/16) * (K/32) * 1024 bytes, allocated by
+ * the caller, not overlapping src0_f16 (GQ_ERR_INVALID_ARG).  A 16-row tile is
+ * one contiguous kilobyte, the unit the GEMV streams.  gq_mul_mat_f16r_f32 is
+ * the product of gq_mul_mat_f16_f32 on that layout, for any M (16 activation
+ * rows per launch): the activations are rounded to fp16 and the f32 sums come
+ * from fp16 tensor instructions (relative error <= 2e-3 of sum |terms|; the
+ * results do not depend on timing).  It uses the stream's workspace like the
+ * other products.  (llama.cpp PR #1632, "Introduction": MUL_MAT with F16
+ * weights; the tile layout is this library's.) */
+size_t gq_f16_repacked_bytes(int64_t N, int64_t K);   /* 0 if N <= 0, K <= 0 or K % 32 */
+gq_status gq_repack_f16(const void *src0_f16, void *f16_repacked, int64_t N, int64_t K,
+                        cudaStream_t stream);
+gq_status gq_mul_mat_f16r_f32(const void *f16_repacked, const float *src1, float *dst,
+                              int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* Workspace.  The products keep a small device workspace per (device, stream):
  * partial sums of weight rows that several CTAs share, with per-row counters
  * that every launch leaves at zero, and (tensor-core path) the quantized

@@ -69,6 +69,9 @@ SIGNATURES = {
     "gq_get_m_threshold": ([], _I),
     "gq_debug_block_dots_q4_0": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_noalloc": ([_P, _P, _P, _I, _I, _I, _P], _S),
+    "gq_f16_repacked_bytes": ([_I, _I], ctypes.c_size_t),
+    "gq_repack_f16": ([_P, _P, _I, _I, _P], _S),
+    "gq_mul_mat_f16r_f32": ([_P, _P, _P, _I, _I, _I, _P], _S),
 }
 
 
@@ -204,6 +207,19 @@ def gq_mul_mat_q4_0_f32_noalloc(q4_repacked, src1, dst, M: int, N: int, K: int, 
                                              _stream(stream)), "gq_mul_mat_q4_0_f32_noalloc")
 
 
+def gq_f16_repacked_bytes(N: int, K: int) -> int:
+    return lib().gq_f16_repacked_bytes(N, K)
+
+
+def gq_repack_f16(src0_f16, f16_repacked, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_repack_f16(_ptr(src0_f16), _ptr(f16_repacked), N, K, _stream(stream)), "gq_repack_f16")
+
+
+def gq_mul_mat_f16r_f32(f16_repacked, src1, dst, M: int, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_mul_mat_f16r_f32(_ptr(f16_repacked), _ptr(src1), _ptr(dst), M, N, K, _stream(stream)),
+           "gq_mul_mat_f16r_f32")
+
+
 def gq_debug_block_dots_q4_0(q4_repacked, q8_blocks, sumi, M: int, N: int, K: int, stream=None) -> None:
     _check(lib().gq_debug_block_dots_q4_0(_ptr(q4_repacked), _ptr(q8_blocks), _ptr(sumi), M, N, K,
                                           _stream(stream)), "gq_debug_block_dots_q4_0")
@@ -270,4 +286,21 @@ def mul_mat_f16_f32(src0_f16, src1, path: int = GQ_PATH_AUTO, out=None):
     M = src1.shape[0]
     dst = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=src1.device)
     gq_mul_mat_f16_f32_path(src0_f16, src1, dst, M, N, K, path)
+    return dst
+
+
+def repack_f16(src0_f16):
+    """F16 CUDA tensor [N, K] -> the 16 x 32 tile layout of gq_repack_f16 (uint8)."""
+    import torch
+    N, K = src0_f16.shape
+    out = torch.empty(gq_f16_repacked_bytes(N, K), dtype=torch.uint8, device=src0_f16.device)
+    gq_repack_f16(src0_f16, out, N, K)
+    return out
+
+
+def mul_mat_f16r_f32(f16_repacked, src1, N: int, out=None):
+    import torch
+    M, K = src1.shape
+    dst = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=src1.device)
+    gq_mul_mat_f16r_f32(f16_repacked, src1, dst, M, N, K)
     return dst

@@ -77,6 +77,11 @@ struct Shape {
     static constexpr int FUSED_LOADS = 4;                   // float4 per consumer thread and round of the fused INIT
 };
 constexpr int CHUNK_BYTES = CHUNK_TILES * TILE_BYTES;
+// Repacked F16 weights: a tile is 16 rows x 32 columns, 64 bytes per row.
+constexpr int F16_TILE_COLS = 32;
+constexpr int F16_TILE_BYTES = 16 * F16_TILE_COLS * 2;
+__host__ __device__ constexpr int tile_bytes(bool f16) { return f16 ? F16_TILE_BYTES : TILE_BYTES; }
+__host__ __device__ constexpr int chunk_bytes(bool f16) { return CHUNK_TILES * tile_bytes(f16); }
 constexpr int MAX_SLOTS = 12;
 constexpr int PART_STRIDE = 16 * 16;               // floats of one partial (16 rows x 16 activation rows)
 constexpr int FIX_BATCH = 8;                       // partials one fix-up lane loads before adding them
@@ -94,11 +99,15 @@ __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + 
 struct Image {
     // Rows are padded by 16 bytes (codes) and one float2 (scales) so that the eight
     // activation rows one MMA fragment reads fall in different shared-memory banks.
+    // F16 rows take an odd number of 64-byte tiles: the two rows of a quarter warp's
+    // 16-byte loads then fill the 128 bytes of the banks once.
     size_t row_bytes, codes, scales, bytes;
     int sc_stride;                                  // float2 per row of scales
-    __host__ __device__ Image(int M, int ntmax) {
-        row_bytes = (size_t)4 * ntmax * 32 + 16;
-        sc_stride = 4 * ntmax + 1;
+    // Q4_0: Q8_0 codes [M][ntmax tiles x 128] then {d8, -8 sum q8} per block;
+    // F16: the activations in fp16, [M][ntmax tiles x 32], no scales.
+    __host__ __device__ Image(int M, int ntmax, bool f16 = false) {
+        row_bytes = f16 ? (size_t)(ntmax | 1) * F16_TILE_COLS * 2 : (size_t)4 * ntmax * 32 + 16;
+        sc_stride = f16 ? 0 : 4 * ntmax + 1;
         codes = 0;
         scales = (size_t)M * row_bytes;
         bytes = align_up(scales + (size_t)M * sc_stride * 8, 16);
@@ -123,11 +132,11 @@ struct Params {
 
 struct Layout {
     size_t bars, ring, act, red, total;
-    __host__ __device__ Layout(int MT, int M, int ntmax, int slots, int maxfix) {
-        const Image im(M, ntmax);
+    __host__ __device__ Layout(int MT, int M, int ntmax, int slots, int maxfix, bool f16 = false) {
+        const Image im(M, ntmax, f16);
         bars = 0;                                         // full[slots], empty[slots], act, fix[maxfix]
         ring = align_up((size_t)(2 * slots + 1 + maxfix) * 8, 128);
-        act = ring + (size_t)slots * CHUNK_BYTES;
+        act = ring + (size_t)slots * chunk_bytes(f16);
         red = act + im.bytes;
         total = red + (size_t)CHUNK_TILES * 16 * MT * 4;
     }
@@ -252,8 +261,9 @@ __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
 // ---------------------------------------------------------------------------
 // COMPUTE
 // ---------------------------------------------------------------------------
-template <int MT, int CWT, int REGS>
+template <int MT, int CWT, int REGS, bool F16W>
 __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4_0_kernel(const Params p) {
+    constexpr int TB = tile_bytes(F16W), CB = chunk_bytes(F16W);
     using SH = Shape<CWT>;
     constexpr int CW = SH::CW, TPW = SH::TPW, CONSUMERS = SH::CONSUMERS, THREADS = SH::THREADS;
     constexpr int PRODUCER_WARP = SH::PRODUCER_WARP, FIXUP_WARP = SH::FIXUP_WARP, FUSED_LOADS = SH::FUSED_LOADS;
@@ -269,8 +279,8 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
                                              (int)((int64_t)p.N16 * (ci + 1) / p.Gs) * nts, nts, 1)
                                   : Segments((int)((int64_t)T * ci / p.Gs), (int)((int64_t)T * (ci + 1) / p.Gs), nts,
                                              p.S);
-    const Layout L(MT, p.M, p.ntmax, p.slots, p.maxfix);
-    const Image im(p.M, p.ntmax);
+    const Layout L(MT, p.M, p.ntmax, p.slots, p.maxfix, F16W);
+    const Image im(p.M, p.ntmax, F16W);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + p.slots;
     uint64_t *actbar = empty + p.slots;
@@ -305,10 +315,10 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
                         failed = true;
                         break;
                     }
-                    const uint32_t bytes = (uint32_t)(min(CHUNK_TILES, u1 - u) * TILE_BYTES);
+                    const uint32_t bytes = (uint32_t)(min(CHUNK_TILES, u1 - u) * TB);
                     mbar_arrive_expect_tx(smem_addr(full + slot), bytes);
-                    bulk_g2s(smem_addr(ring + (size_t)slot * CHUNK_BYTES),
-                             p.w + ((size_t)g * p.NT + ts0 + u) * TILE_BYTES, bytes, smem_addr(full + slot));
+                    bulk_g2s(smem_addr(ring + (size_t)slot * CB),
+                             p.w + ((size_t)g * p.NT + ts0 + u) * TB, bytes, smem_addr(full + slot));
                 }
             }
         }
@@ -381,7 +391,31 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
     const int sc_stride = im.sc_stride;
 
     pdl_wait();                                      // src1, or INIT's wdata, is complete
-    if (p.fused) {
+    if constexpr (F16W) {
+        // INIT in the CTA: this slice's columns of the M activation rows in fp16 (round to
+        // nearest even), eight float4 loads in flight per thread
+        const int per_row = nts * (F16_TILE_COLS / 4);   // float4 of one row's slice
+        const int nf = p.M * per_row;
+#pragma unroll 1
+        for (int f0 = 0; f0 < nf; f0 += 8 * CONSUMERS) {
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int f = f0 + tid + CONSUMERS * i, m = f / per_row, c4 = f % per_row;
+                v[i] = f < nf ? ldg_f4(p.x + (size_t)m * p.K + (size_t)ts0 * F16_TILE_COLS + 4 * c4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int f = f0 + tid + CONSUMERS * i, m = f / per_row, c4 = f % per_row;
+                if (f < nf) {
+                    const __half2 lo = __floats2half2_rn(v[i].x, v[i].y), hi = __floats2half2_rn(v[i].z, v[i].w);
+                    *reinterpret_cast<uint2 *>(act + (size_t)m * im.row_bytes + 8 * c4) =
+                        make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+                }
+            }
+        }
+    } else if (p.fused) {
         // INIT in the CTA: Q8_0 of this slice's columns of the M activation rows.
         // Every load of a round is issued first (one round trip).  A thread holds half a
         // block (16 values, four float4) and the neighbouring lane the other
@@ -450,7 +484,7 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
     // MMA path (eight rows and more): per position, block parity (even / odd blocks, the
     // two halves the dp4a path keeps in lanes jh = 0, 1), activation-row tile and fragment
     // element; the same sums in the same order.
-    constexpr bool MMA = MT >= 8;
+    constexpr bool MMA = F16W || MT >= 8;
     constexpr int NTL = MMA ? MT / 8 : 1;
     float acc[TPW][MMA ? 1 : MT];
     float hacc[MMA ? TPW : 1][2][NTL][4];
@@ -550,8 +584,27 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
                     }
                 }
             };
+            // F16 weights: the tile is 16 rows x 32 columns as stored, 64 bytes per row.  Thread
+            // (fg, ft) takes elements 8ft .. 8ft+7 of rows fg and fg + 8 and of its activation
+            // row: the first four fill k slots 2ft, 2ft+1, 2ft+8, 2ft+9 of one MMA, the last four
+            // those of a second, so the two MMAs add the 32 products of the tile.
+            auto tile_f16 = [&](const int tw, const int ti) {
+                const int tl = u + ti;
+                const uint8_t *tile = ring + (size_t)slot * CB + ti * TB;
+                const uint4 wa = lds128(tile + fg * 64 + 16 * ft);
+                const uint4 wb = lds128(tile + (fg + 8) * 64 + 16 * ft);
+#pragma unroll
+                for (int nt = 0; nt < NTL; nt++) {
+                    const int mb = min(8 * nt + fg, p.M - 1);   // rows past M repeat row M-1
+                    const uint4 xb = lds128(act + (size_t)mb * im.row_bytes + (size_t)tl * 64 + 16 * ft);
+                    float *h = hacc[MMA ? tw : 0][0][nt];
+                    mma_f16_16x8x16(*reinterpret_cast<float(*)[4]>(h), wa.x, wb.x, wa.y, wb.y, xb.x, xb.y);
+                    mma_f16_16x8x16(*reinterpret_cast<float(*)[4]>(h), wa.z, wb.z, wa.w, wb.w, xb.z, xb.w);
+                }
+            };
             auto tile = [&](const int tw, const int ti) {
-                if constexpr (MMA) tile_mma(tw, ti);
+                if constexpr (F16W) tile_f16(tw, ti);
+                else if constexpr (MMA) tile_mma(tw, ti);
                 else tile_dot(tw, ti);
             };
             if (!failed) {
@@ -613,9 +666,9 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
     }
 }
 
-int slices_for(int NT, int MT) {
+int slices_for(int NT, int MT, bool f16) {
     int S = 1;
-    while (S < 8 && 2 * S <= NT && Image(MT, (NT + S - 1) / S).bytes > ACT_BUDGET) S *= 2;
+    while (S < 8 && 2 * S <= NT && Image(MT, (NT + S - 1) / S, f16).bytes > ACT_BUDGET) S *= 2;
     return S;
 }
 
@@ -626,7 +679,8 @@ int env_int(const char *name, int dflt) {
 
 // The dynamic shared-memory limit is raised once per (device, kernel).
 constexpr int MAX_DEV = 64;
-std::atomic<bool> g_smem_set[MAX_DEV][8];
+constexpr int MAX_VARIANTS = 16;
+std::atomic<bool> g_smem_set[MAX_DEV][MAX_VARIANTS];
 
 template <typename Kernel>
 gq_status allow_smem(Kernel kernel, int which) {
@@ -648,9 +702,9 @@ struct Plan {
     int S, ntmax, Gs, maxfix;
 };
 
-Plan plan(int N16, int NT, int MT) {
+Plan plan(int N16, int NT, int MT, bool f16 = false) {
     Plan q;
-    q.S = slices_for(NT, MT);
+    q.S = slices_for(NT, MT, f16);
     q.ntmax = (NT + q.S - 1) / q.S;
     q.Gs = std::max(1, std::min(sm_count() / q.S, N16));   // S == 1: every CTA gets >= 1 row group
     // row groups a CTA touches: at most ceil(N16 / Gs) + 2 (one mbarrier each)
@@ -665,48 +719,64 @@ Plan plan(int N16, int NT, int MT) {
 // that needs one, and the next product's CTAs, then find room).  The 16-warp shape
 // (20 warps) fits one CTA per SM at 96.
 struct Variant {
-    int mt, cw, regs, consumers, threads, fused_loads;
+    int mt, cw, regs;
+    bool f16;
+    int consumers, threads, fused_loads;
     void (*kernel)(Params);
 };
 
-template <int MT, int CW, int REGS>
+template <int MT, int CW, int REGS, bool F16W = false>
 constexpr Variant variant() {
-    return {MT, CW, REGS, Shape<CW>::CONSUMERS, Shape<CW>::THREADS, Shape<CW>::FUSED_LOADS,
-            gemv_q4_0_kernel<MT, CW, REGS>};
+    return {MT, CW, REGS, F16W, Shape<CW>::CONSUMERS, Shape<CW>::THREADS, Shape<CW>::FUSED_LOADS,
+            gemv_q4_0_kernel<MT, CW, REGS, F16W>};
 }
 
-const Variant VARIANTS[] = {variant<1, 8, 88>(),  variant<1, 16, 96>(), variant<2, 16, 96>(),
-                            variant<4, 16, 96>(), variant<8, 16, 96>(), variant<16, 16, 96>()};
+const Variant VARIANTS[] = {variant<1, 8, 88>(),         variant<1, 16, 96>(),       variant<2, 16, 96>(),
+                            variant<4, 16, 96>(),        variant<8, 16, 96>(),       variant<16, 16, 96>(),
+                            variant<8, 8, 88, true>(),   variant<16, 16, 96, true>()};
 constexpr int N_VARIANTS = sizeof(VARIANTS) / sizeof(VARIANTS[0]);
+static_assert(N_VARIANTS <= MAX_VARIANTS, "one shared-memory flag per variant");
 
 // One activation row: 8 consumer warps.  More rows: 16 warps for the ALU work.
 int consumer_warps_for(int M) { return M == 1 ? 8 : 16; }
 
 int regs_for(int cw) { return cw == 16 ? 96 : 88; }
 
-const Variant *variant_for(int mt, int cw, int regs) {
+const Variant *variant_for(int mt, int cw, int regs, bool f16) {
     for (int i = 0; i < N_VARIANTS; i++)
-        if (VARIANTS[i].mt == mt && VARIANTS[i].cw == cw && VARIANTS[i].regs == regs) return &VARIANTS[i];
+        if (VARIANTS[i].mt == mt && VARIANTS[i].cw == cw && VARIANTS[i].regs == regs && VARIANTS[i].f16 == f16)
+            return &VARIANTS[i];
     return nullptr;
 }
 
 }  // namespace
 
-void gemv_q4_0_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes) {
-    const int N16 = (int)((N + 15) / 16), NT = (int)((K + TILE_COLS - 1) / TILE_COLS);
+void gemv_workspace(bool f16, int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes) {
+    const int N16 = (int)((N + 15) / 16);
+    const int NT = f16 ? (int)(K / F16_TILE_COLS) : (int)((K + TILE_COLS - 1) / TILE_COLS);
     size_t db = 0;
-    for (int MT = 1; MT <= 16; MT *= 2) {
-        const Plan q = plan(N16, NT, MT);
+    for (int MT = f16 ? 8 : 1; MT <= 16; MT *= 2) {
+        const Plan q = plan(N16, NT, MT, f16);
         const size_t parts = (size_t)N16 * q.S * 2 * PART_STRIDE * sizeof(float);
-        const size_t images = (size_t)q.S * Image(MT, q.ntmax).bytes;
+        const size_t images = f16 ? 0 : (size_t)q.S * Image(MT, q.ntmax).bytes;   // F16: INIT is always in the CTA
         db = std::max(db, align_up(parts, 256) + images);
     }
     *counter_bytes = (size_t)N16 * sizeof(unsigned int);
     *data_bytes = db;
 }
 
-gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
-                                const Workspace &ws, cudaStream_t s) {
+void gemv_q4_0_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes) {
+    gemv_workspace(false, N, K, counter_bytes, data_bytes);
+}
+
+void gemv_f16r_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes) {
+    gemv_workspace(true, N, K, counter_bytes, data_bytes);
+}
+
+namespace {
+
+gq_status launch_gemv_with(bool f16, const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                           const Workspace &ws, cudaStream_t s) {
     Params p{};
     p.w = (const uint8_t *)rep;
     p.status = device_status_word();
@@ -715,7 +785,7 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
     p.K = (int)K;
     p.nb = (int)(K / QK);
     p.N16 = (int)((N + 15) / 16);
-    p.NT = (int)((K + TILE_COLS - 1) / TILE_COLS);
+    p.NT = f16 ? (int)(K / F16_TILE_COLS) : (int)((K + TILE_COLS - 1) / TILE_COLS);
 
     gq_status st = GQ_OK;
     p.cnt = reinterpret_cast<unsigned int *>(ws.counters);
@@ -724,38 +794,40 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
         p.M = (int)std::min<int64_t>(16, M - m0);
         p.x = x + m0 * K;
         p.dst = dst + m0 * N;
-        const int MT = p.M <= 1 ? 1 : p.M <= 2 ? 2 : p.M <= 4 ? 4 : p.M <= 8 ? 8 : 16;
-        const Plan q = plan(p.N16, p.NT, MT);
+        // F16: tensor-core tiles of 8 or 16 activation rows
+        const int MT = f16 ? (p.M <= 8 ? 8 : 16) : p.M <= 1 ? 1 : p.M <= 2 ? 2 : p.M <= 4 ? 4 : p.M <= 8 ? 8 : 16;
+        const Plan q = plan(p.N16, p.NT, MT, f16);
         p.S = q.S;
         p.ntmax = q.ntmax;
         p.Gs = q.Gs;
         p.maxfix = q.maxfix;
-        const int cw = consumer_warps_for(p.M);
+        const int cw = f16 ? (MT == 8 ? 8 : 16) : consumer_warps_for(p.M);
         const int consumers = cw == 8 ? Shape<8>::CONSUMERS : Shape<16>::CONSUMERS;
         const int fused_loads = cw == 8 ? Shape<8>::FUSED_LOADS : Shape<16>::FUSED_LOADS;
-        // fuse INIT when each consumer thread loads a few float4
-        p.fused = (int64_t)p.M * p.ntmax * 32 <= (int64_t)consumers * fused_loads * FUSED_ROUNDS ? 1 : 0;
-        const Variant *kvp = variant_for(MT, cw, regs_for(cw));
-        if (!kvp) return fail(GQ_ERR_INVALID_ARG, "gemv_q4_0: no kernel for M=%d", p.M);
+        // fuse INIT when each consumer thread loads a few float4 (F16: always)
+        p.fused = f16 || (int64_t)p.M * p.ntmax * 32 <= (int64_t)consumers * fused_loads * FUSED_ROUNDS ? 1 : 0;
+        const Variant *kvp = variant_for(MT, cw, regs_for(cw), f16);
+        if (!kvp) return fail(GQ_ERR_INVALID_ARG, "gemv: no kernel for M=%d", p.M);
         const Variant &kv = *kvp;
         // behind INIT (which waited for every earlier grid) the weights are final; otherwise only
         // a caller that declared its weights static lets the producers start before the wait
         p.early = (!p.fused || static_weights()) ? 1 : 0;
         p.part = reinterpret_cast<float *>(ws.data);
         p.wdata = ws.data + align_up((size_t)p.N16 * p.S * 2 * PART_STRIDE * sizeof(float), 256);
-        const size_t fixed = Layout(MT, p.M, p.ntmax, 0, p.maxfix).total;
+        const size_t fixed = Layout(MT, p.M, p.ntmax, 0, p.maxfix, f16).total;
         auto slots_for = [&](size_t budget) {
-            return (int)std::min<size_t>(MAX_SLOTS, (budget - std::min(budget, fixed + 256)) / (CHUNK_BYTES + 16));
+            return (int)std::min<size_t>(MAX_SLOTS,
+                                         (budget - std::min(budget, fixed + 256)) / (chunk_bytes(f16) + 16));
         };
-        // the 8-warp shape keeps a ring of half the shared memory (MIN_SLOTS_HALF chunks at
+        // the 8-warp Q4_0 shape keeps a ring of half the shared memory (MIN_SLOTS_HALF chunks at
         // least), which measured faster than a full one
-        p.slots = kv.cw == 8 ? slots_for(SMEM_HALF - 1024) : 0;
+        p.slots = kv.cw == 8 && !f16 ? slots_for(SMEM_HALF - 1024) : 0;
         if (p.slots < MIN_SLOTS_HALF) p.slots = slots_for(SMEM_LIMIT - 1024);
         p.slots = std::min(p.slots, env_int("GQ_GEMV_SLOTS", MAX_SLOTS)) & ~(PRODUCERS - 1);
         if (p.slots < 2)
-            return fail(GQ_ERR_INVALID_ARG, "gemv_q4_0: N=%lld K=%lld leaves no room for the weight ring",
+            return fail(GQ_ERR_INVALID_ARG, "gemv: N=%lld K=%lld leaves no room for the weight ring",
                         (long long)N, (long long)K);
-        const size_t smem = Layout(MT, p.M, p.ntmax, p.slots, p.maxfix).total;
+        const size_t smem = Layout(MT, p.M, p.ntmax, p.slots, p.maxfix, f16).total;
         st = allow_smem(kv.kernel, (int)(&kv - VARIANTS));
         if (st != GQ_OK) return st;
         const int threads = kv.threads;
@@ -778,10 +850,27 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
         cfg.gridDim = dim3((unsigned)(p.S * p.Gs), 1, 1);
         cfg.blockDim = dim3((unsigned)threads, 1, 1);
         cfg.dynamicSmemBytes = smem;
-        st = check_cuda(cudaLaunchKernelEx(&cfg, kv.kernel, p), "gemv_q4_0 launch");
+        st = check_cuda(cudaLaunchKernelEx(&cfg, kv.kernel, p), "gemv launch");
         if (st != GQ_OK) return st;
     }
     return GQ_OK;
+}
+
+}  // namespace
+
+gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                                const Workspace &ws, cudaStream_t s) {
+    return launch_gemv_with(false, rep, x, dst, M, N, K, ws, s);
+}
+
+gq_status launch_gemv_f16r(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t s) {
+    size_t cb, db;
+    gemv_f16r_workspace(N, K, &cb, &db);
+    Workspace ws;
+    gq_status st = get_workspace(s, cb, db, &ws);
+    if (st != GQ_OK) return st;
+    return launch_gemv_with(true, rep, x, dst, M, N, K, ws, s);
 }
 
 gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,

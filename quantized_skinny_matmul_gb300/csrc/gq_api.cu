@@ -213,6 +213,10 @@ gq_status gq_reserve_workspace(int64_t M, int64_t N, int64_t K, cudaStream_t str
     GQ_TRY(check_device());
     size_t cb = 0, db = 0;
     gemv_q4_0_workspace(N, K, &cb, &db);
+    size_t cb16 = 0, db16 = 0;
+    gemv_f16r_workspace(N, K, &cb16, &db16);
+    cb = std::max(cb, cb16);
+    db = std::max(db, db16);
     if (M > gq_get_m_threshold()) db = std::max(db, tc_workspace_bytes(M, K));
     Workspace ws;
     GQ_TRY(get_workspace(stream, cb, db, &ws));
@@ -286,6 +290,34 @@ gq_status gq_mul_mat_q4_0_f32(const void *q4_repacked, const float *src1, float 
 gq_status gq_mul_mat_f16_f32(const void *src0_f16, const float *src1, float *dst, int64_t M, int64_t N, int64_t K,
                              cudaStream_t stream) {
     return gq_mul_mat_f16_f32_path(src0_f16, src1, dst, M, N, K, GQ_PATH_AUTO, stream);
+}
+
+size_t gq_f16_repacked_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % QK) return 0;
+    return (size_t)((N + 15) / 16) * (size_t)(K / 32) * 1024;
+}
+
+gq_status gq_repack_f16(const void *src0_f16, void *f16_repacked, int64_t N, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(1, N, K));
+    GQ_TRY(check_ptr(src0_f16, "src0_f16"));
+    GQ_TRY(check_ptr(f16_repacked, "f16_repacked"));
+    const uintptr_t a = (uintptr_t)src0_f16, b = (uintptr_t)f16_repacked;
+    if (a < b + gq_f16_repacked_bytes(N, K) && b < a + (size_t)N * (size_t)K * 2)
+        return fail(GQ_ERR_INVALID_ARG, "src0_f16 and f16_repacked overlap");
+    GQ_TRY(check_device());
+    GQ_TRY(launch_repack_f16(src0_f16, f16_repacked, N, K, stream));
+    return ok();
+}
+
+gq_status gq_mul_mat_f16r_f32(const void *f16_repacked, const float *src1, float *dst, int64_t M, int64_t N,
+                              int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(M, N, K));
+    GQ_TRY(check_ptr(f16_repacked, "f16_repacked"));
+    GQ_TRY(check_ptr(src1, "src1"));
+    GQ_TRY(check_ptr(dst, "dst"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_gemv_f16r(f16_repacked, src1, dst, M, N, K, stream));
+    return ok();
 }
 
 gq_status gq_debug_block_dots_q4_0(const void *q4_repacked, const void *q8_blocks, int32_t *sumi, int64_t M,

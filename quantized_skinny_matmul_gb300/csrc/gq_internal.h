@@ -49,6 +49,12 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
                                 const Workspace &ws, cudaStream_t s);
 gq_status launch_gemv_f16(const void *w16, const float *x, float *dst, int64_t M, int64_t N,
                           int64_t K, cudaStream_t s);
+// F16 weights repacked into 16 x 32 tiles: the repack, and the GEMV on them (the Q4_0
+// GEMV's pipeline with fp16 MMAs on the tiles as stored).
+gq_status launch_repack_f16(const void *w16, void *rep, int64_t N, int64_t K, cudaStream_t s);
+void gemv_f16r_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes);
+gq_status launch_gemv_f16r(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t s);
 // Tensor-core tiles (tcgen05) for M >= 32; workspace: the fp16 activations.
 size_t tc_workspace_bytes(int64_t M, int64_t K);
 gq_status launch_tc_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,

@@ -95,6 +95,22 @@ __global__ void repack_q4_0_kernel(const uint8_t *__restrict__ q4, uint8_t *__re
     }
 }
 
+// F16 weights [N][K] -> tiles of 16 rows x 32 columns, 64 bytes per row, tile (g, t)
+// of row group g and column tile t at (g * NT + t) * 1024.  One thread per 16-byte
+// piece (64 per tile); rows past N are zeros.
+__global__ void repack_f16_kernel(const uint8_t *__restrict__ w, uint8_t *__restrict__ out, int64_t N, int64_t K,
+                                  int64_t NT, int64_t pieces) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < pieces;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = i / 64, pc = i % 64;
+        const int64_t g = tile / NT, t = tile % NT;
+        const int64_t row = 16 * g + pc / 4, col = 32 * t + 8 * (pc % 4);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < N) v = *reinterpret_cast<const uint4 *>(w + (row * K + col) * 2);
+        *reinterpret_cast<uint4 *>(out + i * 16) = v;
+    }
+}
+
 int grid_for(int64_t work_items, int threads) {
     int64_t blocks = (work_items + threads - 1) / threads;
     const int64_t cap = (int64_t)sm_count() * 16;
@@ -124,6 +140,12 @@ gq_status launch_repack_q4_0(const void *q4, void *rep, int64_t N, int64_t K, cu
     const int64_t blocks = (threads + 255) / 256;
     repack_q4_0_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint8_t *)q4, (uint8_t *)rep, N, nb, NT, ntiles);
     return check_cuda(cudaGetLastError(), "repack_q4_0 launch");
+}
+
+gq_status launch_repack_f16(const void *w16, void *rep, int64_t N, int64_t K, cudaStream_t s) {
+    const int64_t NT = K / 32, pieces = (N + 15) / 16 * NT * 64;
+    repack_f16_kernel<<<grid_for(pieces, 256), 256, 0, s>>>((const uint8_t *)w16, (uint8_t *)rep, N, K, NT, pieces);
+    return check_cuda(cudaGetLastError(), "repack_f16 launch");
 }
 
 }  // namespace gq

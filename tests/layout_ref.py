@@ -34,3 +34,27 @@ def repack_loops(q4: np.ndarray) -> np.ndarray:
                     for i in range(2):
                         out[base + 1024 + (r * 4 + j) * 2 + i] = q4[n, b, i] if real else 0
     return out
+
+
+def repack_f16_ref(w16: np.ndarray) -> np.ndarray:
+    """F16 bits [N, K] (uint16) -> the 16 x 32 tile layout of gq_repack_f16, as bytes."""
+    N, K = w16.shape
+    N16, NT = -(-N // 16), K // 32
+    P = np.zeros((N16 * 16, K), np.uint16)
+    P[:N] = w16
+    T = P.reshape(N16, 16, NT, 32).transpose(0, 2, 1, 3)        # [g, t, r, c]
+    return np.ascontiguousarray(T).reshape(-1).view(np.uint8)
+
+
+def repack_f16_loops(w16: np.ndarray) -> np.ndarray:
+    """The same layout element by element, in the words of the header (small sizes)."""
+    N, K = w16.shape
+    N16, NT = -(-N // 16), K // 32
+    out = np.zeros(N16 * NT * 512, np.uint16)
+    for g in range(N16):
+        for t in range(NT):
+            for r in range(16):
+                for c in range(32):
+                    n = 16 * g + r
+                    out[((g * NT + t) * 1024 + r * 64 + 2 * c) // 2] = w16[n, 32 * t + c] if n < N else 0
+    return out.view(np.uint8)

@@ -57,6 +57,9 @@ def test_sizes(lib):
     assert gq.gq_q4_0_repacked_bytes(4096, 11008) == 4096 * 344 * 18
     assert gq.gq_q4_0_repacked_bytes(17, 96) == 2 * 1 * 1152
     assert gq.gq_q4_0_bytes(4, 33) == 0 and gq.gq_q4_0_repacked_bytes(0, 32) == 0
+    assert gq.gq_f16_repacked_bytes(4096, 4096) == 4096 * 4096 * 2
+    assert gq.gq_f16_repacked_bytes(17, 96) == 2 * 3 * 1024
+    assert gq.gq_f16_repacked_bytes(16, 48) == 0
 
 
 FAKE = 0x10000            # 16-byte aligned, never dereferenced: checks fail first
@@ -85,6 +88,10 @@ def test_argument_checks_other_entries(lib):
     assert lib.gq_quantize_q4_0(ODD, FAKE, 4, 64, None) == gq.GQ_ERR_MISALIGNED
     assert lib.gq_quantize_rows_q8_0(FAKE, 0, 4, 64, None) == gq.GQ_ERR_INVALID_ARG
     assert lib.gq_repack_q4_0(FAKE, FAKE, 4, 64, None) == gq.GQ_ERR_INVALID_ARG   # overlap
+    assert lib.gq_repack_f16(FAKE, FAKE + 256, 4, 64, None) == gq.GQ_ERR_INVALID_ARG   # overlap
+    assert lib.gq_repack_f16(FAKE, FAKE, 4, 48, None) == gq.GQ_ERR_INVALID_ARG   # K % 32
+    assert lib.gq_mul_mat_f16r_f32(FAKE, FAKE, ODD, 1, 64, 64, None) == gq.GQ_ERR_MISALIGNED
+    assert lib.gq_mul_mat_f16r_f32(0, FAKE, FAKE, 1, 64, 64, None) == gq.GQ_ERR_INVALID_ARG
     assert lib.gq_debug_block_dots_q4_0(FAKE, FAKE, ODD, 1, 16, 64, None) == gq.GQ_ERR_MISALIGNED
     assert lib.gq_mul_mat_q4_0_f32_path(FAKE, FAKE, FAKE, 1, 64, 64, 7, None) == gq.GQ_ERR_INVALID_ARG
     assert lib.gq_set_m_threshold(-1) == gq.GQ_ERR_INVALID_ARG

@@ -11,3 +11,11 @@ def test_layout_statements_agree(N, nb):
     rng = np.random.default_rng(N * 100 + nb)
     q4 = rng.integers(0, 256, size=(N, nb, 18), dtype=np.uint8)
     assert np.array_equal(repack_ref(q4), repack_loops(q4))
+
+
+@pytest.mark.parametrize("N,K", [(16, 32), (37, 96), (1, 64), (33, 160)])
+def test_f16_layout_statements_agree(N, K):
+    from layout_ref import repack_f16_ref, repack_f16_loops
+    rng = np.random.default_rng(N * 1000 + K)
+    w16 = rng.integers(0, 1 << 16, size=(N, K), dtype=np.uint16)
+    assert np.array_equal(repack_f16_ref(w16), repack_f16_loops(w16))
