@@ -59,18 +59,19 @@ namespace {
 constexpr int CHUNK_TILES = 16;                    // tiles per chunk = tile positions
 constexpr int PRODUCERS = 2;                       // producer warps (bulk-copy issue rate is per warp)
 
-// CTA shapes: 8 consumer warps (two CTAs per SM, so the next product's CTA can
-// stream its weights beside this one) or 16 (one CTA per SM, for the ALU work
-// of several activation rows).  A consumer warp keeps one accumulator per tile
-// position of a chunk, and the row-group sum adds the 16 positions in order:
-// every output is the same sum, in the same order, for both shapes.
-template <int CWT>
+// CTA shapes: 8 consumer warps (with no fix-up warp, two CTAs per SM, so the next
+// product's CTA streams its weights beside this one) or 16 (one CTA per SM, for
+// the ALU work of several activation rows).  A consumer warp keeps one
+// accumulator per tile position of a chunk, and the row-group sum adds the 16
+// positions in order: every output is the same sum, in the same order, for both
+// shapes.  A scheduler holds 16 K registers: five warps of 96 (16 + 2 + 2 warps,
+// one CTA) or, twice over, five of 88 (8 + 2 + 0 warps, two CTAs).
+template <int CWT, int FIXW = (CWT == 8 ? 1 : 2)>
 struct Shape {
     static constexpr int CW = CWT;                          // consumer warps
     static constexpr int TPW = CHUNK_TILES / CWT;           // tile positions per consumer warp
     static constexpr int PRODUCER_WARP = CWT;               // .. + PRODUCERS - 1
-    static constexpr int FIXUPS = CWT == 8 ? 1 : 2;         // fix-up warps (registers: at most 5 warps
-                                                            // of 96 per scheduler, 6 of 80 in the pair)
+    static constexpr int FIXUPS = FIXW;                     // fix-up warps (none: no shared row group)
     static constexpr int FIXUP_WARP = CWT + PRODUCERS;      // .. + FIXUPS - 1
     static constexpr int THREADS = (CWT + PRODUCERS + FIXUPS) * 32;
     static constexpr int CONSUMERS = CWT * 32;
@@ -85,11 +86,12 @@ __host__ __device__ constexpr int chunk_bytes(bool f16) { return CHUNK_TILES * t
 constexpr int MAX_SLOTS = 12;
 constexpr int PART_STRIDE = 16 * 16;               // floats of one partial (16 rows x 16 activation rows)
 constexpr int FIX_BATCH = 8;                       // partials one fix-up lane loads before adding them
-constexpr int FUSED_ROUNDS = 2;                    // load rounds of the fused INIT (more: a separate INIT is faster)
+constexpr int FUSED_ROUNDS = 3;                    // load rounds of the fused INIT (more: a separate INIT is faster)
 constexpr size_t ACT_BUDGET = 112 * 1024;          // wdata image of one slice
 constexpr size_t SMEM_LIMIT = 227 * 1024;
 constexpr size_t SMEM_HALF = 113 * 1024;           // half of the shared memory of an SM
 constexpr int MIN_SLOTS_HALF = 4;
+constexpr int PF_KB = 160;                         // L2 prefetch distance beyond the ring, per CTA
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -126,6 +128,7 @@ struct Params {
     int nb, N16, NT;
     int S, Gs;               // slices, CTAs per slice (grid = S * Gs)
     int slots, ntmax, maxfix;
+    int pf;                  // L2 prefetch distance of the producers, in chunks
     int fused;               // 1: no INIT launch, each CTA quantizes its slice of src1
     int early;               // 1: the producers may read the weights before the grids in front finished
 };
@@ -138,7 +141,7 @@ struct Layout {
         ring = align_up((size_t)(2 * slots + 1 + maxfix) * 8, 128);
         act = ring + (size_t)slots * chunk_bytes(f16);
         red = act + im.bytes;
-        total = red + (size_t)CHUNK_TILES * 16 * MT * 4;
+        total = red + 2 * (size_t)CHUNK_TILES * 16 * MT * 4;   // two buffers: row groups alternate
     }
 };
 
@@ -261,10 +264,10 @@ __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
 // ---------------------------------------------------------------------------
 // COMPUTE
 // ---------------------------------------------------------------------------
-template <int MT, int CWT, int REGS, bool F16W>
-__global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4_0_kernel(const Params p) {
+template <int MT, int CWT, int REGS, bool F16W, int FIXW>
+__global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) gemv_q4_0_kernel(const Params p) {
     constexpr int TB = tile_bytes(F16W), CB = chunk_bytes(F16W);
-    using SH = Shape<CWT>;
+    using SH = Shape<CWT, FIXW>;
     constexpr int CW = SH::CW, TPW = SH::TPW, CONSUMERS = SH::CONSUMERS, THREADS = SH::THREADS;
     constexpr int PRODUCER_WARP = SH::PRODUCER_WARP, FIXUP_WARP = SH::FIXUP_WARP, FUSED_LOADS = SH::FUSED_LOADS;
     constexpr int FIXUPS = SH::FIXUPS;
@@ -297,38 +300,62 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
 
     // ---------------------------------------------------------------- producers
     // Producer warp pw issues the chunks k = pw (mod PRODUCERS); the ring has an
-    // even number of slots, so each producer refills only its own slots.
+    // even number of slots, so each producer refills only its own slots.  The ring
+    // alone keeps too few bytes in flight for HBM; each producer also keeps L2
+    // prefetches of its chunks up to p.pf chunks ahead of its copies, so that the
+    // copies are served from L2.  A prefetch moves nothing into the CTA and L2 is
+    // where all accesses to device memory meet, so prefetches may run before the
+    // grids in front have finished; the copies wait for them when the weights are
+    // not declared static.
     if (warp >= PRODUCER_WARP && warp < PRODUCER_WARP + PRODUCERS) {
         const int pw = warp - PRODUCER_WARP;
-        if (!p.early) pdl_wait();   // the weights may still be written by the grid in front
-        if (lane == 0) {
-            int k = 0;
-            bool failed = false;
-            for (int j = 0; j < seg.n && !failed; j++) {
+        // chunk k of this CTA's sequence: source and size; false past the last chunk
+        auto chunk_at = [&](int k, const uint8_t *&src, uint32_t &bytes) -> bool {
+            for (int j = 0; j < seg.n; j++) {
                 int g, u0, u1;
                 seg.get(j, g, u0, u1);
-                for (int u = u0; u < u1; u += CHUNK_TILES, k++) {
-                    if (k % PRODUCERS != pw) continue;
-                    const int slot = k % p.slots;
-                    if (k >= p.slots &&
-                        !mbar_wait(smem_addr(empty + slot), (uint32_t)(((k / p.slots) - 1) & 1), p.status)) {
-                        failed = true;
-                        break;
-                    }
-                    const uint32_t bytes = (uint32_t)(min(CHUNK_TILES, u1 - u) * TB);
-                    mbar_arrive_expect_tx(smem_addr(full + slot), bytes);
-                    bulk_g2s(smem_addr(ring + (size_t)slot * CB),
-                             p.w + ((size_t)g * p.NT + ts0 + u) * TB, bytes, smem_addr(full + slot));
+                const int n = (u1 - u0 + CHUNK_TILES - 1) / CHUNK_TILES;
+                if (k < n) {
+                    const int u = u0 + k * CHUNK_TILES;
+                    src = p.w + ((size_t)g * p.NT + ts0 + u) * TB;
+                    bytes = (uint32_t)(min(CHUNK_TILES, u1 - u) * TB);
+                    return true;
                 }
+                k -= n;
+            }
+            return false;
+        };
+        int kp = p.early ? pw + p.slots : pw;   // next chunk to prefetch (early: the ring's first copies go first)
+        auto prefetch_to = [&](int kend) {
+            const uint8_t *src;
+            uint32_t bytes;
+            for (; kp < kend && chunk_at(kp, src, bytes); kp += PRODUCERS) bulk_prefetch_l2(src, bytes);
+        };
+        if (!p.early) {
+            if (lane == 0) prefetch_to(p.pf);
+            pdl_wait();   // the weights may still be written by the grid in front
+        }
+        if (lane == 0) {
+            const uint64_t policy = l2_evict_first_policy();   // every weight byte is read once
+            const uint8_t *src;
+            uint32_t bytes;
+            for (int k = pw; chunk_at(k, src, bytes); k += PRODUCERS) {
+                const int slot = k % p.slots;
+                if (k >= p.slots &&
+                    !mbar_wait(smem_addr(empty + slot), (uint32_t)(((k / p.slots) - 1) & 1), p.status))
+                    break;
+                mbar_arrive_expect_tx(smem_addr(full + slot), bytes);
+                bulk_g2s_hint(smem_addr(ring + (size_t)slot * CB), src, bytes, smem_addr(full + slot), policy);
+                prefetch_to(k + p.pf);
             }
         }
         return;
     }
 
     // ---------------------------------------------------------------- fix-up
-    if (warp >= FIXUP_WARP) {
+    if (FIXUPS > 0 && warp >= FIXUP_WARP) {   // (the launch has no shared row group when FIXUPS == 0)
         pdl_wait();
-        for (int f = warp - FIXUP_WARP; f < seg.nshared; f += FIXUPS) {
+        for (int f = warp - FIXUP_WARP; f < seg.nshared; f += (FIXUPS > 0 ? FIXUPS : 1)) {
             const bool ok = mbar_wait(smem_addr(fixbar + f), 0u, p.status);
             if (!__all_sync(0xffffffffu, ok)) break;
             int g, u0, u1;
@@ -391,7 +418,54 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
     const int sc_stride = im.sc_stride;
 
     pdl_wait();                                      // src1, or INIT's wdata, is complete
-    if constexpr (F16W) {
+    // One activation row and one K slice (whole row groups, every segment starts at tile 0):
+    // the tile at position warp + CW * tw of a chunk has index t = warp (mod CW), so each
+    // consumer warp reads only the Q8_0 blocks of its own tiles.  It quantizes them itself,
+    // all its loads issued at once, and no barrier of the CTA is needed.  For the chunk
+    // starting at tile u, lane (tw, jb, q) takes the eight values 8q .. 8q+7 of block jb of
+    // the tile u + warp + CW * tw.
+    constexpr bool LAZY = !F16W && MT == 1;
+    const bool lazy = LAZY && p.S == 1 && p.fused;
+    const int lz_tw = lane >> 4, lz_jb = (lane >> 2) & 3, lz_q = lane & 3;
+    auto lz_load = [&](const int u, float4 (&v)[2]) {
+        const int t = u + warp + CW * lz_tw, blk = 4 * t + lz_jb;
+        const bool live = t < p.NT && blk < p.nb;
+        const float *src = p.x + (size_t)blk * QK + 8 * lz_q;
+        v[0] = live ? ldg_f4(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[1] = live ? ldg_f4(src + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto lz_quant = [&](const int u, const float4 (&v)[2]) {
+        const int t = u + warp + CW * lz_tw, blk = 4 * t + lz_jb;
+        float am = fmaxf(absmax4(v[0]), absmax4(v[1]));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+        const float d = am / 127.0f;
+        uint32_t w[2];
+        pack_q8_words<2>(v, q8_scale(d), w);
+        int qs = sum_q8x4(w[0]) + sum_q8x4(w[1]);
+        qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+        qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+        if (t < p.NT) {
+            *reinterpret_cast<uint2 *>(act + im.codes + (size_t)blk * 32 + 8 * lz_q) = make_uint2(w[0], w[1]);
+            if (lz_q == 0)
+                reinterpret_cast<float2 *>(act + im.scales)[blk] =
+                    make_float2(__half2float(__float2half_rn(d)), __int_as_float(-8 * qs));
+        }
+    };
+    if (lazy) {
+        constexpr int LZ_BATCH = 2;                      // chunks whose values are loaded at once
+        const int nchunk = (p.NT + CHUNK_TILES - 1) / CHUNK_TILES;
+#pragma unroll 1
+        for (int c0 = 0; c0 < nchunk; c0 += LZ_BATCH) {
+            float4 v[LZ_BATCH][2];
+#pragma unroll
+            for (int c = 0; c < LZ_BATCH; c++) lz_load((c0 + c) * CHUNK_TILES, v[c]);   // past NT: zeros
+#pragma unroll
+            for (int c = 0; c < LZ_BATCH; c++)
+                if (c0 + c < nchunk) lz_quant((c0 + c) * CHUNK_TILES, v[c]);        // warp-uniform
+        }
+        __syncwarp();
+    } else if constexpr (F16W) {
         // INIT in the CTA: this slice's columns of the M activation rows in fp16 (round to
         // nearest even), eight float4 loads in flight per thread
         const int per_row = nts * (F16_TILE_COLS / 4);   // float4 of one row's slice
@@ -477,7 +551,7 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
             }
         }
     }
-    consumers_sync<CONSUMERS>();
+    if (!lazy) consumers_sync<CONSUMERS>();
     bool failed = false;
 
     // dp4a path (up to four rows): one accumulator per tile position this warp owns and row.
@@ -625,7 +699,11 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
             }
         }
 
-        // ---- row group g of this slice is complete: add the partials of the 16 tile positions
+        // ---- row group g of this slice is complete: add the partials of the 16 tile positions.
+        // Row groups alternate between two buffers: the threads that add row group j's
+        // partials are done before they reach the barrier of row group j + 1, which every
+        // writer of row group j + 2 has passed, so one barrier per row group suffices.
+        float *redb = red + (j & 1) * CHUNK_TILES * outs;
         if constexpr (MMA) {
 #pragma unroll
             for (int tw = 0; tw < TPW; tw++)
@@ -634,7 +712,7 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
                         const int row = fg + 8 * (i >> 1), m = 8 * nt + 2 * ft + (i & 1);
-                        red[(warp + CW * tw) * outs + m * 16 + row] = hacc[tw][0][nt][i] + hacc[tw][1][nt][i];
+                        redb[(warp + CW * tw) * outs + m * 16 + row] = hacc[tw][0][nt][i] + hacc[tw][1][nt][i];
                         hacc[tw][0][nt][i] = 0.0f;
                         hacc[tw][1][nt][i] = 0.0f;
                     }
@@ -644,7 +722,7 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
 #pragma unroll
                 for (int m = 0; m < MT; m++) {
                     const float other = __shfl_down_sync(0xffffffffu, acc[tw][m], 16);   // blocks jh+1 of the row
-                    if (lane < 16) red[(warp + CW * tw) * outs + m * 16 + n] = acc[tw][m] + other;
+                    if (lane < 16) redb[(warp + CW * tw) * outs + m * 16 + n] = acc[tw][m] + other;
                     acc[tw][m] = 0.0f;
                 }
         }
@@ -652,7 +730,7 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
         if (tid < outs) {
             float v = 0.0f;
 #pragma unroll
-            for (int pos = 0; pos < CHUNK_TILES; pos++) v += red[pos * outs + tid];
+            for (int pos = 0; pos < CHUNK_TILES; pos++) v += redb[pos * outs + tid];
             if (j < seg.nshared) {                     // this CTA's part of a shared row group
                 const int slot_i = ci == owner(T, p.Gs, g * nts) ? 0 : 1;
                 p.part[(((size_t)g * p.S + s) * 2 + slot_i) * PART_STRIDE + tid] = v;
@@ -661,14 +739,17 @@ __global__ void __launch_bounds__(Shape<CWT>::THREADS) __maxnreg__(REGS) gemv_q4
                 if (m < p.M && row < p.N) p.dst[(size_t)m * p.N + row] = v;
             }
         }
-        consumers_sync<CONSUMERS>();                   // red is reused; the partial is written
-        if (j < seg.nshared && tid == 0) mbar_arrive(smem_addr(fixbar + j));
+        if (j < seg.nshared) {                         // the partial is written: the fix-up may read it
+            consumers_sync<CONSUMERS>();
+            if (tid == 0) mbar_arrive(smem_addr(fixbar + j));
+        }
     }
 }
 
-int slices_for(int NT, int MT, bool f16) {
+// K slices for M activation rows: the fewest (a power of two) whose images fit the budget.
+int slices_for(int NT, int M, bool f16) {
     int S = 1;
-    while (S < 8 && 2 * S <= NT && Image(MT, (NT + S - 1) / S, f16).bytes > ACT_BUDGET) S *= 2;
+    while (S < 8 && 2 * S <= NT && Image(M, (NT + S - 1) / S, f16).bytes > ACT_BUDGET) S *= 2;
     return S;
 }
 
@@ -702,9 +783,9 @@ struct Plan {
     int S, ntmax, Gs, maxfix;
 };
 
-Plan plan(int N16, int NT, int MT, bool f16 = false) {
+Plan plan(int N16, int NT, int M, bool f16 = false) {
     Plan q;
-    q.S = slices_for(NT, MT, f16);
+    q.S = slices_for(NT, M, f16);
     q.ntmax = (NT + q.S - 1) / q.S;
     q.Gs = std::max(1, std::min(sm_count() / q.S, N16));   // S == 1: every CTA gets >= 1 row group
     // row groups a CTA touches: at most ceil(N16 / Gs) + 2 (one mbarrier each)
@@ -712,28 +793,32 @@ Plan plan(int N16, int NT, int MT, bool f16 = false) {
     return q;
 }
 
-// Instantiated kernels: activation rows per tile (MT), consumer warps (CW) and the
-// register cap.  A scheduler holds 16 K registers.  The 8-warp shape (11 warps) would
-// fit two CTAs per SM at 80 registers; at 88 it runs one per SM, which measured
-// faster on sequences of products of different shapes (the INIT grid of a product
-// that needs one, and the next product's CTAs, then find room).  The 16-warp shape
-// (20 warps) fits one CTA per SM at 96.
+// Instantiated kernels: activation rows per tile (MT), consumer warps (CW), the
+// register cap and the fix-up warps.  The 8-warp shape without fix-up warps (one
+// K slice: no row group is shared) runs two CTAs per SM, each with half of the
+// shared memory, so that the CTAs of the next product in the stream are resident
+// and stream their weights while this product finishes; with several K slices it
+// keeps one fix-up warp and runs one CTA per SM.  The 16-warp shape (20 warps)
+// runs one CTA per SM at 96 registers.
 struct Variant {
     int mt, cw, regs;
     bool f16;
+    int fixw;
     int consumers, threads, fused_loads;
     void (*kernel)(Params);
 };
 
-template <int MT, int CW, int REGS, bool F16W = false>
+template <int MT, int CW, int REGS, bool F16W, int FIXW>
 constexpr Variant variant() {
-    return {MT, CW, REGS, F16W, Shape<CW>::CONSUMERS, Shape<CW>::THREADS, Shape<CW>::FUSED_LOADS,
-            gemv_q4_0_kernel<MT, CW, REGS, F16W>};
+    using SH = Shape<CW, FIXW>;
+    return {MT, CW, REGS, F16W, FIXW, SH::CONSUMERS, SH::THREADS, SH::FUSED_LOADS,
+            gemv_q4_0_kernel<MT, CW, REGS, F16W, FIXW>};
 }
 
-const Variant VARIANTS[] = {variant<1, 8, 88>(),         variant<1, 16, 96>(),       variant<2, 16, 96>(),
-                            variant<4, 16, 96>(),        variant<8, 16, 96>(),       variant<16, 16, 96>(),
-                            variant<8, 8, 88, true>(),   variant<16, 16, 96, true>()};
+const Variant VARIANTS[] = {
+    variant<1, 8, 88, false, 0>(),  variant<1, 8, 88, false, 1>(),  variant<2, 16, 96, false, 2>(),
+    variant<4, 16, 96, false, 2>(), variant<8, 16, 96, false, 2>(), variant<16, 16, 96, false, 2>(),
+    variant<8, 8, 88, true, 0>(),   variant<8, 8, 88, true, 1>(),   variant<16, 16, 96, true, 2>()};
 constexpr int N_VARIANTS = sizeof(VARIANTS) / sizeof(VARIANTS[0]);
 static_assert(N_VARIANTS <= MAX_VARIANTS, "one shared-memory flag per variant");
 
@@ -742,9 +827,10 @@ int consumer_warps_for(int M) { return M == 1 ? 8 : 16; }
 
 int regs_for(int cw) { return cw == 16 ? 96 : 88; }
 
-const Variant *variant_for(int mt, int cw, int regs, bool f16) {
+const Variant *variant_for(int mt, int cw, int regs, bool f16, int fixw) {
     for (int i = 0; i < N_VARIANTS; i++)
-        if (VARIANTS[i].mt == mt && VARIANTS[i].cw == cw && VARIANTS[i].regs == regs && VARIANTS[i].f16 == f16)
+        if (VARIANTS[i].mt == mt && VARIANTS[i].cw == cw && VARIANTS[i].regs == regs && VARIANTS[i].f16 == f16 &&
+            VARIANTS[i].fixw == fixw)
             return &VARIANTS[i];
     return nullptr;
 }
@@ -755,10 +841,10 @@ void gemv_workspace(bool f16, int64_t N, int64_t K, size_t *counter_bytes, size_
     const int N16 = (int)((N + 15) / 16);
     const int NT = f16 ? (int)(K / F16_TILE_COLS) : (int)((K + TILE_COLS - 1) / TILE_COLS);
     size_t db = 0;
-    for (int MT = f16 ? 8 : 1; MT <= 16; MT *= 2) {
-        const Plan q = plan(N16, NT, MT, f16);
+    for (int M = 1; M <= 16; M++) {
+        const Plan q = plan(N16, NT, M, f16);
         const size_t parts = (size_t)N16 * q.S * 2 * PART_STRIDE * sizeof(float);
-        const size_t images = f16 ? 0 : (size_t)q.S * Image(MT, q.ntmax).bytes;   // F16: INIT is always in the CTA
+        const size_t images = f16 ? 0 : (size_t)q.S * Image(M, q.ntmax).bytes;   // F16: INIT is always in the CTA
         db = std::max(db, align_up(parts, 256) + images);
     }
     *counter_bytes = (size_t)N16 * sizeof(unsigned int);
@@ -796,7 +882,7 @@ gq_status launch_gemv_with(bool f16, const void *rep, const float *x, float *dst
         p.dst = dst + m0 * N;
         // F16: tensor-core tiles of 8 or 16 activation rows
         const int MT = f16 ? (p.M <= 8 ? 8 : 16) : p.M <= 1 ? 1 : p.M <= 2 ? 2 : p.M <= 4 ? 4 : p.M <= 8 ? 8 : 16;
-        const Plan q = plan(p.N16, p.NT, MT, f16);
+        const Plan q = plan(p.N16, p.NT, p.M, f16);   // the images hold p.M rows
         p.S = q.S;
         p.ntmax = q.ntmax;
         p.Gs = q.Gs;
@@ -805,8 +891,13 @@ gq_status launch_gemv_with(bool f16, const void *rep, const float *x, float *dst
         const int consumers = cw == 8 ? Shape<8>::CONSUMERS : Shape<16>::CONSUMERS;
         const int fused_loads = cw == 8 ? Shape<8>::FUSED_LOADS : Shape<16>::FUSED_LOADS;
         // fuse INIT when each consumer thread loads a few float4 (F16: always)
-        p.fused = f16 || (int64_t)p.M * p.ntmax * 32 <= (int64_t)consumers * fused_loads * FUSED_ROUNDS ? 1 : 0;
-        const Variant *kvp = variant_for(MT, cw, regs_for(cw), f16);
+        // (one row and one K slice: each warp quantizes its own blocks as it goes, any K)
+        p.fused = f16 || (MT == 1 && q.S == 1) ||
+                          (int64_t)p.M * p.ntmax * 32 <= (int64_t)consumers * fused_loads * FUSED_ROUNDS
+                      ? 1
+                      : 0;
+        const int fixw = cw == 16 ? 2 : q.S == 1 ? 0 : 1;   // one K slice: no shared row group
+        const Variant *kvp = variant_for(MT, cw, regs_for(cw), f16, fixw);
         if (!kvp) return fail(GQ_ERR_INVALID_ARG, "gemv: no kernel for M=%d", p.M);
         const Variant &kv = *kvp;
         // behind INIT (which waited for every earlier grid) the weights are final; otherwise only
@@ -820,13 +911,18 @@ gq_status launch_gemv_with(bool f16, const void *rep, const float *x, float *dst
                                          (budget - std::min(budget, fixed + 256)) / (chunk_bytes(f16) + 16));
         };
         // the 8-warp Q4_0 shape keeps a ring of half the shared memory (MIN_SLOTS_HALF chunks at
-        // least), which measured faster than a full one
+        // least): two CTAs per SM without fix-up warps; with one, a half ring measured faster than
+        // a full one.  F16 tiles (twice the bytes per weight) keep a full ring, which measured faster.
         p.slots = kv.cw == 8 && !f16 ? slots_for(SMEM_HALF - 1024) : 0;
         if (p.slots < MIN_SLOTS_HALF) p.slots = slots_for(SMEM_LIMIT - 1024);
-        p.slots = std::min(p.slots, env_int("GQ_GEMV_SLOTS", MAX_SLOTS)) & ~(PRODUCERS - 1);
+        const int slots_env = env_int("GQ_GEMV_SLOTS", 0);   // tuning: ring slots, up to what fits
+        if (slots_env > 0) p.slots = std::min(slots_env, slots_for(SMEM_LIMIT - 1024));
+        p.slots &= ~(PRODUCERS - 1);
         if (p.slots < 2)
             return fail(GQ_ERR_INVALID_ARG, "gemv: N=%lld K=%lld leaves no room for the weight ring",
                         (long long)N, (long long)K);
+        const int pf_kb = env_int("GQ_GEMV_PF_KB", PF_KB);   // tuning; negative: no L2 prefetch
+        p.pf = pf_kb < 0 ? 0 : p.slots + pf_kb * 1024 / chunk_bytes(f16);
         const size_t smem = Layout(MT, p.M, p.ntmax, p.slots, p.maxfix, f16).total;
         st = allow_smem(kv.kernel, (int)(&kv - VARIANTS));
         if (st != GQ_OK) return st;

@@ -128,7 +128,7 @@ __device__ __forceinline__ uint32_t pack_q8x4(float4 x, const Q8Scale &q) {
     return pack_bytes(q8_code_s(x.x, q), q8_code_s(x.y, q), q8_code_s(x.z, q), q8_code_s(x.w, q));
 }
 
-// The codes of sixteen values (a half block) into four words.  The nearest
+// The codes of 4N values (N = 4: a half block) into N words.  The nearest
 // integers are formed first; only if some lane of the warp has a value near a
 // half-integer (a few percent of warps) does the warp form the full codes.
 __device__ __forceinline__ int q8_nearest(float x, const Q8Scale &q, bool &near) {
@@ -139,10 +139,11 @@ __device__ __forceinline__ int q8_nearest(float x, const Q8Scale &q, bool &near)
     return c < -127 ? -127 : (c > 127 ? 127 : c);
 }
 
-__device__ __forceinline__ void pack_q8x16(const float4 (&x)[4], const Q8Scale &q, uint32_t (&w)[4]) {
+template <int N>
+__device__ __forceinline__ void pack_q8_words(const float4 (&x)[N], const Q8Scale &q, uint32_t (&w)[N]) {
     bool any = false;
 #pragma unroll
-    for (int k = 0; k < 4; k++) {
+    for (int k = 0; k < N; k++) {
         bool n0, n1, n2, n3;
         const int c0 = q8_nearest(x[k].x, q, n0), c1 = q8_nearest(x[k].y, q, n1);
         const int c2 = q8_nearest(x[k].z, q, n2), c3 = q8_nearest(x[k].w, q, n3);
@@ -151,7 +152,11 @@ __device__ __forceinline__ void pack_q8x16(const float4 (&x)[4], const Q8Scale &
     }
     if (__any_sync(0xffffffffu, any))   // warp-uniform
 #pragma unroll
-        for (int k = 0; k < 4; k++) w[k] = pack_q8x4(x[k], q);
+        for (int k = 0; k < N; k++) w[k] = pack_q8x4(x[k], q);
+}
+
+__device__ __forceinline__ void pack_q8x16(const float4 (&x)[4], const Q8Scale &q, uint32_t (&w)[4]) {
+    pack_q8_words<4>(x, q, w);
 }
 
 // Sum of the four signed codes of a packed word.
@@ -282,6 +287,28 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// An L2 policy for data read once (streamed weights): their lines are the first to be
+// evicted, so they do not push out what is read again (activations, outputs).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// bulk_g2s with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
+}
+
+// Brings [src, src + bytes) into L2 (a hint: no data moves to the SM, nothing waits for it).
+// L2 is where every access to device memory meets, so this never makes a later read stale.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {

@@ -100,7 +100,7 @@ def test_block_dots_exact(oracle, M, N, K):
 GEMV_CASES = [
     (1, 256, 512, 0), (2, 200, 96, 1), (3, 1000, 1024, 2), (7, 64, 32, 3), (8, 515, 544, 4),
     (9, 300, 4096, 5), (16, 4096, 4096, 6), (13, 2000, 512, 7), (1, 4096, 11008, 8), (5, 11008, 128, 9),
-    (24, 100, 256, 10), (40, 77, 352, 11),
+    (24, 100, 256, 10), (40, 77, 352, 11), (1, 300, 96, 12), (1, 100, 20000, 13), (1, 37, 544, 14),
 ]
 
 
@@ -141,6 +141,21 @@ def test_edge_inputs_q4_0(oracle):
     ref, T = oracle.mul_mat_q4_0_f32(q4_ref, x)
     assert_within(dst, ref, T, what="edge q4_0")
     assert np.all(dst[T == 0] == 0)
+
+
+@pytest.mark.parametrize("M,K", [(1, 640), (1, 11008), (2, 640)])
+def test_edge_inputs_q4_0_few_rows(oracle, M, K):
+    """Zero blocks, exact Q8_0 ties and wide ranges with one or two activation rows (the
+    one-row product quantizes its activations per warp, chunk by chunk)."""
+    N = 97
+    w = synth.edge_weights(32, N, K)
+    x = synth.edge_activations(33 + M, M, K)
+    q4, dst = run_q4(w, x, gq.GQ_PATH_GEMV)
+    q4_ref = oracle.quantize_q4_0(w)
+    ref, T = oracle.mul_mat_q4_0_f32(q4_ref, x)
+    assert_within(dst, ref, T, what="edge q4_0")
+    err = np.abs(dst.astype(np.float64) - ref)
+    assert np.all(err <= exact_dot_bound(oracle, q4_ref, x)), "beyond the exact-block-dot bound"
 
 
 @pytest.mark.parametrize("kind", ["q4_0", "f16"])
