@@ -14,9 +14,9 @@ its weights from HBM.
 
 value  = weight-stream GB/s: algorithmic bytes (Q4_0 weights + f32 activations
          + f32 outputs) of all timed steps / device time of the timed steps.
-e2e    = the same through the Python API with pinned host buffers: each step
-         copies its activations host->device, runs the three products and reads
-         the outputs back, synchronizing at the end of the step.
+e2e    = the same through the host-pointer entry point with pinned host
+         buffers: each product copies its activations host->device, runs and
+         copies its outputs back; the step synchronizes at its end.
 extras = F16 weights on the same shapes, the M = 1..32 sweep, the prefill sizes
          (TFLOP/s) and the 32-layer 7B-shaped stack (tokens/s), each timed the
          same way (CUDA graph of back-to-back launches, rotating weight copies).
@@ -314,29 +314,34 @@ def run_ours(args, rank, world, local):
     ms_per_step = t / args.steps * 1e3
     achieved = bytes_per_step * args.steps / t / 1e9          # per GPU, all launches of the one kernel family
 
-    # ---- e2e: the same step through the Python API with pinned host buffers
+    # ---- e2e: the same step through the host-pointer entry point with pinned host buffers:
+    # each product copies its activations host->device, runs, and copies its outputs back
     hx = [xs[i].cpu().pin_memory() for i in range(len(SHAPES))]
     ho = [torch.empty((M, N), dtype=torch.float32).pin_memory() for N, K in SHAPES]
-    dx = [torch.empty_like(x) for x in xs]
     e2e_steps = max(1, min(args.steps, 2000))
-    with torch.cuda.stream(b.stream):
-        for s in range(3):
-            for i, (N, K) in enumerate(SHAPES):
-                dx[i].copy_(hx[i], non_blocking=True)
-                gq.gq_mul_mat_q4_0_f32(weights[s % C][i], dx[i], outs[i], M, N, K)
-                ho[i].copy_(outs[i], non_blocking=True)
-            b.stream.synchronize()
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        t0 = time.perf_counter()
-        for s in range(e2e_steps):
-            for i, (N, K) in enumerate(SHAPES):
-                dx[i].copy_(hx[i], non_blocking=True)
-                gq.gq_mul_mat_q4_0_f32(weights[s % C][i], dx[i], outs[i], M, N, K)
-                ho[i].copy_(outs[i], non_blocking=True)
-            b.stream.synchronize()
-        t_e2e = time.perf_counter() - t0
+    wp = [[w.data_ptr() for w in ws] for ws in weights]
+    hxp, hop = [h.data_ptr() for h in hx], [h.data_ptr() for h in ho]
+    sp = b.stream.cuda_stream
+    for s in range(3):
+        for i, (N, K) in enumerate(SHAPES):
+            gq.gq_mul_mat_q4_0_f32_host(wp[s % C][i], hxp[i], hop[i], M, N, K, sp)
+        b.stream.synchronize()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for s in range(e2e_steps):
+        for i, (N, K) in enumerate(SHAPES):
+            gq.gq_mul_mat_q4_0_f32_host(wp[s % C][i], hxp[i], hop[i], M, N, K, sp)
+        b.stream.synchronize()
+    t_e2e = time.perf_counter() - t0
+    last = (e2e_steps - 1) % C
+    for i, (N, K) in enumerate(SHAPES):            # the host results are the device path's
+        with torch.cuda.stream(b.stream):
+            gq.gq_mul_mat_q4_0_f32(weights[last][i], xs[i], outs[i], M, N, K)
+        b.stream.synchronize()
+        if not torch.equal(ho[i], outs[i].cpu()):
+            raise RuntimeError(f"e2e: host-buffer product {N}x{K} differs from the device product")
     t_e2e = max_over_ranks(t_e2e, dist)
     e2e = {"value": round(whole_job_gbs(bytes_per_step, e2e_steps, world, t_e2e), 3), "unit": "GB/s",
            "h2d_bytes_per_step": sum(4 * M * K for N, K in SHAPES),

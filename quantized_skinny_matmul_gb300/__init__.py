@@ -69,6 +69,7 @@ SIGNATURES = {
     "gq_get_m_threshold": ([], _I),
     "gq_debug_block_dots_q4_0": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_noalloc": ([_P, _P, _P, _I, _I, _I, _P], _S),
+    "gq_mul_mat_q4_0_f32_host": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_f16_repacked_bytes": ([_I, _I], ctypes.c_size_t),
     "gq_repack_f16": ([_P, _P, _I, _I, _P], _S),
     "gq_mul_mat_f16r_f32": ([_P, _P, _P, _I, _I, _I, _P], _S),
@@ -205,6 +206,22 @@ def gq_mul_mat_q4_0_f32_noalloc(q4_repacked, src1, dst, M: int, N: int, K: int, 
     """The Q4_0 product with no device allocation (static scratch in the library)."""
     _check(lib().gq_mul_mat_q4_0_f32_noalloc(_ptr(q4_repacked), _ptr(src1), _ptr(dst), M, N, K,
                                              _stream(stream)), "gq_mul_mat_q4_0_f32_noalloc")
+
+
+def _host_ptr(a) -> int:
+    if isinstance(a, int):
+        return a
+    if getattr(a, "is_cuda", False):
+        raise ValueError("expected a host (CPU) tensor")
+    if not a.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return a.data_ptr()
+
+
+def gq_mul_mat_q4_0_f32_host(q4_repacked, src1_host, dst_host, M: int, N: int, K: int, stream=None) -> None:
+    """The Q4_0 product from host src1 into host dst (copies enqueued on the stream)."""
+    _check(lib().gq_mul_mat_q4_0_f32_host(_ptr(q4_repacked), _host_ptr(src1_host), _host_ptr(dst_host), M, N, K,
+                                          _stream(stream)), "gq_mul_mat_q4_0_f32_host")
 
 
 def gq_f16_repacked_bytes(N: int, K: int) -> int:

@@ -287,6 +287,27 @@ gq_status gq_mul_mat_q4_0_f32(const void *q4_repacked, const float *src1, float 
     return gq_mul_mat_q4_0_f32_path(q4_repacked, src1, dst, M, N, K, GQ_PATH_AUTO, stream);
 }
 
+gq_status gq_mul_mat_q4_0_f32_host(const void *q4_repacked, const float *src1_host, float *dst_host, int64_t M,
+                                   int64_t N, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(M, N, K));
+    GQ_TRY(check_ptr(q4_repacked, "q4_repacked"));
+    if (!src1_host) return fail(GQ_ERR_INVALID_ARG, "src1_host is NULL");
+    if (!dst_host) return fail(GQ_ERR_INVALID_ARG, "dst_host is NULL");
+    GQ_TRY(check_device());
+    const size_t xb = (size_t)M * (size_t)K * sizeof(float), ob = (size_t)M * (size_t)N * sizeof(float);
+    const size_t xs = (xb + 255) / 256 * 256;
+    uint8_t *stage = nullptr;
+    GQ_TRY(get_staging(stream, xs + ob, &stage));
+    float *dx = reinterpret_cast<float *>(stage), *dd = reinterpret_cast<float *>(stage + xs);
+    GQ_TRY(check_cuda(cudaMemcpyAsync(dx, src1_host, xb, cudaMemcpyHostToDevice, stream), "src1 copy to the device"));
+    if (resolve(GQ_PATH_AUTO, M) == GQ_PATH_TC)
+        GQ_TRY(launch_tc_q4_0(q4_repacked, dx, dd, M, N, K, stream));
+    else
+        GQ_TRY(launch_gemv_q4_0(q4_repacked, dx, dd, M, N, K, stream));
+    GQ_TRY(check_cuda(cudaMemcpyAsync(dst_host, dd, ob, cudaMemcpyDeviceToHost, stream), "dst copy to the host"));
+    return ok();
+}
+
 gq_status gq_mul_mat_f16_f32(const void *src0_f16, const float *src1, float *dst, int64_t M, int64_t N, int64_t K,
                              cudaStream_t stream) {
     return gq_mul_mat_f16_f32_path(src0_f16, src1, dst, M, N, K, GQ_PATH_AUTO, stream);

@@ -34,6 +34,8 @@ struct Workspace {
 };
 gq_status get_workspace(cudaStream_t s, size_t counter_bytes, size_t data_bytes, Workspace *out);
 gq_status reset_workspace_counters();
+// Per-(device, stream) device staging buffer of at least `bytes` bytes (grows on demand).
+gq_status get_staging(cudaStream_t s, size_t bytes, uint8_t **out);
 
 // Launchers (arguments already validated by the entry points).
 gq_status launch_quantize_q4_0(const float *w, void *q4, int64_t N, int64_t K, cudaStream_t s);

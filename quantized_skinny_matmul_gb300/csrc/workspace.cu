@@ -83,6 +83,59 @@ gq_status get_workspace(cudaStream_t stream, size_t counter_bytes, size_t data_b
     return GQ_OK;
 }
 
+// Staging buffers of the host-pointer entry points (src1 and dst on the device), one
+// per (device, stream), grown like the workspace.
+namespace {
+struct Staging {
+    int device;
+    cudaStream_t stream;
+    uint8_t *ptr;
+    size_t bytes;
+};
+std::vector<Staging> g_staging;
+}  // namespace
+
+gq_status get_staging(cudaStream_t stream, size_t bytes, uint8_t **out) {
+    bytes = (bytes + 255) / 256 * 256;
+    int dev = 0;
+    gq_status st = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+    if (st != GQ_OK) return st;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    Staging *e = nullptr;
+    for (auto &x : g_staging)
+        if (x.device == dev && x.stream == stream) e = &x;
+    if (e && e->bytes >= bytes) {
+        *out = e->ptr;
+        return GQ_OK;
+    }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    st = check_cuda(cudaStreamIsCapturing(stream, &cap), "cudaStreamIsCapturing");
+    if (st != GQ_OK) return st;
+    if (cap != cudaStreamCaptureStatusNone)
+        return fail(GQ_ERR_NO_MEMORY, "the stream's staging buffer must grow (%zu bytes) while the stream is "
+                    "being captured", bytes);
+    if (e) {
+        st = check_cuda(cudaStreamSynchronize(stream), "cudaStreamSynchronize (staging growth)");
+        if (st != GQ_OK) return st;
+        cudaFree(e->ptr);
+        e->ptr = nullptr;
+        e->bytes = 0;
+    }
+    uint8_t *p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(GQ_ERR_NO_MEMORY, "cudaMalloc of a %zu-byte staging buffer failed", bytes);
+    }
+    if (!e) {
+        g_staging.push_back(Staging{dev, stream, nullptr, 0});
+        e = &g_staging.back();
+    }
+    e->ptr = p;
+    e->bytes = bytes;
+    *out = p;
+    return GQ_OK;
+}
+
 // Zeroes the counters of every workspace of the current device (after a kernel
 // gave up a wait, counters may be left mid-count).
 gq_status reset_workspace_counters() {

@@ -92,6 +92,10 @@ def test_argument_checks_other_entries(lib):
     assert lib.gq_repack_f16(FAKE, FAKE, 4, 48, None) == gq.GQ_ERR_INVALID_ARG   # K % 32
     assert lib.gq_mul_mat_f16r_f32(FAKE, FAKE, ODD, 1, 64, 64, None) == gq.GQ_ERR_MISALIGNED
     assert lib.gq_mul_mat_f16r_f32(0, FAKE, FAKE, 1, 64, 64, None) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_mul_mat_q4_0_f32_host(FAKE, 0, FAKE, 1, 64, 64, None) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_mul_mat_q4_0_f32_host(FAKE, FAKE, 0, 1, 64, 64, None) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_mul_mat_q4_0_f32_host(ODD, FAKE, FAKE, 1, 64, 64, None) == gq.GQ_ERR_MISALIGNED
+    assert lib.gq_mul_mat_q4_0_f32_host(FAKE, FAKE, FAKE, 1, 64, 40, None) == gq.GQ_ERR_INVALID_ARG
     assert lib.gq_debug_block_dots_q4_0(FAKE, FAKE, ODD, 1, 16, 64, None) == gq.GQ_ERR_MISALIGNED
     assert lib.gq_mul_mat_q4_0_f32_path(FAKE, FAKE, FAKE, 1, 64, 64, 7, None) == gq.GQ_ERR_INVALID_ARG
     assert lib.gq_set_m_threshold(-1) == gq.GQ_ERR_INVALID_ARG

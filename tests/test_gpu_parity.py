@@ -217,6 +217,23 @@ def test_full_size_sampled(oracle, M, N, K):
     assert_within(dst16[ms, ns], ref16, T16, what="f16 full size")
 
 
+@pytest.mark.parametrize("M,N,K,pinned", [(1, 4096, 4096, True), (5, 300, 1024, False), (40, 77, 352, True)])
+def test_host_pointer_entry_equals_device_entry(M, N, K, pinned):
+    """gq_mul_mat_q4_0_f32_host (src1 and dst in host memory) gives the device entry's
+    result bit for bit, with page-locked and with pageable host buffers."""
+    w, x = synth.problem(70 + M, M, N, K)
+    rep = gq.repack_q4_0(gq.quantize_q4_0(dev(w)), N, K)
+    want = host(gq.mul_mat_q4_0_f32(rep, dev(x), N))
+    hx = torch.from_numpy(np.ascontiguousarray(x))
+    hd = torch.full((M, N), float("nan"))
+    if pinned:
+        hx, hd = hx.pin_memory(), hd.pin_memory()
+    s = torch.cuda.current_stream()
+    gq.gq_mul_mat_q4_0_f32_host(rep, hx, hd, M, N, K, s)
+    s.synchronize()
+    assert np.array_equal(hd.numpy(), want)
+
+
 def test_concatenated_rows_equal_separate_products():
     """Q/K/V-like matrices sharing an input: one product over the concatenated
     repacked buffers equals the separate products, bit for bit."""
