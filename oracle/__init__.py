@@ -61,6 +61,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "oracle_block_dots": ([P, P, P, I, I, I], None),
         "oracle_mul_mat_q4_0_f32": ([P, P, P, P, I, I, I, I, I], ctypes.c_int),
         "oracle_mul_mat_q4_0_q8_0_at": ([P, P, P, P, I, I, P, P], None),
+        "oracle_block_dots_q8_0": ([P, P, P, I, I, I], None),
+        "oracle_mul_mat_q8_0_f32": ([P, P, P, P, I, I, I, I, I], ctypes.c_int),
+        "oracle_mul_mat_q8_0_q8_0_at": ([P, P, P, P, I, I, P, P], None),
         "oracle_mul_mat_f16_f32": ([P, P, P, P, I, I, I, I, I], None),
         "oracle_mul_mat_f16_f32_at": ([P, P, P, P, I, I, P, P], None),
         "oracle_f32_to_f16_array": ([P, P, I], None),
@@ -183,6 +186,44 @@ class Oracle:
         out = np.empty(ms.size, np.float64)
         T = np.empty(ms.size, np.float64)
         self.lib.oracle_mul_mat_q4_0_q8_0_at(_ptr(q4), _ptr(q8), _ptr(ms), _ptr(ns), ms.size,
+                                             K, _ptr(out), _ptr(T))
+        return out, T
+
+    def block_dots_q8_0(self, qw, qx) -> np.ndarray:
+        """int32 [M, N, K/32]: sum_j qw_j * qx_j for every pair of Q8_0 blocks."""
+        qw = _c(qw, np.uint8)
+        qx = _c(qx, np.uint8)
+        N, nb = qw.shape[0], qw.shape[1]
+        M = qx.shape[0]
+        assert qx.shape[1] == nb
+        out = np.empty((M, N, nb), np.int32)
+        self.lib.oracle_block_dots_q8_0(_ptr(qw), _ptr(qx), _ptr(out), M, N, nb * QK)
+        return out
+
+    def mul_mat_q8_0_f32(self, qw, src1, n_range=None):
+        """(dst, T), both f64 [M, N], for Q8_0 weights; src1 is quantized to Q8_0 inside."""
+        qw = _c(qw, np.uint8)
+        src1 = _c(src1, np.float32)
+        N, nb = qw.shape[0], qw.shape[1]
+        M, K = src1.shape
+        assert K == nb * QK
+        dst = np.zeros((M, N), np.float64)
+        T = np.zeros((M, N), np.float64)
+        b, e = (0, N) if n_range is None else n_range
+        rc = self.lib.oracle_mul_mat_q8_0_f32(_ptr(qw), _ptr(src1), _ptr(dst), _ptr(T), M, N, K, b, e)
+        if rc != 0:
+            raise MemoryError("oracle_mul_mat_q8_0_f32: allocation failed")
+        return dst, T
+
+    def mul_mat_q8_0_q8_0_at(self, qw, qx, ms, ns):
+        qw = _c(qw, np.uint8)
+        qx = _c(qx, np.uint8)
+        ms = _c(ms, np.int64)
+        ns = _c(ns, np.int64)
+        K = qw.shape[1] * QK
+        out = np.empty(ms.size, np.float64)
+        T = np.empty(ms.size, np.float64)
+        self.lib.oracle_mul_mat_q8_0_q8_0_at(_ptr(qw), _ptr(qx), _ptr(ms), _ptr(ns), ms.size,
                                              K, _ptr(out), _ptr(T))
         return out, T
 

@@ -9,7 +9,7 @@
  *
  * What is computed (the llama.cpp MUL_MAT of the q_f32 and f16_f32 kinds):
  *     dst[m][n] = sum_k src0[n][k] * src1[m][k]
- * with src0 either Q4_0 block-quantized weights or F16 weights, and src1 F32
+ * with src0 Q4_0 or Q8_0 block-quantized weights or F16 weights, and src1 F32
  * activations.  For the Q4_0 kind, src1 is first quantized row by row into
  * Q8_0 blocks (the "wdata" buffer) and the product is taken as integer block
  * dot products scaled by the two block scales:
@@ -295,6 +295,83 @@ void oracle_mul_mat_q4_0_q8_0_at(const uint8_t *q4, const uint8_t *q8, const int
     int64_t nb = K / QK;
     for (int64_t i = 0; i < count; i++)
         dot_row_q4_0_q8_0(q4 + ns[i] * nb * Q4_0_BYTES, q8 + ms[i] * nb * Q8_0_BYTES, nb,
+                          &out[i], &T[i]);
+}
+
+/* ---------------------------------------------------------------------------
+ * The q_f32 kind with Q8_0 weights.  llama.cpp pull request #1632,
+ * "Introduction": src0 of the q_f32 kind may be any quantized type; "Results":
+ * Q8_0 is one of the three types measured on 7B.  The weights use the Q8_0
+ * block above (the activations' format), src1 is quantized to Q8_0 exactly as
+ * for Q4_0, and the integer block dot has no offset:
+ *     sumi = sum_{j<32} qw_j * qx_j                   (|sumi| <= 32*127*127)
+ *     dst  = sum_b dw_b * dx_b * sumi_b               (f64; each term exact)
+ *     T    = sum_b |dw_b| |dx_b| sum_j |qw_j| |qx_j|
+ * ------------------------------------------------------------------------- */
+static int32_t block_dot_q8_0(const uint8_t *bw, const uint8_t *bx)
+{
+    int32_t s = 0;
+    for (int j = 0; j < QK; j++)
+        s += (int32_t)q8_code(bw, j) * (int32_t)q8_code(bx, j);
+    return s;
+}
+
+/* sumi: int32 [M][N][K/32] */
+void oracle_block_dots_q8_0(const uint8_t *qw, const uint8_t *qx, int32_t *sumi,
+                            int64_t M, int64_t N, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = 0; n < N; n++)
+            for (int64_t b = 0; b < nb; b++)
+                sumi[(m * N + n) * nb + b] =
+                    block_dot_q8_0(qw + (n * nb + b) * Q8_0_BYTES, qx + (m * nb + b) * Q8_0_BYTES);
+}
+
+static void dot_row_q8_0_q8_0(const uint8_t *roww, const uint8_t *rowx, int64_t nb,
+                              double *dst, double *T)
+{
+    double acc = 0.0, tacc = 0.0;
+    for (int64_t b = 0; b < nb; b++) {
+        const uint8_t *bw = roww + b * Q8_0_BYTES;
+        const uint8_t *bx = rowx + b * Q8_0_BYTES;
+        double dw = (double)oracle_f16_to_f32(get_f16(bw));
+        double dx = (double)oracle_f16_to_f32(get_f16(bx));
+        acc += dw * dx * (double)block_dot_q8_0(bw, bx);
+        int64_t sabs = 0;
+        for (int j = 0; j < QK; j++)
+            sabs += (int64_t)abs(q8_code(bw, j)) * (int64_t)abs(q8_code(bx, j));
+        tacc += fabs(dw) * fabs(dx) * (double)sabs;
+    }
+    *dst = acc;
+    *T = tacc;
+}
+
+/* Full MUL_MAT with Q8_0 weights for the output columns n in [n_begin, n_end).
+ * qw: Q8_0 [N][K/32]; src1: f32 [M][K]; dst, T: f64 [M][N]. */
+int oracle_mul_mat_q8_0_f32(const uint8_t *qw, const float *src1, double *dst, double *T,
+                            int64_t M, int64_t N, int64_t K, int64_t n_begin, int64_t n_end)
+{
+    int64_t nb = K / QK;
+    uint8_t *wdata = (uint8_t *)malloc((size_t)(M * nb * Q8_0_BYTES) + 1);
+    if (!wdata) return 1;
+    oracle_quantize_q8_0(src1, wdata, M, K);
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = n_begin; n < n_end; n++)
+            dot_row_q8_0_q8_0(qw + n * nb * Q8_0_BYTES, wdata + m * nb * Q8_0_BYTES, nb,
+                              &dst[m * N + n], &T[m * N + n]);
+    free(wdata);
+    return 0;
+}
+
+/* Selected outputs (ms[i], ns[i]) with Q8_0 weights from quantized activations qx. */
+void oracle_mul_mat_q8_0_q8_0_at(const uint8_t *qw, const uint8_t *qx, const int64_t *ms,
+                                 const int64_t *ns, int64_t count, int64_t K,
+                                 double *out, double *T)
+{
+    int64_t nb = K / QK;
+    for (int64_t i = 0; i < count; i++)
+        dot_row_q8_0_q8_0(qw + ns[i] * nb * Q8_0_BYTES, qx + ms[i] * nb * Q8_0_BYTES, nb,
                           &out[i], &T[i]);
 }
 

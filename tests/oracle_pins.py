@@ -10,7 +10,8 @@ What pins what:
   * the block byte layouts      -> the hand-derived worked examples in golden/
   * the quantizer's arithmetic  -> exact round trips of representable blocks, the
                                    range and de-quantization error bounds
-  * the integer block dot       -> brute force over every (q4, q8) pair per lane
+  * the integer block dots      -> brute force over every (q4, q8) pair per lane, and
+                                   every Q8_0 weight code against a spread of codes
   * the f64 products            -> float64 dense matmul of the de-quantized
                                    operands (textbook special case), structured
                                    weights with closed-form results, and the
@@ -292,6 +293,59 @@ def pin_f16_matmul(o) -> None:
     assert np.array_equal(at, dst[ms, ns])
 
 
+def pin_q8_0_block_dot_bruteforce(o) -> None:
+    """Q8_0 weights, one lane at a time: sumi = qw * qx for every qw in -127..127 against a
+    spread of qx; the extreme block (all 127 against all -127) gives -32 * 127 * 127."""
+    qwv = np.arange(-127, 128)
+    qxv = np.array([-127, -64, -3, -1, 0, 1, 2, 77, 127])
+    for lane in (0, 9, 16, 31):
+        bw = []
+        for a in qwv:
+            c = np.zeros(32, np.int64)
+            c[lane] = a
+            bw.append(_q8_block(c))
+        bx = []
+        for b in qxv:
+            c = np.zeros(32, np.int64)
+            c[lane] = b
+            bx.append(_q8_block(c))
+        got = o.block_dots_q8_0(np.stack(bw)[:, None, :], np.stack(bx)[:, None, :])[:, :, 0]
+        assert np.array_equal(got, np.outer(qxv, qwv)), f"Q8_0 block dot wrong at lane {lane}"
+    got = o.block_dots_q8_0(_q8_block(np.full(32, 127))[None, None], _q8_block(np.full(32, -127))[None, None])
+    assert int(got[0, 0, 0]) == -516128
+
+
+def pin_q8_0_matmul_vs_dense(o) -> None:
+    """Q8_0 weights: the f64 product equals float64 dequant(src0) @ dequant(wdata)^T to 1e-12
+    of T; random integer blocks give the integer block dots exactly; rows are independent."""
+    rng = np.random.default_rng(17)
+    N, M, nb = 11, 4, 5
+    cw = rng.integers(-127, 128, size=(N, nb, 32))
+    cx = rng.integers(-127, 128, size=(M, nb, 32))
+    qw = np.stack([np.stack([_q8_block(cw[n, b]) for b in range(nb)]) for n in range(N)])
+    qx = np.stack([np.stack([_q8_block(cx[m, b]) for b in range(nb)]) for m in range(M)])
+    assert np.array_equal(o.block_dots_q8_0(qw, qx),
+                          np.einsum("nbj,mbj->mnb", cw.astype(np.int64), cx.astype(np.int64)))
+    for (M, N, K, seed, outl) in ((3, 40, 96, 21, False), (6, 33, 256, 22, True), (1, 17, 32, 23, False)):
+        w, x = synth.problem(seed, M, N, K, outliers=outl)
+        qw = o.quantize_q8_0(w)                       # the weights in the Q8_0 block format
+        qx = o.quantize_q8_0(x)
+        cw_, dw = decode_q8_0(qw)
+        cx_, dx = decode_q8_0(qx)
+        A = (cw_.astype(np.float64) * dw[..., None]).reshape(N, K)
+        B = (cx_.astype(np.float64) * dx[..., None]).reshape(M, K)
+        want, T_want = B @ A.T, np.abs(B) @ np.abs(A).T
+        dst, T = o.mul_mat_q8_0_f32(qw, x)
+        assert np.all(np.abs(dst - want) <= 1e-12 * T_want + 1e-300), "Q8_0 product mismatch"
+        assert np.allclose(T, T_want, rtol=1e-12, atol=0)
+        ms, ns = np.array([0, M - 1, M // 2]), np.array([N - 1, 0, N // 2])
+        at, T_at = o.mul_mat_q8_0_q8_0_at(qw, qx, ms, ns)
+        assert np.array_equal(at, dst[ms, ns]) and np.array_equal(T_at, T[ms, ns])
+        for m in range(M):
+            one, _ = o.mul_mat_q8_0_f32(qw, x[m:m + 1])
+            assert np.array_equal(one[0], dst[m])
+
+
 ALL_PINS = [
     pin_f16_conversion,
     pin_worked_examples,
@@ -303,4 +357,6 @@ ALL_PINS = [
     pin_matmul_vs_dense,
     pin_row_independence,
     pin_f16_matmul,
+    pin_q8_0_block_dot_bruteforce,
+    pin_q8_0_matmul_vs_dense,
 ]

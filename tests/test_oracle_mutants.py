@@ -37,10 +37,14 @@ MUTANTS = {
                             "if (E == 0)       v = ldexpf((float)F, -25);"),
     "dropped_d8": ("acc += d4 * d8 * (double)block_dot(b4, b8);",
                    "acc += d4 * (double)block_dot(b4, b8);"),
-    "transposed_dst": ("&dst[m * N + n], &T[m * N + n]);\n    free(wdata);",
-                       "&dst[n * M + m], &T[n * M + m]);\n    free(wdata);"),
+    "transposed_dst": ("Q4_0_BYTES, wdata + m * nb * Q8_0_BYTES, nb,\n                              &dst[m * N + n], &T[m * N + n]);",
+                       "Q4_0_BYTES, wdata + m * nb * Q8_0_BYTES, nb,\n                              &dst[n * M + m], &T[n * M + m]);"),
     "f16_reversed_k": ("double p = (double)oracle_f16_to_f32(w[k]) * (double)x[k];",
                        "double p = (double)oracle_f16_to_f32(w[k]) * (double)x[K - 1 - k];"),
+    "q8w_dropped_dw": ("acc += dw * dx * (double)block_dot_q8_0(bw, bx);",
+                       "acc += dx * (double)block_dot_q8_0(bw, bx);"),
+    "q8w_shifted_lane": ("s += (int32_t)q8_code(bw, j) * (int32_t)q8_code(bx, j);",
+                         "s += (int32_t)q8_code(bw, j) * (int32_t)q8_code(bx, (j + 1) % QK);"),
     "q8_abs_dropped": ("float a = fabsf(x[j]);\n        if (a > amax) amax = a;",
                        "float a = x[j];\n        if (a > amax) amax = a;"),
 }
