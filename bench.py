@@ -56,6 +56,10 @@ def step_bytes_q4(M, N, K):
     return q4_bytes(N, K) + 4 * M * K + 4 * M * N
 
 
+def step_bytes_q8(M, N, K):
+    return N * K * 34 // 32 + 4 * M * K + 4 * M * N
+
+
 def step_bytes_f16(M, N, K):
     return 2 * N * K + 4 * M * K + 4 * M * N
 
@@ -183,6 +187,14 @@ class GpuBench:
         rep = gq.repack_q4_0(q4, N, K)
         del q4
         return rep
+
+    def q8_weights(self, N, K, seed):
+        torch = self.torch
+        gq = self.gq
+        w = torch.randn((N, K), generator=self.gen(seed), device=self.dev, dtype=torch.float32).mul_(0.02)
+        q8 = gq.quantize_rows_q8_0(w)
+        del w
+        return gq.repack_q8_0(q8, N, K)
 
     def f16_weights(self, N, K, seed):
         torch = self.torch
@@ -409,6 +421,20 @@ def extras(b, weights, C, hbm_peak, bf16_peak, bf16_sustained, args):
         res[f"f16r_m{M}"] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4),
                              "us_per_step": round(t / C16 * 1e6, 2)}
     del r16
+    # Q8_0 weights (repacked tiles), same shapes, M = 1 and M = 8
+    q8_set = sum(N * K * 34 // 32 for N, K in SHAPES)
+    C8 = b.copies_for(q8_set)
+    w8 = [[b.q8_weights(N, K, 7000 + 10 * c + i) for i, (N, K) in enumerate(SHAPES)] for c in range(C8)]
+    for M in (1, 8):
+        xm = [b.acts(M, K, 340 + i) for i, (N, K) in enumerate(SHAPES)]
+        om = [torch.empty((M, N), device=b.dev) for N, K in SHAPES]
+        ls = [lambda c=c, i=i, N=N, K=K, M=M: gq.gq_mul_mat_q8_0_f32(w8[c][i], xm[i], om[i], M, N, K)
+              for c in range(C8) for i, (N, K) in enumerate(SHAPES)]
+        t = b.time_launches(ls)
+        gbs = sum(step_bytes_q8(M, N, K) for N, K in SHAPES) * C8 / t / 1e9
+        res[f"q8_0_m{M}"] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4),
+                             "us_per_step": round(t / C8 * 1e6, 2)}
+    del w8
 
     # M sweep on the two FFN shapes (Q4_0)
     sweep = {}
@@ -550,7 +576,7 @@ def cpu_baseline(seconds: float):
 
 
 def run_profile(spec: str):
-    """A few plain launches of one product, for ncu: KIND:M:N:K with KIND q4_0 | f16 | f16r | q4_0_tc | f16_tc."""
+    """A few plain launches of one product, for ncu: KIND:M:N:K with KIND q4_0 | q8_0 | f16 | f16r | q4_0_tc | f16_tc."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -564,6 +590,9 @@ def run_profile(spec: str):
     if kind.startswith("q4_0"):
         w = b.q4_weights(N, K, 2)
         fn = lambda: gq.gq_mul_mat_q4_0_f32_path(w, x, o, M, N, K, path)
+    elif kind == "q8_0":
+        w = b.q8_weights(N, K, 2)
+        fn = lambda: gq.gq_mul_mat_q8_0_f32(w, x, o, M, N, K)
     elif kind == "f16r":
         w = gq.repack_f16(b.f16_weights(N, K, 2))
         fn = lambda: gq.gq_mul_mat_f16r_f32(w, x, o, M, N, K)

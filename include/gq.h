@@ -180,6 +180,27 @@ gq_status gq_repack_f16(const void *src0_f16, void *f16_repacked, int64_t N, int
 gq_status gq_mul_mat_f16r_f32(const void *f16_repacked, const float *src1, float *dst,
                               int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
+/* Q8_0 weights (llama.cpp PR #1632, "Introduction": src0 of the q_f32 kind may be
+ * any quantized type; "Results": Q8_0 is among the types measured on 7B).  The
+ * weights use the activations' Q8_0 block format: quantize them with
+ * gq_quantize_rows_q8_0 ([N][K/32] x 34 bytes), then copy them once with
+ * gq_repack_q8_0 into tiles of 16 rows x 4 blocks, 2176 bytes each: the 32 codes
+ * of block j of row r at (j * 16 + r) * 32, then the fp16 scale of (r, j) at
+ * 2048 + (r * 4 + j) * 2; tile (g, t) at (g * ceil(K/128) + t) * 2176; padding
+ * holds codes 0 and scale 0.  gq_q8_0_repacked_bytes(N, K) = ceil(N/16) *
+ * ceil(K/128) * 2176 bytes (0 if N <= 0, K <= 0 or K % 32); q8_repacked must not
+ * overlap q8_blocks (GQ_ERR_INVALID_ARG).  gq_mul_mat_q8_0_f32 computes
+ * dst[M][N] = Q8_0(src1) . Q8_0(src0)^T: each output is
+ * sum_b fp16(dw_b) * fp16(dx_b) * sumi_b with the exact int32 block dots
+ * sumi_b = sum_j qw_j * qx_j, accumulated in f32, by the GEMV family for every M
+ * (16 activation rows per launch); it uses the stream's workspace like the other
+ * products and its results do not depend on timing. */
+size_t gq_q8_0_repacked_bytes(int64_t N, int64_t K);
+gq_status gq_repack_q8_0(const void *q8_blocks, void *q8_repacked, int64_t N, int64_t K,
+                         cudaStream_t stream);
+gq_status gq_mul_mat_q8_0_f32(const void *q8_repacked, const float *src1, float *dst,
+                              int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* Workspace.  The products keep a small device workspace per (device, stream):
  * partial sums of weight rows that several CTAs share, with per-row counters
  * that every launch leaves at zero, and (tensor-core path) the quantized

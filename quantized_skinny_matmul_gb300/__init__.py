@@ -70,6 +70,9 @@ SIGNATURES = {
     "gq_debug_block_dots_q4_0": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_noalloc": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_host": ([_P, _P, _P, _I, _I, _I, _P], _S),
+    "gq_q8_0_repacked_bytes": ([_I, _I], ctypes.c_size_t),
+    "gq_repack_q8_0": ([_P, _P, _I, _I, _P], _S),
+    "gq_mul_mat_q8_0_f32": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_f16_repacked_bytes": ([_I, _I], ctypes.c_size_t),
     "gq_repack_f16": ([_P, _P, _I, _I, _P], _S),
     "gq_mul_mat_f16r_f32": ([_P, _P, _P, _I, _I, _I, _P], _S),
@@ -224,6 +227,19 @@ def gq_mul_mat_q4_0_f32_host(q4_repacked, src1_host, dst_host, M: int, N: int, K
                                           _stream(stream)), "gq_mul_mat_q4_0_f32_host")
 
 
+def gq_q8_0_repacked_bytes(N: int, K: int) -> int:
+    return lib().gq_q8_0_repacked_bytes(N, K)
+
+
+def gq_repack_q8_0(q8_blocks, q8_repacked, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_repack_q8_0(_ptr(q8_blocks), _ptr(q8_repacked), N, K, _stream(stream)), "gq_repack_q8_0")
+
+
+def gq_mul_mat_q8_0_f32(q8_repacked, src1, dst, M: int, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_mul_mat_q8_0_f32(_ptr(q8_repacked), _ptr(src1), _ptr(dst), M, N, K, _stream(stream)),
+           "gq_mul_mat_q8_0_f32")
+
+
 def gq_f16_repacked_bytes(N: int, K: int) -> int:
     return lib().gq_f16_repacked_bytes(N, K)
 
@@ -320,4 +336,20 @@ def mul_mat_f16r_f32(f16_repacked, src1, N: int, out=None):
     M, K = src1.shape
     dst = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=src1.device)
     gq_mul_mat_f16r_f32(f16_repacked, src1, dst, M, N, K)
+    return dst
+
+
+def repack_q8_0(q8, N: int, K: int):
+    """Q8_0 weight blocks (uint8 [N, K/32, 34], e.g. from quantize_rows_q8_0) -> the tile layout."""
+    import torch
+    out = torch.empty(gq_q8_0_repacked_bytes(N, K), dtype=torch.uint8, device=q8.device)
+    gq_repack_q8_0(q8, out, N, K)
+    return out
+
+
+def mul_mat_q8_0_f32(q8_repacked, src1, N: int, out=None):
+    import torch
+    M, K = src1.shape
+    dst = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=src1.device)
+    gq_mul_mat_q8_0_f32(q8_repacked, src1, dst, M, N, K)
     return dst

@@ -77,12 +77,19 @@ struct Shape {
     static constexpr int CONSUMERS = CWT * 32;
     static constexpr int FUSED_LOADS = 4;                   // float4 per consumer thread and round of the fused INIT
 };
-constexpr int CHUNK_BYTES = CHUNK_TILES * TILE_BYTES;
 // Repacked F16 weights: a tile is 16 rows x 32 columns, 64 bytes per row.
 constexpr int F16_TILE_COLS = 32;
 constexpr int F16_TILE_BYTES = 16 * F16_TILE_COLS * 2;
-__host__ __device__ constexpr int tile_bytes(bool f16) { return f16 ? F16_TILE_BYTES : TILE_BYTES; }
-__host__ __device__ constexpr int chunk_bytes(bool f16) { return CHUNK_TILES * tile_bytes(f16); }
+// Repacked Q8_0 weights: a tile is 16 rows x 4 blocks like Q4_0; the 32 codes of block j of row r
+// at (j * 16 + r) * 32, then the 64 fp16 scales at 2048 + (r * 4 + j) * 2.
+constexpr int Q8_TILE_SCALE_OFFSET = 16 * TILE_BLOCKS * QK;
+constexpr int Q8_TILE_BYTES = Q8_TILE_SCALE_OFFSET + 16 * TILE_BLOCKS * 2;
+// weight formats of the kernel
+enum : int { WF_Q4 = 0, WF_F16 = 1, WF_Q8 = 2 };
+__host__ __device__ constexpr int tile_bytes(int wf) {
+    return wf == WF_F16 ? F16_TILE_BYTES : wf == WF_Q8 ? Q8_TILE_BYTES : TILE_BYTES;
+}
+__host__ __device__ constexpr int chunk_bytes(int wf) { return CHUNK_TILES * tile_bytes(wf); }
 constexpr int MAX_SLOTS = 12;
 constexpr int PART_STRIDE = 16 * 16;               // floats of one partial (16 rows x 16 activation rows)
 constexpr int FIX_BATCH = 8;                       // partials one fix-up lane loads before adding them
@@ -135,11 +142,11 @@ struct Params {
 
 struct Layout {
     size_t bars, ring, act, red, total;
-    __host__ __device__ Layout(int MT, int M, int ntmax, int slots, int maxfix, bool f16 = false) {
-        const Image im(M, ntmax, f16);
+    __host__ __device__ Layout(int MT, int M, int ntmax, int slots, int maxfix, int wf = WF_Q4) {
+        const Image im(M, ntmax, wf == WF_F16);   // Q8_0 weights use the Q4_0 image
         bars = 0;                                         // full[slots], empty[slots], act, fix[maxfix]
         ring = align_up((size_t)(2 * slots + 1 + maxfix) * 8, 128);
-        act = ring + (size_t)slots * chunk_bytes(f16);
+        act = ring + (size_t)slots * chunk_bytes(wf);
         red = act + im.bytes;
         total = red + 2 * (size_t)CHUNK_TILES * 16 * MT * 4;   // two buffers: row groups alternate
     }
@@ -264,9 +271,11 @@ __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
 // ---------------------------------------------------------------------------
 // COMPUTE
 // ---------------------------------------------------------------------------
-template <int MT, int CWT, int REGS, bool F16W, int FIXW>
+template <int MT, int CWT, int REGS, int WF, int FIXW>
 __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) gemv_q4_0_kernel(const Params p) {
-    constexpr int TB = tile_bytes(F16W), CB = chunk_bytes(F16W);
+    constexpr bool F16W = WF == WF_F16, Q8W = WF == WF_Q8;
+    constexpr int TB = tile_bytes(WF), CB = chunk_bytes(WF);
+    constexpr int SCALES = Q8W ? Q8_TILE_SCALE_OFFSET : TILE_SCALE_OFFSET;   // fp16 scales in a Q4_0 / Q8_0 tile
     using SH = Shape<CWT, FIXW>;
     constexpr int CW = SH::CW, TPW = SH::TPW, CONSUMERS = SH::CONSUMERS, THREADS = SH::THREADS;
     constexpr int PRODUCER_WARP = SH::PRODUCER_WARP, FIXUP_WARP = SH::FIXUP_WARP, FUSED_LOADS = SH::FUSED_LOADS;
@@ -282,7 +291,7 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                                              (int)((int64_t)p.N16 * (ci + 1) / p.Gs) * nts, nts, 1)
                                   : Segments((int)((int64_t)T * ci / p.Gs), (int)((int64_t)T * (ci + 1) / p.Gs), nts,
                                              p.S);
-    const Layout L(MT, p.M, p.ntmax, p.slots, p.maxfix, F16W);
+    const Layout L(MT, p.M, p.ntmax, p.slots, p.maxfix, WF);
     const Image im(p.M, p.ntmax, F16W);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + p.slots;
@@ -587,12 +596,14 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
             // the tile at position ti of the chunk, into the accumulators of position tw
             auto tile_dot = [&](const int tw, const int ti) {
                 const int tl = u + ti;                         // tile index within the slice
-                const uint8_t *tile = ring + (size_t)slot * CHUNK_BYTES + ti * TILE_BYTES;
-                const uint2 d4w = *reinterpret_cast<const uint2 *>(tile + TILE_SCALE_OFFSET + n * 8);
+                const uint8_t *tile = ring + (size_t)slot * CB + ti * TB;
+                const uint2 d4w = *reinterpret_cast<const uint2 *>(tile + SCALES + n * 8);
 #pragma unroll
                 for (int jj = 0; jj < 2; jj++) {
                     const int jb = jh + 2 * jj;                // block of the tile
-                    const uint4 q = lds128(tile + (jb * 16 + n) * 16);
+                    // Q4_0: the 16 code bytes of row n, block jb; Q8_0: its 32 codes
+                    const uint4 q = lds128(tile + (jb * 16 + n) * (Q8W ? 32 : 16));
+                    const uint4 q_hi = Q8W ? lds128(tile + (jb * 16 + n) * 32 + 16) : q;
                     const uint32_t dw = jb & 2 ? d4w.y : d4w.x;
                     const float d4 = (jb & 1) ? half_hi(dw) : half_lo(dw);
                     const int blk = 4 * tl + jb;
@@ -606,7 +617,7 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                         const uint4 a0 = lds128(a + mm * im.row_bytes);
                         const uint4 a1 = lds128(a + mm * im.row_bytes + 16);
                         const float2 sc = act_sc[mm * sc_stride + blk];
-                        const int sumi = block_dot(q, a0, a1, __float_as_int(sc.y));
+                        const int sumi = Q8W ? block_dot_s8(q, q_hi, a0, a1) : block_dot(q, a0, a1, __float_as_int(sc.y));
                         acc[tw][MMA ? 0 : m] = fmaf(d4 * sc.x, (float)sumi, acc[tw][MMA ? 0 : m]);
                     }
                 }
@@ -621,18 +632,26 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
             // f32 result is the exact block dot sumi.
             auto tile_mma = [&](const int tw, const int ti) {
                 const int tl = u + ti;
-                const uint8_t *tile = ring + (size_t)slot * CHUNK_BYTES + ti * TILE_BYTES;
-                const uint2 s0 = *reinterpret_cast<const uint2 *>(tile + TILE_SCALE_OFFSET + fg * 8);
-                const uint2 s1 = *reinterpret_cast<const uint2 *>(tile + TILE_SCALE_OFFSET + (fg + 8) * 8);
+                const uint8_t *tile = ring + (size_t)slot * CB + ti * TB;
+                const uint2 s0 = *reinterpret_cast<const uint2 *>(tile + SCALES + fg * 8);
+                const uint2 s1 = *reinterpret_cast<const uint2 *>(tile + SCALES + (fg + 8) * 8);
 #pragma unroll
                 for (int jb = 0; jb < 4; jb++) {
-                    const uint32_t w0 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg) * 16 + 4 * ft);
-                    const uint32_t w1 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg + 8) * 16 + 4 * ft);
                     uint32_t alo[4], ahi[4];
-                    q4_to_f16x2(w0 & 0x0F0F0F0Fu, alo[0], alo[2]);
-                    q4_to_f16x2(w1 & 0x0F0F0F0Fu, alo[1], alo[3]);
-                    q4_to_f16x2((w0 >> 4) & 0x0F0F0F0Fu, ahi[0], ahi[2]);
-                    q4_to_f16x2((w1 >> 4) & 0x0F0F0F0Fu, ahi[1], ahi[3]);
+                    if constexpr (Q8W) {   // elements 4ft .. 4ft+3 (word ft) and 16 + 4ft .. (word ft + 4)
+                        const uint8_t *r0 = tile + (jb * 16 + fg) * 32 + 4 * ft, *r1 = r0 + 8 * 32;
+                        q8_to_f16x2(*reinterpret_cast<const uint32_t *>(r0), alo[0], alo[2]);
+                        q8_to_f16x2(*reinterpret_cast<const uint32_t *>(r1), alo[1], alo[3]);
+                        q8_to_f16x2(*reinterpret_cast<const uint32_t *>(r0 + 16), ahi[0], ahi[2]);
+                        q8_to_f16x2(*reinterpret_cast<const uint32_t *>(r1 + 16), ahi[1], ahi[3]);
+                    } else {
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg) * 16 + 4 * ft);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg + 8) * 16 + 4 * ft);
+                        q4_to_f16x2(w0 & 0x0F0F0F0Fu, alo[0], alo[2]);
+                        q4_to_f16x2(w1 & 0x0F0F0F0Fu, alo[1], alo[3]);
+                        q4_to_f16x2((w0 >> 4) & 0x0F0F0F0Fu, ahi[0], ahi[2]);
+                        q4_to_f16x2((w1 >> 4) & 0x0F0F0F0Fu, ahi[1], ahi[3]);
+                    }
                     const uint32_t sw0 = jb & 2 ? s0.y : s0.x, sw1 = jb & 2 ? s1.y : s1.x;
                     const float d4r0 = (jb & 1) ? half_hi(sw0) : half_lo(sw0);   // row fg
                     const float d4r1 = (jb & 1) ? half_hi(sw1) : half_lo(sw1);   // row fg + 8
@@ -802,23 +821,25 @@ Plan plan(int N16, int NT, int M, bool f16 = false) {
 // runs one CTA per SM at 96 registers.
 struct Variant {
     int mt, cw, regs;
-    bool f16;
+    int wf;
     int fixw;
     int consumers, threads, fused_loads;
     void (*kernel)(Params);
 };
 
-template <int MT, int CW, int REGS, bool F16W, int FIXW>
+template <int MT, int CW, int REGS, int WF, int FIXW>
 constexpr Variant variant() {
     using SH = Shape<CW, FIXW>;
-    return {MT, CW, REGS, F16W, FIXW, SH::CONSUMERS, SH::THREADS, SH::FUSED_LOADS,
-            gemv_q4_0_kernel<MT, CW, REGS, F16W, FIXW>};
+    return {MT, CW, REGS, WF, FIXW, SH::CONSUMERS, SH::THREADS, SH::FUSED_LOADS,
+            gemv_q4_0_kernel<MT, CW, REGS, WF, FIXW>};
 }
 
 const Variant VARIANTS[] = {
-    variant<1, 8, 88, false, 0>(),  variant<1, 8, 88, false, 1>(),  variant<2, 16, 96, false, 2>(),
-    variant<4, 16, 96, false, 2>(), variant<8, 16, 96, false, 2>(), variant<16, 16, 96, false, 2>(),
-    variant<8, 8, 88, true, 0>(),   variant<8, 8, 88, true, 1>(),   variant<16, 16, 96, true, 2>()};
+    variant<1, 8, 88, WF_Q4, 0>(),   variant<1, 8, 88, WF_Q4, 1>(),   variant<2, 16, 96, WF_Q4, 2>(),
+    variant<4, 16, 96, WF_Q4, 2>(),  variant<8, 16, 96, WF_Q4, 2>(),  variant<16, 16, 96, WF_Q4, 2>(),
+    variant<8, 8, 88, WF_F16, 0>(),  variant<8, 8, 88, WF_F16, 1>(),  variant<16, 16, 96, WF_F16, 2>(),
+    variant<1, 8, 88, WF_Q8, 0>(),   variant<1, 8, 88, WF_Q8, 1>(),   variant<2, 16, 96, WF_Q8, 2>(),
+    variant<4, 16, 96, WF_Q8, 2>(),  variant<8, 16, 96, WF_Q8, 2>(),  variant<16, 16, 96, WF_Q8, 2>()};
 constexpr int N_VARIANTS = sizeof(VARIANTS) / sizeof(VARIANTS[0]);
 static_assert(N_VARIANTS <= MAX_VARIANTS, "one shared-memory flag per variant");
 
@@ -827,9 +848,9 @@ int consumer_warps_for(int M) { return M == 1 ? 8 : 16; }
 
 int regs_for(int cw) { return cw == 16 ? 96 : 88; }
 
-const Variant *variant_for(int mt, int cw, int regs, bool f16, int fixw) {
+const Variant *variant_for(int mt, int cw, int regs, int wf, int fixw) {
     for (int i = 0; i < N_VARIANTS; i++)
-        if (VARIANTS[i].mt == mt && VARIANTS[i].cw == cw && VARIANTS[i].regs == regs && VARIANTS[i].f16 == f16 &&
+        if (VARIANTS[i].mt == mt && VARIANTS[i].cw == cw && VARIANTS[i].regs == regs && VARIANTS[i].wf == wf &&
             VARIANTS[i].fixw == fixw)
             return &VARIANTS[i];
     return nullptr;
@@ -837,7 +858,8 @@ const Variant *variant_for(int mt, int cw, int regs, bool f16, int fixw) {
 
 }  // namespace
 
-void gemv_workspace(bool f16, int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes) {
+void gemv_workspace(int wf, int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes) {
+    const bool f16 = wf == WF_F16;
     const int N16 = (int)((N + 15) / 16);
     const int NT = f16 ? (int)(K / F16_TILE_COLS) : (int)((K + TILE_COLS - 1) / TILE_COLS);
     size_t db = 0;
@@ -852,17 +874,18 @@ void gemv_workspace(bool f16, int64_t N, int64_t K, size_t *counter_bytes, size_
 }
 
 void gemv_q4_0_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes) {
-    gemv_workspace(false, N, K, counter_bytes, data_bytes);
+    gemv_workspace(WF_Q4, N, K, counter_bytes, data_bytes);
 }
 
 void gemv_f16r_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes) {
-    gemv_workspace(true, N, K, counter_bytes, data_bytes);
+    gemv_workspace(WF_F16, N, K, counter_bytes, data_bytes);
 }
 
 namespace {
 
-gq_status launch_gemv_with(bool f16, const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
                            const Workspace &ws, cudaStream_t s) {
+    const bool f16 = wf == WF_F16;
     Params p{};
     p.w = (const uint8_t *)rep;
     p.status = device_status_word();
@@ -897,7 +920,7 @@ gq_status launch_gemv_with(bool f16, const void *rep, const float *x, float *dst
                       ? 1
                       : 0;
         const int fixw = cw == 16 ? 2 : q.S == 1 ? 0 : 1;   // one K slice: no shared row group
-        const Variant *kvp = variant_for(MT, cw, regs_for(cw), f16, fixw);
+        const Variant *kvp = variant_for(MT, cw, regs_for(cw), wf, fixw);
         if (!kvp) return fail(GQ_ERR_INVALID_ARG, "gemv: no kernel for M=%d", p.M);
         const Variant &kv = *kvp;
         // behind INIT (which waited for every earlier grid) the weights are final; otherwise only
@@ -905,15 +928,16 @@ gq_status launch_gemv_with(bool f16, const void *rep, const float *x, float *dst
         p.early = (!p.fused || static_weights()) ? 1 : 0;
         p.part = reinterpret_cast<float *>(ws.data);
         p.wdata = ws.data + align_up((size_t)p.N16 * p.S * 2 * PART_STRIDE * sizeof(float), 256);
-        const size_t fixed = Layout(MT, p.M, p.ntmax, 0, p.maxfix, f16).total;
+        const size_t fixed = Layout(MT, p.M, p.ntmax, 0, p.maxfix, wf).total;
         auto slots_for = [&](size_t budget) {
             return (int)std::min<size_t>(MAX_SLOTS,
-                                         (budget - std::min(budget, fixed + 256)) / (chunk_bytes(f16) + 16));
+                                         (budget - std::min(budget, fixed + 256)) / (chunk_bytes(wf) + 16));
         };
         // the 8-warp Q4_0 shape keeps a ring of half the shared memory (MIN_SLOTS_HALF chunks at
         // least): two CTAs per SM without fix-up warps; with one, a half ring measured faster than
-        // a full one.  F16 tiles (twice the bytes per weight) keep a full ring, which measured faster.
-        p.slots = kv.cw == 8 && !f16 ? slots_for(SMEM_HALF - 1024) : 0;
+        // a full one.  F16 and Q8_0 tiles (more bytes per weight; 34 KB Q8_0 chunks would leave
+        // two slots in half the shared memory) keep a full ring.
+        p.slots = kv.cw == 8 && wf == WF_Q4 ? slots_for(SMEM_HALF - 1024) : 0;
         if (p.slots < MIN_SLOTS_HALF) p.slots = slots_for(SMEM_LIMIT - 1024);
         const int slots_env = env_int("GQ_GEMV_SLOTS", 0);   // tuning: ring slots, up to what fits
         if (slots_env > 0) p.slots = std::min(slots_env, slots_for(SMEM_LIMIT - 1024));
@@ -922,8 +946,8 @@ gq_status launch_gemv_with(bool f16, const void *rep, const float *x, float *dst
             return fail(GQ_ERR_INVALID_ARG, "gemv: N=%lld K=%lld leaves no room for the weight ring",
                         (long long)N, (long long)K);
         const int pf_kb = env_int("GQ_GEMV_PF_KB", PF_KB);   // tuning; negative: no L2 prefetch
-        p.pf = pf_kb < 0 ? 0 : p.slots + pf_kb * 1024 / chunk_bytes(f16);
-        const size_t smem = Layout(MT, p.M, p.ntmax, p.slots, p.maxfix, f16).total;
+        p.pf = pf_kb < 0 ? 0 : p.slots + pf_kb * 1024 / chunk_bytes(wf);
+        const size_t smem = Layout(MT, p.M, p.ntmax, p.slots, p.maxfix, wf).total;
         st = allow_smem(kv.kernel, (int)(&kv - VARIANTS));
         if (st != GQ_OK) return st;
         const int threads = kv.threads;
@@ -956,7 +980,7 @@ gq_status launch_gemv_with(bool f16, const void *rep, const float *x, float *dst
 
 gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
                                 const Workspace &ws, cudaStream_t s) {
-    return launch_gemv_with(false, rep, x, dst, M, N, K, ws, s);
+    return launch_gemv_with(WF_Q4, rep, x, dst, M, N, K, ws, s);
 }
 
 gq_status launch_gemv_f16r(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
@@ -966,7 +990,7 @@ gq_status launch_gemv_f16r(const void *rep, const float *x, float *dst, int64_t 
     Workspace ws;
     gq_status st = get_workspace(s, cb, db, &ws);
     if (st != GQ_OK) return st;
-    return launch_gemv_with(true, rep, x, dst, M, N, K, ws, s);
+    return launch_gemv_with(WF_F16, rep, x, dst, M, N, K, ws, s);
 }
 
 gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
@@ -977,6 +1001,16 @@ gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t 
     gq_status st = get_workspace(s, cb, db, &ws);
     if (st != GQ_OK) return st;
     return launch_gemv_q4_0_with(rep, x, dst, M, N, K, ws, s);
+}
+
+gq_status launch_gemv_q8_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t s) {
+    size_t cb, db;
+    gemv_workspace(WF_Q8, N, K, &cb, &db);
+    Workspace ws;
+    gq_status st = get_workspace(s, cb, db, &ws);
+    if (st != GQ_OK) return st;
+    return launch_gemv_with(WF_Q8, rep, x, dst, M, N, K, ws, s);
 }
 
 }  // namespace gq

@@ -313,6 +313,34 @@ gq_status gq_mul_mat_f16_f32(const void *src0_f16, const float *src1, float *dst
     return gq_mul_mat_f16_f32_path(src0_f16, src1, dst, M, N, K, GQ_PATH_AUTO, stream);
 }
 
+size_t gq_q8_0_repacked_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % QK) return 0;
+    return (size_t)((N + 15) / 16) * (size_t)((K / QK + TILE_BLOCKS - 1) / TILE_BLOCKS) * 2176;
+}
+
+gq_status gq_repack_q8_0(const void *q8_blocks, void *q8_repacked, int64_t N, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(1, N, K));
+    GQ_TRY(check_ptr(q8_blocks, "q8_blocks"));
+    GQ_TRY(check_ptr(q8_repacked, "q8_repacked"));
+    const uintptr_t a = (uintptr_t)q8_blocks, b = (uintptr_t)q8_repacked;
+    if (a < b + gq_q8_0_repacked_bytes(N, K) && b < a + gq_q8_0_bytes(N, K))
+        return fail(GQ_ERR_INVALID_ARG, "q8_blocks and q8_repacked overlap");
+    GQ_TRY(check_device());
+    GQ_TRY(launch_repack_q8_0(q8_blocks, q8_repacked, N, K, stream));
+    return ok();
+}
+
+gq_status gq_mul_mat_q8_0_f32(const void *q8_repacked, const float *src1, float *dst, int64_t M, int64_t N,
+                              int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(M, N, K));
+    GQ_TRY(check_ptr(q8_repacked, "q8_repacked"));
+    GQ_TRY(check_ptr(src1, "src1"));
+    GQ_TRY(check_ptr(dst, "dst"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_gemv_q8_0(q8_repacked, src1, dst, M, N, K, stream));
+    return ok();
+}
+
 size_t gq_f16_repacked_bytes(int64_t N, int64_t K) {
     if (N <= 0 || K <= 0 || K % QK) return 0;
     return (size_t)((N + 15) / 16) * (size_t)(K / 32) * 1024;

@@ -197,6 +197,20 @@ __device__ __forceinline__ int block_dot(uint4 w, uint4 a0, uint4 a1, int corr) 
     return lo + (hi >> 4);
 }
 
+// Q8_0 weights: w0, w1 the 32 signed codes of a block, a0, a1 the activation codes (exact int32).
+__device__ __forceinline__ int block_dot_s8(uint4 w0, uint4 w1, uint4 a0, uint4 a1) {
+    int s0 = 0, s1 = 0;
+    s0 = __dp4a((int)w0.x, (int)a0.x, s0);
+    s1 = __dp4a((int)w1.x, (int)a1.x, s1);
+    s0 = __dp4a((int)w0.y, (int)a0.y, s0);
+    s1 = __dp4a((int)w1.y, (int)a1.y, s1);
+    s0 = __dp4a((int)w0.z, (int)a0.z, s0);
+    s1 = __dp4a((int)w1.z, (int)a1.z, s1);
+    s0 = __dp4a((int)w0.w, (int)a0.w, s0);
+    s1 = __dp4a((int)w1.w, (int)a1.w, s1);
+    return s0 + s1;
+}
+
 // D(16x8, f32) += A(16x16, f16, row) . B(16x8, f16, col)
 __device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                 uint32_t a3, uint32_t b0, uint32_t b1) {

@@ -57,6 +57,10 @@ gq_status launch_repack_f16(const void *w16, void *rep, int64_t N, int64_t K, cu
 void gemv_f16r_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes);
 gq_status launch_gemv_f16r(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
                            cudaStream_t s);
+// Q8_0 weights: the repack into 16-row x 4-block tiles (2176 bytes) and the GEMV on them.
+gq_status launch_repack_q8_0(const void *q8, void *rep, int64_t N, int64_t K, cudaStream_t s);
+gq_status launch_gemv_q8_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t s);
 // Tensor-core tiles (tcgen05) for M >= 32; workspace: the fp16 activations.
 size_t tc_workspace_bytes(int64_t M, int64_t K);
 gq_status launch_tc_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,

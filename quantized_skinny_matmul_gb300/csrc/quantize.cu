@@ -111,6 +111,37 @@ __global__ void repack_f16_kernel(const uint8_t *__restrict__ w, uint8_t *__rest
     }
 }
 
+// Q8_0 blocks [N][nb] x 34 -> tiles of 16 rows x 4 blocks: the 32 codes of block j of row r at
+// (j * 16 + r) * 32, then the fp16 scale at 2048 + (r * 4 + j) * 2; tile (g, t) at (g * NT + t) * 2176.
+// One thread per (tile, row, block); rows past N and blocks past nb hold codes 0 and scale 0.
+__global__ void repack_q8_0_kernel(const uint8_t *__restrict__ q8, uint8_t *__restrict__ out, int64_t N,
+                                   int64_t nb, int64_t NT, int64_t items) {
+    constexpr int TB = 16 * TILE_BLOCKS * (QK + 2), SC = 16 * TILE_BLOCKS * QK;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = i / 64, rj = i % 64;
+        const int r = (int)(rj / 4), j = (int)(rj % 4);
+        const int64_t g = tile / NT, t = tile % NT;
+        const int64_t n = 16 * g + r, b = 4 * t + j;
+        uint8_t *dt = out + tile * TB;
+        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
+        uint16_t d = 0;
+        if (n < N && b < nb) {
+            const uint8_t *src = q8 + (n * nb + b) * 34;
+            uint32_t w[8];
+            for (int k = 0; k < 8; k++)
+                w[k] = (uint32_t)src[2 + 4 * k] | ((uint32_t)src[3 + 4 * k] << 8) | ((uint32_t)src[4 + 4 * k] << 16) |
+                       ((uint32_t)src[5 + 4 * k] << 24);
+            c0 = make_uint4(w[0], w[1], w[2], w[3]);
+            c1 = make_uint4(w[4], w[5], w[6], w[7]);
+            d = (uint16_t)(src[0] | (src[1] << 8));
+        }
+        *reinterpret_cast<uint4 *>(dt + (j * 16 + r) * 32) = c0;
+        *reinterpret_cast<uint4 *>(dt + (j * 16 + r) * 32 + 16) = c1;
+        *reinterpret_cast<uint16_t *>(dt + SC + (r * 4 + j) * 2) = d;
+    }
+}
+
 int grid_for(int64_t work_items, int threads) {
     int64_t blocks = (work_items + threads - 1) / threads;
     const int64_t cap = (int64_t)sm_count() * 16;
@@ -140,6 +171,12 @@ gq_status launch_repack_q4_0(const void *q4, void *rep, int64_t N, int64_t K, cu
     const int64_t blocks = (threads + 255) / 256;
     repack_q4_0_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint8_t *)q4, (uint8_t *)rep, N, nb, NT, ntiles);
     return check_cuda(cudaGetLastError(), "repack_q4_0 launch");
+}
+
+gq_status launch_repack_q8_0(const void *q8, void *rep, int64_t N, int64_t K, cudaStream_t s) {
+    const int64_t nb = K / QK, NT = (nb + TILE_BLOCKS - 1) / TILE_BLOCKS, items = (N + 15) / 16 * NT * 64;
+    repack_q8_0_kernel<<<grid_for(items, 256), 256, 0, s>>>((const uint8_t *)q8, (uint8_t *)rep, N, nb, NT, items);
+    return check_cuda(cudaGetLastError(), "repack_q8_0 launch");
 }
 
 gq_status launch_repack_f16(const void *w16, void *rep, int64_t N, int64_t K, cudaStream_t s) {

@@ -58,3 +58,33 @@ def repack_f16_loops(w16: np.ndarray) -> np.ndarray:
                     n = 16 * g + r
                     out[((g * NT + t) * 1024 + r * 64 + 2 * c) // 2] = w16[n, 32 * t + c] if n < N else 0
     return out.view(np.uint8)
+
+
+def repack_q8_0_ref(q8: np.ndarray) -> np.ndarray:
+    """Q8_0 blocks [N, nb, 34] -> the tile layout of gq_repack_q8_0, as bytes."""
+    N, nb = q8.shape[0], q8.shape[1]
+    N16, NT = -(-N // 16), -(-nb // 4)
+    P = np.zeros((N16 * 16, NT * 4, 34), np.uint8)
+    P[:N, :nb] = q8
+    T = P.reshape(N16, 16, NT, 4, 34).transpose(0, 2, 3, 1, 4)   # [g, t, j, r, 34]
+    out = np.empty((N16, NT, 2176), np.uint8)
+    out[:, :, :2048] = T[..., 2:].reshape(N16, NT, 2048)
+    out[:, :, 2048:] = T[..., :2].transpose(0, 1, 3, 2, 4).reshape(N16, NT, 128)   # [r, j, 2]
+    return out.reshape(-1)
+
+
+def repack_q8_0_loops(q8: np.ndarray) -> np.ndarray:
+    """The same layout, byte by byte, in the words of the header (small sizes)."""
+    N, nb = q8.shape[0], q8.shape[1]
+    N16, NT = -(-N // 16), -(-nb // 4)
+    out = np.zeros(N16 * NT * 2176, np.uint8)
+    for g in range(N16):
+        for t in range(NT):
+            base = (g * NT + t) * 2176
+            for j in range(4):
+                for r in range(16):
+                    n, b = 16 * g + r, 4 * t + j
+                    if n < N and b < nb:
+                        out[base + (j * 16 + r) * 32: base + (j * 16 + r) * 32 + 32] = q8[n, b, 2:]
+                        out[base + 2048 + (r * 4 + j) * 2: base + 2048 + (r * 4 + j) * 2 + 2] = q8[n, b, :2]
+    return out

@@ -19,3 +19,11 @@ def test_f16_layout_statements_agree(N, K):
     rng = np.random.default_rng(N * 1000 + K)
     w16 = rng.integers(0, 1 << 16, size=(N, K), dtype=np.uint16)
     assert np.array_equal(repack_f16_ref(w16), repack_f16_loops(w16))
+
+
+@pytest.mark.parametrize("N,nb", [(16, 4), (37, 3), (33, 9), (1, 1)])
+def test_q8_0_layout_statements_agree(N, nb):
+    from layout_ref import repack_q8_0_ref, repack_q8_0_loops
+    rng = np.random.default_rng(N * 10 + nb)
+    q8 = rng.integers(0, 256, size=(N, nb, 34), dtype=np.uint8)
+    assert np.array_equal(repack_q8_0_ref(q8), repack_q8_0_loops(q8))
