@@ -9,8 +9,8 @@
  *
  * What is computed (the llama.cpp MUL_MAT of the q_f32 and f16_f32 kinds):
  *     dst[m][n] = sum_k src0[n][k] * src1[m][k]
- * with src0 Q4_0 or Q8_0 block-quantized weights or F16 weights, and src1 F32
- * activations.  For the Q4_0 kind, src1 is first quantized row by row into
+ * with src0 Q4_0, Q5_0 or Q8_0 block-quantized weights or F16 weights, and src1
+ * F32 activations.  For the Q4_0 kind, src1 is first quantized row by row into
  * Q8_0 blocks (the "wdata" buffer) and the product is taken as integer block
  * dot products scaled by the two block scales:
  *   - llama.cpp pull request #1632, "Introduction": the three MUL_MAT kinds
@@ -47,6 +47,7 @@
 #define QK 32            /* values per block */
 #define Q4_0_BYTES 18    /* 2-byte scale + 16 bytes of nibbles */
 #define Q8_0_BYTES 34    /* 2-byte scale + 32 int8 */
+#define Q5_0_BYTES 22    /* 2-byte scale + 4 bytes of fifth bits + 16 bytes of nibbles */
 
 /* ---------------------------------------------------------------------------
  * IEEE 754 binary16, written from the format's definition.
@@ -185,8 +186,55 @@ void oracle_quantize_q8_0(const float *x, uint8_t *out, int64_t M, int64_t K)
 }
 
 /* ---------------------------------------------------------------------------
+ * Q5_0 quantization of one block of 32 weights.  llama.cpp PR #1632, "Results":
+ * Q5_0 is one of the three types measured on 7B; the pages do not define it,
+ * and this library reads it as Q4_0 with five-bit codes: block (22 bytes) =
+ * fp16 d, a little-endian 32-bit word qh whose bit j is bit 4 of q_j, then 16
+ * bytes with the low four bits of q_i in the low nibble and those of q_{i+16}
+ * in the high nibble of byte i.  m = the element of largest magnitude (the
+ * first one wins), d = m / -16, q_j = clamp(round(x_j / d) + 16, 0, 31)
+ * (q_j = 16 when d == 0); the weight is (q_j - 16) * fp16(d).
+ * ------------------------------------------------------------------------- */
+static void quantize_block_q5_0(const float *x, uint8_t *out)
+{
+    float amax = 0.0f, vmax = 0.0f;
+    for (int j = 0; j < QK; j++) {
+        float a = fabsf(x[j]);
+        if (a > amax) { amax = a; vmax = x[j]; }   /* strict: the first wins */
+    }
+    float d = vmax / -16.0f;
+    int q[QK];
+    for (int j = 0; j < QK; j++) {
+        if (d != 0.0f) {
+            int v = (int)roundf(x[j] / d) + 16;
+            q[j] = v < 0 ? 0 : (v > 31 ? 31 : v);
+        } else {
+            q[j] = 16;
+        }
+    }
+    uint32_t qh = 0;
+    for (int j = 0; j < QK; j++)
+        qh |= (uint32_t)((q[j] >> 4) & 1) << j;
+    put_f16(out, oracle_f32_to_f16(d));
+    for (int k = 0; k < 4; k++)
+        out[2 + k] = (uint8_t)(qh >> (8 * k));
+    for (int i = 0; i < QK / 2; i++)
+        out[6 + i] = (uint8_t)((q[i] & 0x0f) | ((q[i + QK / 2] & 0x0f) << 4));
+}
+
+/* w: f32 [N][K]; out: Q5_0 blocks [N][K/32] x 22 bytes. */
+void oracle_quantize_q5_0(const float *w, uint8_t *out, int64_t N, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < nb; b++)
+            quantize_block_q5_0(w + n * K + b * QK, out + (n * nb + b) * Q5_0_BYTES);
+}
+
+/* ---------------------------------------------------------------------------
  * De-quantization (for the invariant checks): value = (q - 8) * d  (Q4_0),
- * value = q * d (Q8_0), in f64 (both products are exact).
+ * value = (q - 16) * d (Q5_0), value = q * d (Q8_0), in f64 (the products are
+ * exact).
  * ------------------------------------------------------------------------- */
 static int q4_code(const uint8_t *blk, int j)
 {
@@ -195,6 +243,26 @@ static int q4_code(const uint8_t *blk, int j)
 }
 
 static int q8_code(const uint8_t *blk, int j) { return (int)(int8_t)blk[2 + j]; }
+
+static int q5_code(const uint8_t *blk, int j)
+{
+    uint32_t qh = (uint32_t)blk[2] | ((uint32_t)blk[3] << 8) | ((uint32_t)blk[4] << 16) | ((uint32_t)blk[5] << 24);
+    uint8_t byte = blk[6 + (j % (QK / 2))];
+    int lo = j < QK / 2 ? (byte & 0x0f) : (byte >> 4);
+    return lo | (int)(((qh >> j) & 1u) << 4);
+}
+
+void oracle_dequantize_q5_0(const uint8_t *q5, double *out, int64_t N, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = q5 + (n * nb + b) * Q5_0_BYTES;
+            double d = (double)oracle_f16_to_f32(get_f16(blk));
+            for (int j = 0; j < QK; j++)
+                out[n * K + b * QK + j] = (double)(q5_code(blk, j) - 16) * d;
+        }
+}
 
 void oracle_dequantize_q4_0(const uint8_t *q4, double *out, int64_t N, int64_t K)
 {
@@ -372,6 +440,75 @@ void oracle_mul_mat_q8_0_q8_0_at(const uint8_t *qw, const uint8_t *qx, const int
     int64_t nb = K / QK;
     for (int64_t i = 0; i < count; i++)
         dot_row_q8_0_q8_0(qw + ns[i] * nb * Q8_0_BYTES, qx + ms[i] * nb * Q8_0_BYTES, nb,
+                          &out[i], &T[i]);
+}
+
+/* ---------------------------------------------------------------------------
+ * The q_f32 kind with Q5_0 weights (the format above), src1 in Q8_0 as for
+ * Q4_0:  sumi = sum_{j<32} (q5_j - 16) * q8_j      (|sumi| <= 32*16*127)
+ *        dst = sum_b d5_b * d8_b * sumi_b (f64),  T = sum_b |d5| |d8| sum_j |q5_j - 16| |q8_j|
+ * ------------------------------------------------------------------------- */
+static int32_t block_dot_q5_0(const uint8_t *b5, const uint8_t *b8)
+{
+    int32_t s = 0;
+    for (int j = 0; j < QK; j++)
+        s += (int32_t)(q5_code(b5, j) - 16) * (int32_t)q8_code(b8, j);
+    return s;
+}
+
+/* sumi: int32 [M][N][K/32] */
+void oracle_block_dots_q5_0(const uint8_t *q5, const uint8_t *q8, int32_t *sumi,
+                            int64_t M, int64_t N, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = 0; n < N; n++)
+            for (int64_t b = 0; b < nb; b++)
+                sumi[(m * N + n) * nb + b] =
+                    block_dot_q5_0(q5 + (n * nb + b) * Q5_0_BYTES, q8 + (m * nb + b) * Q8_0_BYTES);
+}
+
+static void dot_row_q5_0_q8_0(const uint8_t *row5, const uint8_t *row8, int64_t nb,
+                              double *dst, double *T)
+{
+    double acc = 0.0, tacc = 0.0;
+    for (int64_t b = 0; b < nb; b++) {
+        const uint8_t *b5 = row5 + b * Q5_0_BYTES;
+        const uint8_t *b8 = row8 + b * Q8_0_BYTES;
+        double d5 = (double)oracle_f16_to_f32(get_f16(b5));
+        double d8 = (double)oracle_f16_to_f32(get_f16(b8));
+        acc += d5 * d8 * (double)block_dot_q5_0(b5, b8);
+        int64_t sabs = 0;
+        for (int j = 0; j < QK; j++)
+            sabs += (int64_t)abs(q5_code(b5, j) - 16) * (int64_t)abs(q8_code(b8, j));
+        tacc += fabs(d5) * fabs(d8) * (double)sabs;
+    }
+    *dst = acc;
+    *T = tacc;
+}
+
+int oracle_mul_mat_q5_0_f32(const uint8_t *q5, const float *src1, double *dst, double *T,
+                            int64_t M, int64_t N, int64_t K, int64_t n_begin, int64_t n_end)
+{
+    int64_t nb = K / QK;
+    uint8_t *wdata = (uint8_t *)malloc((size_t)(M * nb * Q8_0_BYTES) + 1);
+    if (!wdata) return 1;
+    oracle_quantize_q8_0(src1, wdata, M, K);
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = n_begin; n < n_end; n++)
+            dot_row_q5_0_q8_0(q5 + n * nb * Q5_0_BYTES, wdata + m * nb * Q8_0_BYTES, nb,
+                              &dst[m * N + n], &T[m * N + n]);
+    free(wdata);
+    return 0;
+}
+
+void oracle_mul_mat_q5_0_q8_0_at(const uint8_t *q5, const uint8_t *q8, const int64_t *ms,
+                                 const int64_t *ns, int64_t count, int64_t K,
+                                 double *out, double *T)
+{
+    int64_t nb = K / QK;
+    for (int64_t i = 0; i < count; i++)
+        dot_row_q5_0_q8_0(q5 + ns[i] * nb * Q5_0_BYTES, q8 + ms[i] * nb * Q8_0_BYTES, nb,
                           &out[i], &T[i]);
 }
 

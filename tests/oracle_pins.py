@@ -40,6 +40,16 @@ def decode_q4_0(q4: np.ndarray):
     return codes, d
 
 
+def decode_q5_0(q5: np.ndarray):
+    """(codes uint8 [..., 32] in 0..31, fp16 scale as f64 [...]) from Q5_0 bytes."""
+    d = q5[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    qh = q5[..., 2:6].copy().view(np.uint32)[..., 0]
+    qs = q5[..., 6:22]
+    lo = np.concatenate([qs & 0x0F, qs >> 4], axis=-1)
+    hi = (qh[..., None] >> np.arange(32, dtype=np.uint32)) & 1
+    return (lo | (hi << 4)).astype(np.uint8), d
+
+
 def decode_q8_0(q8: np.ndarray):
     d = q8[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
     codes = q8[..., 2:34].view(np.int8)
@@ -108,6 +118,8 @@ def pin_worked_examples(o) -> None:
     for name, kind, x, want in parse_golden():
         if kind == "q4_0":
             got = o.quantize_q4_0(x.reshape(1, 32)).tobytes()
+        elif kind == "q5_0":
+            got = o.quantize_q5_0(x.reshape(1, 32)).tobytes()
         else:
             got = o.quantize_q8_0(x.reshape(1, 32)).tobytes()
         assert got == want, f"{name}: {got.hex(' ')} != {want.hex(' ')}"
@@ -293,6 +305,92 @@ def pin_f16_matmul(o) -> None:
     assert np.array_equal(at, dst[ms, ns])
 
 
+def _q5_block(codes, d16_bits=0x3C00) -> np.ndarray:
+    codes = np.asarray(codes, np.int64)
+    out = np.empty(22, np.uint8)
+    out[0], out[1] = d16_bits & 0xFF, d16_bits >> 8
+    qh = int(sum(((int(c) >> 4) & 1) << j for j, c in enumerate(codes)))
+    out[2:6] = np.frombuffer(qh.to_bytes(4, "little"), np.uint8)
+    out[6:] = ((codes[:16] & 0x0F) | ((codes[16:] & 0x0F) << 4)).astype(np.uint8)
+    return out
+
+
+def pin_q5_0_quantizer(o) -> None:
+    """Q5_0: exact round trips of codes times a power of two (a -16 code present) and of their
+    negation; codes in 0..31; de-quantization error within |d|/2 (|d| where clamped);
+    zero blocks are a zero scale with code 16."""
+    rng = np.random.default_rng(25)
+    N, nb = 48, 8
+    c = rng.integers(-16, 16, size=(N, nb, 32))
+    c[:, :, 3] = -16
+    e = rng.integers(-12, 4, size=(N, nb, 1))
+    x = (c * np.exp2(e)).astype(np.float32).reshape(N, nb * 32)
+    codes, d = decode_q5_0(o.quantize_q5_0(x))
+    assert np.array_equal(codes.astype(np.int64) - 16, c)
+    assert np.array_equal(d, np.exp2(e[..., 0]).astype(np.float64))
+    codes, d = decode_q5_0(o.quantize_q5_0(-x))
+    assert np.array_equal(d, -np.exp2(e[..., 0]).astype(np.float64))
+    assert np.array_equal(codes.astype(np.int64) - 16, c)
+    assert np.array_equal(o.dequantize_q5_0(o.quantize_q5_0(x)), x.astype(np.float64))
+    w = synth.edge_weights(26, 40, 512)
+    codes, d5 = decode_q5_0(o.quantize_q5_0(w))
+    assert codes.min() >= 0 and codes.max() <= 31
+    wb = w.reshape(codes.shape).astype(np.float64)
+    am = np.abs(wb).max(-1)
+    first = np.argmax(np.abs(wb) == am[..., None], axis=-1)
+    vmax = np.take_along_axis(wb, first[..., None], -1)[..., 0]
+    dq = (vmax.astype(np.float32) / np.float32(-16.0)).astype(np.float64)
+    assert np.array_equal(d5, dq.astype(np.float16).astype(np.float64))
+    err = np.abs(wb - (codes.astype(np.float64) - 16) * d5[..., None])
+    with np.errstate(divide="ignore", invalid="ignore"):
+        clamp = np.abs(wb / dq[..., None]) > 15.5
+    bound = np.where(clamp, np.abs(dq)[..., None], np.abs(dq)[..., None] / 2) * (1 + 1e-6) \
+        + 16 * np.abs(dq - d5)[..., None]
+    assert np.all(err <= bound + 1e-30), "Q5_0 de-quantization error above its bound"
+    z = np.all(wb == 0, axis=-1)
+    assert np.all(d5[z] == 0) and np.all(codes[z] == 16)
+
+
+def pin_q5_0_block_dot_and_product(o) -> None:
+    """Q5_0: block dots by brute force for every code against every Q8_0 code in a few lanes;
+    the product against the float64 dense matmul of the de-quantized operands; row independence."""
+    q5v = np.arange(32)
+    q8v = np.arange(-127, 128)
+    for lane in (0, 4, 15, 16, 20, 31):
+        b5 = []
+        for a in q5v:
+            c = np.full(32, 16)
+            c[lane] = a
+            b5.append(_q5_block(c))
+        b8 = []
+        for b in q8v:
+            c = np.zeros(32, np.int64)
+            c[lane] = b
+            b8.append(_q8_block(c))
+        got = o.block_dots_q5_0(np.stack(b5)[:, None, :], np.stack(b8)[:, None, :])[:, :, 0]
+        assert np.array_equal(got, np.outer(q8v, q5v - 16)), f"Q5_0 block dot wrong at lane {lane}"
+    got = o.block_dots_q5_0(_q5_block(np.zeros(32))[None, None], _q8_block(np.full(32, -127))[None, None])
+    assert int(got[0, 0, 0]) == 65024
+    for (M, N, K, seed, outl) in ((3, 40, 96, 31, False), (5, 33, 256, 32, True), (1, 17, 32, 33, False)):
+        w, x = synth.problem(seed, M, N, K, outliers=outl)
+        q5 = o.quantize_q5_0(w)
+        q8 = o.quantize_q8_0(x)
+        A = o.dequantize_q5_0(q5)
+        B = o.dequantize_q8_0(q8)
+        c5, d5 = decode_q5_0(q5)
+        assert np.array_equal(A, ((c5.astype(np.float64) - 16) * d5[..., None]).reshape(N, K))
+        want, T_want = B @ A.T, np.abs(B) @ np.abs(A).T
+        dst, T = o.mul_mat_q5_0_f32(q5, x)
+        assert np.all(np.abs(dst - want) <= 1e-12 * T_want + 1e-300), "Q5_0 product mismatch"
+        assert np.allclose(T, T_want, rtol=1e-12, atol=0)
+        ms, ns = np.array([0, M - 1, M // 2]), np.array([N - 1, 0, N // 2])
+        at, T_at = o.mul_mat_q5_0_q8_0_at(q5, q8, ms, ns)
+        assert np.array_equal(at, dst[ms, ns]) and np.array_equal(T_at, T[ms, ns])
+        for m in range(M):
+            one, _ = o.mul_mat_q5_0_f32(q5, x[m:m + 1])
+            assert np.array_equal(one[0], dst[m])
+
+
 def pin_q8_0_block_dot_bruteforce(o) -> None:
     """Q8_0 weights, one lane at a time: sumi = qw * qx for every qw in -127..127 against a
     spread of qx; the extreme block (all 127 against all -127) gives -32 * 127 * 127."""
@@ -359,4 +457,6 @@ ALL_PINS = [
     pin_f16_matmul,
     pin_q8_0_block_dot_bruteforce,
     pin_q8_0_matmul_vs_dense,
+    pin_q5_0_quantizer,
+    pin_q5_0_block_dot_and_product,
 ]

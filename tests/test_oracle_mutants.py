@@ -20,8 +20,10 @@ MUTANTS = {
                      "out[2 + i] = (uint8_t)((q[i] << 4) | q[i + QK / 2]);"),
     "q4_offset": ("s += (int32_t)(q4_code(b4, j) - 8) * (int32_t)q8_code(b8, j);",
                   "s += (int32_t)(q4_code(b4, j) - 7) * (int32_t)q8_code(b8, j);"),
-    "q4_tie_break": ("if (a > amax) { amax = a; vmax = x[j]; }",
-                     "if (a >= amax) { amax = a; vmax = x[j]; }"),
+    "q4_tie_break": ("if (a > amax) { amax = a; vmax = x[j]; }   /* strict: the first wins */\n    }\n    float d = vmax / -8.0f;",
+                     "if (a >= amax) { amax = a; vmax = x[j]; }\n    }\n    float d = vmax / -8.0f;"),
+    "q5_tie_break": ("if (a > amax) { amax = a; vmax = x[j]; }   /* strict: the first wins */\n    }\n    float d = vmax / -16.0f;",
+                     "if (a >= amax) { amax = a; vmax = x[j]; }\n    }\n    float d = vmax / -16.0f;"),
     "q4_scale_sign": ("float d = vmax / -8.0f;", "float d = vmax / 8.0f;"),
     "q4_round_even": ("int v = (int)roundf(x[j] / d) + 8;", "int v = (int)rintf(x[j] / d) + 8;"),
     "q8_round_even": ("v = (int)roundf(x[j] / d);", "v = (int)rintf(x[j] / d);"),
@@ -45,6 +47,12 @@ MUTANTS = {
                        "acc += dx * (double)block_dot_q8_0(bw, bx);"),
     "q8w_shifted_lane": ("s += (int32_t)q8_code(bw, j) * (int32_t)q8_code(bx, j);",
                          "s += (int32_t)q8_code(bw, j) * (int32_t)q8_code(bx, (j + 1) % QK);"),
+    "q5_offset": ("s += (int32_t)(q5_code(b5, j) - 16) * (int32_t)q8_code(b8, j);",
+                  "s += (int32_t)(q5_code(b5, j) - 15) * (int32_t)q8_code(b8, j);"),
+    "q5_fifth_bit_order": ("qh |= (uint32_t)((q[j] >> 4) & 1) << j;",
+                           "qh |= (uint32_t)((q[j] >> 4) & 1) << (QK - 1 - j);"),
+    "q5_scale_divisor": ("float d = vmax / -16.0f;", "float d = vmax / -15.0f;"),
+    "q5_clamp": ("q[j] = v < 0 ? 0 : (v > 31 ? 31 : v);", "q[j] = v < 0 ? 0 : (v > 31 ? 15 : v);"),
     "q8_abs_dropped": ("float a = fabsf(x[j]);\n        if (a > amax) amax = a;",
                        "float a = x[j];\n        if (a > amax) amax = a;"),
 }
