@@ -201,6 +201,33 @@ gq_status gq_repack_q8_0(const void *q8_blocks, void *q8_repacked, int64_t N, in
 gq_status gq_mul_mat_q8_0_f32(const void *q8_repacked, const float *src1, float *dst,
                               int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
+/* Q5_0 weights (llama.cpp PR #1632, "Results": Q5_0 is among the types measured
+ * on 7B; the pages do not define it, and this library reads it as Q4_0 with
+ * five-bit codes).  Block (22 bytes): fp16 d, a little-endian 32-bit word whose
+ * bit j is bit 4 of q_j, then 16 bytes with the low four bits of q_i in the low
+ * nibble and those of q_{i+16} in the high nibble of byte i; m = the element of
+ * largest magnitude (the first one on a tie), d = m / -16,
+ * q_j = clamp(round(x_j / d) + 16, 0, 31) (16 when d == 0), the weight is
+ * (q_j - 16) * fp16(d).  gq_quantize_q5_0 writes gq_q5_0_bytes(N, K) =
+ * N * K/32 * 22 bytes, byte-exact; gq_repack_q5_0 copies them once into tiles of
+ * 16 rows x 4 blocks, 1408 bytes each: the nibble bytes of block j of row r at
+ * (j * 16 + r) * 16, its fifth bits at 1024 + (j * 16 + r) * 4 (bit 8b + 7 - s
+ * holds the fifth bit of element b of group s; groups 0..3 are elements
+ * 4s .. 4s+3, groups 4..7 elements 16 + 4(s-4) ..), then the fp16 scales at
+ * 1280 + (r * 4 + j) * 2; tile (g, t) at (g * ceil(K/128) + t) * 1408; padding
+ * holds code 16 and scale 0.  gq_q5_0_repacked_bytes(N, K) = ceil(N/16) *
+ * ceil(K/128) * 1408.  gq_mul_mat_q5_0_f32: dst[M][N] = Q8_0(src1) . Q5_0(src0)^T,
+ * each output sum_b fp16(d5_b) * fp16(d8_b) * sumi_b with the exact int32 block
+ * dots sumi_b = sum_j (q5_j - 16) * q8_j, accumulated in f32 (the GEMV family for
+ * every M, 16 rows per launch; the stream's workspace as for the other products). */
+size_t gq_q5_0_bytes(int64_t N, int64_t K);            /* 0 if N <= 0, K <= 0 or K % 32 */
+size_t gq_q5_0_repacked_bytes(int64_t N, int64_t K);
+gq_status gq_quantize_q5_0(const float *w, void *q5_blocks, int64_t N, int64_t K, cudaStream_t stream);
+gq_status gq_repack_q5_0(const void *q5_blocks, void *q5_repacked, int64_t N, int64_t K,
+                         cudaStream_t stream);
+gq_status gq_mul_mat_q5_0_f32(const void *q5_repacked, const float *src1, float *dst,
+                              int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* Workspace.  The products keep a small device workspace per (device, stream):
  * partial sums of weight rows that several CTAs share, with per-row counters
  * that every launch leaves at zero, and (tensor-core path) the quantized

@@ -70,6 +70,11 @@ SIGNATURES = {
     "gq_debug_block_dots_q4_0": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_noalloc": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_host": ([_P, _P, _P, _I, _I, _I, _P], _S),
+    "gq_q5_0_bytes": ([_I, _I], ctypes.c_size_t),
+    "gq_q5_0_repacked_bytes": ([_I, _I], ctypes.c_size_t),
+    "gq_quantize_q5_0": ([_P, _P, _I, _I, _P], _S),
+    "gq_repack_q5_0": ([_P, _P, _I, _I, _P], _S),
+    "gq_mul_mat_q5_0_f32": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_q8_0_repacked_bytes": ([_I, _I], ctypes.c_size_t),
     "gq_repack_q8_0": ([_P, _P, _I, _I, _P], _S),
     "gq_mul_mat_q8_0_f32": ([_P, _P, _P, _I, _I, _I, _P], _S),
@@ -227,6 +232,27 @@ def gq_mul_mat_q4_0_f32_host(q4_repacked, src1_host, dst_host, M: int, N: int, K
                                           _stream(stream)), "gq_mul_mat_q4_0_f32_host")
 
 
+def gq_q5_0_bytes(N: int, K: int) -> int:
+    return lib().gq_q5_0_bytes(N, K)
+
+
+def gq_q5_0_repacked_bytes(N: int, K: int) -> int:
+    return lib().gq_q5_0_repacked_bytes(N, K)
+
+
+def gq_quantize_q5_0(w, q5_blocks, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_quantize_q5_0(_ptr(w), _ptr(q5_blocks), N, K, _stream(stream)), "gq_quantize_q5_0")
+
+
+def gq_repack_q5_0(q5_blocks, q5_repacked, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_repack_q5_0(_ptr(q5_blocks), _ptr(q5_repacked), N, K, _stream(stream)), "gq_repack_q5_0")
+
+
+def gq_mul_mat_q5_0_f32(q5_repacked, src1, dst, M: int, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_mul_mat_q5_0_f32(_ptr(q5_repacked), _ptr(src1), _ptr(dst), M, N, K, _stream(stream)),
+           "gq_mul_mat_q5_0_f32")
+
+
 def gq_q8_0_repacked_bytes(N: int, K: int) -> int:
     return lib().gq_q8_0_repacked_bytes(N, K)
 
@@ -352,4 +378,28 @@ def mul_mat_q8_0_f32(q8_repacked, src1, N: int, out=None):
     M, K = src1.shape
     dst = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=src1.device)
     gq_mul_mat_q8_0_f32(q8_repacked, src1, dst, M, N, K)
+    return dst
+
+
+def quantize_q5_0(w):
+    """f32 CUDA tensor [N, K] -> Q5_0 bytes, uint8 [N, K/32, 22]."""
+    import torch
+    N, K = w.shape
+    out = torch.empty((N, K // 32, 22), dtype=torch.uint8, device=w.device)
+    gq_quantize_q5_0(w, out, N, K)
+    return out
+
+
+def repack_q5_0(q5, N: int, K: int):
+    import torch
+    out = torch.empty(gq_q5_0_repacked_bytes(N, K), dtype=torch.uint8, device=q5.device)
+    gq_repack_q5_0(q5, out, N, K)
+    return out
+
+
+def mul_mat_q5_0_f32(q5_repacked, src1, N: int, out=None):
+    import torch
+    M, K = src1.shape
+    dst = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=src1.device)
+    gq_mul_mat_q5_0_f32(q5_repacked, src1, dst, M, N, K)
     return dst

@@ -84,10 +84,15 @@ constexpr int F16_TILE_BYTES = 16 * F16_TILE_COLS * 2;
 // at (j * 16 + r) * 32, then the 64 fp16 scales at 2048 + (r * 4 + j) * 2.
 constexpr int Q8_TILE_SCALE_OFFSET = 16 * TILE_BLOCKS * QK;
 constexpr int Q8_TILE_BYTES = Q8_TILE_SCALE_OFFSET + 16 * TILE_BLOCKS * 2;
+// Repacked Q5_0 weights: 16 rows x 4 blocks; the nibble bytes as in Q4_0 (1024 bytes), the fifth
+// bits of block j of row r at 1024 + (j * 16 + r) * 4, then the fp16 scales at 1280 + (r * 4 + j) * 2.
+constexpr int Q5_TILE_HIGH_OFFSET = TILE_SCALE_OFFSET;
+constexpr int Q5_TILE_SCALE_OFFSET = Q5_TILE_HIGH_OFFSET + 16 * TILE_BLOCKS * 4;
+constexpr int Q5_TILE_BYTES = Q5_TILE_SCALE_OFFSET + 16 * TILE_BLOCKS * 2;
 // weight formats of the kernel
-enum : int { WF_Q4 = 0, WF_F16 = 1, WF_Q8 = 2 };
+enum : int { WF_Q4 = 0, WF_F16 = 1, WF_Q8 = 2, WF_Q5 = 3 };
 __host__ __device__ constexpr int tile_bytes(int wf) {
-    return wf == WF_F16 ? F16_TILE_BYTES : wf == WF_Q8 ? Q8_TILE_BYTES : TILE_BYTES;
+    return wf == WF_F16 ? F16_TILE_BYTES : wf == WF_Q8 ? Q8_TILE_BYTES : wf == WF_Q5 ? Q5_TILE_BYTES : TILE_BYTES;
 }
 __host__ __device__ constexpr int chunk_bytes(int wf) { return CHUNK_TILES * tile_bytes(wf); }
 constexpr int MAX_SLOTS = 12;
@@ -273,9 +278,10 @@ __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
 // ---------------------------------------------------------------------------
 template <int MT, int CWT, int REGS, int WF, int FIXW>
 __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) gemv_q4_0_kernel(const Params p) {
-    constexpr bool F16W = WF == WF_F16, Q8W = WF == WF_Q8;
+    constexpr bool F16W = WF == WF_F16, Q8W = WF == WF_Q8, Q5W = WF == WF_Q5;
     constexpr int TB = tile_bytes(WF), CB = chunk_bytes(WF);
-    constexpr int SCALES = Q8W ? Q8_TILE_SCALE_OFFSET : TILE_SCALE_OFFSET;   // fp16 scales in a Q4_0 / Q8_0 tile
+    // fp16 scales in a Q4_0 / Q5_0 / Q8_0 tile
+    constexpr int SCALES = Q8W ? Q8_TILE_SCALE_OFFSET : Q5W ? Q5_TILE_SCALE_OFFSET : TILE_SCALE_OFFSET;
     using SH = Shape<CWT, FIXW>;
     constexpr int CW = SH::CW, TPW = SH::TPW, CONSUMERS = SH::CONSUMERS, THREADS = SH::THREADS;
     constexpr int PRODUCER_WARP = SH::PRODUCER_WARP, FIXUP_WARP = SH::FIXUP_WARP, FUSED_LOADS = SH::FUSED_LOADS;
@@ -617,7 +623,12 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                         const uint4 a0 = lds128(a + mm * im.row_bytes);
                         const uint4 a1 = lds128(a + mm * im.row_bytes + 16);
                         const float2 sc = act_sc[mm * sc_stride + blk];
-                        const int sumi = Q8W ? block_dot_s8(q, q_hi, a0, a1) : block_dot(q, a0, a1, __float_as_int(sc.y));
+                        const int sumi =
+                            Q8W   ? block_dot_s8(q, q_hi, a0, a1)
+                            : Q5W ? block_dot_q5(q, *reinterpret_cast<const uint32_t *>(tile + Q5_TILE_HIGH_OFFSET +
+                                                                                     (jb * 16 + n) * 4),
+                                                 a0, a1, 2 * __float_as_int(sc.y))   // -16 sum of the codes
+                                  : block_dot(q, a0, a1, __float_as_int(sc.y));
                         acc[tw][MMA ? 0 : m] = fmaf(d4 * sc.x, (float)sumi, acc[tw][MMA ? 0 : m]);
                     }
                 }
@@ -644,6 +655,20 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                         q8_to_f16x2(*reinterpret_cast<const uint32_t *>(r1), alo[1], alo[3]);
                         q8_to_f16x2(*reinterpret_cast<const uint32_t *>(r0 + 16), ahi[0], ahi[2]);
                         q8_to_f16x2(*reinterpret_cast<const uint32_t *>(r1 + 16), ahi[1], ahi[3]);
+                    } else if constexpr (Q5W) {   // word ft of rows fg, fg + 8 with their fifth bits
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg) * 16 + 4 * ft);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg + 8) * 16 + 4 * ft);
+                        const uint32_t h0 = *reinterpret_cast<const uint32_t *>(tile + Q5_TILE_HIGH_OFFSET + (jb * 16 + fg) * 4);
+                        const uint32_t h1 = *reinterpret_cast<const uint32_t *>(tile + Q5_TILE_HIGH_OFFSET + (jb * 16 + fg + 8) * 4);
+                        // the group shift depends on ft: lo bits of group ft at 8b + 7 - ft, hi at 8b + 3 - ft
+                        const uint32_t l0 = (w0 & 0x0F0F0F0Fu) | (((h0 << ft) >> 3) & 0x10101010u);
+                        const uint32_t l1 = (w1 & 0x0F0F0F0Fu) | (((h1 << ft) >> 3) & 0x10101010u);
+                        const uint32_t u0 = ((w0 >> 4) & 0x0F0F0F0Fu) | ((h0 << (1 + ft)) & 0x10101010u);
+                        const uint32_t u1 = ((w1 >> 4) & 0x0F0F0F0Fu) | ((h1 << (1 + ft)) & 0x10101010u);
+                        q5_to_f16x2(l0, alo[0], alo[2]);
+                        q5_to_f16x2(l1, alo[1], alo[3]);
+                        q5_to_f16x2(u0, ahi[0], ahi[2]);
+                        q5_to_f16x2(u1, ahi[1], ahi[3]);
                     } else {
                         const uint32_t w0 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg) * 16 + 4 * ft);
                         const uint32_t w1 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg + 8) * 16 + 4 * ft);
@@ -779,7 +804,7 @@ int env_int(const char *name, int dflt) {
 
 // The dynamic shared-memory limit is raised once per (device, kernel).
 constexpr int MAX_DEV = 64;
-constexpr int MAX_VARIANTS = 16;
+constexpr int MAX_VARIANTS = 24;
 std::atomic<bool> g_smem_set[MAX_DEV][MAX_VARIANTS];
 
 template <typename Kernel>
@@ -839,7 +864,9 @@ const Variant VARIANTS[] = {
     variant<4, 16, 96, WF_Q4, 2>(),  variant<8, 16, 96, WF_Q4, 2>(),  variant<16, 16, 96, WF_Q4, 2>(),
     variant<8, 8, 88, WF_F16, 0>(),  variant<8, 8, 88, WF_F16, 1>(),  variant<16, 16, 96, WF_F16, 2>(),
     variant<1, 8, 88, WF_Q8, 0>(),   variant<1, 8, 88, WF_Q8, 1>(),   variant<2, 16, 96, WF_Q8, 2>(),
-    variant<4, 16, 96, WF_Q8, 2>(),  variant<8, 16, 96, WF_Q8, 2>(),  variant<16, 16, 96, WF_Q8, 2>()};
+    variant<4, 16, 96, WF_Q8, 2>(),  variant<8, 16, 96, WF_Q8, 2>(),  variant<16, 16, 96, WF_Q8, 2>(),
+    variant<1, 8, 88, WF_Q5, 0>(),   variant<1, 8, 88, WF_Q5, 1>(),   variant<2, 16, 96, WF_Q5, 2>(),
+    variant<4, 16, 96, WF_Q5, 2>(),  variant<8, 16, 96, WF_Q5, 2>(),  variant<16, 16, 96, WF_Q5, 2>()};
 constexpr int N_VARIANTS = sizeof(VARIANTS) / sizeof(VARIANTS[0]);
 static_assert(N_VARIANTS <= MAX_VARIANTS, "one shared-memory flag per variant");
 
@@ -933,11 +960,11 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
             return (int)std::min<size_t>(MAX_SLOTS,
                                          (budget - std::min(budget, fixed + 256)) / (chunk_bytes(wf) + 16));
         };
-        // the 8-warp Q4_0 shape keeps a ring of half the shared memory (MIN_SLOTS_HALF chunks at
+        // the 8-warp Q4_0 / Q5_0 shape keeps a ring of half the shared memory (MIN_SLOTS_HALF chunks at
         // least): two CTAs per SM without fix-up warps; with one, a half ring measured faster than
         // a full one.  F16 and Q8_0 tiles (more bytes per weight; 34 KB Q8_0 chunks would leave
         // two slots in half the shared memory) keep a full ring.
-        p.slots = kv.cw == 8 && wf == WF_Q4 ? slots_for(SMEM_HALF - 1024) : 0;
+        p.slots = kv.cw == 8 && (wf == WF_Q4 || wf == WF_Q5) ? slots_for(SMEM_HALF - 1024) : 0;
         if (p.slots < MIN_SLOTS_HALF) p.slots = slots_for(SMEM_LIMIT - 1024);
         const int slots_env = env_int("GQ_GEMV_SLOTS", 0);   // tuning: ring slots, up to what fits
         if (slots_env > 0) p.slots = std::min(slots_env, slots_for(SMEM_LIMIT - 1024));
@@ -1011,6 +1038,16 @@ gq_status launch_gemv_q8_0(const void *rep, const float *x, float *dst, int64_t 
     gq_status st = get_workspace(s, cb, db, &ws);
     if (st != GQ_OK) return st;
     return launch_gemv_with(WF_Q8, rep, x, dst, M, N, K, ws, s);
+}
+
+gq_status launch_gemv_q5_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t s) {
+    size_t cb, db;
+    gemv_workspace(WF_Q5, N, K, &cb, &db);
+    Workspace ws;
+    gq_status st = get_workspace(s, cb, db, &ws);
+    if (st != GQ_OK) return st;
+    return launch_gemv_with(WF_Q5, rep, x, dst, M, N, K, ws, s);
 }
 
 }  // namespace gq

@@ -313,6 +313,48 @@ gq_status gq_mul_mat_f16_f32(const void *src0_f16, const float *src1, float *dst
     return gq_mul_mat_f16_f32_path(src0_f16, src1, dst, M, N, K, GQ_PATH_AUTO, stream);
 }
 
+size_t gq_q5_0_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % QK) return 0;
+    return (size_t)N * (size_t)(K / QK) * 22;
+}
+
+size_t gq_q5_0_repacked_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % QK) return 0;
+    return (size_t)((N + 15) / 16) * (size_t)((K / QK + TILE_BLOCKS - 1) / TILE_BLOCKS) * 1408;
+}
+
+gq_status gq_quantize_q5_0(const float *w, void *q5_blocks, int64_t N, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(1, N, K));
+    GQ_TRY(check_ptr(w, "w"));
+    GQ_TRY(check_ptr(q5_blocks, "q5_blocks"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_quantize_q5_0(w, q5_blocks, N, K, stream));
+    return ok();
+}
+
+gq_status gq_repack_q5_0(const void *q5_blocks, void *q5_repacked, int64_t N, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(1, N, K));
+    GQ_TRY(check_ptr(q5_blocks, "q5_blocks"));
+    GQ_TRY(check_ptr(q5_repacked, "q5_repacked"));
+    const uintptr_t a = (uintptr_t)q5_blocks, b = (uintptr_t)q5_repacked;
+    if (a < b + gq_q5_0_repacked_bytes(N, K) && b < a + gq_q5_0_bytes(N, K))
+        return fail(GQ_ERR_INVALID_ARG, "q5_blocks and q5_repacked overlap");
+    GQ_TRY(check_device());
+    GQ_TRY(launch_repack_q5_0(q5_blocks, q5_repacked, N, K, stream));
+    return ok();
+}
+
+gq_status gq_mul_mat_q5_0_f32(const void *q5_repacked, const float *src1, float *dst, int64_t M, int64_t N,
+                              int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(M, N, K));
+    GQ_TRY(check_ptr(q5_repacked, "q5_repacked"));
+    GQ_TRY(check_ptr(src1, "src1"));
+    GQ_TRY(check_ptr(dst, "dst"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_gemv_q5_0(q5_repacked, src1, dst, M, N, K, stream));
+    return ok();
+}
+
 size_t gq_q8_0_repacked_bytes(int64_t N, int64_t K) {
     if (N <= 0 || K <= 0 || K % QK) return 0;
     return (size_t)((N + 15) / 16) * (size_t)((K / QK + TILE_BLOCKS - 1) / TILE_BLOCKS) * 2176;

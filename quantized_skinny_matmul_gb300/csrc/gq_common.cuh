@@ -211,6 +211,31 @@ __device__ __forceinline__ int block_dot_s8(uint4 w0, uint4 w1, uint4 a0, uint4 
     return s0 + s1;
 }
 
+// Q5_0 weights in a repacked tile: w the 16 nibble bytes of a block (the Q4_0 order), h the
+// block's 32 fifth bits arranged so that bit 8b + 7 - s holds the fifth bit of element b of group
+// s (groups 0..3: elements 4s .. 4s+3, the low nibbles of word s; groups 4..7: elements
+// 16 + 4(s-4) .., the high nibbles).  The five-bit codes of word w then are
+// (w & 0x0F) | ((h >> (3 - w)) & 0x10) per byte (low) and ((w >> 4) & 0x0F) | ((h << (1 + w)) & 0x10)
+// (high).  corr = -16 * sum of the activation codes; the result is sum_j (q5_j - 16) q8_j.
+__device__ __forceinline__ uint32_t q5_lo(uint32_t w, uint32_t h, int word) {
+    return (w & 0x0F0F0F0Fu) | ((h >> (3 - word)) & 0x10101010u);
+}
+__device__ __forceinline__ uint32_t q5_hi(uint32_t w, uint32_t h, int word) {
+    return ((w >> 4) & 0x0F0F0F0Fu) | ((h << (1 + word)) & 0x10101010u);
+}
+__device__ __forceinline__ int block_dot_q5(uint4 w, uint32_t h, uint4 a0, uint4 a1, int corr) {
+    int lo = corr, hi = 0;
+    lo = dp4a_u8s8(q5_lo(w.x, h, 0), a0.x, lo);
+    hi = dp4a_u8s8(q5_hi(w.x, h, 0), a1.x, hi);
+    lo = dp4a_u8s8(q5_lo(w.y, h, 1), a0.y, lo);
+    hi = dp4a_u8s8(q5_hi(w.y, h, 1), a1.y, hi);
+    lo = dp4a_u8s8(q5_lo(w.z, h, 2), a0.z, lo);
+    hi = dp4a_u8s8(q5_hi(w.z, h, 2), a1.z, hi);
+    lo = dp4a_u8s8(q5_lo(w.w, h, 3), a0.w, lo);
+    hi = dp4a_u8s8(q5_hi(w.w, h, 3), a1.w, hi);
+    return lo + hi;
+}
+
 // D(16x8, f32) += A(16x16, f16, row) . B(16x8, f16, col)
 __device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                 uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -219,6 +244,15 @@ __device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], uint32_t a0, uint
         "{%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four codes 0..31 (one per byte) -> two half2 of (q - 16), exact (as q4_to_f16x2, bias 1040).
+__device__ __forceinline__ void q5_to_f16x2(uint32_t v, uint32_t &h01, uint32_t &h23) {
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6410), __ushort_as_half(0x6410));   // 1040
+    uint32_t a = __byte_perm(v, 0x64646464u, 0x4140u), b = __byte_perm(v, 0x64646464u, 0x4342u);
+    __half2 x = __hsub2(*reinterpret_cast<__half2 *>(&a), bias), y = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
+    h01 = *reinterpret_cast<uint32_t *>(&x);
+    h23 = *reinterpret_cast<uint32_t *>(&y);
 }
 
 // Four codes 0..15 (one per byte) -> two half2 of (q - 8), exact: the bytes become the

@@ -38,6 +38,36 @@ __global__ void quantize_q4_0_kernel(const float *__restrict__ w, uint8_t *__res
     }
 }
 
+// Q5_0 of weight blocks: one warp per block, lane j holds element j.  d = (signed max) / -16,
+// q = clamp(round(x / d) + 16, 0, 31) (16 when d == 0); block = fp16 d, the fifth bits as a
+// little-endian word (bit j from lane j), 16 bytes of low nibbles (q_i | q_{i+16} << 4).
+__global__ void quantize_q5_0_kernel(const float *__restrict__ w, uint8_t *__restrict__ out, int64_t nblocks) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = warp; b < nblocks; b += nwarps) {
+        const float x = w[b * QK + lane];
+        const unsigned int abits = __float_as_uint(fabsf(x));
+        const unsigned int amax = __reduce_max_sync(0xffffffffu, abits);
+        const unsigned int first = __ffs(__ballot_sync(0xffffffffu, abits == amax)) - 1;
+        float vmax = __shfl_sync(0xffffffffu, x, first);
+        if (amax == 0u) vmax = 0.0f;
+        const float d = vmax / -16.0f;
+        int q = 16;
+        if (d != 0.0f) {
+            const int v = (int)roundf(x / d) + 16;
+            q = v < 0 ? 0 : (v > 31 ? 31 : v);
+        }
+        const unsigned int qh = __ballot_sync(0xffffffffu, (q >> 4) & 1);
+        const int qhi = __shfl_down_sync(0xffffffffu, q, 16);
+        uint8_t *o = out + b * 22;                         // 2-byte aligned: 22 * b is even
+        if (lane < 16) o[6 + lane] = (uint8_t)((q & 0x0F) | ((qhi & 0x0F) << 4));
+        if (lane < 4) o[2 + lane] = (uint8_t)(qh >> (8 * lane));
+        if (lane == 0) *reinterpret_cast<unsigned short *>(o) = __half_as_ushort(__float2half_rn(d));
+    }
+}
+
 // Q8_0 of activation rows: the INIT stage that produces wdata (Arm China NUMA
 // article, "MulMat 算子優化").
 __global__ void quantize_rows_q8_0_kernel(const float *__restrict__ x, uint8_t *__restrict__ out,
@@ -142,6 +172,42 @@ __global__ void repack_q8_0_kernel(const uint8_t *__restrict__ q8, uint8_t *__re
     }
 }
 
+// Q5_0 blocks [N][nb] x 22 -> tiles of 16 rows x 4 blocks, 1408 bytes: the 16 nibble bytes of
+// block j of row r at (j * 16 + r) * 16, its fifth bits at 1024 + (j * 16 + r) * 4 arranged as
+// block_dot_q5 reads them (bit 8b + 7 - s = fifth bit of element b of group s: groups 0..3 are
+// elements 4s .., groups 4..7 elements 16 + 4(s - 4) ..), then the fp16 scales at
+// 1280 + (r * 4 + j) * 2.  One thread per (tile, row, block); padding holds codes 16 and scale 0.
+__global__ void repack_q5_0_kernel(const uint8_t *__restrict__ q5, uint8_t *__restrict__ out, int64_t N,
+                                   int64_t nb, int64_t NT, int64_t items) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = i / 64, rj = i % 64;
+        const int r = (int)(rj / 4), j = (int)(rj % 4);
+        const int64_t g = tile / NT, t = tile % NT;
+        const int64_t n = 16 * g + r, b = 4 * t + j;
+        uint8_t *dt = out + tile * 1408;
+        uint32_t nib[4] = {0u, 0u, 0u, 0u}, qh = 0xFFFFFFFFu;   // padding: code 16 = nibble 0, fifth bit 1
+        uint16_t d = 0;
+        if (n < N && b < nb) {
+            const uint8_t *src = q5 + (n * nb + b) * 22;
+            d = (uint16_t)(src[0] | (src[1] << 8));
+            qh = (uint32_t)src[2] | ((uint32_t)src[3] << 8) | ((uint32_t)src[4] << 16) | ((uint32_t)src[5] << 24);
+            for (int k = 0; k < 4; k++)
+                nib[k] = (uint32_t)src[6 + 4 * k] | ((uint32_t)src[7 + 4 * k] << 8) | ((uint32_t)src[8 + 4 * k] << 16) |
+                         ((uint32_t)src[9 + 4 * k] << 24);
+        }
+        uint32_t h = 0;
+        for (int sg = 0; sg < 8; sg++)
+            for (int bb = 0; bb < 4; bb++) {
+                const int e = sg < 4 ? 4 * sg + bb : 16 + 4 * (sg - 4) + bb;
+                h |= ((qh >> e) & 1u) << (8 * bb + 7 - sg);
+            }
+        *reinterpret_cast<uint4 *>(dt + (j * 16 + r) * 16) = make_uint4(nib[0], nib[1], nib[2], nib[3]);
+        *reinterpret_cast<uint32_t *>(dt + 1024 + (j * 16 + r) * 4) = h;
+        *reinterpret_cast<uint16_t *>(dt + 1280 + (r * 4 + j) * 2) = d;
+    }
+}
+
 int grid_for(int64_t work_items, int threads) {
     int64_t blocks = (work_items + threads - 1) / threads;
     const int64_t cap = (int64_t)sm_count() * 16;
@@ -171,6 +237,18 @@ gq_status launch_repack_q4_0(const void *q4, void *rep, int64_t N, int64_t K, cu
     const int64_t blocks = (threads + 255) / 256;
     repack_q4_0_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint8_t *)q4, (uint8_t *)rep, N, nb, NT, ntiles);
     return check_cuda(cudaGetLastError(), "repack_q4_0 launch");
+}
+
+gq_status launch_quantize_q5_0(const float *w, void *q5, int64_t N, int64_t K, cudaStream_t s) {
+    const int64_t nblocks = N * (K / QK);
+    quantize_q5_0_kernel<<<grid_for(nblocks * 32, 256), 256, 0, s>>>(w, (uint8_t *)q5, nblocks);
+    return check_cuda(cudaGetLastError(), "quantize_q5_0 launch");
+}
+
+gq_status launch_repack_q5_0(const void *q5, void *rep, int64_t N, int64_t K, cudaStream_t s) {
+    const int64_t nb = K / QK, NT = (nb + TILE_BLOCKS - 1) / TILE_BLOCKS, items = (N + 15) / 16 * NT * 64;
+    repack_q5_0_kernel<<<grid_for(items, 256), 256, 0, s>>>((const uint8_t *)q5, (uint8_t *)rep, N, nb, NT, items);
+    return check_cuda(cudaGetLastError(), "repack_q5_0 launch");
 }
 
 gq_status launch_repack_q8_0(const void *q8, void *rep, int64_t N, int64_t K, cudaStream_t s) {

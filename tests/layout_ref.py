@@ -88,3 +88,38 @@ def repack_q8_0_loops(q8: np.ndarray) -> np.ndarray:
                         out[base + (j * 16 + r) * 32: base + (j * 16 + r) * 32 + 32] = q8[n, b, 2:]
                         out[base + 2048 + (r * 4 + j) * 2: base + 2048 + (r * 4 + j) * 2 + 2] = q8[n, b, :2]
     return out
+
+
+def _q5_high_word(qh: int) -> int:
+    """The fifth bits of one block as gq_repack_q5_0 stores them (bit 8b + 7 - s = the fifth
+    bit of element b of group s; groups 0..3 = elements 4s.., groups 4..7 = 16 + 4(s-4)..)."""
+    h = 0
+    for s in range(8):
+        for b in range(4):
+            e = 4 * s + b if s < 4 else 16 + 4 * (s - 4) + b
+            h |= ((qh >> e) & 1) << (8 * b + 7 - s)
+    return h
+
+
+def repack_q5_0_ref(q5: np.ndarray) -> np.ndarray:
+    """Q5_0 blocks [N, nb, 22] -> the tile layout of gq_repack_q5_0, as bytes (element by
+    element from the header's description; small sizes)."""
+    N, nb = q5.shape[0], q5.shape[1]
+    N16, NT = -(-N // 16), -(-nb // 4)
+    out = np.zeros(N16 * NT * 1408, np.uint8)
+    pad_high = np.frombuffer(_q5_high_word(0xFFFFFFFF).to_bytes(4, "little"), np.uint8)
+    for g in range(N16):
+        for t in range(NT):
+            base = (g * NT + t) * 1408
+            for j in range(4):
+                for r in range(16):
+                    n, b = 16 * g + r, 4 * t + j
+                    o_nib, o_hi, o_sc = base + (j * 16 + r) * 16, base + 1024 + (j * 16 + r) * 4, base + 1280 + (r * 4 + j) * 2
+                    if n < N and b < nb:
+                        out[o_nib:o_nib + 16] = q5[n, b, 6:22]
+                        qh = int.from_bytes(bytes(q5[n, b, 2:6]), "little")
+                        out[o_hi:o_hi + 4] = np.frombuffer(_q5_high_word(qh).to_bytes(4, "little"), np.uint8)
+                        out[o_sc:o_sc + 2] = q5[n, b, 0:2]
+                    else:
+                        out[o_hi:o_hi + 4] = pad_high          # code 16: nibble 0, fifth bit 1; scale 0
+    return out

@@ -27,3 +27,18 @@ def test_q8_0_layout_statements_agree(N, nb):
     rng = np.random.default_rng(N * 10 + nb)
     q8 = rng.integers(0, 256, size=(N, nb, 34), dtype=np.uint8)
     assert np.array_equal(repack_q8_0_ref(q8), repack_q8_0_loops(q8))
+
+
+def test_q5_0_high_word_gives_the_codes():
+    """The stored fifth-bit word, shifted and masked as the kernel does for word w of a block,
+    puts the fifth bit of each element at bit 4 of that element's byte."""
+    from layout_ref import _q5_high_word
+    rng = np.random.default_rng(3)
+    for qh in [0, 0xFFFFFFFF, 0x0000FFFF, 0xFFFF0000] + [int(v) for v in rng.integers(0, 1 << 32, 20)]:
+        h = _q5_high_word(qh)
+        for w in range(4):
+            lo = (h >> (3 - w)) & 0x10101010
+            hi = (h << (1 + w)) & 0x10101010 & 0xFFFFFFFF
+            for b in range(4):
+                assert ((lo >> (8 * b + 4)) & 1) == (qh >> (4 * w + b)) & 1
+                assert ((hi >> (8 * b + 4)) & 1) == (qh >> (16 + 4 * w + b)) & 1
