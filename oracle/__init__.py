@@ -29,6 +29,7 @@ QK = 32
 Q4_0_BYTES = 18
 Q8_0_BYTES = 34
 Q5_0_BYTES = 22
+Q4_1_BYTES = 20
 
 CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
           "-Wall", "-Wextra"]
@@ -64,6 +65,11 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "oracle_mul_mat_q4_0_q8_0_at": ([P, P, P, P, I, I, P, P], None),
         "oracle_block_dots_q8_0": ([P, P, P, I, I, I], None),
         "oracle_quantize_q5_0": ([P, P, I, I], None),
+        "oracle_quantize_q4_1": ([P, P, I, I], None),
+        "oracle_dequantize_q4_1": ([P, P, I, I], None),
+        "oracle_block_sums_q4_1": ([P, P, P, I, I, I], None),
+        "oracle_mul_mat_q4_1_f32": ([P, P, P, P, I, I, I, I, I], ctypes.c_int),
+        "oracle_mul_mat_q4_1_q8_0_at": ([P, P, P, P, I, I, P, P], None),
         "oracle_dequantize_q5_0": ([P, P, I, I], None),
         "oracle_block_dots_q5_0": ([P, P, P, I, I, I], None),
         "oracle_mul_mat_q5_0_f32": ([P, P, P, P, I, I, I, I, I], ctypes.c_int),
@@ -192,6 +198,60 @@ class Oracle:
         out = np.empty(ms.size, np.float64)
         T = np.empty(ms.size, np.float64)
         self.lib.oracle_mul_mat_q4_0_q8_0_at(_ptr(q4), _ptr(q8), _ptr(ms), _ptr(ns), ms.size,
+                                             K, _ptr(out), _ptr(T))
+        return out, T
+
+    def quantize_q4_1(self, w) -> np.ndarray:
+        """f32 [N, K] -> Q4_1 bytes, uint8 [N, K/32, 20]."""
+        w = _c(w, np.float32)
+        N, K = w.shape
+        assert K % QK == 0
+        out = np.empty((N, K // QK, Q4_1_BYTES), np.uint8)
+        self.lib.oracle_quantize_q4_1(_ptr(w), _ptr(out), N, K)
+        return out
+
+    def dequantize_q4_1(self, q41) -> np.ndarray:
+        q41 = _c(q41, np.uint8)
+        N, nb = q41.shape[0], q41.shape[1]
+        out = np.empty((N, nb * QK), np.float64)
+        self.lib.oracle_dequantize_q4_1(_ptr(q41), _ptr(out), N, nb * QK)
+        return out
+
+    def block_sums_q4_1(self, q41, q8) -> np.ndarray:
+        """int32 [M, N, K/32, 2]: (sum_j q_j * q8_j, sum_j q8_j) for every block pair."""
+        q41 = _c(q41, np.uint8)
+        q8 = _c(q8, np.uint8)
+        N, nb = q41.shape[0], q41.shape[1]
+        M = q8.shape[0]
+        assert q8.shape[1] == nb
+        out = np.empty((M, N, nb, 2), np.int32)
+        self.lib.oracle_block_sums_q4_1(_ptr(q41), _ptr(q8), _ptr(out), M, N, nb * QK)
+        return out
+
+    def mul_mat_q4_1_f32(self, q41, src1, n_range=None):
+        """(dst, T), both f64 [M, N], for Q4_1 weights; src1 is quantized to Q8_0 inside."""
+        q41 = _c(q41, np.uint8)
+        src1 = _c(src1, np.float32)
+        N, nb = q41.shape[0], q41.shape[1]
+        M, K = src1.shape
+        assert K == nb * QK
+        dst = np.zeros((M, N), np.float64)
+        T = np.zeros((M, N), np.float64)
+        b, e = (0, N) if n_range is None else n_range
+        rc = self.lib.oracle_mul_mat_q4_1_f32(_ptr(q41), _ptr(src1), _ptr(dst), _ptr(T), M, N, K, b, e)
+        if rc != 0:
+            raise MemoryError("oracle_mul_mat_q4_1_f32: allocation failed")
+        return dst, T
+
+    def mul_mat_q4_1_q8_0_at(self, q41, q8, ms, ns):
+        q41 = _c(q41, np.uint8)
+        q8 = _c(q8, np.uint8)
+        ms = _c(ms, np.int64)
+        ns = _c(ns, np.int64)
+        K = q41.shape[1] * QK
+        out = np.empty(ms.size, np.float64)
+        T = np.empty(ms.size, np.float64)
+        self.lib.oracle_mul_mat_q4_1_q8_0_at(_ptr(q41), _ptr(q8), _ptr(ms), _ptr(ns), ms.size,
                                              K, _ptr(out), _ptr(T))
         return out, T
 

@@ -9,8 +9,8 @@
  *
  * What is computed (the llama.cpp MUL_MAT of the q_f32 and f16_f32 kinds):
  *     dst[m][n] = sum_k src0[n][k] * src1[m][k]
- * with src0 Q4_0, Q5_0 or Q8_0 block-quantized weights or F16 weights, and src1
- * F32 activations.  For the Q4_0 kind, src1 is first quantized row by row into
+ * with src0 Q4_0, Q4_1, Q5_0 or Q8_0 block-quantized weights or F16 weights,
+ * and src1 F32 activations.  For the Q4_0 kind, src1 is first quantized row by row into
  * Q8_0 blocks (the "wdata" buffer) and the product is taken as integer block
  * dot products scaled by the two block scales:
  *   - llama.cpp pull request #1632, "Introduction": the three MUL_MAT kinds
@@ -48,6 +48,7 @@
 #define Q4_0_BYTES 18    /* 2-byte scale + 16 bytes of nibbles */
 #define Q8_0_BYTES 34    /* 2-byte scale + 32 int8 */
 #define Q5_0_BYTES 22    /* 2-byte scale + 4 bytes of fifth bits + 16 bytes of nibbles */
+#define Q4_1_BYTES 20    /* 2-byte scale + 2-byte minimum + 16 bytes of nibbles */
 
 /* ---------------------------------------------------------------------------
  * IEEE 754 binary16, written from the format's definition.
@@ -232,9 +233,51 @@ void oracle_quantize_q5_0(const float *w, uint8_t *out, int64_t N, int64_t K)
 }
 
 /* ---------------------------------------------------------------------------
+ * Q4_1 quantization of one block of 32 weights.  llama.cpp PR #1632,
+ * "Introduction": Q4_1 is named beside Q4_0 as a src0 type of the q_f32 kind;
+ * the pages do not define it, and this library reads it as a scale and a
+ * minimum per block: block (20 bytes) = fp16 d, fp16 m, then 16 bytes with q_i
+ * in the low nibble and q_{i+16} in the high nibble of byte i.  lo, hi = the
+ * smallest and largest element, d = (hi - lo) / 15, m = lo,
+ * q_j = clamp(round((x_j - lo) / d), 0, 15) (q_j = 0 when d == 0), all in f32;
+ * the weight is q_j * fp16(d) + fp16(m).
+ * ------------------------------------------------------------------------- */
+static void quantize_block_q4_1(const float *x, uint8_t *out)
+{
+    float lo = x[0], hi = x[0];
+    for (int j = 1; j < QK; j++) {
+        if (x[j] < lo) lo = x[j];
+        if (x[j] > hi) hi = x[j];
+    }
+    float d = (hi - lo) / 15.0f;
+    int q[QK];
+    for (int j = 0; j < QK; j++) {
+        if (d != 0.0f) {
+            int v = (int)roundf((x[j] - lo) / d);
+            q[j] = v < 0 ? 0 : (v > 15 ? 15 : v);
+        } else {
+            q[j] = 0;
+        }
+    }
+    put_f16(out, oracle_f32_to_f16(d));
+    put_f16(out + 2, oracle_f32_to_f16(lo));
+    for (int i = 0; i < QK / 2; i++)
+        out[4 + i] = (uint8_t)(q[i] | (q[i + QK / 2] << 4));
+}
+
+/* w: f32 [N][K]; out: Q4_1 blocks [N][K/32] x 20 bytes. */
+void oracle_quantize_q4_1(const float *w, uint8_t *out, int64_t N, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < nb; b++)
+            quantize_block_q4_1(w + n * K + b * QK, out + (n * nb + b) * Q4_1_BYTES);
+}
+
+/* ---------------------------------------------------------------------------
  * De-quantization (for the invariant checks): value = (q - 8) * d  (Q4_0),
- * value = (q - 16) * d (Q5_0), value = q * d (Q8_0), in f64 (the products are
- * exact).
+ * value = (q - 16) * d (Q5_0), value = q * d + m (Q4_1), value = q * d (Q8_0),
+ * in f64 (exact).
  * ------------------------------------------------------------------------- */
 static int q4_code(const uint8_t *blk, int j)
 {
@@ -250,6 +293,25 @@ static int q5_code(const uint8_t *blk, int j)
     uint8_t byte = blk[6 + (j % (QK / 2))];
     int lo = j < QK / 2 ? (byte & 0x0f) : (byte >> 4);
     return lo | (int)(((qh >> j) & 1u) << 4);
+}
+
+static int q41_code(const uint8_t *blk, int j)
+{
+    uint8_t byte = blk[4 + (j % (QK / 2))];
+    return j < QK / 2 ? (byte & 0x0f) : (byte >> 4);
+}
+
+void oracle_dequantize_q4_1(const uint8_t *q41, double *out, int64_t N, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = q41 + (n * nb + b) * Q4_1_BYTES;
+            double d = (double)oracle_f16_to_f32(get_f16(blk));
+            double m = (double)oracle_f16_to_f32(get_f16(blk + 2));
+            for (int j = 0; j < QK; j++)
+                out[n * K + b * QK + j] = (double)q41_code(blk, j) * d + m;
+        }
 }
 
 void oracle_dequantize_q5_0(const uint8_t *q5, double *out, int64_t N, int64_t K)
@@ -509,6 +571,84 @@ void oracle_mul_mat_q5_0_q8_0_at(const uint8_t *q5, const uint8_t *q8, const int
     int64_t nb = K / QK;
     for (int64_t i = 0; i < count; i++)
         dot_row_q5_0_q8_0(q5 + ns[i] * nb * Q5_0_BYTES, q8 + ms[i] * nb * Q8_0_BYTES, nb,
+                          &out[i], &T[i]);
+}
+
+/* ---------------------------------------------------------------------------
+ * The q_f32 kind with Q4_1 weights (the format above), src1 in Q8_0:
+ *   sum_j (q_j d + m) (q8_j d8) = d d8 sumi + m d8 sx,  sumi = sum_j q_j q8_j,  sx = sum_j q8_j
+ *   dst = sum_b (d_b d8_b sumi_b + m_b d8_b sx_b)   (f64; each product exact)
+ *   T   = sum_b |d8_b| sum_j |q_j d_b + m_b| |q8_j|
+ * ------------------------------------------------------------------------- */
+/* sumi and sx of one block pair: out[0] = sum_j q_j q8_j, out[1] = sum_j q8_j */
+static void block_sums_q4_1(const uint8_t *b41, const uint8_t *b8, int32_t out[2])
+{
+    int32_t s = 0, sx = 0;
+    for (int j = 0; j < QK; j++) {
+        s += (int32_t)q41_code(b41, j) * (int32_t)q8_code(b8, j);
+        sx += (int32_t)q8_code(b8, j);
+    }
+    out[0] = s;
+    out[1] = sx;
+}
+
+/* sums: int32 [M][N][K/32][2] */
+void oracle_block_sums_q4_1(const uint8_t *q41, const uint8_t *q8, int32_t *sums,
+                            int64_t M, int64_t N, int64_t K)
+{
+    int64_t nb = K / QK;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = 0; n < N; n++)
+            for (int64_t b = 0; b < nb; b++)
+                block_sums_q4_1(q41 + (n * nb + b) * Q4_1_BYTES, q8 + (m * nb + b) * Q8_0_BYTES,
+                                sums + ((m * N + n) * nb + b) * 2);
+}
+
+static void dot_row_q4_1_q8_0(const uint8_t *row41, const uint8_t *row8, int64_t nb,
+                              double *dst, double *T)
+{
+    double acc = 0.0, tacc = 0.0;
+    for (int64_t b = 0; b < nb; b++) {
+        const uint8_t *b41 = row41 + b * Q4_1_BYTES;
+        const uint8_t *b8 = row8 + b * Q8_0_BYTES;
+        double d = (double)oracle_f16_to_f32(get_f16(b41));
+        double mn = (double)oracle_f16_to_f32(get_f16(b41 + 2));
+        double d8 = (double)oracle_f16_to_f32(get_f16(b8));
+        int32_t sums[2];
+        block_sums_q4_1(b41, b8, sums);
+        acc += d * d8 * (double)sums[0];
+        acc += mn * d8 * (double)sums[1];
+        double t = 0.0;
+        for (int j = 0; j < QK; j++)
+            t += fabs((double)q41_code(b41, j) * d + mn) * (double)abs(q8_code(b8, j));
+        tacc += fabs(d8) * t;
+    }
+    *dst = acc;
+    *T = tacc;
+}
+
+int oracle_mul_mat_q4_1_f32(const uint8_t *q41, const float *src1, double *dst, double *T,
+                            int64_t M, int64_t N, int64_t K, int64_t n_begin, int64_t n_end)
+{
+    int64_t nb = K / QK;
+    uint8_t *wdata = (uint8_t *)malloc((size_t)(M * nb * Q8_0_BYTES) + 1);
+    if (!wdata) return 1;
+    oracle_quantize_q8_0(src1, wdata, M, K);
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = n_begin; n < n_end; n++)
+            dot_row_q4_1_q8_0(q41 + n * nb * Q4_1_BYTES, wdata + m * nb * Q8_0_BYTES, nb,
+                              &dst[m * N + n], &T[m * N + n]);
+    free(wdata);
+    return 0;
+}
+
+void oracle_mul_mat_q4_1_q8_0_at(const uint8_t *q41, const uint8_t *q8, const int64_t *ms,
+                                 const int64_t *ns, int64_t count, int64_t K,
+                                 double *out, double *T)
+{
+    int64_t nb = K / QK;
+    for (int64_t i = 0; i < count; i++)
+        dot_row_q4_1_q8_0(q41 + ns[i] * nb * Q4_1_BYTES, q8 + ms[i] * nb * Q8_0_BYTES, nb,
                           &out[i], &T[i]);
 }
 

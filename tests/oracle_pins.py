@@ -40,6 +40,14 @@ def decode_q4_0(q4: np.ndarray):
     return codes, d
 
 
+def decode_q4_1(q41: np.ndarray):
+    """(codes uint8 [..., 32], fp16 d as f64 [...], fp16 m as f64 [...]) from Q4_1 bytes."""
+    d = q41[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    m = q41[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+    qs = q41[..., 4:20]
+    return np.concatenate([qs & 0x0F, qs >> 4], axis=-1), d, m
+
+
 def decode_q5_0(q5: np.ndarray):
     """(codes uint8 [..., 32] in 0..31, fp16 scale as f64 [...]) from Q5_0 bytes."""
     d = q5[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
@@ -120,6 +128,8 @@ def pin_worked_examples(o) -> None:
             got = o.quantize_q4_0(x.reshape(1, 32)).tobytes()
         elif kind == "q5_0":
             got = o.quantize_q5_0(x.reshape(1, 32)).tobytes()
+        elif kind == "q4_1":
+            got = o.quantize_q4_1(x.reshape(1, 32)).tobytes()
         else:
             got = o.quantize_q8_0(x.reshape(1, 32)).tobytes()
         assert got == want, f"{name}: {got.hex(' ')} != {want.hex(' ')}"
@@ -391,6 +401,86 @@ def pin_q5_0_block_dot_and_product(o) -> None:
             assert np.array_equal(one[0], dst[m])
 
 
+def _q41_block(codes, d16_bits=0x3C00, m16_bits=0x0000) -> np.ndarray:
+    codes = np.asarray(codes, np.uint8)
+    out = np.empty(20, np.uint8)
+    out[0], out[1] = d16_bits & 0xFF, d16_bits >> 8
+    out[2], out[3] = m16_bits & 0xFF, m16_bits >> 8
+    out[4:] = codes[:16] | (codes[16:] << 4)
+    return out
+
+
+def pin_q4_1_quantizer(o) -> None:
+    """Q4_1: exact round trips of lo + code * 2^e with codes 0 and 15 present; codes in 0..15;
+    the scale and minimum are fp16 of (max - min) / 15 and of min; de-quantization error within
+    d/2 plus the fp16 roundings; constant blocks are code 0 with m = the value."""
+    rng = np.random.default_rng(27)
+    N, nb = 48, 8
+    c = rng.integers(0, 16, size=(N, nb, 32))
+    c[:, :, 5], c[:, :, 9] = 0, 15
+    e = rng.integers(-10, 2, size=(N, nb, 1))
+    lo = rng.integers(-40, 40, size=(N, nb, 1))
+    x = ((lo + c) * np.exp2(e)).astype(np.float32).reshape(N, nb * 32)
+    codes, d, m = decode_q4_1(o.quantize_q4_1(x))
+    assert np.array_equal(codes.astype(np.int64), c)
+    assert np.array_equal(d, np.exp2(e[..., 0]).astype(np.float64))
+    assert np.array_equal(m, (lo * np.exp2(e))[..., 0].astype(np.float64))
+    assert np.array_equal(o.dequantize_q4_1(o.quantize_q4_1(x)), x.astype(np.float64))
+    w = synth.edge_weights(28, 40, 512)
+    codes, d, m = decode_q4_1(o.quantize_q4_1(w))
+    assert codes.min() >= 0 and codes.max() <= 15
+    wb = w.reshape(codes.shape).astype(np.float64)
+    lo32, hi32 = wb.min(-1).astype(np.float32), wb.max(-1).astype(np.float32)
+    d32 = ((hi32 - lo32) / np.float32(15.0)).astype(np.float64)
+    assert np.array_equal(d, d32.astype(np.float16).astype(np.float64))
+    assert np.array_equal(m, lo32.astype(np.float16).astype(np.float64))
+    err = np.abs(wb - (codes.astype(np.float64) * d[..., None] + m[..., None]))
+    bound = (d32 / 2 * (1 + 1e-6) + 15 * np.abs(d32 - d) + np.abs(lo32.astype(np.float64) - m))[..., None] \
+        + 1e-6 * np.abs(wb)
+    assert np.all(err <= bound + 1e-30), "Q4_1 de-quantization error above its bound"
+    const = np.all(wb == wb[..., :1], axis=-1)
+    assert np.all(codes[const] == 0) and np.all(d[const] == 0)
+
+
+def pin_q4_1_block_sums_and_product(o) -> None:
+    """Q4_1: (sum q q8, sum q8) by brute force for every code against every Q8_0 code in a few
+    lanes; the product against the float64 dense matmul of the de-quantized operands; rows."""
+    qv = np.arange(16)
+    q8v = np.arange(-127, 128)
+    for lane in (0, 7, 16, 31):
+        b41 = []
+        for a in qv:
+            cc = np.zeros(32, np.int64)
+            cc[lane] = a
+            b41.append(_q41_block(cc))
+        b8 = []
+        for b in q8v:
+            cc = np.zeros(32, np.int64)
+            cc[lane] = b
+            b8.append(_q8_block(cc))
+        got = o.block_sums_q4_1(np.stack(b41)[:, None, :], np.stack(b8)[:, None, :])[:, :, 0, :]
+        assert np.array_equal(got[..., 0], np.outer(q8v, qv)), f"Q4_1 block dot wrong at lane {lane}"
+        assert np.array_equal(got[..., 1], np.repeat(q8v[:, None], 16, axis=1))
+    for (M, N, K, seed, outl) in ((3, 40, 96, 35, False), (5, 33, 256, 36, True), (1, 17, 32, 37, False)):
+        w, x = synth.problem(seed, M, N, K, outliers=outl)
+        q41 = o.quantize_q4_1(w)
+        q8 = o.quantize_q8_0(x)
+        A = o.dequantize_q4_1(q41)
+        c, d, m = decode_q4_1(q41)
+        assert np.array_equal(A, (c.astype(np.float64) * d[..., None] + m[..., None]).reshape(N, K))
+        B = o.dequantize_q8_0(q8)
+        want, T_want = B @ A.T, np.abs(B) @ np.abs(A).T
+        dst, T = o.mul_mat_q4_1_f32(q41, x)
+        assert np.all(np.abs(dst - want) <= 1e-12 * T_want + 1e-300), "Q4_1 product mismatch"
+        assert np.allclose(T, T_want, rtol=1e-12, atol=0)
+        ms, ns = np.array([0, M - 1, M // 2]), np.array([N - 1, 0, N // 2])
+        at, T_at = o.mul_mat_q4_1_q8_0_at(q41, q8, ms, ns)
+        assert np.array_equal(at, dst[ms, ns]) and np.array_equal(T_at, T[ms, ns])
+        for mm in range(M):
+            one, _ = o.mul_mat_q4_1_f32(q41, x[mm:mm + 1])
+            assert np.array_equal(one[0], dst[mm])
+
+
 def pin_q8_0_block_dot_bruteforce(o) -> None:
     """Q8_0 weights, one lane at a time: sumi = qw * qx for every qw in -127..127 against a
     spread of qx; the extreme block (all 127 against all -127) gives -32 * 127 * 127."""
@@ -459,4 +549,6 @@ ALL_PINS = [
     pin_q8_0_matmul_vs_dense,
     pin_q5_0_quantizer,
     pin_q5_0_block_dot_and_product,
+    pin_q4_1_quantizer,
+    pin_q4_1_block_sums_and_product,
 ]

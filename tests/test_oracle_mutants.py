@@ -31,8 +31,10 @@ MUTANTS = {
     "q4_codes_from_fp16_scale": ("int v = (int)roundf(x[j] / d) + 8;",
                                  "int v = (int)roundf(x[j] / oracle_f16_to_f32(oracle_f32_to_f16(d))) + 8;"),
     "q4_zero_block_code": ("q[j] = 8;", "q[j] = 0;"),
-    "q4_high_nibble": ("return j < QK / 2 ? (byte & 0x0f) : (byte >> 4);",
-                       "return j < QK / 2 ? (byte & 0x0f) : (byte & 0x0f);"),
+    "q4_high_nibble": ("uint8_t byte = blk[2 + (j % (QK / 2))];\n    return j < QK / 2 ? (byte & 0x0f) : (byte >> 4);",
+                       "uint8_t byte = blk[2 + (j % (QK / 2))];\n    return j < QK / 2 ? (byte & 0x0f) : (byte & 0x0f);"),
+    "q41_high_nibble": ("uint8_t byte = blk[4 + (j % (QK / 2))];\n    return j < QK / 2 ? (byte & 0x0f) : (byte >> 4);",
+                        "uint8_t byte = blk[4 + (j % (QK / 2))];\n    return j < QK / 2 ? (byte & 0x0f) : (byte & 0x0f);"),
     "f16_ties_away": ("if (rem > half || (rem == half && (q & 1u))) q++;",
                       "if (rem >= half) q++;"),
     "f16_subnormal_scale": ("if (E == 0)       v = ldexpf((float)F, -24);",
@@ -53,6 +55,9 @@ MUTANTS = {
                            "qh |= (uint32_t)((q[j] >> 4) & 1) << (QK - 1 - j);"),
     "q5_scale_divisor": ("float d = vmax / -16.0f;", "float d = vmax / -15.0f;"),
     "q5_clamp": ("q[j] = v < 0 ? 0 : (v > 31 ? 31 : v);", "q[j] = v < 0 ? 0 : (v > 31 ? 15 : v);"),
+    "q41_min_term_dropped": ("        acc += mn * d8 * (double)sums[1];\n", ""),
+    "q41_divisor": ("float d = (hi - lo) / 15.0f;", "float d = (hi - lo) / 16.0f;"),
+    "q41_offset_from_max": ("int v = (int)roundf((x[j] - lo) / d);", "int v = (int)roundf((x[j] - hi) / d) + 15;"),
     "q8_abs_dropped": ("float a = fabsf(x[j]);\n        if (a > amax) amax = a;",
                        "float a = x[j];\n        if (a > amax) amax = a;"),
 }
