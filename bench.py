@@ -60,6 +60,10 @@ def step_bytes_q8(M, N, K):
     return N * K * 34 // 32 + 4 * M * K + 4 * M * N
 
 
+def step_bytes_q41(M, N, K):
+    return N * K * 20 // 32 + 4 * M * K + 4 * M * N
+
+
 def step_bytes_q5(M, N, K):
     return N * K * 22 // 32 + 4 * M * K + 4 * M * N
 
@@ -199,6 +203,14 @@ class GpuBench:
         q8 = gq.quantize_rows_q8_0(w)
         del w
         return gq.repack_q8_0(q8, N, K)
+
+    def q41_weights(self, N, K, seed):
+        torch = self.torch
+        gq = self.gq
+        w = torch.randn((N, K), generator=self.gen(seed), device=self.dev, dtype=torch.float32).mul_(0.02)
+        q41 = gq.quantize_q4_1(w)
+        del w
+        return gq.repack_q4_1(q41, N, K)
 
     def q5_weights(self, N, K, seed):
         torch = self.torch
@@ -458,6 +470,15 @@ def extras(b, weights, C, hbm_peak, bf16_peak, bf16_sustained, args):
     gbs = sum(step_bytes_q5(1, N, K) for N, K in SHAPES) * C5 / t / 1e9
     res["q5_0_m1"] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4), "us_per_step": round(t / C5 * 1e6, 2)}
     del w5
+    # Q4_1 weights (repacked tiles), same shapes, M = 1
+    C41 = b.copies_for(sum(N * K * 20 // 32 for N, K in SHAPES))
+    w41 = [[b.q41_weights(N, K, 7700 + 10 * c + i) for i, (N, K) in enumerate(SHAPES)] for c in range(C41)]
+    ls = [lambda c=c, i=i, N=N, K=K: gq.gq_mul_mat_q4_1_f32(w41[c][i], x1[i], o1[i], 1, N, K)
+          for c in range(C41) for i, (N, K) in enumerate(SHAPES)]
+    t = b.time_launches(ls)
+    gbs = sum(step_bytes_q41(1, N, K) for N, K in SHAPES) * C41 / t / 1e9
+    res["q4_1_m1"] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4), "us_per_step": round(t / C41 * 1e6, 2)}
+    del w41
 
     # M sweep on the two FFN shapes (Q4_0)
     sweep = {}
@@ -599,7 +620,7 @@ def cpu_baseline(seconds: float):
 
 
 def run_profile(spec: str):
-    """A few plain launches of one product, for ncu: KIND:M:N:K with KIND q4_0 | q5_0 | q8_0 | f16 | f16r | q4_0_tc | f16_tc."""
+    """A few plain launches of one product, for ncu: KIND:M:N:K with KIND q4_0 | q4_1 | q5_0 | q8_0 | f16 | f16r | q4_0_tc | f16_tc."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -613,6 +634,9 @@ def run_profile(spec: str):
     if kind.startswith("q4_0"):
         w = b.q4_weights(N, K, 2)
         fn = lambda: gq.gq_mul_mat_q4_0_f32_path(w, x, o, M, N, K, path)
+    elif kind == "q4_1":
+        w = b.q41_weights(N, K, 2)
+        fn = lambda: gq.gq_mul_mat_q4_1_f32(w, x, o, M, N, K)
     elif kind == "q5_0":
         w = b.q5_weights(N, K, 2)
         fn = lambda: gq.gq_mul_mat_q5_0_f32(w, x, o, M, N, K)

@@ -201,6 +201,31 @@ gq_status gq_repack_q8_0(const void *q8_blocks, void *q8_repacked, int64_t N, in
 gq_status gq_mul_mat_q8_0_f32(const void *q8_repacked, const float *src1, float *dst,
                               int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
+/* Q4_1 weights (llama.cpp PR #1632, "Introduction": named beside Q4_0 as a src0
+ * type of the q_f32 kind; the pages do not define it, and this library reads it
+ * as a scale and a minimum per block).  Block (20 bytes): fp16 d, fp16 m, then 16
+ * bytes with q_i in the low nibble and q_{i+16} in the high nibble of byte i;
+ * lo / hi = the first element equal to the block's minimum / maximum,
+ * d = (hi - lo) / 15, m = lo, q_j = clamp(round((x_j - lo) / d), 0, 15) (0 when
+ * d == 0), all in f32; the weight is q_j * fp16(d) + fp16(m).  gq_quantize_q4_1
+ * writes gq_q4_1_bytes(N, K) = N * K/32 * 20 bytes, byte-exact;
+ * gq_repack_q4_1 copies them once into tiles of 16 rows x 4 blocks, 1280 bytes
+ * each: the nibble bytes of block j of row r at (j * 16 + r) * 16, the fp16
+ * scales at 1024 + (r * 4 + j) * 2, the fp16 minimums at 1152 + (r * 4 + j) * 2;
+ * tile (g, t) at (g * ceil(K/128) + t) * 1280; padding is zero.
+ * gq_q4_1_repacked_bytes(N, K) = ceil(N/16) * ceil(K/128) * 1280.
+ * gq_mul_mat_q4_1_f32: dst[M][N] = Q8_0(src1) . Q4_1(src0)^T, each output
+ * sum_b (fp16(d_b) fp16(d8_b) sumi_b + fp16(m_b) fp16(d8_b) sx_b) with the exact
+ * int32 sums sumi_b = sum_j q_j q8_j and sx_b = sum_j q8_j, accumulated in f32
+ * (the GEMV family for every M; the stream's workspace as for the other products). */
+size_t gq_q4_1_bytes(int64_t N, int64_t K);            /* 0 if N <= 0, K <= 0 or K % 32 */
+size_t gq_q4_1_repacked_bytes(int64_t N, int64_t K);
+gq_status gq_quantize_q4_1(const float *w, void *q41_blocks, int64_t N, int64_t K, cudaStream_t stream);
+gq_status gq_repack_q4_1(const void *q41_blocks, void *q41_repacked, int64_t N, int64_t K,
+                         cudaStream_t stream);
+gq_status gq_mul_mat_q4_1_f32(const void *q41_repacked, const float *src1, float *dst,
+                              int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* Q5_0 weights (llama.cpp PR #1632, "Results": Q5_0 is among the types measured
  * on 7B; the pages do not define it, and this library reads it as Q4_0 with
  * five-bit codes).  Block (22 bytes): fp16 d, a little-endian 32-bit word whose

@@ -70,6 +70,11 @@ SIGNATURES = {
     "gq_debug_block_dots_q4_0": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_noalloc": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_host": ([_P, _P, _P, _I, _I, _I, _P], _S),
+    "gq_q4_1_bytes": ([_I, _I], ctypes.c_size_t),
+    "gq_q4_1_repacked_bytes": ([_I, _I], ctypes.c_size_t),
+    "gq_quantize_q4_1": ([_P, _P, _I, _I, _P], _S),
+    "gq_repack_q4_1": ([_P, _P, _I, _I, _P], _S),
+    "gq_mul_mat_q4_1_f32": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_q5_0_bytes": ([_I, _I], ctypes.c_size_t),
     "gq_q5_0_repacked_bytes": ([_I, _I], ctypes.c_size_t),
     "gq_quantize_q5_0": ([_P, _P, _I, _I, _P], _S),
@@ -230,6 +235,27 @@ def gq_mul_mat_q4_0_f32_host(q4_repacked, src1_host, dst_host, M: int, N: int, K
     """The Q4_0 product from host src1 into host dst (copies enqueued on the stream)."""
     _check(lib().gq_mul_mat_q4_0_f32_host(_ptr(q4_repacked), _host_ptr(src1_host), _host_ptr(dst_host), M, N, K,
                                           _stream(stream)), "gq_mul_mat_q4_0_f32_host")
+
+
+def gq_q4_1_bytes(N: int, K: int) -> int:
+    return lib().gq_q4_1_bytes(N, K)
+
+
+def gq_q4_1_repacked_bytes(N: int, K: int) -> int:
+    return lib().gq_q4_1_repacked_bytes(N, K)
+
+
+def gq_quantize_q4_1(w, q41_blocks, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_quantize_q4_1(_ptr(w), _ptr(q41_blocks), N, K, _stream(stream)), "gq_quantize_q4_1")
+
+
+def gq_repack_q4_1(q41_blocks, q41_repacked, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_repack_q4_1(_ptr(q41_blocks), _ptr(q41_repacked), N, K, _stream(stream)), "gq_repack_q4_1")
+
+
+def gq_mul_mat_q4_1_f32(q41_repacked, src1, dst, M: int, N: int, K: int, stream=None) -> None:
+    _check(lib().gq_mul_mat_q4_1_f32(_ptr(q41_repacked), _ptr(src1), _ptr(dst), M, N, K, _stream(stream)),
+           "gq_mul_mat_q4_1_f32")
 
 
 def gq_q5_0_bytes(N: int, K: int) -> int:
@@ -402,4 +428,28 @@ def mul_mat_q5_0_f32(q5_repacked, src1, N: int, out=None):
     M, K = src1.shape
     dst = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=src1.device)
     gq_mul_mat_q5_0_f32(q5_repacked, src1, dst, M, N, K)
+    return dst
+
+
+def quantize_q4_1(w):
+    """f32 CUDA tensor [N, K] -> Q4_1 bytes, uint8 [N, K/32, 20]."""
+    import torch
+    N, K = w.shape
+    out = torch.empty((N, K // 32, 20), dtype=torch.uint8, device=w.device)
+    gq_quantize_q4_1(w, out, N, K)
+    return out
+
+
+def repack_q4_1(q41, N: int, K: int):
+    import torch
+    out = torch.empty(gq_q4_1_repacked_bytes(N, K), dtype=torch.uint8, device=q41.device)
+    gq_repack_q4_1(q41, out, N, K)
+    return out
+
+
+def mul_mat_q4_1_f32(q41_repacked, src1, N: int, out=None):
+    import torch
+    M, K = src1.shape
+    dst = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=src1.device)
+    gq_mul_mat_q4_1_f32(q41_repacked, src1, dst, M, N, K)
     return dst

@@ -89,10 +89,18 @@ constexpr int Q8_TILE_BYTES = Q8_TILE_SCALE_OFFSET + 16 * TILE_BLOCKS * 2;
 constexpr int Q5_TILE_HIGH_OFFSET = TILE_SCALE_OFFSET;
 constexpr int Q5_TILE_SCALE_OFFSET = Q5_TILE_HIGH_OFFSET + 16 * TILE_BLOCKS * 4;
 constexpr int Q5_TILE_BYTES = Q5_TILE_SCALE_OFFSET + 16 * TILE_BLOCKS * 2;
+// Repacked Q4_1 weights: the nibble bytes as in Q4_0, the fp16 scales at 1024 + (r * 4 + j) * 2 and
+// the fp16 minimums at 1152 + (r * 4 + j) * 2.
+constexpr int Q41_TILE_MIN_OFFSET = TILE_SCALE_OFFSET + 16 * TILE_BLOCKS * 2;
+constexpr int Q41_TILE_BYTES = Q41_TILE_MIN_OFFSET + 16 * TILE_BLOCKS * 2;
 // weight formats of the kernel
-enum : int { WF_Q4 = 0, WF_F16 = 1, WF_Q8 = 2, WF_Q5 = 3 };
+enum : int { WF_Q4 = 0, WF_F16 = 1, WF_Q8 = 2, WF_Q5 = 3, WF_Q41 = 4 };
 __host__ __device__ constexpr int tile_bytes(int wf) {
-    return wf == WF_F16 ? F16_TILE_BYTES : wf == WF_Q8 ? Q8_TILE_BYTES : wf == WF_Q5 ? Q5_TILE_BYTES : TILE_BYTES;
+    return wf == WF_F16  ? F16_TILE_BYTES
+           : wf == WF_Q8 ? Q8_TILE_BYTES
+           : wf == WF_Q5 ? Q5_TILE_BYTES
+           : wf == WF_Q41 ? Q41_TILE_BYTES
+                          : TILE_BYTES;
 }
 __host__ __device__ constexpr int chunk_bytes(int wf) { return CHUNK_TILES * tile_bytes(wf); }
 constexpr int MAX_SLOTS = 12;
@@ -278,7 +286,7 @@ __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
 // ---------------------------------------------------------------------------
 template <int MT, int CWT, int REGS, int WF, int FIXW>
 __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) gemv_q4_0_kernel(const Params p) {
-    constexpr bool F16W = WF == WF_F16, Q8W = WF == WF_Q8, Q5W = WF == WF_Q5;
+    constexpr bool F16W = WF == WF_F16, Q8W = WF == WF_Q8, Q5W = WF == WF_Q5, Q41W = WF == WF_Q41;
     constexpr int TB = tile_bytes(WF), CB = chunk_bytes(WF);
     // fp16 scales in a Q4_0 / Q5_0 / Q8_0 tile
     constexpr int SCALES = Q8W ? Q8_TILE_SCALE_OFFSET : Q5W ? Q5_TILE_SCALE_OFFSET : TILE_SCALE_OFFSET;
@@ -604,6 +612,7 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                 const int tl = u + ti;                         // tile index within the slice
                 const uint8_t *tile = ring + (size_t)slot * CB + ti * TB;
                 const uint2 d4w = *reinterpret_cast<const uint2 *>(tile + SCALES + n * 8);
+                const uint2 m4w = Q41W ? *reinterpret_cast<const uint2 *>(tile + Q41_TILE_MIN_OFFSET + n * 8) : d4w;
 #pragma unroll
                 for (int jj = 0; jj < 2; jj++) {
                     const int jb = jh + 2 * jj;                // block of the tile
@@ -612,6 +621,8 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                     const uint4 q_hi = Q8W ? lds128(tile + (jb * 16 + n) * 32 + 16) : q;
                     const uint32_t dw = jb & 2 ? d4w.y : d4w.x;
                     const float d4 = (jb & 1) ? half_hi(dw) : half_lo(dw);
+                    const uint32_t mw = jb & 2 ? m4w.y : m4w.x;
+                    const float m4 = (jb & 1) ? half_hi(mw) : half_lo(mw);   // Q4_1: the block minimum
                     const int blk = 4 * tl + jb;
                     const uint8_t *a = act + im.codes + (size_t)blk * 32;
 #pragma unroll
@@ -628,8 +639,12 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                             : Q5W ? block_dot_q5(q, *reinterpret_cast<const uint32_t *>(tile + Q5_TILE_HIGH_OFFSET +
                                                                                      (jb * 16 + n) * 4),
                                                  a0, a1, 2 * __float_as_int(sc.y))   // -16 sum of the codes
-                                  : block_dot(q, a0, a1, __float_as_int(sc.y));
+                            : Q41W ? block_dot(q, a0, a1, 0)                  // sum_j q_j q8_j
+                                   : block_dot(q, a0, a1, __float_as_int(sc.y));
                         acc[tw][MMA ? 0 : m] = fmaf(d4 * sc.x, (float)sumi, acc[tw][MMA ? 0 : m]);
+                        if constexpr (Q41W)   // + m d8 sum_j q8_j (the image holds -8 sum_j q8_j)
+                            acc[tw][MMA ? 0 : m] =
+                                fmaf(m4 * sc.x, (float)(-(__float_as_int(sc.y) >> 3)), acc[tw][MMA ? 0 : m]);
                     }
                 }
             };
@@ -646,6 +661,8 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                 const uint8_t *tile = ring + (size_t)slot * CB + ti * TB;
                 const uint2 s0 = *reinterpret_cast<const uint2 *>(tile + SCALES + fg * 8);
                 const uint2 s1 = *reinterpret_cast<const uint2 *>(tile + SCALES + (fg + 8) * 8);
+                const uint2 mn0 = Q41W ? *reinterpret_cast<const uint2 *>(tile + Q41_TILE_MIN_OFFSET + fg * 8) : s0;
+                const uint2 mn1 = Q41W ? *reinterpret_cast<const uint2 *>(tile + Q41_TILE_MIN_OFFSET + (fg + 8) * 8) : s1;
 #pragma unroll
                 for (int jb = 0; jb < 4; jb++) {
                     uint32_t alo[4], ahi[4];
@@ -655,6 +672,13 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                         q8_to_f16x2(*reinterpret_cast<const uint32_t *>(r1), alo[1], alo[3]);
                         q8_to_f16x2(*reinterpret_cast<const uint32_t *>(r0 + 16), ahi[0], ahi[2]);
                         q8_to_f16x2(*reinterpret_cast<const uint32_t *>(r1 + 16), ahi[1], ahi[3]);
+                    } else if constexpr (Q41W) {   // the codes q themselves (the minimum term is added below)
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg) * 16 + 4 * ft);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg + 8) * 16 + 4 * ft);
+                        q4u_to_f16x2(w0 & 0x0F0F0F0Fu, alo[0], alo[2]);
+                        q4u_to_f16x2(w1 & 0x0F0F0F0Fu, alo[1], alo[3]);
+                        q4u_to_f16x2((w0 >> 4) & 0x0F0F0F0Fu, ahi[0], ahi[2]);
+                        q4u_to_f16x2((w1 >> 4) & 0x0F0F0F0Fu, ahi[1], ahi[3]);
                     } else if constexpr (Q5W) {   // word ft of rows fg, fg + 8 with their fifth bits
                         const uint32_t w0 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg) * 16 + 4 * ft);
                         const uint32_t w1 = *reinterpret_cast<const uint32_t *>(tile + (jb * 16 + fg + 8) * 16 + 4 * ft);
@@ -680,6 +704,9 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                     const uint32_t sw0 = jb & 2 ? s0.y : s0.x, sw1 = jb & 2 ? s1.y : s1.x;
                     const float d4r0 = (jb & 1) ? half_hi(sw0) : half_lo(sw0);   // row fg
                     const float d4r1 = (jb & 1) ? half_hi(sw1) : half_lo(sw1);   // row fg + 8
+                    const uint32_t mw0 = jb & 2 ? mn0.y : mn0.x, mw1 = jb & 2 ? mn1.y : mn1.x;
+                    const float m4r0 = (jb & 1) ? half_hi(mw0) : half_lo(mw0);   // Q4_1 minimums
+                    const float m4r1 = (jb & 1) ? half_hi(mw1) : half_lo(mw1);
                     const int blk = 4 * tl + jb;
 #pragma unroll
                     for (int nt = 0; nt < NTL; nt++) {
@@ -699,6 +726,14 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                         h[1] = fmaf(d4r0 * d8c1, d[1], h[1]);   // row fg,     activation row 2ft + 1
                         h[2] = fmaf(d4r1 * d8c0, d[2], h[2]);   // row fg + 8, activation row 2ft
                         h[3] = fmaf(d4r1 * d8c1, d[3], h[3]);   // row fg + 8, activation row 2ft + 1
+                        if constexpr (Q41W) {   // + m d8 sum_j q8_j, as in the dp4a path
+                            const float sx0 = (float)(-(__float_as_int(act_sc[mc0 * sc_stride + blk].y) >> 3));
+                            const float sx1 = (float)(-(__float_as_int(act_sc[mc1 * sc_stride + blk].y) >> 3));
+                            h[0] = fmaf(m4r0 * d8c0, sx0, h[0]);
+                            h[1] = fmaf(m4r0 * d8c1, sx1, h[1]);
+                            h[2] = fmaf(m4r1 * d8c0, sx0, h[2]);
+                            h[3] = fmaf(m4r1 * d8c1, sx1, h[3]);
+                        }
                     }
                 }
             };
@@ -804,7 +839,7 @@ int env_int(const char *name, int dflt) {
 
 // The dynamic shared-memory limit is raised once per (device, kernel).
 constexpr int MAX_DEV = 64;
-constexpr int MAX_VARIANTS = 24;
+constexpr int MAX_VARIANTS = 32;
 std::atomic<bool> g_smem_set[MAX_DEV][MAX_VARIANTS];
 
 template <typename Kernel>
@@ -866,7 +901,9 @@ const Variant VARIANTS[] = {
     variant<1, 8, 88, WF_Q8, 0>(),   variant<1, 8, 88, WF_Q8, 1>(),   variant<2, 16, 96, WF_Q8, 2>(),
     variant<4, 16, 96, WF_Q8, 2>(),  variant<8, 16, 96, WF_Q8, 2>(),  variant<16, 16, 96, WF_Q8, 2>(),
     variant<1, 8, 88, WF_Q5, 0>(),   variant<1, 8, 88, WF_Q5, 1>(),   variant<2, 16, 96, WF_Q5, 2>(),
-    variant<4, 16, 96, WF_Q5, 2>(),  variant<8, 16, 96, WF_Q5, 2>(),  variant<16, 16, 96, WF_Q5, 2>()};
+    variant<4, 16, 96, WF_Q5, 2>(),  variant<8, 16, 96, WF_Q5, 2>(),  variant<16, 16, 96, WF_Q5, 2>(),
+    variant<1, 8, 88, WF_Q41, 0>(),  variant<1, 8, 88, WF_Q41, 1>(),  variant<2, 16, 96, WF_Q41, 2>(),
+    variant<4, 16, 96, WF_Q41, 2>(), variant<8, 16, 96, WF_Q41, 2>(), variant<16, 16, 96, WF_Q41, 2>()};
 constexpr int N_VARIANTS = sizeof(VARIANTS) / sizeof(VARIANTS[0]);
 static_assert(N_VARIANTS <= MAX_VARIANTS, "one shared-memory flag per variant");
 
@@ -960,11 +997,11 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
             return (int)std::min<size_t>(MAX_SLOTS,
                                          (budget - std::min(budget, fixed + 256)) / (chunk_bytes(wf) + 16));
         };
-        // the 8-warp Q4_0 / Q5_0 shape keeps a ring of half the shared memory (MIN_SLOTS_HALF chunks at
+        // the 8-warp Q4_0 / Q4_1 / Q5_0 shape keeps a ring of half the shared memory (MIN_SLOTS_HALF chunks at
         // least): two CTAs per SM without fix-up warps; with one, a half ring measured faster than
         // a full one.  F16 and Q8_0 tiles (more bytes per weight; 34 KB Q8_0 chunks would leave
         // two slots in half the shared memory) keep a full ring.
-        p.slots = kv.cw == 8 && (wf == WF_Q4 || wf == WF_Q5) ? slots_for(SMEM_HALF - 1024) : 0;
+        p.slots = kv.cw == 8 && (wf == WF_Q4 || wf == WF_Q5 || wf == WF_Q41) ? slots_for(SMEM_HALF - 1024) : 0;
         if (p.slots < MIN_SLOTS_HALF) p.slots = slots_for(SMEM_LIMIT - 1024);
         const int slots_env = env_int("GQ_GEMV_SLOTS", 0);   // tuning: ring slots, up to what fits
         if (slots_env > 0) p.slots = std::min(slots_env, slots_for(SMEM_LIMIT - 1024));
@@ -1048,6 +1085,16 @@ gq_status launch_gemv_q5_0(const void *rep, const float *x, float *dst, int64_t 
     gq_status st = get_workspace(s, cb, db, &ws);
     if (st != GQ_OK) return st;
     return launch_gemv_with(WF_Q5, rep, x, dst, M, N, K, ws, s);
+}
+
+gq_status launch_gemv_q4_1(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t s) {
+    size_t cb, db;
+    gemv_workspace(WF_Q41, N, K, &cb, &db);
+    Workspace ws;
+    gq_status st = get_workspace(s, cb, db, &ws);
+    if (st != GQ_OK) return st;
+    return launch_gemv_with(WF_Q41, rep, x, dst, M, N, K, ws, s);
 }
 
 }  // namespace gq

@@ -313,6 +313,48 @@ gq_status gq_mul_mat_f16_f32(const void *src0_f16, const float *src1, float *dst
     return gq_mul_mat_f16_f32_path(src0_f16, src1, dst, M, N, K, GQ_PATH_AUTO, stream);
 }
 
+size_t gq_q4_1_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % QK) return 0;
+    return (size_t)N * (size_t)(K / QK) * 20;
+}
+
+size_t gq_q4_1_repacked_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % QK) return 0;
+    return (size_t)((N + 15) / 16) * (size_t)((K / QK + TILE_BLOCKS - 1) / TILE_BLOCKS) * 1280;
+}
+
+gq_status gq_quantize_q4_1(const float *w, void *q41_blocks, int64_t N, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(1, N, K));
+    GQ_TRY(check_ptr(w, "w"));
+    GQ_TRY(check_ptr(q41_blocks, "q41_blocks"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_quantize_q4_1(w, q41_blocks, N, K, stream));
+    return ok();
+}
+
+gq_status gq_repack_q4_1(const void *q41_blocks, void *q41_repacked, int64_t N, int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(1, N, K));
+    GQ_TRY(check_ptr(q41_blocks, "q41_blocks"));
+    GQ_TRY(check_ptr(q41_repacked, "q41_repacked"));
+    const uintptr_t a = (uintptr_t)q41_blocks, b = (uintptr_t)q41_repacked;
+    if (a < b + gq_q4_1_repacked_bytes(N, K) && b < a + gq_q4_1_bytes(N, K))
+        return fail(GQ_ERR_INVALID_ARG, "q41_blocks and q41_repacked overlap");
+    GQ_TRY(check_device());
+    GQ_TRY(launch_repack_q4_1(q41_blocks, q41_repacked, N, K, stream));
+    return ok();
+}
+
+gq_status gq_mul_mat_q4_1_f32(const void *q41_repacked, const float *src1, float *dst, int64_t M, int64_t N,
+                              int64_t K, cudaStream_t stream) {
+    GQ_TRY(check_sizes(M, N, K));
+    GQ_TRY(check_ptr(q41_repacked, "q41_repacked"));
+    GQ_TRY(check_ptr(src1, "src1"));
+    GQ_TRY(check_ptr(dst, "dst"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_gemv_q4_1(q41_repacked, src1, dst, M, N, K, stream));
+    return ok();
+}
+
 size_t gq_q5_0_bytes(int64_t N, int64_t K) {
     if (N <= 0 || K <= 0 || K % QK) return 0;
     return (size_t)N * (size_t)(K / QK) * 22;

@@ -246,6 +246,15 @@ __device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], uint32_t a0, uint
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Four codes 0..15 (one per byte) -> two half2 of q itself, exact (as q4_to_f16x2, bias 1024).
+__device__ __forceinline__ void q4u_to_f16x2(uint32_t v, uint32_t &h01, uint32_t &h23) {
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));   // 1024
+    uint32_t a = __byte_perm(v, 0x64646464u, 0x4140u), b = __byte_perm(v, 0x64646464u, 0x4342u);
+    __half2 x = __hsub2(*reinterpret_cast<__half2 *>(&a), bias), y = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
+    h01 = *reinterpret_cast<uint32_t *>(&x);
+    h23 = *reinterpret_cast<uint32_t *>(&y);
+}
+
 // Four codes 0..31 (one per byte) -> two half2 of (q - 16), exact (as q4_to_f16x2, bias 1040).
 __device__ __forceinline__ void q5_to_f16x2(uint32_t v, uint32_t &h01, uint32_t &h23) {
     const __half2 bias = __halves2half2(__ushort_as_half(0x6410), __ushort_as_half(0x6410));   // 1040

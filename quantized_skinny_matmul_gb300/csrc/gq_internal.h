@@ -66,6 +66,11 @@ gq_status launch_quantize_q5_0(const float *w, void *q5, int64_t N, int64_t K, c
 gq_status launch_repack_q5_0(const void *q5, void *rep, int64_t N, int64_t K, cudaStream_t s);
 gq_status launch_gemv_q5_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
                            cudaStream_t s);
+// Q4_1 weights: the quantizer, the repack into 16-row x 4-block tiles (1280 bytes), the GEMV.
+gq_status launch_quantize_q4_1(const float *w, void *q41, int64_t N, int64_t K, cudaStream_t s);
+gq_status launch_repack_q4_1(const void *q41, void *rep, int64_t N, int64_t K, cudaStream_t s);
+gq_status launch_gemv_q4_1(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t s);
 // Tensor-core tiles (tcgen05) for M >= 32; workspace: the fp16 activations.
 size_t tc_workspace_bytes(int64_t M, int64_t K);
 gq_status launch_tc_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,

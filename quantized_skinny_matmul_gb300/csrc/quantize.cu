@@ -68,6 +68,41 @@ __global__ void quantize_q5_0_kernel(const float *__restrict__ w, uint8_t *__res
     }
 }
 
+// Q4_1 of weight blocks: one warp per block.  lo / hi = the first element (in index order)
+// equal to the block's minimum / maximum, d = (hi - lo) / 15, q = clamp(round((x - lo) / d), 0, 15)
+// (0 when d == 0); block = fp16 d, fp16 lo, 16 bytes q_i | q_{i+16} << 4.
+__global__ void quantize_q4_1_kernel(const float *__restrict__ w, uint8_t *__restrict__ out, int64_t nblocks) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = warp; b < nblocks; b += nwarps) {
+        const float x = w[b * QK + lane];
+        float mn = x, mx = x;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        // the values equal to the extreme compare equal whatever their zero sign: take the first
+        const float lo = __shfl_sync(0xffffffffu, x, __ffs(__ballot_sync(0xffffffffu, x == mn)) - 1);
+        const float hi = __shfl_sync(0xffffffffu, x, __ffs(__ballot_sync(0xffffffffu, x == mx)) - 1);
+        const float d = (hi - lo) / 15.0f;
+        int q = 0;
+        if (d != 0.0f) {
+            const int v = (int)roundf((x - lo) / d);
+            q = v < 0 ? 0 : (v > 15 ? 15 : v);
+        }
+        const int qhi = __shfl_down_sync(0xffffffffu, q, 16);
+        uint8_t *o = out + b * 20;                         // 4-byte aligned: 20 * b
+        if (lane < 16) o[4 + lane] = (uint8_t)(q | (qhi << 4));
+        if (lane == 0) {
+            *reinterpret_cast<unsigned short *>(o) = __half_as_ushort(__float2half_rn(d));
+            *reinterpret_cast<unsigned short *>(o + 2) = __half_as_ushort(__float2half_rn(lo));
+        }
+    }
+}
+
 // Q8_0 of activation rows: the INIT stage that produces wdata (Arm China NUMA
 // article, "MulMat 算子優化").
 __global__ void quantize_rows_q8_0_kernel(const float *__restrict__ x, uint8_t *__restrict__ out,
@@ -208,6 +243,33 @@ __global__ void repack_q5_0_kernel(const uint8_t *__restrict__ q5, uint8_t *__re
     }
 }
 
+// Q4_1 blocks [N][nb] x 20 -> tiles of 16 rows x 4 blocks, 1280 bytes: the 16 nibble bytes of
+// block j of row r at (j * 16 + r) * 16, the fp16 scales at 1024 + (r * 4 + j) * 2 and the fp16
+// minimums at 1152 + (r * 4 + j) * 2.  One thread per (tile, row, block); padding is all zeros.
+__global__ void repack_q4_1_kernel(const uint8_t *__restrict__ q41, uint8_t *__restrict__ out, int64_t N,
+                                   int64_t nb, int64_t NT, int64_t items) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = i / 64, rj = i % 64;
+        const int r = (int)(rj / 4), j = (int)(rj % 4);
+        const int64_t g = tile / NT, t = tile % NT;
+        const int64_t n = 16 * g + r, b = 4 * t + j;
+        uint8_t *dt = out + tile * 1280;
+        uint4 nib = make_uint4(0u, 0u, 0u, 0u);
+        uint16_t d = 0, m = 0;
+        if (n < N && b < nb) {
+            const uint8_t *src = q41 + (n * nb + b) * 20;   // 4-byte aligned
+            d = *reinterpret_cast<const uint16_t *>(src);
+            m = *reinterpret_cast<const uint16_t *>(src + 2);
+            const uint32_t *q = reinterpret_cast<const uint32_t *>(src + 4);
+            nib = make_uint4(q[0], q[1], q[2], q[3]);
+        }
+        *reinterpret_cast<uint4 *>(dt + (j * 16 + r) * 16) = nib;
+        *reinterpret_cast<uint16_t *>(dt + 1024 + (r * 4 + j) * 2) = d;
+        *reinterpret_cast<uint16_t *>(dt + 1152 + (r * 4 + j) * 2) = m;
+    }
+}
+
 int grid_for(int64_t work_items, int threads) {
     int64_t blocks = (work_items + threads - 1) / threads;
     const int64_t cap = (int64_t)sm_count() * 16;
@@ -237,6 +299,18 @@ gq_status launch_repack_q4_0(const void *q4, void *rep, int64_t N, int64_t K, cu
     const int64_t blocks = (threads + 255) / 256;
     repack_q4_0_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint8_t *)q4, (uint8_t *)rep, N, nb, NT, ntiles);
     return check_cuda(cudaGetLastError(), "repack_q4_0 launch");
+}
+
+gq_status launch_quantize_q4_1(const float *w, void *q41, int64_t N, int64_t K, cudaStream_t s) {
+    const int64_t nblocks = N * (K / QK);
+    quantize_q4_1_kernel<<<grid_for(nblocks * 32, 256), 256, 0, s>>>(w, (uint8_t *)q41, nblocks);
+    return check_cuda(cudaGetLastError(), "quantize_q4_1 launch");
+}
+
+gq_status launch_repack_q4_1(const void *q41, void *rep, int64_t N, int64_t K, cudaStream_t s) {
+    const int64_t nb = K / QK, NT = (nb + TILE_BLOCKS - 1) / TILE_BLOCKS, items = (N + 15) / 16 * NT * 64;
+    repack_q4_1_kernel<<<grid_for(items, 256), 256, 0, s>>>((const uint8_t *)q41, (uint8_t *)rep, N, nb, NT, items);
+    return check_cuda(cudaGetLastError(), "repack_q4_1 launch");
 }
 
 gq_status launch_quantize_q5_0(const float *w, void *q5, int64_t N, int64_t K, cudaStream_t s) {

@@ -123,3 +123,34 @@ def repack_q5_0_ref(q5: np.ndarray) -> np.ndarray:
                     else:
                         out[o_hi:o_hi + 4] = pad_high          # code 16: nibble 0, fifth bit 1; scale 0
     return out
+
+
+def repack_q4_1_ref(q41: np.ndarray) -> np.ndarray:
+    """Q4_1 blocks [N, nb, 20] -> the tile layout of gq_repack_q4_1, as bytes."""
+    N, nb = q41.shape[0], q41.shape[1]
+    N16, NT = -(-N // 16), -(-nb // 4)
+    P = np.zeros((N16 * 16, NT * 4, 20), np.uint8)
+    P[:N, :nb] = q41
+    T = P.reshape(N16, 16, NT, 4, 20).transpose(0, 2, 3, 1, 4)   # [g, t, j, r, 20]
+    out = np.empty((N16, NT, 1280), np.uint8)
+    out[:, :, :1024] = T[..., 4:].reshape(N16, NT, 1024)
+    out[:, :, 1024:1152] = T[..., 0:2].transpose(0, 1, 3, 2, 4).reshape(N16, NT, 128)   # d [r, j]
+    out[:, :, 1152:] = T[..., 2:4].transpose(0, 1, 3, 2, 4).reshape(N16, NT, 128)       # m [r, j]
+    return out.reshape(-1)
+
+
+def repack_q4_1_loops(q41: np.ndarray) -> np.ndarray:
+    N, nb = q41.shape[0], q41.shape[1]
+    N16, NT = -(-N // 16), -(-nb // 4)
+    out = np.zeros(N16 * NT * 1280, np.uint8)
+    for g in range(N16):
+        for t in range(NT):
+            base = (g * NT + t) * 1280
+            for j in range(4):
+                for r in range(16):
+                    n, b = 16 * g + r, 4 * t + j
+                    if n < N and b < nb:
+                        out[base + (j * 16 + r) * 16: base + (j * 16 + r) * 16 + 16] = q41[n, b, 4:]
+                        out[base + 1024 + (r * 4 + j) * 2: base + 1024 + (r * 4 + j) * 2 + 2] = q41[n, b, 0:2]
+                        out[base + 1152 + (r * 4 + j) * 2: base + 1152 + (r * 4 + j) * 2 + 2] = q41[n, b, 2:4]
+    return out

@@ -63,6 +63,8 @@ def test_sizes(lib):
     assert gq.gq_q8_0_repacked_bytes(4096, 4096) == 4096 * 128 * 34
     assert gq.gq_q5_0_bytes(4096, 4096) == 4096 * 128 * 22 == gq.gq_q5_0_repacked_bytes(4096, 4096)
     assert gq.gq_q5_0_repacked_bytes(17, 96) == 2 * 1 * 1408 and gq.gq_q5_0_bytes(4, 33) == 0
+    assert gq.gq_q4_1_bytes(4096, 4096) == 4096 * 128 * 20 == gq.gq_q4_1_repacked_bytes(4096, 4096)
+    assert gq.gq_q4_1_repacked_bytes(17, 96) == 2 * 1 * 1280
     assert gq.gq_q8_0_repacked_bytes(17, 96) == 2 * 1 * 2176 and gq.gq_q8_0_repacked_bytes(16, 48) == 0
 
 
@@ -98,6 +100,9 @@ def test_argument_checks_other_entries(lib):
     assert lib.gq_mul_mat_f16r_f32(0, FAKE, FAKE, 1, 64, 64, None) == gq.GQ_ERR_INVALID_ARG
     assert lib.gq_repack_q8_0(FAKE, FAKE + 64, 4, 64, None) == gq.GQ_ERR_INVALID_ARG   # overlap
     assert lib.gq_repack_q5_0(FAKE, FAKE + 32, 4, 64, None) == gq.GQ_ERR_INVALID_ARG   # overlap
+    assert lib.gq_repack_q4_1(FAKE, FAKE + 32, 4, 64, None) == gq.GQ_ERR_INVALID_ARG   # overlap
+    assert lib.gq_quantize_q4_1(ODD, FAKE, 4, 64, None) == gq.GQ_ERR_MISALIGNED
+    assert lib.gq_mul_mat_q4_1_f32(FAKE, FAKE, FAKE, 0, 64, 64, None) == gq.GQ_ERR_INVALID_ARG
     assert lib.gq_quantize_q5_0(FAKE, FAKE, 4, 40, None) == gq.GQ_ERR_INVALID_ARG
     assert lib.gq_mul_mat_q5_0_f32(FAKE, ODD, FAKE, 1, 64, 64, None) == gq.GQ_ERR_MISALIGNED
     assert lib.gq_mul_mat_q8_0_f32(FAKE, FAKE, ODD, 1, 64, 64, None) == gq.GQ_ERR_MISALIGNED

@@ -42,3 +42,11 @@ def test_q5_0_high_word_gives_the_codes():
             for b in range(4):
                 assert ((lo >> (8 * b + 4)) & 1) == (qh >> (4 * w + b)) & 1
                 assert ((hi >> (8 * b + 4)) & 1) == (qh >> (16 + 4 * w + b)) & 1
+
+
+@pytest.mark.parametrize("N,nb", [(16, 4), (37, 3), (33, 9), (1, 1)])
+def test_q4_1_layout_statements_agree(N, nb):
+    from layout_ref import repack_q4_1_ref, repack_q4_1_loops
+    rng = np.random.default_rng(N * 7 + nb)
+    q41 = rng.integers(0, 256, size=(N, nb, 20), dtype=np.uint8)
+    assert np.array_equal(repack_q4_1_ref(q41), repack_q4_1_loops(q41))
