@@ -479,6 +479,16 @@ def extras(b, weights, C, hbm_peak, bf16_peak, bf16_sustained, args):
     gbs = sum(step_bytes_q41(1, N, K) for N, K in SHAPES) * C41 / t / 1e9
     res["q4_1_m1"] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4), "us_per_step": round(t / C41 * 1e6, 2)}
     del w41
+    # per-shape dispatch profiles (Q4_0): both families benched at M = 16..256; the smallest
+    # benched M at which the tile family is faster, per shape
+    disp = {}
+    for i, (N, K) in enumerate(SHAPES):
+        prof = gq.tune_dispatch(weights[0][i], N, K, Ms=(16, 32, 64, 128, 256), reps=10, install=False)
+        cross = [M for M, tg, tt in zip(prof["M"], prof["gemv_us"], prof["tc_us"]) if tt < tg]
+        disp[f"{N}x{K}"] = {"tile_faster_from_M": cross[0] if cross else None,
+                            "gemv_us": [round(t, 2) for t in prof["gemv_us"]],
+                            "tc_us": [round(t, 2) for t in prof["tc_us"]], "M": prof["M"]}
+    res["dispatch_q4_0"] = disp
 
     # M sweep on the two FFN shapes (Q4_0)
     sweep = {}

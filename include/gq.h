@@ -68,7 +68,8 @@ typedef enum gq_status {
 
 /* Which kernel family serves a product. */
 typedef enum gq_path {
-    GQ_PATH_AUTO = 0,   /* M <= threshold: the GEMV family, else the tensor-core tiles */
+    GQ_PATH_AUTO = 0,   /* the shape's dispatch profile, if one is set; else M <= threshold:
+                           the GEMV family, above it the tensor-core tiles */
     GQ_PATH_GEMV = 1,   /* the skinny GEMV kernels (any M; M > 16 runs in 16-row slices) */
     GQ_PATH_TC = 2      /* the tcgen05 tensor-core tile kernels (any M) */
 } gq_path;
@@ -279,6 +280,25 @@ gq_status gq_mul_mat_f16_f32_path(const void *src0_f16, const float *src1, float
  * Process-wide; GQ_ERR_INVALID_ARG if t < 0. */
 gq_status gq_set_m_threshold(int64_t t);
 int64_t gq_get_m_threshold(void);
+
+/* Per-shape dispatch profiles (llama.cpp PR #1632, "Solutions", item 4: the
+ * shape is matched by N and K, the time of every kernel profile is estimated for
+ * the given M by interpolating between benched M, and the fastest is taken).  A
+ * profile holds, for one weight kind and one (N, K), the benched times of the
+ * GEMV family and of the tile family at `count` values of M (strictly increasing,
+ * positive; the times finite and non-negative, in any unit).  GQ_PATH_AUTO then
+ * runs, for M rows, the family whose time is smaller when each curve is taken as
+ * linear through its two benched points around M (the two end points outside the
+ * benched range); shapes without a profile use the M threshold.  A new profile
+ * for a shape replaces the old one.  Process-wide, thread-safe; no GPU work.
+ * gq_choose_path reports the family GQ_PATH_AUTO would run.  The Python helper
+ * tune_dispatch() benches both families on the current device and installs the
+ * profile. */
+typedef enum { GQ_KIND_Q4_0 = 0, GQ_KIND_F16 = 1 } gq_weight_kind;
+gq_status gq_set_dispatch_profile(int kind, int64_t N, int64_t K, const int64_t *Ms, const double *t_gemv,
+                                  const double *t_tc, int64_t count);
+gq_status gq_clear_dispatch_profiles(void);
+gq_path gq_choose_path(int kind, int64_t N, int64_t K, int64_t M);
 
 /* The Q4_0 product of gq_mul_mat_q4_0_f32, for callers that cannot allocate
  * device memory: code recording into a CUDA graph while the stream is captured

@@ -70,6 +70,9 @@ SIGNATURES = {
     "gq_debug_block_dots_q4_0": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_noalloc": ([_P, _P, _P, _I, _I, _I, _P], _S),
     "gq_mul_mat_q4_0_f32_host": ([_P, _P, _P, _I, _I, _I, _P], _S),
+    "gq_set_dispatch_profile": ([ctypes.c_int, _I, _I, _P, _P, _P, _I], _S),
+    "gq_clear_dispatch_profiles": ([], _S),
+    "gq_choose_path": ([ctypes.c_int, _I, _I, _I], ctypes.c_int),
     "gq_q4_1_bytes": ([_I, _I], ctypes.c_size_t),
     "gq_q4_1_repacked_bytes": ([_I, _I], ctypes.c_size_t),
     "gq_quantize_q4_1": ([_P, _P, _I, _I, _P], _S),
@@ -235,6 +238,30 @@ def gq_mul_mat_q4_0_f32_host(q4_repacked, src1_host, dst_host, M: int, N: int, K
     """The Q4_0 product from host src1 into host dst (copies enqueued on the stream)."""
     _check(lib().gq_mul_mat_q4_0_f32_host(_ptr(q4_repacked), _host_ptr(src1_host), _host_ptr(dst_host), M, N, K,
                                           _stream(stream)), "gq_mul_mat_q4_0_f32_host")
+
+
+GQ_KIND_Q4_0 = 0
+GQ_KIND_F16 = 1
+
+
+def gq_set_dispatch_profile(kind: int, N: int, K: int, Ms, t_gemv, t_tc) -> None:
+    """Install the benched times of both kernel families at the given M for one shape."""
+    n = len(Ms)
+    if len(t_gemv) != n or len(t_tc) != n:
+        raise ValueError("one time per M and family")
+    m_arr = (ctypes.c_int64 * n)(*[int(m) for m in Ms])
+    g_arr = (ctypes.c_double * n)(*[float(t) for t in t_gemv])
+    t_arr = (ctypes.c_double * n)(*[float(t) for t in t_tc])
+    _check(lib().gq_set_dispatch_profile(kind, N, K, ctypes.addressof(m_arr), ctypes.addressof(g_arr),
+                                         ctypes.addressof(t_arr), n), "gq_set_dispatch_profile")
+
+
+def gq_clear_dispatch_profiles() -> None:
+    _check(lib().gq_clear_dispatch_profiles(), "gq_clear_dispatch_profiles")
+
+
+def gq_choose_path(kind: int, N: int, K: int, M: int) -> int:
+    return lib().gq_choose_path(kind, N, K, M)
 
 
 def gq_q4_1_bytes(N: int, K: int) -> int:
@@ -453,3 +480,37 @@ def mul_mat_q4_1_f32(q41_repacked, src1, N: int, out=None):
     dst = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=src1.device)
     gq_mul_mat_q4_1_f32(q41_repacked, src1, dst, M, N, K)
     return dst
+
+
+def tune_dispatch(weights, N: int, K: int, kind: int = GQ_KIND_Q4_0,
+                  Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 512), reps: int = 20, install: bool = True):
+    """Bench both kernel families on the current device for one shape and install the profile.
+
+    ``weights`` are the product's weights on the device (Q4_0 repacked, or row-major F16).
+    Each M is timed with CUDA events over ``reps`` back-to-back products after a warm-up.
+    Returns {"M": [...], "gemv_us": [...], "tc_us": [...]}.
+    """
+    import torch
+    fn = gq_mul_mat_q4_0_f32_path if kind == GQ_KIND_Q4_0 else gq_mul_mat_f16_f32_path
+    out = {"M": [], "gemv_us": [], "tc_us": []}
+    gen = torch.Generator(device=weights.device).manual_seed(1234)
+    for M in Ms:
+        x = torch.randn((M, K), generator=gen, device=weights.device, dtype=torch.float32)
+        dst = torch.empty((M, N), device=weights.device, dtype=torch.float32)
+        times = []
+        for path in (GQ_PATH_GEMV, GQ_PATH_TC):
+            for _ in range(3):
+                fn(weights, x, dst, M, N, K, path)
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            start.record()
+            for _ in range(reps):
+                fn(weights, x, dst, M, N, K, path)
+            end.record()
+            end.synchronize()
+            times.append(start.elapsed_time(end) * 1e3 / reps)
+        out["M"].append(int(M))
+        out["gemv_us"].append(times[0])
+        out["tc_us"].append(times[1])
+    if install:
+        gq_set_dispatch_profile(kind, N, K, out["M"], out["gemv_us"], out["tc_us"])
+    return out

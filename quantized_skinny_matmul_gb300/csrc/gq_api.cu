@@ -5,7 +5,9 @@
 #include <cstdio>
 #include <cstring>
 #include <algorithm>
+#include <cmath>
 #include <mutex>
+#include <vector>
 
 #include "gq_common.cuh"
 #include "gq_internal.h"
@@ -244,13 +246,81 @@ static gq_status check_path(gq_path path) {
     return GQ_OK;
 }
 
-// Which family serves M rows: Smallem, "La courbe, une première fois" (the
-// narrow kernel up to 16 rows, tiles above); llama.cpp PR #1632, "Introduction"
-// (the M >= 32 rule and how sensitive the choice is around it).
-static gq_path resolve(gq_path path, int64_t M) {
-    if (path != GQ_PATH_AUTO) return path;
+// Per-shape dispatch profiles: benched times of both kernel families at a few M
+// (llama.cpp PR #1632, "Solutions", item 4: match the shape by N and K, estimate
+// the time of every profile for the given M by interpolating between the benched
+// M -- the M-time curve is close to linear -- and take the fastest).
+namespace {
+struct Profile {
+    int kind;
+    int64_t N, K;
+    std::vector<int64_t> Ms;
+    std::vector<double> t_gemv, t_tc;
+};
+std::mutex g_prof_mutex;
+std::vector<Profile> g_profiles;
+
+// Linear through the two benched points around M (the two end points outside the range).
+double interpolate(const std::vector<int64_t> &Ms, const std::vector<double> &t, int64_t M) {
+    const size_t n = Ms.size();
+    if (n == 1) return t[0];
+    size_t i = 0;
+    while (i + 2 < n && Ms[i + 1] <= M) i++;
+    return t[i] + (t[i + 1] - t[i]) * (double)(M - Ms[i]) / (double)(Ms[i + 1] - Ms[i]);
+}
+}  // namespace
+
+// Which family serves M rows: a benched profile of the shape when there is one, else
+// the M threshold (Smallem, "La courbe, une première fois": the narrow kernel up to 16
+// rows, tiles above; llama.cpp PR #1632, "Introduction": the M >= 32 rule and how
+// sensitive the choice is around it).
+static gq_path choose_path(int kind, int64_t N, int64_t K, int64_t M) {
+    {
+        std::lock_guard<std::mutex> lock(g_prof_mutex);
+        for (const Profile &pr : g_profiles)
+            if (pr.kind == kind && pr.N == N && pr.K == K)
+                return interpolate(pr.Ms, pr.t_tc, M) < interpolate(pr.Ms, pr.t_gemv, M) ? GQ_PATH_TC : GQ_PATH_GEMV;
+    }
     return M <= g_m_threshold.load() ? GQ_PATH_GEMV : GQ_PATH_TC;
 }
+
+static gq_path resolve(gq_path path, int kind, int64_t M, int64_t N, int64_t K) {
+    if (path != GQ_PATH_AUTO) return path;
+    return choose_path(kind, N, K, M);
+}
+
+gq_status gq_set_dispatch_profile(int kind, int64_t N, int64_t K, const int64_t *Ms, const double *t_gemv,
+                                  const double *t_tc, int64_t count) {
+    if (kind != GQ_KIND_Q4_0 && kind != GQ_KIND_F16) return fail(GQ_ERR_INVALID_ARG, "unknown weight kind %d", kind);
+    if (N <= 0 || K <= 0 || K % QK) return fail(GQ_ERR_INVALID_ARG, "N and K must be positive, K a multiple of 32");
+    if (count < 1 || !Ms || !t_gemv || !t_tc) return fail(GQ_ERR_INVALID_ARG, "a profile needs at least one point");
+    Profile pr{kind, N, K, {}, {}, {}};
+    for (int64_t i = 0; i < count; i++) {
+        if (Ms[i] <= 0 || (i > 0 && Ms[i] <= Ms[i - 1]))
+            return fail(GQ_ERR_INVALID_ARG, "the M of a profile must be positive and increasing");
+        if (!std::isfinite(t_gemv[i]) || !std::isfinite(t_tc[i]) || t_gemv[i] < 0 || t_tc[i] < 0)
+            return fail(GQ_ERR_INVALID_ARG, "profile times must be finite and non-negative");
+        pr.Ms.push_back(Ms[i]);
+        pr.t_gemv.push_back(t_gemv[i]);
+        pr.t_tc.push_back(t_tc[i]);
+    }
+    std::lock_guard<std::mutex> lock(g_prof_mutex);
+    for (Profile &old : g_profiles)
+        if (old.kind == kind && old.N == N && old.K == K) {
+            old = pr;
+            return ok();
+        }
+    g_profiles.push_back(pr);
+    return ok();
+}
+
+gq_status gq_clear_dispatch_profiles(void) {
+    std::lock_guard<std::mutex> lock(g_prof_mutex);
+    g_profiles.clear();
+    return ok();
+}
+
+gq_path gq_choose_path(int kind, int64_t N, int64_t K, int64_t M) { return choose_path(kind, N, K, M); }
 
 gq_status gq_mul_mat_q4_0_f32_path(const void *q4_repacked, const float *src1, float *dst, int64_t M, int64_t N,
                                    int64_t K, gq_path path, cudaStream_t stream) {
@@ -260,7 +330,7 @@ gq_status gq_mul_mat_q4_0_f32_path(const void *q4_repacked, const float *src1, f
     GQ_TRY(check_ptr(src1, "src1"));
     GQ_TRY(check_ptr(dst, "dst"));
     GQ_TRY(check_device());
-    if (resolve(path, M) == GQ_PATH_TC)
+    if (resolve(path, GQ_KIND_Q4_0, M, N, K) == GQ_PATH_TC)
         GQ_TRY(launch_tc_q4_0(q4_repacked, src1, dst, M, N, K, stream));
     else
         GQ_TRY(launch_gemv_q4_0(q4_repacked, src1, dst, M, N, K, stream));
@@ -275,7 +345,7 @@ gq_status gq_mul_mat_f16_f32_path(const void *src0_f16, const float *src1, float
     GQ_TRY(check_ptr(src1, "src1"));
     GQ_TRY(check_ptr(dst, "dst"));
     GQ_TRY(check_device());
-    if (resolve(path, M) == GQ_PATH_TC)
+    if (resolve(path, GQ_KIND_F16, M, N, K) == GQ_PATH_TC)
         GQ_TRY(launch_tc_f16(src0_f16, src1, dst, M, N, K, stream));
     else
         GQ_TRY(launch_gemv_f16(src0_f16, src1, dst, M, N, K, stream));
@@ -300,7 +370,7 @@ gq_status gq_mul_mat_q4_0_f32_host(const void *q4_repacked, const float *src1_ho
     GQ_TRY(get_staging(stream, xs + ob, &stage));
     float *dx = reinterpret_cast<float *>(stage), *dd = reinterpret_cast<float *>(stage + xs);
     GQ_TRY(check_cuda(cudaMemcpyAsync(dx, src1_host, xb, cudaMemcpyHostToDevice, stream), "src1 copy to the device"));
-    if (resolve(GQ_PATH_AUTO, M) == GQ_PATH_TC)
+    if (resolve(GQ_PATH_AUTO, GQ_KIND_Q4_0, M, N, K) == GQ_PATH_TC)
         GQ_TRY(launch_tc_q4_0(q4_repacked, dx, dd, M, N, K, stream));
     else
         GQ_TRY(launch_gemv_q4_0(q4_repacked, dx, dd, M, N, K, stream));

@@ -121,3 +121,33 @@ def test_binding_raises(lib):
     with pytest.raises(gq.GQError) as e:
         gq.gq_mul_mat_q4_0_f32(FAKE, FAKE, FAKE, 1, 64, 48, stream=0)
     assert e.value.status == gq.GQ_ERR_INVALID_ARG and "multiple of 32" in str(e.value)
+
+
+def test_dispatch_profiles(lib):
+    """A benched profile decides GQ_PATH_AUTO by linear interpolation in M (no GPU involved)."""
+    gq.gq_clear_dispatch_profiles()
+    # GEMV 10, 20, 40 and tiles 25, 22, 30 at M = 16, 32, 64
+    gq.gq_set_dispatch_profile(gq.GQ_KIND_Q4_0, 64, 128, [16, 32, 64], [10, 20, 40], [25, 22, 30])
+    cases = {8: gq.GQ_PATH_GEMV,      # extrapolated: 5 vs 26.5
+             16: gq.GQ_PATH_GEMV, 24: gq.GQ_PATH_GEMV, 32: gq.GQ_PATH_GEMV,   # 20 vs 22 at 32
+             48: gq.GQ_PATH_TC,       # 30 vs 26
+             64: gq.GQ_PATH_TC, 128: gq.GQ_PATH_TC}   # extrapolated: 80 vs 46
+    for M, want in cases.items():
+        assert gq.gq_choose_path(gq.GQ_KIND_Q4_0, 64, 128, M) == want, M
+    # another kind or shape falls back to the M threshold
+    assert gq.gq_choose_path(gq.GQ_KIND_F16, 64, 128, 48) == gq.GQ_PATH_TC
+    assert gq.gq_choose_path(gq.GQ_KIND_Q4_0, 64, 256, 8) == gq.GQ_PATH_GEMV
+    assert gq.gq_choose_path(gq.GQ_KIND_Q4_0, 64, 256, 48) == gq.GQ_PATH_TC
+    # a new profile replaces the old one; one point is a constant curve
+    gq.gq_set_dispatch_profile(gq.GQ_KIND_Q4_0, 64, 128, [32], [1.0], [2.0])
+    assert gq.gq_choose_path(gq.GQ_KIND_Q4_0, 64, 128, 512) == gq.GQ_PATH_GEMV
+    with pytest.raises(gq.GQError):
+        gq.gq_set_dispatch_profile(gq.GQ_KIND_Q4_0, 64, 128, [32, 16], [1, 2], [1, 2])   # M not increasing
+    with pytest.raises(gq.GQError):
+        gq.gq_set_dispatch_profile(gq.GQ_KIND_Q4_0, 64, 100, [16], [1], [2])             # K % 32
+    with pytest.raises(gq.GQError):
+        gq.gq_set_dispatch_profile(7, 64, 128, [16], [1], [2])                           # kind
+    with pytest.raises(gq.GQError):
+        gq.gq_set_dispatch_profile(gq.GQ_KIND_Q4_0, 64, 128, [16], [float("nan")], [2])
+    gq.gq_clear_dispatch_profiles()
+    assert gq.gq_choose_path(gq.GQ_KIND_Q4_0, 64, 128, 48) == gq.GQ_PATH_TC

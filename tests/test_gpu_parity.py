@@ -247,3 +247,25 @@ def test_concatenated_rows_equal_separate_products():
         whole = host(gq.mul_mat_q4_0_f32(both, x, sum(Ns)))
         parts = [host(gq.mul_mat_q4_0_f32(r, x, N)) for r, N in zip(reps, Ns)]
         assert np.array_equal(whole, np.concatenate(parts, axis=1)), f"M={M}"
+
+
+def test_tuned_dispatch_profile(oracle):
+    """tune_dispatch benches both families on the device; GQ_PATH_AUTO then follows the
+    faster one at every benched M, and its products stay within the tolerance."""
+    N, K = 512, 1024
+    w, _ = synth.problem(80, 1, N, K)
+    rep = gq.repack_q4_0(gq.quantize_q4_0(dev(w)), N, K)
+    try:
+        prof = gq.tune_dispatch(rep, N, K, Ms=(1, 16, 32, 64), reps=5)
+        for M, tg, tt in zip(prof["M"], prof["gemv_us"], prof["tc_us"]):
+            assert tg > 0 and tt > 0
+            want = gq.GQ_PATH_TC if tt < tg else gq.GQ_PATH_GEMV
+            assert gq.gq_choose_path(gq.GQ_KIND_Q4_0, N, K, M) == want
+        q4_ref = oracle.quantize_q4_0(w)
+        for M in (24, 48):
+            _, x = synth.problem(81 + M, M, N, K)
+            dst = host(gq.mul_mat_q4_0_f32(rep, dev(x), N))
+            ref, T = oracle.mul_mat_q4_0_f32(q4_ref, x)
+            assert_within(dst, ref, T, what=f"auto M={M}")
+    finally:
+        gq.gq_clear_dispatch_profiles()
