@@ -10,14 +10,21 @@
 // One CTA computes a 128 (weight rows) x BN (activation rows) tile of
 // dst^T = W . X^T over all of K with tcgen05.mma kind::f16 and an f32
 // accumulator in tensor memory:
-//   warp 0      producer: bulk copies of the repacked Q4_0 tiles (or TMA loads
-//               of the F16 weights) and TMA loads of the fp16 activations;
+//   warp 0      weight producer: one 2D TMA load per 128-column step of the
+//               eight repacked Q4_0 tiles of the CTA's rows (or two TMA loads
+//               of the F16 weights straight into the MMA's operand ring);
+//   warp 10     activation producer: TMA loads of the fp16 activations;
 //   warp 1      allocates tensor memory; one thread issues the MMAs and commits
-//               them to mbarriers;
-//   warps 2..5  (Q4_0) de-quantize each 128 x 128 weight tile into fp16,
+//               them to the mbarriers that free the operand stages;
+//   warps 2..9  (Q4_0) de-quantize each 128 x 128 weight tile into fp16,
 //               (q - 8) * d rounded once, in the 128-byte-swizzled K-major
-//               layout the MMA reads; then all four read the accumulator back
-//               (tcgen05.ld) and store dst.
+//               layout the MMA reads (each warp 32 rows x 64 columns); then
+//               they read the accumulators back (tcgen05.ld) and store dst.
+// Each ring has its own producer, so the weight stream from device memory runs
+// as many stages ahead as its ring holds, whatever the MMA and activation rings
+// are waiting for.  The MMAs of a stage rotate over 2 (BN = 128) or 4
+// independent accumulators in tensor memory, so consecutive MMAs do not wait
+// for each other's results; the epilogue adds them in a fixed order.
 // The activations are quantized first by a small kernel into a workspace copy
 // B[m][k] = fp16(q8 * d8) (Q4_0), or rounded to fp16 (F16): the same Q8_0
 // values as the GEMV path, each rounded once to fp16, so the result is within
@@ -38,24 +45,35 @@ constexpr int BM = 128;                          // weight rows per CTA = MMA M 
 constexpr int BK = 128;                          // K per pipeline stage (one repacked tile column)
 constexpr int ATOM_BYTES = BM * 128;             // one 128-row x 64-half swizzle atom: 16 KB
 constexpr int A_STAGE = BM * BK * 2;             // 32 KB
-constexpr int RAW_STAGE = 8 * TILE_BYTES;        // 8 row groups of 16 rows x one tile
-constexpr int STAGES = 2;
-constexpr int RAW_STAGES = 4;
-constexpr int THREADS = 192;
-constexpr int CONVERTERS = 128;
+constexpr int RAW_ROWGROUPS = BM / 16;           // repacked row groups of a CTA
+constexpr int RAW_STAGE = RAW_ROWGROUPS * TILE_BYTES;   // 8 row groups of 16 rows x one tile
+constexpr int RAW_WORDS = TILE_BYTES / 8;        // a repacked tile in 8-byte TMA elements
+constexpr int CONVERTER_WARPS = 8;               // warps 2 .. 9
+constexpr int ACT_PRODUCER_WARP = 2 + CONVERTER_WARPS;
+constexpr int THREADS = (ACT_PRODUCER_WARP + 1) * 32;
+constexpr int MAX_SA = 4, MAX_SB = 4, MAX_RAW = 4;
 
-template <int BN>
+// Ring depths and the shared-memory map (offsets from a 1024-aligned base).
+// Q4_0: A holds the converted fp16 weights, RAW the repacked bytes as loaded;
+// F16: the weights go straight into A.  Depths fill the 227 KB of an SM.
+template <int BN, bool QUANT>
 struct TcLayout {
+    static constexpr int SA = BN == 128 ? 3 : 4;
+    static constexpr int SB = BN == 32 ? 4 : 3;
+    static constexpr int RAW = QUANT ? (BN == 128 ? 3 : 4) : 0;
+    static constexpr int NACC = BN == 128 ? 2 : 4;          // accumulators in tensor memory
+    static constexpr uint32_t TMEM_COLS = NACC * BN;         // 128 or 256: a power of two >= 32
     static constexpr int B_STAGE = BN * BK * 2;
     static constexpr int a = 0;
-    static constexpr int b = a + STAGES * A_STAGE;
-    static constexpr int raw = b + STAGES * B_STAGE;
-    static constexpr int bars = raw + RAW_STAGES * RAW_STAGE;
+    static constexpr int b = a + SA * A_STAGE;
+    static constexpr int raw = b + SB * B_STAGE;
+    static constexpr int bars = raw + RAW * RAW_STAGE;
     static constexpr int total = bars + 256;     // from a 1024-aligned base
+    static_assert(SA <= MAX_SA && SB <= MAX_SB && RAW <= MAX_RAW, "barrier table too small");
+    static_assert(total + 1024 <= 227 * 1024, "shared memory");
 };
 
 struct TcParams {
-    const uint8_t *w;        // Q4_0: repacked weights
     float *dst;
     unsigned int *status;
     int M, N, K;
@@ -65,13 +83,15 @@ struct TcParams {
 // barrier indices
 enum : int {
     RAW_FULL = 0,
-    RAW_EMPTY = RAW_FULL + RAW_STAGES,
-    B_FULL = RAW_EMPTY + RAW_STAGES,
-    A_FULL = B_FULL + STAGES,
-    AB_EMPTY = A_FULL + STAGES,
-    ACC_FULL = AB_EMPTY + STAGES,
+    RAW_EMPTY = RAW_FULL + MAX_RAW,
+    B_FULL = RAW_EMPTY + MAX_RAW,
+    B_EMPTY = B_FULL + MAX_SB,
+    A_FULL = B_EMPTY + MAX_SB,
+    A_EMPTY = A_FULL + MAX_SA,
+    ACC_FULL = A_EMPTY + MAX_SA,
     NUM_BARS = ACC_FULL + 1
 };
+static_assert(NUM_BARS * 8 + 4 <= 256, "barrier area");
 
 // ---------------------------------------------------------------------------
 // tcgen05 / TMA wrappers
@@ -169,7 +189,8 @@ template <int BN, bool QUANT>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_a,
                    const TcParams p) {
-    using L = TcLayout<BN>;
+    using L = TcLayout<BN, QUANT>;
+    constexpr int SA = L::SA, SB = L::SB, RAW = QUANT ? L::RAW : 1;   // RAW: ring of the Q4_0 path only
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
@@ -180,22 +201,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto bar = [&](int i) { return smem_addr(bars + i); };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < RAW_STAGES; i++) {
+        for (int i = 0; i < L::RAW; i++) {
             mbar_init(bar(RAW_FULL + i), 1);
-            mbar_init(bar(RAW_EMPTY + i), CONVERTERS / 32);
+            mbar_init(bar(RAW_EMPTY + i), CONVERTER_WARPS);
         }
-        for (int i = 0; i < STAGES; i++) {
+        for (int i = 0; i < SB; i++) {
             mbar_init(bar(B_FULL + i), 1);
-            mbar_init(bar(A_FULL + i), QUANT ? CONVERTERS / 32 : 1);
-            mbar_init(bar(AB_EMPTY + i), 1);
+            mbar_init(bar(B_EMPTY + i), 1);
+        }
+        for (int i = 0; i < SA; i++) {
+            mbar_init(bar(A_FULL + i), QUANT ? CONVERTER_WARPS : 1);
+            mbar_init(bar(A_EMPTY + i), 1);
         }
         mbar_init(bar(ACC_FULL), 1);
     }
     fence_barrier_init();
-    if (warp == 1) {   // tensor memory: BN f32 columns x 128 lanes
-        constexpr uint32_t cols = BN < 32 ? 32 : BN;
+    if (warp == 1) {   // tensor memory: NACC accumulators of BN f32 columns x 128 lanes
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                     "r"(cols)
+                     "r"(L::TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -208,35 +231,40 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool failed = false;
 
     if (warp == 0) {
-        // ---------------------------------------------------------- producer
+        // ---------------------------------------------------------- weight producer
         if (lane == 0) {
             for (int kt = 0; kt < NT && !failed; kt++) {
                 if (QUANT) {
-                    const int rs = kt % RAW_STAGES;
-                    if (kt >= RAW_STAGES) wait_or_fail(bar(RAW_EMPTY + rs), (uint32_t)((kt / RAW_STAGES - 1) & 1),
-                                                       failed, p.status);
+                    // the eight row groups' tiles of column step kt: one box of 8 x 1152 bytes
+                    // (row groups past the matrix are filled with zeros: weight 0 after conversion)
+                    const int rs = kt % RAW;
+                    if (kt >= RAW) wait_or_fail(bar(RAW_EMPTY + rs), (uint32_t)((kt / RAW - 1) & 1), failed, p.status);
                     if (failed) break;
-                    const int g0 = n0 / 16;
-                    const int ng = min(8, p.N16 - g0);
-                    mbar_arrive_expect_tx(bar(RAW_FULL + rs), (uint32_t)(ng * TILE_BYTES));
-                    for (int gi = 0; gi < ng; gi++)
-                        bulk_g2s(smem_addr(smem + L::raw + rs * RAW_STAGE + gi * TILE_BYTES),
-                                 p.w + ((size_t)(g0 + gi) * NT + kt) * TILE_BYTES, TILE_BYTES, bar(RAW_FULL + rs));
+                    mbar_arrive_expect_tx(bar(RAW_FULL + rs), (uint32_t)RAW_STAGE);
+                    tma_load_2d(smem_addr(smem + L::raw + rs * RAW_STAGE), &map_a, kt * RAW_WORDS, n0 / 16,
+                                bar(RAW_FULL + rs));
+                } else {
+                    const int sa = kt % SA;
+                    if (kt >= SA) wait_or_fail(bar(A_EMPTY + sa), (uint32_t)((kt / SA - 1) & 1), failed, p.status);
+                    if (failed) break;
+                    mbar_arrive_expect_tx(bar(A_FULL + sa), (uint32_t)A_STAGE);
+                    tma_load_2d(smem_addr(smem + L::a + sa * A_STAGE), &map_a, kt * BK, n0, bar(A_FULL + sa));
+                    tma_load_2d(smem_addr(smem + L::a + sa * A_STAGE + ATOM_BYTES), &map_a, kt * BK + 64, n0,
+                                bar(A_FULL + sa));
                 }
-                const int s = kt % STAGES;
-                if (kt >= STAGES)
-                    wait_or_fail(bar(AB_EMPTY + s), (uint32_t)((kt / STAGES - 1) & 1), failed, p.status);
+            }
+        }
+    } else if (warp == ACT_PRODUCER_WARP) {
+        // ---------------------------------------------------------- activation producer
+        if (lane == 0) {
+            for (int kt = 0; kt < NT && !failed; kt++) {
+                const int sb = kt % SB;
+                if (kt >= SB) wait_or_fail(bar(B_EMPTY + sb), (uint32_t)((kt / SB - 1) & 1), failed, p.status);
                 if (failed) break;
-                mbar_arrive_expect_tx(bar(B_FULL + s), (uint32_t)L::B_STAGE);
-                tma_load_2d(smem_addr(smem + L::b + s * L::B_STAGE), &map_b, kt * BK, m0, bar(B_FULL + s));
-                tma_load_2d(smem_addr(smem + L::b + s * L::B_STAGE + BN * 128), &map_b, kt * BK + 64, m0,
-                            bar(B_FULL + s));
-                if (!QUANT) {
-                    mbar_arrive_expect_tx(bar(A_FULL + s), (uint32_t)A_STAGE);
-                    tma_load_2d(smem_addr(smem + L::a + s * A_STAGE), &map_a, kt * BK, n0, bar(A_FULL + s));
-                    tma_load_2d(smem_addr(smem + L::a + s * A_STAGE + ATOM_BYTES), &map_a, kt * BK + 64, n0,
-                                bar(A_FULL + s));
-                }
+                mbar_arrive_expect_tx(bar(B_FULL + sb), (uint32_t)L::B_STAGE);
+                tma_load_2d(smem_addr(smem + L::b + sb * L::B_STAGE), &map_b, kt * BK, m0, bar(B_FULL + sb));
+                tma_load_2d(smem_addr(smem + L::b + sb * L::B_STAGE + BN * 128), &map_b, kt * BK + 64, m0,
+                            bar(B_FULL + sb));
             }
         }
     } else if (warp == 1) {
@@ -244,46 +272,52 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = f16_idesc(BM, BN);
             for (int kt = 0; kt < NT && !failed; kt++) {
-                const int s = kt % STAGES;
-                const uint32_t par = (uint32_t)((kt / STAGES) & 1);
-                wait_or_fail(bar(A_FULL + s), par, failed, p.status);
-                wait_or_fail(bar(B_FULL + s), par, failed, p.status);
+                const int sa = kt % SA, sb = kt % SB;
+                wait_or_fail(bar(A_FULL + sa), (uint32_t)((kt / SA) & 1), failed, p.status);
+                wait_or_fail(bar(B_FULL + sb), (uint32_t)((kt / SB) & 1), failed, p.status);
                 if (failed) break;
                 tc_fence_after();
-                const uint32_t a_base = smem_addr(smem + L::a + s * A_STAGE);
-                const uint32_t b_base = smem_addr(smem + L::b + s * L::B_STAGE);
+                const uint32_t a_base = smem_addr(smem + L::a + sa * A_STAGE);
+                const uint32_t b_base = smem_addr(smem + L::b + sb * L::B_STAGE);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; kk++) {
                     const uint32_t koff = (uint32_t)((kk & 3) * 32);
                     const uint64_t ad = sw128_desc(a_base + (kk >> 2) * ATOM_BYTES + koff);
                     const uint64_t bd = sw128_desc(b_base + (kk >> 2) * (BN * 128) + koff);
-                    mma_f16(tmem, ad, bd, idesc, (kt | kk) != 0 ? 1u : 0u);
+                    // accumulator kk % NACC; its first MMA overwrites it
+                    mma_f16(tmem + (uint32_t)((kk % L::NACC) * BN), ad, bd, idesc,
+                            (kt > 0 || kk >= L::NACC) ? 1u : 0u);
                 }
-                mma_commit(bar(AB_EMPTY + s));   // stage s may be refilled once these MMAs completed
+                // the stages may be refilled once these MMAs completed
+                mma_commit(bar(A_EMPTY + sa));
+                mma_commit(bar(B_EMPTY + sb));
             }
             if (!failed) mma_commit(bar(ACC_FULL));
         }
     } else {
         // ---------------------------------------------------------- converters, then epilogue
-        const int t = threadIdx.x - 64;            // weight row of the tile, 0..127
+        // warp 2 + 4h + i converts rows 32i .. 32i + 31, columns 64h .. 64h + 63 of each stage
+        const int ct = threadIdx.x - 64;
+        const int t = ct & (BM - 1), h = ct >> 7;   // weight row of the tile 0..127, column half
         if (QUANT) {
             const int gi = t >> 4, rr = t & 15;
             const bool row_ok = n0 + t < p.N;
             for (int kt = 0; kt < NT; kt++) {
-                const int rs = kt % RAW_STAGES, s = kt % STAGES;
-                wait_or_fail(bar(RAW_FULL + rs), (uint32_t)((kt / RAW_STAGES) & 1), failed, p.status);
-                if (kt >= STAGES) wait_or_fail(bar(AB_EMPTY + s), (uint32_t)((kt / STAGES - 1) & 1), failed, p.status);
+                const int rs = kt % RAW, sa = kt % SA;
+                wait_or_fail(bar(RAW_FULL + rs), (uint32_t)((kt / RAW) & 1), failed, p.status);
+                if (kt >= SA) wait_or_fail(bar(A_EMPTY + sa), (uint32_t)((kt / SA - 1) & 1), failed, p.status);
                 if (!failed) {
                     const uint8_t *tile = smem + L::raw + rs * RAW_STAGE + gi * TILE_BYTES;
-                    uint8_t *a_stage = smem + L::a + s * A_STAGE;
-                    const uint2 sw = row_ok ? *reinterpret_cast<const uint2 *>(tile + TILE_SCALE_OFFSET + rr * 8)
-                                            : make_uint2(0u, 0u);
+                    uint8_t *a_stage = smem + L::a + sa * A_STAGE;
+                    // scales of blocks 2h and 2h + 1 of row rr
+                    const uint32_t dw =
+                        row_ok ? *reinterpret_cast<const uint32_t *>(tile + TILE_SCALE_OFFSET + rr * 8 + h * 4) : 0u;
 #pragma unroll
-                    for (int j = 0; j < 4; j++) {
+                    for (int jj = 0; jj < 2; jj++) {
+                        const int j = 2 * h + jj;
                         const uint4 w = row_ok ? lds128(tile + (j * 16 + rr) * 16) : make_uint4(0x88888888u, 0x88888888u,
                                                                                               0x88888888u, 0x88888888u);
-                        const uint32_t dw = (j & 2) ? sw.y : sw.x;
-                        const __half d = __ushort_as_half((unsigned short)((j & 1) ? (dw >> 16) : (dw & 0xffffu)));
+                        const __half d = __ushort_as_half((unsigned short)(jj ? (dw >> 16) : (dw & 0xffffu)));
                         const __half2 d2 = __halves2half2(d, d);
                         // chunk u of 8 values: u=0 low nibbles of bytes 0..7, u=1 bytes 8..15, u=2,3 high nibbles
 #pragma unroll
@@ -300,20 +334,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive_plain(bar(RAW_EMPTY + rs));
-                    mbar_arrive_plain(bar(A_FULL + s));
+                    mbar_arrive_plain(bar(A_FULL + sa));
                 }
             }
         }
-        // epilogue: this warp reads tensor-memory lanes 32 * (warp % 4) .. + 31
+        // epilogue: this warp reads tensor-memory lanes 32 * (warp % 4) .. + 31, column
+        // chunks h, h + 2, ... of 32, and adds the accumulators in order
         wait_or_fail(bar(ACC_FULL), 0u, failed, p.status);
         tc_fence_after();
         const int q = warp & 3;
         const int row = n0 + 32 * q + lane;
         if (!failed) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = 32 * h; c0 < BN; c0 += 64) {
                 float v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+#pragma unroll 1
+                for (int a = 1; a < L::NACC; a++) {
+                    float u[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * BN + c0), u);
+#pragma unroll
+                    for (int i = 0; i < 32; i++) v[i] += u[i];
+                }
                 if (row < p.N) {
 #pragma unroll
                     for (int i = 0; i < 32; i++) {
@@ -329,8 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        constexpr uint32_t cols = BN < 32 ? 32 : BN;
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(L::TMEM_COLS) : "memory");
     }
 }
 
@@ -400,6 +441,24 @@ gq_status f16_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K, i
     return GQ_OK;
 }
 
+// Repacked Q4_0 weights as a 2D tensor of row groups: row g holds the NT tiles of
+// row group g (NT * 1152 bytes), read as 8-byte elements; a box is one tile
+// column of 8 row groups.  Row groups past the matrix read as zeros.
+gq_status q4_raw_map(CUtensorMap *map, const void *base, int64_t N16, int64_t NT) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    gq_status st = encoder(&enc);
+    if (st != GQ_OK) return st;
+    const cuuint64_t dims[2] = {(cuuint64_t)(NT * RAW_WORDS), (cuuint64_t)N16};
+    const cuuint64_t strides[1] = {(cuuint64_t)(NT * TILE_BYTES)};
+    const cuuint32_t box[2] = {(cuuint32_t)RAW_WORDS, (cuuint32_t)RAW_ROWGROUPS};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GQ_ERR_CUDA, "cuTensorMapEncodeTiled (repacked weights) failed (%d)", (int)r);
+    return GQ_OK;
+}
+
 constexpr int MAX_DEV = 64;
 std::atomic<bool> g_tc_smem_set[MAX_DEV][6];
 
@@ -417,7 +476,7 @@ gq_status allow_tc_smem(Kernel kernel, int which, int bytes) {
 
 template <int BN, bool QUANT>
 gq_status launch_tc(const CUtensorMap &mb, const CUtensorMap &ma, const TcParams &p, cudaStream_t s, int which) {
-    constexpr int smem = TcLayout<BN>::total + 1024;
+    constexpr int smem = TcLayout<BN, QUANT>::total + 1024;
     auto kernel = tc_gemm_kernel<BN, QUANT>;
     gq_status st = allow_tc_smem(kernel, which, smem);
     if (st != GQ_OK) return st;
@@ -447,7 +506,6 @@ gq_status launch_tc_common(bool quant, const void *w, const float *x, float *dst
     p.NT = (int)((K + BK - 1) / BK);
     p.N16 = (int)((N + 15) / 16);
     p.dst = dst;
-    p.w = (const uint8_t *)w;
 
     Workspace ws;
     gq_status st = get_workspace(s, 0, tc_workspace_bytes(M, K), &ws);
@@ -476,10 +534,8 @@ gq_status launch_tc_common(bool quant, const void *w, const float *x, float *dst
     memset(&ma, 0, sizeof(ma));
     st = f16_map(&mb, b, M, K, bn);
     if (st != GQ_OK) return st;
-    if (!quant) {
-        st = f16_map(&ma, w, N, K, BM);
-        if (st != GQ_OK) return st;
-    }
+    st = quant ? q4_raw_map(&ma, w, p.N16, p.NT) : f16_map(&ma, w, N, K, BM);
+    if (st != GQ_OK) return st;
     if (quant) {
         if (bn == 32) return launch_tc<32, true>(mb, ma, p, s, 0);
         if (bn == 64) return launch_tc<64, true>(mb, ma, p, s, 1);
