@@ -7,7 +7,7 @@
 // converting operands to bf16 cost more than the tensor cores saved there,
 // which is why the conversion happens in shared memory on the way in).
 //
-// One CTA computes a 128 (weight rows) x BN (activation rows) tile of
+// One CTA computes a 128 (weight rows) x BN (activation rows, 32 .. 256) tile of
 // dst^T = W . X^T over all of K with tcgen05.mma kind::f16 and an f32
 // accumulator in tensor memory:
 //   warp 0      weight producer: one 2D TMA load per 128-column step of the
@@ -58,11 +58,11 @@ constexpr int MAX_SA = 4, MAX_SB = 4, MAX_RAW = 4;
 // F16: the weights go straight into A.  Depths fill the 227 KB of an SM.
 template <int BN, bool QUANT>
 struct TcLayout {
-    static constexpr int SA = BN == 128 ? 3 : 4;
-    static constexpr int SB = BN == 32 ? 4 : 3;
-    static constexpr int RAW = QUANT ? (BN == 128 ? 3 : 4) : 0;
-    static constexpr int NACC = BN == 128 ? 2 : 4;          // accumulators in tensor memory
-    static constexpr uint32_t TMEM_COLS = NACC * BN;         // 128 or 256: a power of two >= 32
+    static constexpr int SA = BN == 256 ? 2 : BN == 128 ? 3 : 4;
+    static constexpr int SB = BN == 256 ? 2 : BN == 32 ? 4 : 3;
+    static constexpr int RAW = QUANT ? (BN >= 128 ? 3 : 4) : 0;
+    static constexpr int NACC = BN >= 128 ? 2 : 4;          // accumulators in tensor memory
+    static constexpr uint32_t TMEM_COLS = NACC * BN;         // 128, 256 or 512: a power of two >= 32
     static constexpr int B_STAGE = BN * BK * 2;
     static constexpr int a = 0;
     static constexpr int b = a + SA * A_STAGE;
@@ -460,7 +460,7 @@ gq_status q4_raw_map(CUtensorMap *map, const void *base, int64_t N16, int64_t NT
 }
 
 constexpr int MAX_DEV = 64;
-std::atomic<bool> g_tc_smem_set[MAX_DEV][6];
+std::atomic<bool> g_tc_smem_set[MAX_DEV][8];
 
 template <typename Kernel>
 gq_status allow_tc_smem(Kernel kernel, int which, int bytes) {
@@ -493,7 +493,17 @@ gq_status launch_tc(const CUtensorMap &mb, const CUtensorMap &ma, const TcParams
     return check_cuda(cudaLaunchKernelEx(&cfg, kernel, mb, ma, p), "tc_gemm launch");
 }
 
-int tile_n(int64_t M) { return M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+// Activation rows per tile, the MMA's N.  Each tcgen05.mma costs about the same
+// time up to N = 256 on this GPU, so 256-wide tiles do twice the work per
+// instruction; they are taken when 128-wide tiles would need more than one wave
+// of CTAs, where the halved grid still fills the SMs.
+int tile_n(int64_t M, int64_t N) {
+    if (M <= 32) return 32;
+    if (M <= 64) return 64;
+    if (M <= 128) return 128;
+    const int64_t grid128 = ((M + 127) / 128) * ((N + BM - 1) / BM);
+    return grid128 > sm_count() ? 256 : 128;
+}
 
 gq_status launch_tc_common(bool quant, const void *w, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
                            cudaStream_t s) {
@@ -529,7 +539,7 @@ gq_status launch_tc_common(bool quant, const void *w, const float *x, float *dst
         st = check_cuda(cudaLaunchKernelEx(&cfg, act_f16_kernel, x, b, n), "activation pre-pass");
     if (st != GQ_OK) return st;
 
-    const int bn = tile_n(M);
+    const int bn = tile_n(M, N);
     CUtensorMap mb, ma;
     memset(&ma, 0, sizeof(ma));
     st = f16_map(&mb, b, M, K, bn);
@@ -539,11 +549,13 @@ gq_status launch_tc_common(bool quant, const void *w, const float *x, float *dst
     if (quant) {
         if (bn == 32) return launch_tc<32, true>(mb, ma, p, s, 0);
         if (bn == 64) return launch_tc<64, true>(mb, ma, p, s, 1);
-        return launch_tc<128, true>(mb, ma, p, s, 2);
+        if (bn == 128) return launch_tc<128, true>(mb, ma, p, s, 2);
+        return launch_tc<256, true>(mb, ma, p, s, 3);
     }
-    if (bn == 32) return launch_tc<32, false>(mb, ma, p, s, 3);
-    if (bn == 64) return launch_tc<64, false>(mb, ma, p, s, 4);
-    return launch_tc<128, false>(mb, ma, p, s, 5);
+    if (bn == 32) return launch_tc<32, false>(mb, ma, p, s, 4);
+    if (bn == 64) return launch_tc<64, false>(mb, ma, p, s, 5);
+    if (bn == 128) return launch_tc<128, false>(mb, ma, p, s, 6);
+    return launch_tc<256, false>(mb, ma, p, s, 7);
 }
 
 }  // namespace

@@ -2,7 +2,7 @@
 
 The tile kernels round each de-quantized operand once to fp16 and accumulate in
 f32, so every output must be within 2e-3 of T = sum_k |term_k|.  Shapes cover
-ragged N (row tiles of 128), ragged M (activation tiles of 32/64/128), K not a
+ragged N (row tiles of 128), ragged M (activation tiles of 32/64/128/256), K not a
 multiple of the 128-column stage, and the full-size prefill matrices (sampled).
 """
 import numpy as np
@@ -64,9 +64,11 @@ def test_tc_f16(oracle, M, N, K, seed):
     assert_within(dst, ref, T, "f16 tc")
 
 
-@pytest.mark.parametrize("M,N,K", [(64, 11008, 4096), (128, 11008, 4096), (512, 4096, 4096), (128, 4096, 11008)])
+@pytest.mark.parametrize("M,N,K", [(64, 11008, 4096), (128, 11008, 4096), (512, 4096, 4096), (128, 4096, 11008),
+                                   (256, 11008, 4096)])
 def test_tc_full_size_sampled(oracle, M, N, K):
-    """The prefill shapes, outliers included, in the configuration the benchmark times (auto dispatch)."""
+    """The prefill shapes, outliers included, in the configuration the benchmark times (auto dispatch);
+    M = 256 on 11008 rows takes the 256-wide activation tile."""
     w, x = synth.problem(400 + M, M, N, K, outliers=True)
     rep = gq.repack_q4_0(gq.quantize_q4_0(dev(w)), N, K)
     dst = host(gq.mul_mat_q4_0_f32(rep, dev(x), N))
