@@ -269,14 +269,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = f16_idesc(BM, BN);
-            for (int kt = 0; kt < NT && !failed; kt++) {
-                const int sa = kt % SA, sb = kt % SB;
-                wait_or_fail(bar(A_FULL + sa), (uint32_t)((kt / SA) & 1), failed, p.status);
-                wait_or_fail(bar(B_FULL + sb), (uint32_t)((kt / SB) & 1), failed, p.status);
-                if (failed) break;
-                tc_fence_after();
+        // The whole warp runs the loop and waits; lane 0 issues the MMAs and commits.
+        constexpr uint32_t idesc = f16_idesc(BM, BN);
+        for (int kt = 0; kt < NT; kt++) {
+            const int sa = kt % SA, sb = kt % SB;
+            wait_or_fail(bar(A_FULL + sa), (uint32_t)((kt / SA) & 1), failed, p.status);
+            wait_or_fail(bar(B_FULL + sb), (uint32_t)((kt / SB) & 1), failed, p.status);
+            if (__any_sync(0xffffffffu, failed)) {
+                failed = true;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
                 const uint32_t a_base = smem_addr(smem + L::a + sa * A_STAGE);
                 const uint32_t b_base = smem_addr(smem + L::b + sb * L::B_STAGE);
 #pragma unroll
@@ -292,8 +296,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mma_commit(bar(A_EMPTY + sa));
                 mma_commit(bar(B_EMPTY + sb));
             }
-            if (!failed) mma_commit(bar(ACC_FULL));
+            __syncwarp();
         }
+        if (lane == 0 && !failed) mma_commit(bar(ACC_FULL));
     } else {
         // ---------------------------------------------------------- converters, then epilogue
         // warp 2 + 4h + i converts rows 32i .. 32i + 31, columns 64h .. 64h + 63 of each stage
