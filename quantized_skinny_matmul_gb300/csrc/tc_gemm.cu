@@ -15,7 +15,9 @@
 //               of the F16 weights straight into the MMA's operand ring);
 //   warp 10     activation producer: TMA loads of the fp16 activations;
 //   warp 1      allocates tensor memory; one thread issues the MMAs and commits
-//               them to the mbarriers that free the operand stages;
+//               them to the mbarrier that frees the operand stage (one wait and
+//               one commit per step: each mbarrier operation of this thread
+//               measurably delays the next MMAs);
 //   warps 2..9  (Q4_0) de-quantize each 128 x 128 weight tile into fp16,
 //               (q - 8) * d rounded once, in the 128-byte-swizzled K-major
 //               layout the MMA reads (each warp 32 rows x 64 columns); then
@@ -51,25 +53,25 @@ constexpr int RAW_WORDS = TILE_BYTES / 8;        // a repacked tile in 8-byte TM
 constexpr int CONVERTER_WARPS = 8;               // warps 2 .. 9
 constexpr int ACT_PRODUCER_WARP = 2 + CONVERTER_WARPS;
 constexpr int THREADS = (ACT_PRODUCER_WARP + 1) * 32;
-constexpr int MAX_SA = 4, MAX_SB = 4, MAX_RAW = 4;
+constexpr int MAX_STAGES = 4, MAX_RAW = 4;
 
 // Ring depths and the shared-memory map (offsets from a 1024-aligned base).
-// Q4_0: A holds the converted fp16 weights, RAW the repacked bytes as loaded;
-// F16: the weights go straight into A.  Depths fill the 227 KB of an SM.
+// A stage holds the operands of one MMA step: the fp16 weight tile (Q4_0:
+// converted from the RAW ring, which holds the repacked bytes as loaded; F16:
+// loaded as is) and the activation tile.  Depths fill the 227 KB of an SM.
 template <int BN, bool QUANT>
 struct TcLayout {
-    static constexpr int SA = BN == 256 ? 2 : BN == 128 ? 3 : 4;
-    static constexpr int SB = BN == 256 ? 2 : BN == 32 ? 4 : 3;
-    static constexpr int RAW = QUANT ? (BN >= 128 ? 3 : 4) : 0;
+    static constexpr int ST = BN == 256 ? 2 : BN == 128 ? 3 : 4;
+    static constexpr int RAW = QUANT ? (BN >= 64 ? 3 : 4) : 0;
     static constexpr int NACC = BN >= 128 ? 2 : 4;          // accumulators in tensor memory
     static constexpr uint32_t TMEM_COLS = NACC * BN;         // 128, 256 or 512: a power of two >= 32
     static constexpr int B_STAGE = BN * BK * 2;
     static constexpr int a = 0;
-    static constexpr int b = a + SA * A_STAGE;
-    static constexpr int raw = b + SB * B_STAGE;
+    static constexpr int b = a + ST * A_STAGE;
+    static constexpr int raw = b + ST * B_STAGE;
     static constexpr int bars = raw + RAW * RAW_STAGE;
     static constexpr int total = bars + 256;     // from a 1024-aligned base
-    static_assert(SA <= MAX_SA && SB <= MAX_SB && RAW <= MAX_RAW, "barrier table too small");
+    static_assert(ST <= MAX_STAGES && RAW <= MAX_RAW, "barrier table too small");
     static_assert(total + 1024 <= 227 * 1024, "shared memory");
 };
 
@@ -80,15 +82,17 @@ struct TcParams {
     int NT, N16;             // tiles of 128 columns, row groups of 16
 };
 
-// barrier indices
+// barrier indices.  FULL[s] completes when both operands of stage s are in place:
+// the activation producer's arrival with its TMA bytes, and the eight converter
+// warps' arrivals (Q4_0) or the weight producer's arrival with its TMA bytes (F16).
+// EMPTY[s] completes when the MMAs that read stage s have completed.  The MMA
+// thread thus handles one barrier wait and one commit per step.
 enum : int {
     RAW_FULL = 0,
     RAW_EMPTY = RAW_FULL + MAX_RAW,
-    B_FULL = RAW_EMPTY + MAX_RAW,
-    B_EMPTY = B_FULL + MAX_SB,
-    A_FULL = B_EMPTY + MAX_SB,
-    A_EMPTY = A_FULL + MAX_SA,
-    ACC_FULL = A_EMPTY + MAX_SA,
+    FULL = RAW_EMPTY + MAX_RAW,
+    EMPTY = FULL + MAX_STAGES,
+    ACC_FULL = EMPTY + MAX_STAGES,
     NUM_BARS = ACC_FULL + 1
 };
 static_assert(NUM_BARS * 8 + 4 <= 256, "barrier area");
@@ -190,7 +194,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_a,
                    const TcParams p) {
     using L = TcLayout<BN, QUANT>;
-    constexpr int SA = L::SA, SB = L::SB, RAW = QUANT ? L::RAW : 1;   // RAW: ring of the Q4_0 path only
+    constexpr int ST = L::ST, RAW = QUANT ? L::RAW : 1;   // RAW: ring of the Q4_0 path only
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
@@ -205,13 +209,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bar(RAW_FULL + i), 1);
             mbar_init(bar(RAW_EMPTY + i), CONVERTER_WARPS);
         }
-        for (int i = 0; i < SB; i++) {
-            mbar_init(bar(B_FULL + i), 1);
-            mbar_init(bar(B_EMPTY + i), 1);
-        }
-        for (int i = 0; i < SA; i++) {
-            mbar_init(bar(A_FULL + i), QUANT ? CONVERTER_WARPS : 1);
-            mbar_init(bar(A_EMPTY + i), 1);
+        for (int i = 0; i < ST; i++) {
+            mbar_init(bar(FULL + i), QUANT ? CONVERTER_WARPS + 1 : 2);
+            mbar_init(bar(EMPTY + i), 1);
         }
         mbar_init(bar(ACC_FULL), 1);
     }
@@ -244,13 +244,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tma_load_2d(smem_addr(smem + L::raw + rs * RAW_STAGE), &map_a, kt * RAW_WORDS, n0 / 16,
                                 bar(RAW_FULL + rs));
                 } else {
-                    const int sa = kt % SA;
-                    if (kt >= SA) wait_or_fail(bar(A_EMPTY + sa), (uint32_t)((kt / SA - 1) & 1), failed, p.status);
+                    const int st = kt % ST;
+                    if (kt >= ST) wait_or_fail(bar(EMPTY + st), (uint32_t)((kt / ST - 1) & 1), failed, p.status);
                     if (failed) break;
-                    mbar_arrive_expect_tx(bar(A_FULL + sa), (uint32_t)A_STAGE);
-                    tma_load_2d(smem_addr(smem + L::a + sa * A_STAGE), &map_a, kt * BK, n0, bar(A_FULL + sa));
-                    tma_load_2d(smem_addr(smem + L::a + sa * A_STAGE + ATOM_BYTES), &map_a, kt * BK + 64, n0,
-                                bar(A_FULL + sa));
+                    mbar_arrive_expect_tx(bar(FULL + st), (uint32_t)A_STAGE);
+                    tma_load_2d(smem_addr(smem + L::a + st * A_STAGE), &map_a, kt * BK, n0, bar(FULL + st));
+                    tma_load_2d(smem_addr(smem + L::a + st * A_STAGE + ATOM_BYTES), &map_a, kt * BK + 64, n0,
+                                bar(FULL + st));
                 }
             }
         }
@@ -258,13 +258,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------------------------------------------------- activation producer
         if (lane == 0) {
             for (int kt = 0; kt < NT && !failed; kt++) {
-                const int sb = kt % SB;
-                if (kt >= SB) wait_or_fail(bar(B_EMPTY + sb), (uint32_t)((kt / SB - 1) & 1), failed, p.status);
+                const int st = kt % ST;
+                if (kt >= ST) wait_or_fail(bar(EMPTY + st), (uint32_t)((kt / ST - 1) & 1), failed, p.status);
                 if (failed) break;
-                mbar_arrive_expect_tx(bar(B_FULL + sb), (uint32_t)L::B_STAGE);
-                tma_load_2d(smem_addr(smem + L::b + sb * L::B_STAGE), &map_b, kt * BK, m0, bar(B_FULL + sb));
-                tma_load_2d(smem_addr(smem + L::b + sb * L::B_STAGE + BN * 128), &map_b, kt * BK + 64, m0,
-                            bar(B_FULL + sb));
+                mbar_arrive_expect_tx(bar(FULL + st), (uint32_t)L::B_STAGE);
+                tma_load_2d(smem_addr(smem + L::b + st * L::B_STAGE), &map_b, kt * BK, m0, bar(FULL + st));
+                tma_load_2d(smem_addr(smem + L::b + st * L::B_STAGE + BN * 128), &map_b, kt * BK + 64, m0,
+                            bar(FULL + st));
             }
         }
     } else if (warp == 1) {
@@ -272,17 +272,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         // The whole warp runs the loop and waits; lane 0 issues the MMAs and commits.
         constexpr uint32_t idesc = f16_idesc(BM, BN);
         for (int kt = 0; kt < NT; kt++) {
-            const int sa = kt % SA, sb = kt % SB;
-            wait_or_fail(bar(A_FULL + sa), (uint32_t)((kt / SA) & 1), failed, p.status);
-            wait_or_fail(bar(B_FULL + sb), (uint32_t)((kt / SB) & 1), failed, p.status);
+            const int st = kt % ST;
+            wait_or_fail(bar(FULL + st), (uint32_t)((kt / ST) & 1), failed, p.status);
             if (__any_sync(0xffffffffu, failed)) {
                 failed = true;
                 break;
             }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t a_base = smem_addr(smem + L::a + sa * A_STAGE);
-                const uint32_t b_base = smem_addr(smem + L::b + sb * L::B_STAGE);
+                const uint32_t a_base = smem_addr(smem + L::a + st * A_STAGE);
+                const uint32_t b_base = smem_addr(smem + L::b + st * L::B_STAGE);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; kk++) {
                     const uint32_t koff = (uint32_t)((kk & 3) * 32);
@@ -292,9 +291,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mma_f16(tmem + (uint32_t)((kk % L::NACC) * BN), ad, bd, idesc,
                             (kt > 0 || kk >= L::NACC) ? 1u : 0u);
                 }
-                // the stages may be refilled once these MMAs completed
-                mma_commit(bar(A_EMPTY + sa));
-                mma_commit(bar(B_EMPTY + sb));
+                mma_commit(bar(EMPTY + st));   // the stage may be refilled once these MMAs completed
             }
             __syncwarp();
         }
@@ -308,12 +305,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int gi = t >> 4, rr = t & 15;
             const bool row_ok = n0 + t < p.N;
             for (int kt = 0; kt < NT; kt++) {
-                const int rs = kt % RAW, sa = kt % SA;
+                const int rs = kt % RAW, st = kt % ST;
                 wait_or_fail(bar(RAW_FULL + rs), (uint32_t)((kt / RAW) & 1), failed, p.status);
-                if (kt >= SA) wait_or_fail(bar(A_EMPTY + sa), (uint32_t)((kt / SA - 1) & 1), failed, p.status);
+                if (kt >= ST) wait_or_fail(bar(EMPTY + st), (uint32_t)((kt / ST - 1) & 1), failed, p.status);
                 if (!failed) {
                     const uint8_t *tile = smem + L::raw + rs * RAW_STAGE + gi * TILE_BYTES;
-                    uint8_t *a_stage = smem + L::a + sa * A_STAGE;
+                    uint8_t *a_stage = smem + L::a + st * A_STAGE;
                     // scales of blocks 2h and 2h + 1 of row rr
                     const uint32_t dw =
                         row_ok ? *reinterpret_cast<const uint32_t *>(tile + TILE_SCALE_OFFSET + rr * 8 + h * 4) : 0u;
@@ -339,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive_plain(bar(RAW_EMPTY + rs));
-                    mbar_arrive_plain(bar(A_FULL + sa));
+                    mbar_arrive_plain(bar(FULL + st));
                 }
             }
         }
