@@ -151,6 +151,8 @@ struct Params {
     int pf;                  // L2 prefetch distance of the producers, in chunks
     int fused;               // 1: no INIT launch, each CTA quantizes its slice of src1
     int early;               // 1: the producers may read the weights before the grids in front finished
+    int seq_slice;           // >= 0: this launch takes K slice seq_slice over whole row groups per CTA
+                             // (one launch per slice); slices after the first add into dst
 };
 
 struct Layout {
@@ -296,12 +298,18 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
     constexpr int FIXUPS = SH::FIXUPS;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int s = blockIdx.x / p.Gs, ci = blockIdx.x % p.Gs;
+    // one launch per K slice: several activation rows only (the host never asks it of the
+    // one-row kernels, which then compile without it)
+    const int seq_slice = (F16W || MT > 1) ? p.seq_slice : -1;
+    const bool one_slice = p.S == 1 || seq_slice >= 0;   // whole row groups per CTA
+    const int s = seq_slice >= 0 ? seq_slice : (int)(blockIdx.x / p.Gs);
+    const int ci = seq_slice >= 0 ? (int)blockIdx.x : (int)(blockIdx.x % p.Gs);
     int ts0, nts;
     slice_of(p.NT, p.S, s, ts0, nts);
     const int T = p.N16 * nts;   // tiles of the slice (< 2^31: N * K <= 2^40)
-    // S == 1: whole row groups per CTA (no shared row group); S > 1: equal tile ranges
-    const Segments seg = p.S == 1 ? Segments((int)((int64_t)p.N16 * ci / p.Gs) * nts,
+    // one slice per launch: whole row groups per CTA (no shared row group); S > 1 slices in
+    // one launch: equal tile ranges
+    const Segments seg = one_slice ? Segments((int)((int64_t)p.N16 * ci / p.Gs) * nts,
                                              (int)((int64_t)p.N16 * (ci + 1) / p.Gs) * nts, nts, 1)
                                   : Segments((int)((int64_t)T * ci / p.Gs), (int)((int64_t)T * (ci + 1) / p.Gs), nts,
                                              p.S);
@@ -815,7 +823,10 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
                 p.part[(((size_t)g * p.S + s) * 2 + slot_i) * PART_STRIDE + tid] = v;
             } else {
                 const int m = tid / 16, row = 16 * g + tid % 16;
-                if (m < p.M && row < p.N) p.dst[(size_t)m * p.N + row] = v;
+                if (m < p.M && row < p.N) {   // a later slice's launch adds to the earlier ones' sum
+                    float *o = p.dst + (size_t)m * p.N + row;
+                    *o = seq_slice > 0 ? *o + v : v;
+                }
             }
         }
         if (j < seg.nshared) {                         // the partial is written: the fix-up may read it
@@ -974,6 +985,13 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
         p.ntmax = q.ntmax;
         p.Gs = q.Gs;
         p.maxfix = q.maxfix;
+        // Several K slices with several activation rows: one launch per slice, each CTA (one per
+        // SM, at most one per row group) owning whole row groups and the later slices adding into
+        // dst, instead of one launch whose S groups of CTAs share row groups and add partials
+        // across CTAs (measured about twice as slow).  One activation row keeps the single launch.
+        const bool seq = q.S > 1 && (f16 || MT > 1);
+        p.seq_slice = -1;
+        if (seq) p.Gs = std::max(1, std::min(sm_count(), p.N16));
         const int cw = f16 ? (MT == 8 ? 8 : 16) : consumer_warps_for(p.M);
         const int consumers = cw == 8 ? Shape<8>::CONSUMERS : Shape<16>::CONSUMERS;
         const int fused_loads = cw == 8 ? Shape<8>::FUSED_LOADS : Shape<16>::FUSED_LOADS;
@@ -1031,11 +1049,14 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
             st = check_cuda(cudaLaunchKernelEx(&cfg, wdata_kernel, p), "gemv_q4_0 INIT launch");
             if (st != GQ_OK) return st;
         }
-        cfg.gridDim = dim3((unsigned)(p.S * p.Gs), 1, 1);
+        cfg.gridDim = dim3((unsigned)(seq ? p.Gs : p.S * p.Gs), 1, 1);
         cfg.blockDim = dim3((unsigned)threads, 1, 1);
         cfg.dynamicSmemBytes = smem;
-        st = check_cuda(cudaLaunchKernelEx(&cfg, kv.kernel, p), "gemv launch");
-        if (st != GQ_OK) return st;
+        for (int sl = 0; sl < (seq ? p.S : 1); sl++) {
+            if (seq) p.seq_slice = sl;
+            st = check_cuda(cudaLaunchKernelEx(&cfg, kv.kernel, p), "gemv launch");
+            if (st != GQ_OK) return st;
+        }
     }
     return GQ_OK;
 }
