@@ -258,7 +258,9 @@ gq_status gq_mul_mat_q5_0_f32(const void *q5_repacked, const float *src1, float 
  * partial sums of weight rows that several CTAs share, with per-row counters
  * that every launch leaves at zero, and (tensor-core path) the quantized
  * activations.  It is allocated with cudaMalloc the first time a stream needs it
- * and grows when a larger problem comes; growth synchronizes that stream.  A
+ * and grows when a larger problem comes (at least doubling); growth synchronizes
+ * that stream, and the replaced buffer stays allocated until the process exits,
+ * so launches and graphs that took its address remain valid.  A
  * call that would grow it while the stream is being captured into a CUDA graph
  * returns GQ_ERR_NO_MEMORY: reserve it first with this call, on the stream that
  * will be captured, for the largest M, N, K it will run.  Graphs captured on a

@@ -4,10 +4,14 @@
 // through a small global buffer and a per-row-group arrival counter; the
 // tensor-core path stages its quantized activations there.  Counters start at
 // zero and every launch leaves them at zero again, so the buffer is reused as it
-// is.  A stream's workspace grows on demand: growth synchronizes that stream,
-// frees the old buffer and allocates a new one (cudaMalloc), so it must not
-// happen while the stream is being captured into a graph; gq_reserve_workspace
-// lets a caller size it beforehand.
+// is.  A stream's workspace grows on demand: growth synchronizes that stream and
+// allocates a new buffer (cudaMalloc), so it must not happen while the stream is
+// being captured into a graph; gq_reserve_workspace lets a caller size it
+// beforehand.  A replaced buffer is retired, not freed: another host thread may
+// have taken its address for a launch on the same stream just before the growth,
+// and that launch (or a CUDA graph captured with the old address) must still find
+// valid memory.  Each growth at least doubles the data part, so the retired
+// buffers of a stream hold less than its current one.
 #include <mutex>
 #include <vector>
 
@@ -27,6 +31,7 @@ struct Entry {
 
 std::mutex g_mutex;
 std::vector<Entry> g_entries;
+std::vector<uint8_t *> g_retired;   // replaced buffers, kept until the process exits
 
 }  // namespace
 
@@ -55,10 +60,10 @@ gq_status get_workspace(cudaStream_t stream, size_t counter_bytes, size_t data_b
     size_t cb = counter_bytes, db = data_bytes;
     if (e) {
         cb = std::max(cb, e->counter_bytes);
-        db = std::max(db, e->bytes - e->counter_bytes);
+        db = std::max(db, 2 * (e->bytes - e->counter_bytes));   // at least double (see above)
         st = check_cuda(cudaStreamSynchronize(stream), "cudaStreamSynchronize (workspace growth)");
         if (st != GQ_OK) return st;
-        cudaFree(e->ptr);
+        g_retired.push_back(e->ptr);
         e->ptr = nullptr;
     }
     uint8_t *p = nullptr;
@@ -115,9 +120,10 @@ gq_status get_staging(cudaStream_t stream, size_t bytes, uint8_t **out) {
         return fail(GQ_ERR_NO_MEMORY, "the stream's staging buffer must grow (%zu bytes) while the stream is "
                     "being captured", bytes);
     if (e) {
+        bytes = std::max(bytes, 2 * e->bytes);   // at least double, as for the workspace
         st = check_cuda(cudaStreamSynchronize(stream), "cudaStreamSynchronize (staging growth)");
         if (st != GQ_OK) return st;
-        cudaFree(e->ptr);
+        g_retired.push_back(e->ptr);   // as for the workspace: a concurrent launch may still use it
         e->ptr = nullptr;
         e->bytes = 0;
     }
