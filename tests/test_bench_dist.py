@@ -71,3 +71,6 @@ def test_reference_arm_prints_on_rank_zero_only():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    # exactly the requested steps: W untimed, K timed, each a bounded sample of the workload
+    assert line["steps"] == 5 and line["warmup"] == 3
+    assert line["cpu_baseline"]["sample"].startswith("5 timed steps after 3 warm-up steps")
