@@ -22,9 +22,10 @@
 //               (q - 8) * d rounded once, in the 128-byte-swizzled K-major
 //               layout the MMA reads (each warp 32 rows x 64 columns); then
 //               they read the accumulators back (tcgen05.ld) and store dst.
-// Each ring has its own producer, so the weight stream from device memory runs
-// as many stages ahead as its ring holds, whatever the MMA and activation rings
-// are waiting for.  The MMAs of a stage rotate over 2 (BN = 128) or 4
+// The raw weight bytes have a ring of their own with their own producer, so the
+// weight stream from device memory runs as many stages ahead as that ring holds,
+// whatever the operand ring (converted weights and activations of one MMA step
+// per stage) is waiting for.  The MMAs of a stage rotate over 2 (BN >= 128) or 4
 // independent accumulators in tensor memory, so consecutive MMAs do not wait
 // for each other's results; the epilogue adds them in a fixed order.
 // The activations are quantized first by a small kernel into a workspace copy
