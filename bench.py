@@ -610,20 +610,23 @@ def cpu_baseline(seconds: float):
         w = (rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02))
         prepared.append((o.quantize_q4_0(w), rng.standard_normal((1, K), dtype=np.float32), N, K))
 
-    def one_step():
-        with cf.ThreadPoolExecutor(cores) as ex:
+    with cf.ThreadPoolExecutor(cores) as ex:          # one pool for the whole sample
+        def one_step():
+            futs = []
             for q4, x, N, K in prepared:
                 bounds = [(N * i // cores, N * (i + 1) // cores) for i in range(cores)]
-                list(ex.map(lambda b: o.mul_mat_q4_0_f32(q4, x, n_range=b), bounds))
+                futs += [ex.submit(o.mul_mat_q4_0_f32, q4, x, b) for b in bounds]
+            for f in futs:
+                f.result()
 
-    steps = 0
-    t0 = time.perf_counter()
-    while True:
-        one_step()
-        steps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
+        steps = 0
+        t0 = time.perf_counter()
+        while True:
+            one_step()
+            steps += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
     bytes_per_step = sum(step_bytes_q4(1, N, K) for N, K in SHAPES)
     return {"value": round(bytes_per_step * steps / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{steps} steps of the 3 decode matvecs (M=1), {el:.1f} s, rows of N split over {cores} threads"}
