@@ -279,7 +279,9 @@ gq_status gq_mul_mat_f16_f32_path(const void *src0_f16, const float *src1, float
 /* M threshold of GQ_PATH_AUTO: M <= threshold runs the GEMV family.  Default 16
  * (Smallem, "Générer à plusieurs", section "La courbe, une première fois": the
  * narrow kernel serves products of at most 16 rows, the tiles the rest).
- * Process-wide; GQ_ERR_INVALID_ARG if t < 0. */
+ * Process-wide; GQ_ERR_INVALID_ARG if t < 0.  The environment variable
+ * GQ_M_THRESHOLD, read when the library loads, replaces the default when it
+ * holds a non-negative decimal integer (other values are ignored). */
 gq_status gq_set_m_threshold(int64_t t);
 int64_t gq_get_m_threshold(void);
 

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <algorithm>
 #include <cmath>
@@ -26,6 +27,19 @@ std::atomic<int> g_arch_ok[MAX_DEVICES];      // 0 unknown, 1 sm_103, -1 other
 std::atomic<int> g_sm_count[MAX_DEVICES];
 std::atomic<unsigned int *> g_status_ptr[MAX_DEVICES];
 std::atomic<int64_t> g_m_threshold{16};
+
+// GQ_M_THRESHOLD, when set to a non-negative decimal integer, replaces the default M
+// threshold at load time (for dispatch experiments without code changes); any other
+// value is ignored.
+struct ThresholdFromEnvironment {
+    ThresholdFromEnvironment() {
+        const char *v = getenv("GQ_M_THRESHOLD");
+        if (!v || !*v) return;
+        char *end = nullptr;
+        const long long t = strtoll(v, &end, 10);
+        if (end && *end == '\0' && t >= 0) g_m_threshold.store((int64_t)t);
+    }
+} g_threshold_from_environment;
 std::atomic<int> g_static_weights{0};
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }

@@ -151,3 +151,20 @@ def test_dispatch_profiles(lib):
         gq.gq_set_dispatch_profile(gq.GQ_KIND_Q4_0, 64, 128, [16], [float("nan")], [2])
     gq.gq_clear_dispatch_profiles()
     assert gq.gq_choose_path(gq.GQ_KIND_Q4_0, 64, 128, 48) == gq.GQ_PATH_TC
+
+
+@pytest.mark.parametrize("value,expected", [("24", 24), ("0", 0), ("-3", 16), ("abc", 16), ("12x", 16), (None, 16)])
+def test_threshold_from_environment(value, expected):
+    """GQ_M_THRESHOLD replaces the default M threshold when the library loads (a fresh
+    process per case); values that are not non-negative integers leave the default."""
+    import subprocess
+    import sys
+    env = dict(os.environ)
+    env.pop("GQ_M_THRESHOLD", None)
+    if value is not None:
+        env["GQ_M_THRESHOLD"] = value
+    code = "import quantized_skinny_matmul_gb300 as gq; print(gq.gq_get_m_threshold())"
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120,
+                         cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert out.returncode == 0, out.stderr
+    assert int(out.stdout.strip().splitlines()[-1]) == expected
