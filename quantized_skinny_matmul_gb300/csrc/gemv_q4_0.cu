@@ -235,10 +235,6 @@ __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS) : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 // Release of this thread's (and, through a preceding barrier, its CTA's or
 // warp's) earlier writes and acquire of the other arrivals' writes.
 __device__ __forceinline__ unsigned int atomic_add_acq_rel_gpu(unsigned int *p, unsigned int v) {
@@ -978,6 +974,11 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
         p.M = (int)std::min<int64_t>(16, M - m0);
         p.x = x + m0 * K;
         p.dst = dst + m0 * N;
+        if (p.M == 1 && wf == WF_Q4 && gemv_m1_supported(N, K) && env_int("GQ_GEMV_M1", 1) != 0) {
+            st = launch_gemv_m1_q4_0(rep, p.x, p.dst, N, K, s);   // one row: its own kernel, no workspace
+            if (st != GQ_OK) return st;
+            continue;
+        }
         // F16: tensor-core tiles of 8 or 16 activation rows
         const int MT = f16 ? (p.M <= 8 ? 8 : 16) : p.M <= 1 ? 1 : p.M <= 2 ? 2 : p.M <= 4 ? 4 : p.M <= 8 ? 8 : 16;
         const Plan q = plan(p.N16, p.NT, p.M, f16);   // the images hold p.M rows

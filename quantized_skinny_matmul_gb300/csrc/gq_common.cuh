@@ -155,6 +155,26 @@ __device__ __forceinline__ void pack_q8_words(const float4 (&x)[N], const Q8Scal
         for (int k = 0; k < N; k++) w[k] = pack_q8x4(x[k], q);
 }
 
+// The codes of 4N values.  The nearest integer of y = x * (1/d) comes from the low mantissa
+// bits of y + 1.5 * 2^23 (|y| <= 127.5 here, so that byte is the code in two's complement);
+// only if some lane of the warp has a value whose y lies within 2^-14 of a half-integer
+// does the warp form the exact codes instead (one warp-uniform branch, rarely taken).
+template <int N>
+__device__ __forceinline__ void pack_q8_words_fast(const float4 (&x)[N], const Q8Scale &q, uint32_t (&w)[N]) {
+    bool near = false;
+    auto one = [&](float v) {
+        const float y = (v * q.s) * q.r;
+        const float t = y + 12582912.0f;
+        near |= q8_near_half(y, t - 12582912.0f);
+        return (int)__float_as_uint(t);
+    };
+#pragma unroll
+    for (int k = 0; k < N; k++) w[k] = pack_bytes(one(x[k].x), one(x[k].y), one(x[k].z), one(x[k].w));
+    if (__any_sync(0xffffffffu, near))
+#pragma unroll
+        for (int k = 0; k < N; k++) w[k] = pack_q8x4(x[k], q);
+}
+
 __device__ __forceinline__ void pack_q8x16(const float4 (&x)[4], const Q8Scale &q, uint32_t (&w)[4]) {
     pack_q8_words<4>(x, q, w);
 }
@@ -338,6 +358,10 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // 1-D bulk copy; dst, src 16-byte aligned, bytes a multiple of 16.

@@ -49,6 +49,10 @@ void gemv_q4_0_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *da
 // The Q4_0 GEMV on a given workspace (counters zero on entry, left at zero).
 gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
                                 const Workspace &ws, cudaStream_t s);
+// The one-row Q4_0 product (whole row groups per CTA, no workspace): whether it serves
+// [N][K], and its launch.
+bool gemv_m1_supported(int64_t N, int64_t K);
+gq_status launch_gemv_m1_q4_0(const void *rep, const float *x, float *dst, int64_t N, int64_t K, cudaStream_t s);
 gq_status launch_gemv_f16(const void *w16, const float *x, float *dst, int64_t M, int64_t N,
                           int64_t K, cudaStream_t s);
 // F16 weights repacked into 16 x 32 tiles: the repack, and the GEMV on them (the Q4_0
