@@ -44,6 +44,7 @@ if ROOT not in sys.path:
 
 SHAPES = ((4096, 4096), (11008, 4096), (4096, 11008))
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0     # GB300 HBM3e, nominal
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -325,6 +326,8 @@ def run_ours(args, rank, world, local):
 
     warm_plan, timed_plan = plan(args.warmup), plan(args.steps)
     sampler = ClockSampler(b.smi_id()).start()
+    for g in {id(g): g for g in timed_plan}.values():   # untimed: each timed graph's first replay
+        b.time_graph(g, 1)
     soak_until = time.time() + 0.5          # untimed: let the clocks settle under load
     while time.time() < soak_until:
         for g in warm_plan:
@@ -399,8 +402,9 @@ def run_ours(args, rank, world, local):
     traffic = profile_traffic()
     out["roofline"] = {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
                        "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                       "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
                        "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
-                       "kernel": "gemv_q4_0_kernel<1, 8>", "launches": launches_per_step * args.steps,
+                       "kernel": "gemv_m1_q4_0_kernel<16>", "launches": launches_per_step * args.steps,
                        "algorithmic_bytes_per_launch": round(bytes_per_step / launches_per_step)}
 
     if rank == 0 and world == 1:
@@ -528,14 +532,18 @@ def extras(b, weights, C, hbm_peak, bf16_peak, bf16_sustained, args):
         stack_bytes = sum(q4_bytes(N, K) for _, N, K in synth.LAYER_SHAPES) * synth.N_LAYERS
         st = {"weight_bytes": stack_bytes}
         for M in (1, 8):
-            xs = {K: b.acts(M, K, 600 + K + M) for K in (4096, 11008)}
+            # every product of every layer has its own activations (seeded per layer and product),
+            # generated on the device before the timed graphs
+            xs = [[b.acts(M, K, 100000 + synth.stack_seed(l, p)) for p, (_, N, K) in enumerate(synth.LAYER_SHAPES)]
+                  for l in range(synth.N_LAYERS)]
             outs = {N: torch.empty((M, N), device=b.dev) for N in (4096, 11008)}
             ls = []
             for l in range(synth.N_LAYERS):
                 for p, (_, N, K) in enumerate(synth.LAYER_SHAPES):
                     ls.append(lambda l=l, p=p, N=N, K=K, M=M, xs=xs, outs=outs:
-                              gq.gq_mul_mat_q4_0_f32(layers[l][p], xs[K], outs[N], M, N, K))
+                              gq.gq_mul_mat_q4_0_f32(layers[l][p], xs[l][p], outs[N], M, N, K))
             t = b.time_launches(ls, max_graph=len(ls))
+            del xs
             st[f"M{M}"] = {"ms_per_token_pass": round(t * 1e3, 4), "tokens_per_s": round(M / t, 1),
                            "GB/s": round(stack_bytes / t / 1e9, 1), "frac_of_hbm": round(stack_bytes / t / 1e9 / hbm_peak, 4)}
         res["stack_32_layers"] = st
@@ -557,14 +565,17 @@ def extras(b, weights, C, hbm_peak, bf16_peak, bf16_sustained, args):
         del layers
         sf = {"weight_bytes": stack_bytes, "products_per_layer": len(groups)}
         for M in (1, 8):
-            xs = {K: b.acts(M, K, 600 + K + M) for K in (4096, 11008)}
+            # one activation per fused product and layer (the products of a group share it)
+            xs = [[b.acts(M, K, 200000 + synth.stack_seed(l, gi)) for gi, (w, N, K) in enumerate(fused[l])]
+                  for l in range(synth.N_LAYERS)]
             outs = {N: torch.empty((M, N), device=b.dev) for _, N, _ in fused[0]}
             ls = []
             for l in range(synth.N_LAYERS):
-                for (w, N, K) in fused[l]:
-                    ls.append(lambda w=w, N=N, K=K, M=M, xs=xs, outs=outs:
-                              gq.gq_mul_mat_q4_0_f32(w, xs[K], outs[N], M, N, K))
+                for gi, (w, N, K) in enumerate(fused[l]):
+                    ls.append(lambda w=w, N=N, K=K, M=M, xs=xs, outs=outs, l=l, gi=gi:
+                              gq.gq_mul_mat_q4_0_f32(w, xs[l][gi], outs[N], M, N, K))
             t = b.time_launches(ls, max_graph=len(ls))
+            del xs
             sf[f"M{M}"] = {"ms_per_token_pass": round(t * 1e3, 4), "tokens_per_s": round(M / t, 1),
                            "GB/s": round(stack_bytes / t / 1e9, 1), "frac_of_hbm": round(stack_bytes / t / 1e9 / hbm_peak, 4)}
         res["stack_32_layers_fused_qkv_gate_up"] = sf
@@ -574,7 +585,7 @@ def extras(b, weights, C, hbm_peak, bf16_peak, bf16_sustained, args):
 
 def profile_traffic():
     """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "gemv_q4_0_decode_m1.md")
+    path = os.path.join(ROOT, "profiles", "gemv_m1_q4_0_decode.md")
     try:
         text = open(path).read()
     except OSError:
@@ -591,7 +602,7 @@ def profile_traffic():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("gemv_q4_0.cu", "gq_common.cuh"):
+    for f in ("gemv_m1.cu", "gq_common.cuh"):
         with open(os.path.join(ROOT, "quantized_skinny_matmul_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
