@@ -263,7 +263,9 @@ gq_status gq_mul_mat_q5_0_f32(const void *q5_repacked, const float *src1, float 
  * so launches and graphs that took its address remain valid.  A
  * call that would grow it while the stream is being captured into a CUDA graph
  * returns GQ_ERR_NO_MEMORY: reserve it first with this call, on the stream that
- * will be captured, for the largest M, N, K it will run.  Graphs captured on a
+ * will be captured, for the largest M, N, K it will run.  A growth whose
+ * cudaMalloc fails returns GQ_ERR_NO_MEMORY and leaves the current workspace in
+ * place (smaller problems keep running on it).  Graphs captured on a
  * stream use that stream's workspace: do not replay them concurrently with
  * other work on that stream's workspace. */
 gq_status gq_reserve_workspace(int64_t M, int64_t N, int64_t K, cudaStream_t stream);
@@ -304,18 +306,21 @@ gq_status gq_set_dispatch_profile(int kind, int64_t N, int64_t K, const int64_t 
 gq_status gq_clear_dispatch_profiles(void);
 gq_path gq_choose_path(int kind, int64_t N, int64_t K, int64_t M);
 
-/* The Q4_0 product of gq_mul_mat_q4_0_f32, for callers that cannot allocate
- * device memory: code recording into a CUDA graph while the stream is captured
- * (allocation is refused during global-mode capture) and applications whose
- * device memory belongs to a pooling allocator that must see every byte.
+/* The Q4_0 product of gq_mul_mat_q4_0_f32, for callers that cannot let a library
+ * allocate device memory: serving processes whose own pooling allocator has
+ * reserved the device memory up front (for example for a KV cache) and must
+ * account for every byte, plug-ins loaded by a runtime that forbids them to
+ * allocate, and latency-bound loops in which cudaMalloc (which can synchronize
+ * the device) may not run.
  * (The pages have no counterpart: this is an interface of this library.)
  * All scratch space comes from one static device array of 4 MiB that every
  * device loading the library holds until the process exits; nothing is ever
  * allocated or freed.  It always runs the GEMV family (any M, 16 rows per
  * launch).  GQ_ERR_INVALID_ARG when [N][K] needs more scratch than 4 MiB (for
  * example N = 11008 with K up to 11008 fits).  The first call on a device
- * resolves the array's device address (cudaGetSymbolAddress): make it before
- * any stream capture.  Each call re-zeroes the array's counters on `stream`
+ * resolves the array's device address (cudaGetSymbolAddress) and keeps it for
+ * the life of the process: make that call before any stream capture, and do not
+ * use this entry point on a device after cudaDeviceReset.  Each call re-zeroes the array's counters on `stream`
  * (cudaMemsetAsync) and then uses the whole array: calls that overlap on the
  * GPU, from any streams, race on it and give wrong results. */
 gq_status gq_mul_mat_q4_0_f32_noalloc(const void *q4_repacked, const float *src1, float *dst,

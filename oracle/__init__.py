@@ -14,6 +14,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import tempfile
 import threading
@@ -38,10 +39,24 @@ _lock = threading.Lock()
 _lib = None
 
 
+def _for_this_cpu(path: str) -> bool:
+    """Whether the shared library at path is an ELF object for this host's CPU."""
+    machines = {"x86_64": 62, "amd64": 62, "aarch64": 183, "arm64": 183}
+    want = machines.get(platform.machine().lower())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    return (len(head) == 20 and head[:4] == b"\x7fELF"
+            and (want is None or int.from_bytes(head[18:20], "little") == want))
+
+
 def build(src: str = _SRC, out: str = _LIB_PATH, force: bool = False) -> str:
-    """Compile the oracle C source into a shared library (skipped when up to date)."""
+    """Compile the oracle C source into a shared library (skipped when up to date and built
+    for this CPU)."""
     if (not force and os.path.exists(out)
-            and os.path.getmtime(out) >= os.path.getmtime(src)):
+            and os.path.getmtime(out) >= os.path.getmtime(src) and _for_this_cpu(out)):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
     fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(out))

@@ -12,6 +12,7 @@ from __future__ import annotations
 import argparse
 import concurrent.futures as cf
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -48,8 +49,25 @@ def _deps():
     return max(os.path.getmtime(f) for f in files)
 
 
+_ELF_MACHINE = {"x86_64": 62, "amd64": 62, "aarch64": 183, "arm64": 183}
+
+
+def built_for_this_machine(path: str) -> bool:
+    """Whether the ELF file at path targets this host's CPU (a copy built on another machine does not)."""
+    want = _ELF_MACHINE.get(platform.machine().lower())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    if len(head) < 20 or head[:4] != b"\x7fELF":
+        return False
+    return want is None or int.from_bytes(head[18:20], "little") == want
+
+
 def up_to_date() -> bool:
-    return os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _deps()
+    return (os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _deps()
+            and built_for_this_machine(LIB_PATH))
 
 
 def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:

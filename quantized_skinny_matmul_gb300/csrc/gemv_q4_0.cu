@@ -1,52 +1,43 @@
-// gemv_q4_0.cu -- the persistent Q4_0 x Q8_0 GEMV (up to 16 activation rows
-// per launch), the hot path of single-token and small-batch decode.
+// gemv_q4_0.cu -- the persistent GEMV of the weight formats in repacked tiles
+// (Q4_0, Q8_0, Q5_0, Q4_1 and F16 tiles) for up to 16 activation rows per
+// launch: small-batch decode.  (The one-row Q4_0 product, single-token decode,
+// runs the kernel of gemv_m1.cu.)
 //
 // In this regime every weight byte is read once and the product is bound by
 // HBM (Smallem, "Générer à plusieurs", introduction and "Où la courbe
 // s'aplatit": with B sequences each weight read serves B products; DeepSpeed-
 // Inference notes, III.A: small batches are limited by the bandwidth of reading
-// the weights).  One call is two launches on the caller's stream:
+// the weights).
 //
-//  1. INIT (llama.cpp PR #1632, "Introduction": the q_f32 kind quantizes src1
-//     in its INIT stage; Arm China NUMA article, "MulMat 算子優化": src1 goes to
-//     the wdata buffer that every worker reads).  For M > 4 a small kernel
-//     quantizes the M activation rows to Q8_0 once and writes them to the
-//     workspace as "wdata images", one per K slice, already in the shared-memory
-//     layout the consumers read: codes, then per block the scale and -8 * sum of
-//     codes.  When M times the slice width is small (at most eight 16-byte loads
-//     per consumer thread) each CTA quantizes its own slice into shared memory
-//     instead (the article's per-node wdata copies, because quantizing is
-//     cheap), which saves a launch.
-//  2. COMPUTE, persistent, one CTA per SM.  K is cut into S slices (S depends
-//     on K and on how many activation rows share the launch); with one slice
-//     each CTA owns a run of whole row groups, balanced to within one row group,
-//     and with several slices the repacked tiles of each slice, in
-//     row-group-major order, are divided evenly between the CTAs of the slice
-//     (split-K for small grids: Smallem, "La courbe, une première fois"; output
-//     tiles plus input-dimension tiles: DeepSpeed-Inference notes, III.C.1).
-//       * Two producer warps stream the CTA's share through a ring of shared-
-//         memory chunks with bulk (TMA) copies.  Behind INIT they start at their
-//         first instruction: the launch is programmatic-dependent on INIT, and
-//         INIT waited for every earlier grid before letting this one start, so
-//         the weights are final.  Without INIT they first wait for the grids
-//         before.
-//       * Sixteen consumer warps wait for INIT, load their slice's wdata image
-//         into shared memory, then take one tile of every chunk each.  A lane
-//         owns whole block-rows (row r, blocks j and j+2 of the tile): each
-//         block dot is eight dp4a on the unpacked nibbles and
-//         the activation codes, exact in int32, and the f32 sum takes
-//         d4 * d8 * sumi block by block.  (The int8 tensor instructions run at a
-//         small fraction of the fp16 rate on this GPU; dp4a keeps the integer
-//         dots on the CUDA cores.)
-//       * At the end of each row group the consumer warps' partials are added in
-//         shared memory (DeepSpeed-Inference notes, III.C.2: make the partials of
-//         one output contiguous and reduce them in one pass).  A row group that
-//         one CTA owns is stored directly.  A row group shared with other CTAs
-//         goes to its slot in the workspace, and a fix-up warp bumps the row
-//         group's counter; the CTA that arrives last adds all partials in a
-//         fixed order and stores the result.  Shared row groups are
-//         processed first, so their fix-ups overlap the stream; no CTA ever
-//         waits for another and the result does not depend on timing.
+//  * K slices.  K is cut into S slices so that a CTA's image of the activations
+//    fits in shared memory (S depends on K and on the number of rows).  With
+//    several activation rows a product runs one launch per slice: every CTA
+//    owns whole row groups (16 weight rows) and the launches of later slices
+//    add their sums into dst in slice order (split-K for small grids: Smallem,
+//    "La courbe, une première fois"; DeepSpeed-Inference notes, III.C.1).  With
+//    one row and several slices (very long rows) one launch runs all slices:
+//    the tiles of a slice are divided evenly between its CTAs, and a row group
+//    that CTAs share is added by a fix-up warp of the CTA that arrives last, in
+//    a fixed order.
+//  * INIT (llama.cpp PR #1632, "Introduction": the q_f32 kind quantizes src1
+//    to Q8_0 before the block dots; Arm China NUMA article, "MulMat 算子優化":
+//    every worker reads the wdata).  With one row each consumer warp
+//    quantizes the blocks of its own tiles; with several rows the CTA
+//    quantizes its slice of the rows into shared memory (up to three load
+//    rounds), or, for larger rows, a small kernel (wdata_kernel) writes the
+//    images of all slices to the workspace once and the GEMV loads its slice.
+//  * COMPUTE, persistent, at most one CTA per SM (two for one row: the CTA of
+//    the next product is resident beside this one).  Two producer warps stream
+//    the CTA's tiles through a ring of shared-memory chunks with bulk (TMA)
+//    copies and keep L2 prefetches ahead of it; with static weights they start
+//    before the wait on the grids in front.  8 or 16 consumer warps take the
+//    tiles of each chunk by position: up to four rows, eight dp4a per block on
+//    the unpacked nibbles and the codes (exact int32) scaled by d4 * d8; eight
+//    rows and more, two m16n8k16 fp16 MMAs per block whose f32 result is the
+//    exact block dot (the codes and (q - 8) are exact in fp16).  At the end of
+//    a row group the positions' partials are added in shared memory in a fixed
+//    order (DeepSpeed-Inference notes, III.C.2: make the partials of one
+//    output contiguous and reduce them in one pass).
 #include <algorithm>
 #include <atomic>
 
@@ -151,6 +142,7 @@ struct Params {
     int pf;                  // L2 prefetch distance of the producers, in chunks
     int fused;               // 1: no INIT launch, each CTA quantizes its slice of src1
     int early;               // 1: the producers may read the weights before the grids in front finished
+    int init_early;          // 1: INIT lets the GEMV start before the grids in front finished (static weights)
     int seq_slice;           // >= 0: this launch takes K slice seq_slice over whole row groups per CTA
                              // (one launch per slice); slices after the first add into dst
 };
@@ -249,7 +241,7 @@ __device__ __forceinline__ unsigned int atomic_add_acq_rel_gpu(unsigned int *p, 
 // slice that holds it.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
-    if (p.early) pdl_launch_dependents();   // weights are static: the GEMV may stream them at once
+    if (p.init_early) pdl_launch_dependents();   // weights are static: the GEMV may stream them at once
     pdl_wait();                 // src1 and the workspace are final: every earlier grid has completed
     pdl_launch_dependents();    // (no-op if already triggered) every grid before INIT is complete
     const Image im(p.M, p.ntmax);
@@ -1009,6 +1001,9 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
         // behind INIT (which waited for every earlier grid) the weights are final; otherwise only
         // a caller that declared its weights static lets the producers start before the wait
         p.early = (!p.fused || static_weights()) ? 1 : 0;
+        // INIT itself triggers the GEMV before its own wait only for static weights; otherwise the
+        // GEMV starts once INIT has waited for every earlier grid
+        p.init_early = static_weights() ? 1 : 0;
         p.part = reinterpret_cast<float *>(ws.data);
         p.wdata = ws.data + align_up((size_t)p.N16 * p.S * 2 * PART_STRIDE * sizeof(float), 256);
         const size_t fixed = Layout(MT, p.M, p.ntmax, 0, p.maxfix, wf).total;

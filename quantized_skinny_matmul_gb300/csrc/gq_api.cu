@@ -233,7 +233,9 @@ gq_status gq_reserve_workspace(int64_t M, int64_t N, int64_t K, cudaStream_t str
     gemv_f16r_workspace(N, K, &cb16, &db16);
     cb = std::max(cb, cb16);
     db = std::max(db, db16);
-    if (M > gq_get_m_threshold()) db = std::max(db, tc_workspace_bytes(M, K));
+    // the tile path's activations: whatever the dispatcher picks for M (a tuned profile may send M
+    // rows to the tile path below the threshold), the reserve covers it
+    db = std::max(db, tc_workspace_bytes(M, K));
     Workspace ws;
     GQ_TRY(get_workspace(stream, cb, db, &ws));
     return ok();

@@ -3,13 +3,13 @@
 // gq_mul_mat_q4_0_f32 takes its scratch space (per-row counters, partial sums,
 // quantized activations) from a per-stream workspace that the library obtains
 // with cudaMalloc the first time a stream needs it.  Some callers cannot let a
-// library call cudaMalloc: code that records its work into a CUDA graph while
-// the stream is being captured (allocation is refused during global-mode
-// capture), and applications whose device memory is owned by a pooling
-// allocator that accounts for every byte and must not see allocations behind
-// its back.  This entry point gives them the same product with all of its
-// scratch space in one statically sized device array that is part of the
-// loaded library, so nothing is allocated, ever.
+// library call cudaMalloc: serving processes whose pooling allocator reserved
+// the device memory up front and must account for every byte, plug-ins hosted
+// by a runtime that forbids them to allocate, and latency-bound loops in which
+// cudaMalloc (which can synchronize the device) may not run.  This entry point
+// gives them the same product with all of its scratch space in one statically
+// sized device array that is part of the loaded library, so nothing is
+// allocated, ever.
 #include <mutex>
 
 #include "gq_common.cuh"

@@ -4,10 +4,11 @@
 // through a small global buffer and a per-row-group arrival counter; the
 // tensor-core path stages its quantized activations there.  Counters start at
 // zero and every launch leaves them at zero again, so the buffer is reused as it
-// is.  A stream's workspace grows on demand: growth synchronizes that stream and
-// allocates a new buffer (cudaMalloc), so it must not happen while the stream is
-// being captured into a graph; gq_reserve_workspace lets a caller size it
-// beforehand.  A replaced buffer is retired, not freed: another host thread may
+// is.  A stream's workspace grows on demand: growth allocates a new buffer
+// (cudaMalloc), zeroes its counters and synchronizes that stream, so it must not
+// happen while the stream is being captured into a graph; gq_reserve_workspace
+// lets a caller size it beforehand.  A growth that fails leaves the current
+// buffer in use.  A replaced buffer is retired, not freed: another host thread may
 // have taken its address for a launch on the same stream just before the growth,
 // and that launch (or a CUDA graph captured with the old address) must still find
 // valid memory.  Each growth at least doubles the data part, so the retired
@@ -61,22 +62,23 @@ gq_status get_workspace(cudaStream_t stream, size_t counter_bytes, size_t data_b
     if (e) {
         cb = std::max(cb, e->counter_bytes);
         db = std::max(db, 2 * (e->bytes - e->counter_bytes));   // at least double (see above)
-        st = check_cuda(cudaStreamSynchronize(stream), "cudaStreamSynchronize (workspace growth)");
-        if (st != GQ_OK) return st;
-        g_retired.push_back(e->ptr);
-        e->ptr = nullptr;
     }
+    // The new buffer is allocated and its counters zeroed first; the entry changes only once
+    // both succeeded, so a failed growth leaves the stream's current workspace in place.
     uint8_t *p = nullptr;
     if (cudaMalloc(&p, cb + db) != cudaSuccess) {
         cudaGetLastError();
         return fail(GQ_ERR_NO_MEMORY, "cudaMalloc of a %zu-byte workspace failed", cb + db);
     }
     st = check_cuda(cudaMemsetAsync(p, 0, cb, stream), "workspace counter reset");
+    if (st == GQ_OK && e) st = check_cuda(cudaStreamSynchronize(stream), "cudaStreamSynchronize (workspace growth)");
     if (st != GQ_OK) {
         cudaFree(p);
         return st;
     }
-    if (!e) {
+    if (e) {
+        g_retired.push_back(e->ptr);
+    } else {
         g_entries.push_back(Entry{dev, stream, nullptr, 0, 0});
         e = &g_entries.back();
     }

@@ -168,3 +168,19 @@ def test_threshold_from_environment(value, expected):
                          cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     assert out.returncode == 0, out.stderr
     assert int(out.stdout.strip().splitlines()[-1]) == expected
+
+
+def test_build_rejects_a_library_for_another_cpu(tmp_path):
+    """An in-tree libgq.so built on another machine (the GPU machine is aarch64, this one may be
+    x86-64) is not taken as up to date."""
+    import platform
+    from quantized_skinny_matmul_gb300 import _build
+    this = {"x86_64": 62, "amd64": 62, "aarch64": 183, "arm64": 183}.get(platform.machine().lower())
+    if this is None:
+        pytest.skip("unknown host CPU")
+    other = 183 if this == 62 else 62
+    for machine, want in ((this, True), (other, False)):
+        f = tmp_path / f"lib{machine}.so"
+        f.write_bytes(b"\x7fELF" + bytes(14) + machine.to_bytes(2, "little") + bytes(44))
+        assert _build.built_for_this_machine(str(f)) is want
+    assert _build.built_for_this_machine(str(tmp_path / "missing.so")) is False

@@ -208,13 +208,15 @@ def test_sentinels_untouched(path):
 
 
 # --------------------------------------------------------------------------- full size
-FULL_CASES = [(M, N, K) for (N, K) in synth.DECODE_SHAPES for M in (1, 8, 16)]
+FULL_CASES = ([(M, N, K) for (N, K) in synth.DECODE_SHAPES for M in (1, 8, 16)]
+              + [(M, N, K) for (N, K) in synth.DECODE_SHAPES[1:] for M in (2, 4, 32)])
 
 
 @pytest.mark.parametrize("M,N,K", FULL_CASES)
 def test_full_size_sampled(oracle, M, N, K):
-    """The 7B-shaped decode matrices, in the launch configuration the benchmark
-    times: all quantized bytes exact, 2048 sampled outputs against the oracle."""
+    """The 7B-shaped decode matrices and the small-batch sweep (M = 2, 4, 32 on the two FFN
+    shapes), in the launch configuration the benchmark times (automatic dispatch): all quantized
+    bytes exact, 2048 sampled outputs against the oracle."""
     w, x = synth.problem(100 + M, M, N, K)
     q4, dst = run_q4(w, x, gq.GQ_PATH_AUTO)
     q4_ref = oracle.quantize_q4_0(w)
@@ -294,3 +296,47 @@ def test_tuned_dispatch_profile(oracle):
             assert_within(dst, ref, T, what=f"auto M={M}")
     finally:
         gq.gq_clear_dispatch_profiles()
+
+
+def test_failed_workspace_growth_keeps_the_current_buffer(oracle):
+    """A growth of the stream's workspace whose cudaMalloc fails returns GQ_ERR_NO_MEMORY and
+    leaves the current workspace in place: products that fit it still run correctly on it."""
+    s = torch.cuda.Stream()
+    M, N, K = 9, 300, 4096
+    w, x = synth.problem(90, M, N, K)
+    rep = gq.repack_q4_0(gq.quantize_q4_0(dev(w)), N, K)
+    gq.gq_reserve_workspace(M, N, K, stream=s)
+    with pytest.raises(gq.GQError) as e:
+        gq.gq_reserve_workspace(1 << 30, 16, 1024, stream=s)   # 2 TiB of tile-path activations
+    assert e.value.status == gq.GQ_ERR_NO_MEMORY
+    xd = dev(x)
+    out = torch.full((M, N), float("nan"), device="cuda")
+    with torch.cuda.stream(s):
+        gq.gq_mul_mat_q4_0_f32_path(rep, xd, out, M, N, K, gq.GQ_PATH_GEMV, stream=s)
+    s.synchronize()
+    q4_ref = oracle.quantize_q4_0(w)
+    ref, T = oracle.mul_mat_q4_0_f32(q4_ref, x)
+    got = out.cpu().numpy()
+    assert_within(got, ref, T, what="after a failed growth")
+    assert np.all(np.abs(got.astype(np.float64) - ref) <= exact_dot_bound(oracle, q4_ref, x))
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_concatenated_decode_products_full_size(oracle, M):
+    """The fused decode products of the 32-layer stack: Q|K|V (three 4096 x 4096 matrices,
+    12,288 rows) and gate|up (two 11008 x 4096 matrices, 22,016 rows) as one product over the
+    concatenated repacked buffers, 2048 sampled outputs each against the oracle."""
+    K = 4096
+    for Ns, seed in (((4096, 4096, 4096), 700), ((11008, 11008), 710)):
+        ws = [synth.weights(seed + i, N, K) for i, N in enumerate(Ns)]
+        reps = [gq.repack_q4_0(gq.quantize_q4_0(dev(w)), N, K) for w, N in zip(ws, Ns)]
+        both = gq.concat_rows_q4_0(reps, Ns, K)
+        del reps
+        Nt = sum(Ns)
+        x = synth.activations(seed + 9 + M, M, K)
+        dst = host(gq.mul_mat_q4_0_f32(both, dev(x), Nt))
+        q4 = np.concatenate([oracle.quantize_q4_0(w) for w in ws])
+        rng = np.random.default_rng(seed + M)
+        ms, ns = rng.integers(0, M, 2048), rng.integers(0, Nt, 2048)
+        ref, T = oracle.mul_mat_q4_0_q8_0_at(q4, oracle.quantize_q8_0(x), ms, ns)
+        assert_within(dst[ms, ns], ref, T, what=f"concatenated {Nt} x {K}, M = {M}")

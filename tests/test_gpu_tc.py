@@ -65,7 +65,7 @@ def test_tc_f16(oracle, M, N, K, seed):
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 11008, 4096), (128, 11008, 4096), (512, 4096, 4096), (128, 4096, 11008),
-                                   (256, 11008, 4096)])
+                                   (256, 11008, 4096), (64, 4096, 4096), (128, 4096, 4096), (512, 11008, 4096)])
 def test_tc_full_size_sampled(oracle, M, N, K):
     """The prefill shapes, outliers included, in the configuration the benchmark times (auto dispatch);
     M = 256 on 11008 rows takes the 256-wide activation tile."""
