@@ -328,6 +328,13 @@ __device__ __forceinline__ uint32_t map_shared_rank(const void *smem_ptr, uint32
     return r;
 }
 
+// The same, from a shared-memory address of this CTA.
+__device__ __forceinline__ uint32_t map_shared_rank_addr(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");

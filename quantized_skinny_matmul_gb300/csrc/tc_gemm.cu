@@ -28,6 +28,9 @@
 // per stage) is waiting for.  The MMAs of a stage rotate over 2 (BN >= 128) or 4
 // independent accumulators in tensor memory, so consecutive MMAs do not wait
 // for each other's results; the epilogue adds them in a fixed order.
+// When the output tiles are too few to occupy the GPU, K is split over a cluster
+// of 2, 4 or 8 CTAs along z: each accumulates its K range, and the cluster adds
+// the partial tiles in a fixed order through distributed shared memory.
 // The activations are quantized first by a small kernel into a workspace copy
 // B[m][k] = fp16(q8 * d8) (Q4_0), or rounded to fp16 (F16): the same Q8_0
 // values as the GEMV path, each rounded once to fp16, so the result is within
@@ -35,7 +38,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
+#include <cstdlib>
 #include <mutex>
 
 #include "gq_common.cuh"
@@ -67,6 +72,8 @@ struct TcLayout {
     static constexpr int NACC = BN >= 128 ? 2 : 4;          // accumulators in tensor memory
     static constexpr uint32_t TMEM_COLS = NACC * BN;         // 128, 256 or 512: a power of two >= 32
     static constexpr int B_STAGE = BN * BK * 2;
+    static constexpr int PSTRIDE = BN + 4;                   // floats per row of a split-K partial
+    static constexpr bool CAN_SPLIT = BM * PSTRIDE * 4 <= ST * A_STAGE;   // the partial fits the operand memory
     static constexpr int a = 0;
     static constexpr int b = a + ST * A_STAGE;
     static constexpr int raw = b + ST * B_STAGE;
@@ -202,7 +209,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * BN, n0 = blockIdx.y * BM;
-    const int NT = p.NT;
+    // split-K: CTA z of the cluster along z takes k steps [kt0, kt0 + NT) of the p.NT steps
+    const int S = (int)gridDim.z, z = (int)blockIdx.z;
+    const int kt0 = (int)((int64_t)p.NT * z / S), NT = (int)((int64_t)p.NT * (z + 1) / S) - kt0;
     auto bar = [&](int i) { return smem_addr(bars + i); };
 
     if (threadIdx.x == 0) {
@@ -242,15 +251,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (kt >= RAW) wait_or_fail(bar(RAW_EMPTY + rs), (uint32_t)((kt / RAW - 1) & 1), failed, p.status);
                     if (failed) break;
                     mbar_arrive_expect_tx(bar(RAW_FULL + rs), (uint32_t)RAW_STAGE);
-                    tma_load_2d(smem_addr(smem + L::raw + rs * RAW_STAGE), &map_a, kt * RAW_WORDS, n0 / 16,
+                    tma_load_2d(smem_addr(smem + L::raw + rs * RAW_STAGE), &map_a, (kt0 + kt) * RAW_WORDS, n0 / 16,
                                 bar(RAW_FULL + rs));
                 } else {
                     const int st = kt % ST;
                     if (kt >= ST) wait_or_fail(bar(EMPTY + st), (uint32_t)((kt / ST - 1) & 1), failed, p.status);
                     if (failed) break;
                     mbar_arrive_expect_tx(bar(FULL + st), (uint32_t)A_STAGE);
-                    tma_load_2d(smem_addr(smem + L::a + st * A_STAGE), &map_a, kt * BK, n0, bar(FULL + st));
-                    tma_load_2d(smem_addr(smem + L::a + st * A_STAGE + ATOM_BYTES), &map_a, kt * BK + 64, n0,
+                    tma_load_2d(smem_addr(smem + L::a + st * A_STAGE), &map_a, (kt0 + kt) * BK, n0, bar(FULL + st));
+                    tma_load_2d(smem_addr(smem + L::a + st * A_STAGE + ATOM_BYTES), &map_a, (kt0 + kt) * BK + 64, n0,
                                 bar(FULL + st));
                 }
             }
@@ -263,8 +272,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (kt >= ST) wait_or_fail(bar(EMPTY + st), (uint32_t)((kt / ST - 1) & 1), failed, p.status);
                 if (failed) break;
                 mbar_arrive_expect_tx(bar(FULL + st), (uint32_t)L::B_STAGE);
-                tma_load_2d(smem_addr(smem + L::b + st * L::B_STAGE), &map_b, kt * BK, m0, bar(FULL + st));
-                tma_load_2d(smem_addr(smem + L::b + st * L::B_STAGE + BN * 128), &map_b, kt * BK + 64, m0,
+                tma_load_2d(smem_addr(smem + L::b + st * L::B_STAGE), &map_b, (kt0 + kt) * BK, m0, bar(FULL + st));
+                tma_load_2d(smem_addr(smem + L::b + st * L::B_STAGE + BN * 128), &map_b, (kt0 + kt) * BK + 64, m0,
                             bar(FULL + st));
             }
         }
@@ -345,20 +354,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         // chunks h, h + 2, ... of 32, and adds the accumulators in order
         wait_or_fail(bar(ACC_FULL), 0u, failed, p.status);
         tc_fence_after();
-        const int q = warp & 3;
+    }
+    const int q = warp & 3, h = (threadIdx.x - 64) >> 7;   // (epilogue warps 2 .. 9)
+    const bool epi = warp >= 2 && warp < 2 + CONVERTER_WARPS;
+    // the tile's sums of this thread's row (weight row 32 q + lane) for columns c0 .. c0 + 31
+    auto read_acc = [&](const int c0, float (&v)[32]) {
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+#pragma unroll 1
+        for (int a = 1; a < L::NACC; a++) {
+            float u[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * BN + c0), u);
+#pragma unroll
+            for (int i = 0; i < 32; i++) v[i] += u[i];
+        }
+    };
+    if (S == 1) {
         const int row = n0 + 32 * q + lane;
-        if (!failed) {
+        if (epi && !failed) {
 #pragma unroll 1
             for (int c0 = 32 * h; c0 < BN; c0 += 64) {
                 float v[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
-#pragma unroll 1
-                for (int a = 1; a < L::NACC; a++) {
-                    float u[32];
-                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * BN + c0), u);
-#pragma unroll
-                    for (int i = 0; i < 32; i++) v[i] += u[i];
-                }
+                read_acc(c0, v);
                 if (row < p.N) {
 #pragma unroll
                     for (int i = 0; i < 32; i++) {
@@ -368,8 +384,46 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
         }
+    } else {
+        // Split-K: the S CTAs of the cluster each computed the partial sums of one tile over
+        // their K ranges.  Once every CTA's MMAs have completed (first cluster barrier: from then
+        // on the operand memory of every CTA is free), each CTA sends row r of its partial to CTA
+        // r / (128 / S), into that CTA's slot for it: buf[z][r % (128 / S)][columns].  After the
+        // second barrier CTA z adds its 128 / S rows over the S partials in the order
+        // z' = 0 .. S - 1, from its own shared memory, and stores them.  Every thread of every
+        // CTA passes both barriers; no CTA touches another's memory after the second.
+        const int R = BM / S;                            // S divides 128
+        cluster_sync();
+        if (epi && !failed) {
+            const int r = 32 * q + lane;
+#pragma unroll 1
+            for (int c0 = 32 * h; c0 < BN; c0 += 64) {
+                float v[32];
+                read_acc(c0, v);
+                const uint32_t dst_a = map_shared_rank_addr(
+                    smem_addr(smem + L::a) + (uint32_t)(((z * R + r % R) * L::PSTRIDE + c0) * 4), (uint32_t)(r / R));
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst_a + 4 * i), "f"(v[i]),
+                                 "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
+                                 : "memory");
+            }
+        }
+        cluster_sync();
+        if (epi && !failed) {
+            const int t = threadIdx.x - 64;              // 0 .. 255
+            const int rr = t % R, cstep = CONVERTER_WARPS * 32 / R;   // 256 / R column groups
+            const float *buf = reinterpret_cast<const float *>(smem + L::a);
+            const int n = n0 + R * z + rr;
+#pragma unroll 4
+            for (int c = t / R; c < BN; c += cstep) {
+                float v = 0.0f;
+                for (int zz = 0; zz < S; zz++) v += buf[(zz * R + rr) * L::PSTRIDE + c];
+                const int m = m0 + c;
+                if (m < p.M && n < p.N) p.dst[(size_t)m * p.N + n] = v;
+            }
+        }
     }
-
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -477,22 +531,55 @@ gq_status allow_tc_smem(Kernel kernel, int which, int bytes) {
     return st;
 }
 
+// Split-K factor for a grid of `tiles` output tiles of NT k steps: the largest power of two
+// S <= 8 with tiles * S CTAs in one wave (one CTA per SM) and at least 4 k steps per CTA
+// (Smallem, "La courbe, une première fois": split the common dimension when the output
+// tiles are too few to occupy the GPU; DeepSpeed-Inference notes, III.C.1).  GQ_TC_SPLIT
+// (1, 2, 4 or 8), when set, replaces it (a tuning and test switch).
+int split_for(int64_t tiles, int NT, bool can_split) {
+    if (!can_split) return 1;
+    const char *e = getenv("GQ_TC_SPLIT");
+    if (e && *e) {
+        const int f = atoi(e);
+        if (f == 1 || f == 2 || f == 4 || f == 8) return std::min(f, std::max(1, NT));
+    }
+    int S = 1;
+    while (S < 8 && tiles * 2 * S <= sm_count() && NT / (2 * S) >= 4) S *= 2;
+    return S;
+}
+
 template <int BN, bool QUANT>
 gq_status launch_tc(const CUtensorMap &mb, const CUtensorMap &ma, const TcParams &p, cudaStream_t s, int which) {
-    constexpr int smem = TcLayout<BN, QUANT>::total + 1024;
+    using L = TcLayout<BN, QUANT>;
+    constexpr int smem = L::total + 1024;
     auto kernel = tc_gemm_kernel<BN, QUANT>;
     gq_status st = allow_tc_smem(kernel, which, smem);
     if (st != GQ_OK) return st;
+    const int64_t gx = (p.M + BN - 1) / BN, gy = (p.N + BM - 1) / BM;
+    int S = split_for(gx * gy, p.NT, L::CAN_SPLIT);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.M + BN - 1) / BN), (unsigned)((p.N + BM - 1) / BM), 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    for (;;) {
+        cfg.gridDim = dim3((unsigned)gx, (unsigned)gy, (unsigned)S);
+        attr[1].val.clusterDim.x = 1;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = (unsigned)S;
+        cfg.numAttrs = S > 1 ? 2 : 1;
+        if (S == 1) break;
+        // the clusters of a split are co-scheduled on one GPC: keep the split only if every
+        // cluster of the grid is resident at once
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, kernel, &cfg) == cudaSuccess && (int64_t)active >= gx * gy) break;
+        cudaGetLastError();
+        S /= 2;
+    }
     return check_cuda(cudaLaunchKernelEx(&cfg, kernel, mb, ma, p), "tc_gemm launch");
 }
 

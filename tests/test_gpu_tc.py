@@ -99,3 +99,26 @@ def test_dispatch_threshold():
         assert np.array_equal(auto, gemv)
     finally:
         gq.gq_set_m_threshold(16)
+
+
+@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("M,N,K", [(40, 300, 4096), (32, 131, 3200), (100, 520, 2048), (128, 256, 4096)])
+def test_tc_split_k(oracle, monkeypatch, split, M, N, K):
+    """Split-K over a cluster of 2, 4 or 8 CTAs (forced with GQ_TC_SPLIT): ragged M and N, K
+    ranges of unequal length; within the tolerance of the oracle and within f32 reordering of
+    the unsplit tiles' result."""
+    w, x = synth.problem(600 + split + M, M, N, K, outliers=True)
+    rep = gq.repack_q4_0(gq.quantize_q4_0(dev(w)), N, K)
+    monkeypatch.setenv("GQ_TC_SPLIT", "1")
+    whole = host(gq.mul_mat_q4_0_f32(rep, dev(x), N, path=gq.GQ_PATH_TC))
+    monkeypatch.setenv("GQ_TC_SPLIT", str(split))
+    dst = host(gq.mul_mat_q4_0_f32(rep, dev(x), N, path=gq.GQ_PATH_TC))
+    again = host(gq.mul_mat_q4_0_f32(rep, dev(x), N, path=gq.GQ_PATH_TC))
+    assert np.array_equal(dst, again), "split-K result is not deterministic"
+    ref, T = oracle.mul_mat_q4_0_f32(oracle.quantize_q4_0(w), x)
+    assert_within(dst, ref, T, f"q4_0 tc split {split}")
+    assert np.all(np.abs(dst.astype(np.float64) - whole) <= 1e-5 * T + 1e-30), "split and unsplit tiles disagree"
+    wb = synth.f16_bits(w)
+    d16 = host(gq.mul_mat_f16_f32(dev(wb.view(np.int16)), dev(x), path=gq.GQ_PATH_TC))
+    ref16, T16 = oracle.mul_mat_f16_f32(wb, x)
+    assert_within(d16, ref16, T16, f"f16 tc split {split}")
