@@ -69,7 +69,8 @@ typedef enum gq_status {
 /* Which kernel family serves a product. */
 typedef enum gq_path {
     GQ_PATH_AUTO = 0,   /* the shape's dispatch profile, if one is set; else M <= threshold:
-                           the GEMV family, above it the tensor-core tiles */
+                           the GEMV family, above it the tensor-core tiles (Q4_0 rows also
+                           take the tiles when the GEMV would need several K slices for them) */
     GQ_PATH_GEMV = 1,   /* the skinny GEMV kernels (any M; M > 16 runs in 16-row slices) */
     GQ_PATH_TC = 2      /* the tcgen05 tensor-core tile kernels (any M) */
 } gq_path;
@@ -280,7 +281,10 @@ gq_status gq_mul_mat_f16_f32_path(const void *src0_f16, const float *src1, float
 
 /* M threshold of GQ_PATH_AUTO: M <= threshold runs the GEMV family.  Default 16
  * (Smallem, "Générer à plusieurs", section "La courbe, une première fois": the
- * narrow kernel serves products of at most 16 rows, the tiles the rest).
+ * narrow kernel serves products of at most 16 rows, the tiles the rest).  Q4_0
+ * products of 2 .. threshold rows whose activation image needs several K slices
+ * (one GEMV launch per slice, for example 9 to 16 rows at K = 11008) take the
+ * tiles, which split K within one launch.
  * Process-wide; GQ_ERR_INVALID_ARG if t < 0.  The environment variable
  * GQ_M_THRESHOLD, read when the library loads, replaces the default when it
  * holds a non-negative decimal integer (other values are ignored). */

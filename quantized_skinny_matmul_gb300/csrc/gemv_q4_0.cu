@@ -936,6 +936,12 @@ void gemv_workspace(int wf, int64_t N, int64_t K, size_t *counter_bytes, size_t 
     *data_bytes = db;
 }
 
+int gemv_q4_0_slices(int64_t N, int64_t K, int64_t M) {
+    const int N16 = (int)((N + 15) / 16);
+    const int NT = (int)((K + TILE_COLS - 1) / TILE_COLS);
+    return plan(N16, NT, (int)std::min<int64_t>(16, std::max<int64_t>(1, M))).S;
+}
+
 void gemv_q4_0_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes) {
     gemv_workspace(WF_Q4, N, K, counter_bytes, data_bytes);
 }

@@ -290,6 +290,10 @@ double interpolate(const std::vector<int64_t> &Ms, const std::vector<double> &t,
 // the M threshold (Smallem, "La courbe, une première fois": the narrow kernel up to 16
 // rows, tiles above; llama.cpp PR #1632, "Introduction": the M >= 32 rule and how
 // sensitive the choice is around it).
+//
+// Without a profile, Q4_0 rows also go to the tiles when the GEMV would need several K slices
+// for them (one launch per slice: measured slower than the split-K tiles, for example
+// 4096 x 11008 at M = 16: 28.0 against 20.9 us).  One row always takes the GEMV.
 static gq_path choose_path(int kind, int64_t N, int64_t K, int64_t M) {
     {
         std::lock_guard<std::mutex> lock(g_prof_mutex);
@@ -297,7 +301,9 @@ static gq_path choose_path(int kind, int64_t N, int64_t K, int64_t M) {
             if (pr.kind == kind && pr.N == N && pr.K == K)
                 return interpolate(pr.Ms, pr.t_tc, M) < interpolate(pr.Ms, pr.t_gemv, M) ? GQ_PATH_TC : GQ_PATH_GEMV;
     }
-    return M <= g_m_threshold.load() ? GQ_PATH_GEMV : GQ_PATH_TC;
+    if (M > g_m_threshold.load()) return GQ_PATH_TC;
+    if (kind == GQ_KIND_Q4_0 && M > 1 && gemv_q4_0_slices(N, K, M) > 1) return GQ_PATH_TC;
+    return GQ_PATH_GEMV;
 }
 
 static gq_path resolve(gq_path path, int kind, int64_t M, int64_t N, int64_t K) {

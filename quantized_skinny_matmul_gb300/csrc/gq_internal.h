@@ -44,6 +44,9 @@ gq_status launch_repack_q4_0(const void *q4, void *rep, int64_t N, int64_t K, cu
 
 gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N,
                            int64_t K, cudaStream_t s);
+// K slices the Q4_0 GEMV runs for M (up to 16) activation rows of an [N][K] weight (one launch
+// per slice for several rows).
+int gemv_q4_0_slices(int64_t N, int64_t K, int64_t M);
 // Workspace bytes (counters, data) the Q4_0 GEMV needs for an [N][K] weight.
 void gemv_q4_0_workspace(int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes);
 // The Q4_0 GEMV on a given workspace (counters zero on entry, left at zero).

@@ -290,13 +290,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t a_base = smem_addr(smem + L::a + st * A_STAGE);
-                const uint32_t b_base = smem_addr(smem + L::b + st * L::B_STAGE);
+                // The descriptors of the stage's operands; a K step of 16 halves inside a swizzle
+                // atom moves the start address by 32 bytes, an atom by its size: both are added to
+                // the descriptor's start-address field (address / 16, no carry out of the field).
+                const uint64_t ad0 = sw128_desc(smem_addr(smem + L::a + st * A_STAGE));
+                const uint64_t bd0 = sw128_desc(smem_addr(smem + L::b + st * L::B_STAGE));
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; kk++) {
-                    const uint32_t koff = (uint32_t)((kk & 3) * 32);
-                    const uint64_t ad = sw128_desc(a_base + (kk >> 2) * ATOM_BYTES + koff);
-                    const uint64_t bd = sw128_desc(b_base + (kk >> 2) * (BN * 128) + koff);
+                    const uint64_t ad = ad0 + (uint64_t)(((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4);
+                    const uint64_t bd = bd0 + (uint64_t)(((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
                     // accumulator kk % NACC; its first MMA overwrites it
                     mma_f16(tmem + (uint32_t)((kk % L::NACC) * BN), ad, bd, idesc,
                             (kt > 0 || kk >= L::NACC) ? 1u : 0u);

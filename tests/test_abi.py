@@ -184,3 +184,20 @@ def test_build_rejects_a_library_for_another_cpu(tmp_path):
         f.write_bytes(b"\x7fELF" + bytes(14) + machine.to_bytes(2, "little") + bytes(44))
         assert _build.built_for_this_machine(str(f)) is want
     assert _build.built_for_this_machine(str(tmp_path / "missing.so")) is False
+
+
+def test_dispatch_takes_the_tiles_when_the_gemv_needs_several_slices(lib):
+    """Without a profile, Q4_0 products of up to 16 rows take the GEMV unless its activation
+    image needs several K slices for them (one launch per slice), as at K = 11008 with 9 or more
+    rows; one row always takes the GEMV (no GPU involved)."""
+    gq.gq_clear_dispatch_profiles()
+    Q = gq.GQ_KIND_Q4_0
+    for M in (1, 2, 8):
+        assert gq.gq_choose_path(Q, 4096, 11008, M) == gq.GQ_PATH_GEMV, M
+    for M in (9, 12, 16, 17, 64):
+        assert gq.gq_choose_path(Q, 4096, 11008, M) == gq.GQ_PATH_TC, M
+    for N, K in ((4096, 4096), (11008, 4096)):
+        for M in (1, 8, 16):
+            assert gq.gq_choose_path(Q, N, K, M) == gq.GQ_PATH_GEMV, (N, K, M)
+        assert gq.gq_choose_path(Q, N, K, 17) == gq.GQ_PATH_TC
+    assert gq.gq_choose_path(Q, 64, 100000, 1) == gq.GQ_PATH_GEMV
