@@ -1,4 +1,5 @@
-"""The CPU oracle for the quantized skinny MUL_MAT -- test infrastructure.
+"""The CPU oracle for the quantized skinny MUL_MAT and the INT8 KV-cache decode
+attention -- test infrastructure.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg may import this package.  The product library (``quantized_skinny_matmul_gb300``)
@@ -95,6 +96,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "oracle_mul_mat_f16_f32_at": ([P, P, P, P, I, I, P, P], None),
         "oracle_f32_to_f16_array": ([P, P, I], None),
         "oracle_f16_to_f32_array": ([P, P, I], None),
+        "oracle_kv_quantize_i8": ([P, P, P, I, I], None),
+        "oracle_kv_dequantize_i8": ([P, P, P, I, I], None),
+        "oracle_attn_decode_i8": ([P, P, P, P, P, P, ctypes.c_double, P, P, P, I, I, I, I, I],
+                                  ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -385,6 +390,54 @@ class Oracle:
         self.lib.oracle_mul_mat_f16_f32_at(_ptr(w), _ptr(src1), _ptr(ms), _ptr(ns), ms.size,
                                            w.shape[1], _ptr(out), _ptr(T))
         return out, T
+
+    # -- INT8 KV cache ----------------------------------------------------
+    def kv_quantize_i8(self, x):
+        """f32 [..., D] -> (int8 codes [..., D], f32 scales [...]): one scale per row of D."""
+        x = _c(x, np.float32)
+        D = x.shape[-1]
+        rows = x.size // D if D else 0
+        q = np.empty(x.shape, np.int8)
+        s = np.empty(x.shape[:-1], np.float32)
+        self.lib.oracle_kv_quantize_i8(_ptr(x), _ptr(q), _ptr(s), rows, D)
+        return q, s
+
+    def kv_dequantize_i8(self, q, s) -> np.ndarray:
+        """f64 [..., D]: codes times their row's scale."""
+        q = _c(q, np.int8)
+        s = _c(s, np.float32)
+        D = q.shape[-1]
+        assert s.shape == q.shape[:-1]
+        out = np.empty(q.shape, np.float64)
+        self.lib.oracle_kv_dequantize_i8(_ptr(q), _ptr(s), _ptr(out), q.size // D if D else 0, D)
+        return out
+
+    def attn_decode_i8(self, q, k, ks, v, vs, lens, c):
+        """Decode attention over an INT8 cache: (out, E) f64 [B, Hq, D] and S f64 [B, Hq].
+
+        q f32 [B, Hq, D]; k, v int8 [B, Hkv, Tcap, D]; ks, vs f32 [B, Hkv, Tcap];
+        lens int32 [B]; c the softmax scale.
+        """
+        q = _c(q, np.float32)
+        k, v = _c(k, np.int8), _c(v, np.int8)
+        ks, vs = _c(ks, np.float32), _c(vs, np.float32)
+        lens = _c(lens, np.int32)
+        B, Hq, D = q.shape
+        _, Hkv, Tcap, _ = k.shape
+        assert k.shape == v.shape == (B, Hkv, Tcap, D)
+        assert ks.shape == vs.shape == (B, Hkv, Tcap) and lens.shape == (B,)
+        out = np.zeros((B, Hq, D), np.float64)
+        E = np.zeros((B, Hq, D), np.float64)
+        S = np.zeros((B, Hq), np.float64)
+        rc = self.lib.oracle_attn_decode_i8(_ptr(q), _ptr(k), _ptr(ks), _ptr(v), _ptr(vs),
+                                            _ptr(lens), float(c), _ptr(out), _ptr(E), _ptr(S),
+                                            B, Hq, Hkv, Tcap, D)
+        if rc == -2:
+            raise MemoryError("oracle_attn_decode_i8: allocation failed")
+        if rc != 0:
+            raise ValueError("oracle_attn_decode_i8: Hq must be a multiple of Hkv and "
+                             "0 <= lens[b] <= Tcap")
+        return out, E, S
 
 
 _default: Oracle | None = None

@@ -33,6 +33,9 @@
  *   with the f32 d; fp16(d) is IEEE round-to-nearest-even and is the scale
  *   that is stored and used to de-quantize.
  *
+ * The end of the file holds the INT8 KV cache (per-token, per-head scales) and
+ * the decode attention over it; its own header there says what it follows.
+ *
  * Floating point: the quantizers decide integer codes, so they work in f32 as
  * the kernels do (the operands are F32).  Everything that is a sum is formed
  * in f64: each term d4 * d8 * sumi is exact in f64 (11 + 11 + 16 bits), so the
@@ -693,4 +696,131 @@ void oracle_f32_to_f16_array(const float *x, uint16_t *out, int64_t n)
 void oracle_f16_to_f32_array(const uint16_t *h, float *out, int64_t n)
 {
     for (int64_t i = 0; i < n; i++) out[i] = oracle_f16_to_f32(h[i]);
+}
+
+/* ---------------------------------------------------------------------------
+ * The INT8 KV cache and the decode attention that reads it.
+ *
+ * xFasterTransformer (arXiv 2407.07304), "2.2 Effective KV cache
+ * Optimization": after the first token, attention over the cache is a pair of
+ * memory-bound GEMVs; the cache is stored as INT8 with its own scale for each
+ * token and each head, and the INT8 operand is widened to FP32 before the
+ * multiply-add.  Section "2.1 LLM Optimization" (SlimAttention) fixes the
+ * order for one query row: the whole row of scores first, then the softmax
+ * over it, then the product of the softmax with the values.
+ *
+ * The page gives the granularity of the scale but not its formula.  This
+ * library reads it like the Q8_0 scale above: for the D values x[0..D-1] of
+ * one token and one head, s = amax / 127 in f32, q_j = round(x_j / s) (IEEE f32
+ * division, ties away from zero; 0 when s == 0), and the cached value is
+ * q_j * s.  Inputs must be finite.
+ *
+ * Layouts: codes int8 [B][Hkv][Tcap][D], scales f32 [B][Hkv][Tcap], queries
+ * f32 [B][Hq][D] with Hq = G * Hkv (grouped queries: query head h reads KV
+ * head h / G), lens int32 [B] with 0 <= lens[b] <= Tcap, output [B][Hq][D].
+ * For query head h of sequence b, over the tokens t < lens[b]:
+ *     score_t = c * ks_t * sum_j q_j * k_tj          (c: the softmax scale)
+ *     p_t     = exp(score_t - max_u score_u) / sum_u exp(score_u - max_u score_u)
+ *     out_j   = sum_t p_t * vs_t * v_tj
+ * and an empty sequence gives out = 0.  Every sum is formed in f64 (each
+ * product q_j * k_tj of an f32 and an int8 is exact there).  For error bounds
+ * the oracle also returns E[b][h][j] = sum_t p_t * |vs_t * v_tj| and
+ * S[b][h] = max_t |c * ks_t| * sum_j |q_j * k_tj|.
+ * ------------------------------------------------------------------------- */
+void oracle_kv_quantize_i8(const float *x, int8_t *q, float *scale, int64_t rows, int64_t D)
+{
+    for (int64_t r = 0; r < rows; r++) {
+        const float *xr = x + r * D;
+        float amax = 0.0f;
+        for (int64_t j = 0; j < D; j++) {
+            float a = fabsf(xr[j]);
+            if (a > amax) amax = a;
+        }
+        float s = amax / 127.0f;
+        scale[r] = s;
+        for (int64_t j = 0; j < D; j++) {
+            int v = 0;
+            if (s != 0.0f) {
+                v = (int)roundf(xr[j] / s);
+                v = v < -127 ? -127 : (v > 127 ? 127 : v);
+            }
+            q[r * D + j] = (int8_t)v;
+        }
+    }
+}
+
+void oracle_kv_dequantize_i8(const int8_t *q, const float *scale, double *out, int64_t rows,
+                             int64_t D)
+{
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t j = 0; j < D; j++)
+            out[r * D + j] = (double)q[r * D + j] * (double)scale[r];
+}
+
+int oracle_attn_decode_i8(const float *q, const int8_t *k, const float *ks, const int8_t *v,
+                          const float *vs, const int32_t *lens, double c, double *out,
+                          double *E, double *S, int64_t B, int64_t Hq, int64_t Hkv,
+                          int64_t Tcap, int64_t D)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0)
+        return -1;
+    int64_t G = Hq / Hkv;
+    double *p = (double *)malloc((size_t)(Tcap > 0 ? Tcap : 1) * sizeof(double));
+    if (!p)
+        return -2;
+    for (int64_t b = 0; b < B; b++) {
+        int64_t L = lens[b];
+        if (L < 0 || L > Tcap) {
+            free(p);
+            return -1;
+        }
+        for (int64_t h = 0; h < Hq; h++) {
+            int64_t hk = h / G;
+            const float *qv = q + (b * Hq + h) * D;
+            const int8_t *kb = k + (b * Hkv + hk) * Tcap * D;
+            const int8_t *vb = v + (b * Hkv + hk) * Tcap * D;
+            const float *ksb = ks + (b * Hkv + hk) * Tcap;
+            const float *vsb = vs + (b * Hkv + hk) * Tcap;
+            double *o = out + (b * Hq + h) * D;
+            double *e = E + (b * Hq + h) * D;
+            double smax = 0.0;
+            /* the row of scores */
+            for (int64_t t = 0; t < L; t++) {
+                double dot = 0.0, adot = 0.0;
+                for (int64_t j = 0; j < D; j++) {
+                    double term = (double)qv[j] * (double)kb[t * D + j];
+                    dot += term;
+                    adot += fabs(term);
+                }
+                p[t] = c * (double)ksb[t] * dot;
+                double a = fabs(c * (double)ksb[t]) * adot;
+                if (a > smax) smax = a;
+            }
+            S[b * Hq + h] = smax;
+            /* the softmax over it */
+            double m = -INFINITY;
+            for (int64_t t = 0; t < L; t++)
+                if (p[t] > m) m = p[t];
+            double l = 0.0;
+            for (int64_t t = 0; t < L; t++) {
+                p[t] = exp(p[t] - m);
+                l += p[t];
+            }
+            for (int64_t t = 0; t < L; t++)
+                p[t] /= l;
+            /* its product with the values */
+            for (int64_t j = 0; j < D; j++) {
+                double acc = 0.0, eacc = 0.0;
+                for (int64_t t = 0; t < L; t++) {
+                    double term = p[t] * (double)vsb[t] * (double)vb[t * D + j];
+                    acc += term;
+                    eacc += fabs(term);
+                }
+                o[j] = acc;
+                e[j] = eacc;
+            }
+        }
+    }
+    free(p);
+    return 0;
 }

@@ -16,6 +16,13 @@ What pins what:
                                    operands (textbook special case), structured
                                    weights with closed-form results, and the
                                    row independence of the batched product
+  * the INT8 KV quantizer       -> worked examples in golden/, exact round trips of
+                                   representable rows, the de-quantization bound
+  * the decode attention        -> textbook attention on the de-quantized cache (numpy
+                                   matmul and scipy's softmax), and special cases with
+                                   closed forms: one token, equal keys, a zero softmax
+                                   scale, an empty sequence, a dominant score far beyond
+                                   exp's range, tokens past the length, a permutation
 """
 from __future__ import annotations
 
@@ -130,6 +137,9 @@ def pin_worked_examples(o) -> None:
             got = o.quantize_q5_0(x.reshape(1, 32)).tobytes()
         elif kind == "q4_1":
             got = o.quantize_q4_1(x.reshape(1, 32)).tobytes()
+        elif kind == "kv_i8":
+            codes, scale = o.kv_quantize_i8(x.reshape(1, 32))
+            got = scale.astype("<f4").tobytes() + codes.tobytes()
         else:
             got = o.quantize_q8_0(x.reshape(1, 32)).tobytes()
         assert got == want, f"{name}: {got.hex(' ')} != {want.hex(' ')}"
@@ -534,6 +544,134 @@ def pin_q8_0_matmul_vs_dense(o) -> None:
             assert np.array_equal(one[0], dst[m])
 
 
+# ---------------------------------------------------------------------------
+# INT8 KV cache (xFasterTransformer, "2.2 Effective KV cache Optimization")
+# ---------------------------------------------------------------------------
+def pin_kv_quantizer(o) -> None:
+    rng = np.random.default_rng(31)
+    # rows c * 2^e with a +-127 code present quantize to exactly c with scale 2^e
+    R, D = 96, 128
+    c = rng.integers(-127, 128, size=(R, D))
+    c[np.arange(R), rng.integers(D, size=R)] = 127 * np.where(rng.random(R) < 0.5, 1, -1)
+    e = rng.integers(-20, 6, size=(R, 1))
+    x = (c * np.exp2(e)).astype(np.float32)
+    codes, scale = o.kv_quantize_i8(x)
+    assert np.array_equal(codes.astype(np.int64), c)
+    assert np.array_equal(scale.astype(np.float64), np.exp2(e[:, 0]).astype(np.float64))
+    # Gaussian rows with a wide spread of magnitudes: range, the f32 scale recomputed
+    # from its definition, and the round-to-nearest error bound
+    x = rng.standard_normal((R, D)).astype(np.float32) * np.exp2(rng.integers(-30, 30, size=(R, 1))).astype(np.float32)
+    x[0] = 0.0
+    codes, scale = o.kv_quantize_i8(x)
+    assert codes.min() >= -127 and codes.max() <= 127
+    want_s = np.abs(x).max(-1) / np.float32(127.0)
+    assert np.array_equal(scale, want_s)
+    xd = x.astype(np.float64)
+    err = np.abs(xd - codes.astype(np.float64) * scale[:, None].astype(np.float64))
+    assert np.all(err <= scale[:, None].astype(np.float64) * (0.5 + 1e-6)), "INT8 KV bound"
+    amax_at = np.argmax(np.abs(x), axis=-1)
+    assert np.all(np.abs(codes[np.arange(1, R), amax_at[1:]]) == 127)
+    assert scale[0] == 0 and np.all(codes[0] == 0)
+    deq = o.kv_dequantize_i8(codes, scale)
+    assert np.array_equal(deq, codes.astype(np.float64) * scale[:, None].astype(np.float64))
+
+
+def _kv_case(rng, B, Hkv, Tcap, D, key_scale=1.0):
+    k = rng.integers(-127, 128, size=(B, Hkv, Tcap, D)).astype(np.int8)
+    v = rng.integers(-127, 128, size=(B, Hkv, Tcap, D)).astype(np.int8)
+    ks = (np.exp(rng.standard_normal((B, Hkv, Tcap)) * 0.3) * key_scale / 127).astype(np.float32)
+    vs = (np.exp(rng.standard_normal((B, Hkv, Tcap)) * 0.3) / 127).astype(np.float32)
+    return k, ks, v, vs
+
+
+def _textbook_attention(q, k, ks, v, vs, lens, c):
+    """Scaled dot-product attention of each query row over the de-quantized cache."""
+    from scipy.special import softmax
+    B, Hq, D = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    Kd = k.astype(np.float64) * ks[..., None].astype(np.float64)
+    Vd = v.astype(np.float64) * vs[..., None].astype(np.float64)
+    out = np.zeros((B, Hq, D))
+    E = np.zeros((B, Hq, D))
+    for b in range(B):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        for h in range(Hq):
+            kv = h // G
+            p = softmax(c * (Kd[b, kv, :L] @ q[b, h].astype(np.float64)))
+            out[b, h] = p @ Vd[b, kv, :L]
+            E[b, h] = p @ np.abs(Vd[b, kv, :L])
+    return out, E
+
+
+def pin_attn_vs_textbook(o) -> None:
+    rng = np.random.default_rng(32)
+    for (B, Hq, Hkv, Tcap, D, lens) in ((3, 4, 2, 37, 64, [37, 1, 20]),
+                                        (2, 8, 8, 50, 128, [50, 33]),
+                                        (1, 6, 1, 9, 32, [9])):
+        k, ks, v, vs = _kv_case(rng, B, Hkv, Tcap, D, key_scale=2.0)
+        q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+        lens = np.array(lens, np.int32)
+        c = 1.0 / np.sqrt(D)
+        out, E, S = o.attn_decode_i8(q, k, ks, v, vs, lens, c)
+        want, E_want = _textbook_attention(q, k, ks, v, vs, lens, c)
+        assert np.all(np.abs(out - want) <= 1e-12 * E_want + 1e-300), "attention vs textbook"
+        assert np.allclose(E, E_want, rtol=1e-12, atol=0)
+        # S: the largest absolute score magnitude bound over the tokens
+        G = Hq // Hkv
+        for b in range(B):
+            for h in range(Hq):
+                L = int(lens[b])
+                terms = np.abs(q[b, h].astype(np.float64) * k[b, h // G, :L].astype(np.float64))
+                want_s = (c * ks[b, h // G, :L].astype(np.float64) * terms.sum(-1)).max(initial=0.0)
+                assert np.isclose(S[b, h], want_s, rtol=1e-12, atol=0)
+
+
+def pin_attn_special_cases(o) -> None:
+    rng = np.random.default_rng(33)
+    B, Hq, Hkv, Tcap, D = 5, 4, 2, 24, 64
+    k, ks, v, vs = _kv_case(rng, B, Hkv, Tcap, D)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    c = 1.0 / np.sqrt(D)
+    Vd = v.astype(np.float64) * vs[..., None].astype(np.float64)
+    # sequence 0: one token, p = 1 exactly
+    # sequence 1: every token has the same key codes and scale, so p is uniform
+    k[1] = k[1, :, :1]
+    ks[1] = ks[1, :, :1]
+    # sequence 2: empty; sequence 3: full; sequence 4: one score far beyond exp's range
+    k[4], ks[4] = 0, np.float32(1.0)
+    k[4, :, 7] = 127
+    lens = np.array([1, Tcap, 0, Tcap, Tcap], np.int32)
+    q[4] = np.abs(q[4]) + np.float32(1.0)           # score of token 7 >= 127 * 64 * c, others 0
+    out, E, S = o.attn_decode_i8(q, k, ks, v, vs, lens, c)
+    G = Hq // Hkv
+    for h in range(Hq):
+        assert np.array_equal(out[0, h], Vd[0, h // G, 0])
+        assert np.allclose(out[1, h], Vd[1, h // G].mean(0), rtol=1e-12, atol=1e-15)
+        assert np.array_equal(out[4, h], Vd[4, h // G, 7])
+    assert np.all(out[2] == 0) and np.all(E[2] == 0)
+    # a zero softmax scale gives the plain mean of the values
+    out0, _, _ = o.attn_decode_i8(q, k, ks, v, vs, lens, 0.0)
+    for h in range(Hq):
+        assert np.allclose(out0[3, h], Vd[3, h // G].mean(0), rtol=1e-12, atol=1e-15)
+    # tokens past the length take no part, whatever they hold
+    lens2 = lens.copy()
+    lens2[3] = 10
+    k2, v2 = k.copy(), v.copy()
+    k2[3, :, 10:] = 127
+    v2[3, :, 10:] = -127
+    a, _, _ = o.attn_decode_i8(q, k, ks, v, vs, lens2, c)
+    b, _, _ = o.attn_decode_i8(q, k2, ks, v2, vs, lens2, c)
+    assert np.array_equal(a[3], b[3])
+    # permuting the tokens (with their scales) leaves the output unchanged up to rounding
+    perm = rng.permutation(Tcap)
+    kp, ksp, vp, vsp = k[:, :, perm], ks[:, :, perm], v[:, :, perm], vs[:, :, perm]
+    outp, _, _ = o.attn_decode_i8(q, kp, ksp, vp, vsp, lens, c)
+    assert np.all(np.abs(outp[3] - out[3]) <= 1e-12 * E[3] + 1e-300)
+
+
 ALL_PINS = [
     pin_f16_conversion,
     pin_worked_examples,
@@ -551,4 +689,7 @@ ALL_PINS = [
     pin_q5_0_block_dot_and_product,
     pin_q4_1_quantizer,
     pin_q4_1_block_sums_and_product,
+    pin_kv_quantizer,
+    pin_attn_vs_textbook,
+    pin_attn_special_cases,
 ]

@@ -58,6 +58,22 @@ MUTANTS = {
     "q41_min_term_dropped": ("        acc += mn * d8 * (double)sums[1];\n", ""),
     "q41_divisor": ("float d = (hi - lo) / 15.0f;", "float d = (hi - lo) / 16.0f;"),
     "q41_offset_from_max": ("int v = (int)roundf((x[j] - lo) / d);", "int v = (int)roundf((x[j] - hi) / d) + 15;"),
+    "kv_divisor": ("float s = amax / 127.0f;", "float s = amax / 128.0f;"),
+    "kv_round_even": ("v = (int)roundf(xr[j] / s);", "v = (int)rintf(xr[j] / s);"),
+    "kv_scale_through_fp16": ("float s = amax / 127.0f;\n        scale[r] = s;",
+                              "float s = oracle_f16_to_f32(oracle_f32_to_f16(amax / 127.0f));\n        scale[r] = s;"),
+    "attn_key_scale_dropped": ("p[t] = c * (double)ksb[t] * dot;", "p[t] = c * dot;"),
+    "attn_value_scale_from_keys": ("double term = p[t] * (double)vsb[t] * (double)vb[t * D + j];",
+                                   "double term = p[t] * (double)ksb[t] * (double)vb[t * D + j];"),
+    "attn_values_from_keys": ("double term = p[t] * (double)vsb[t] * (double)vb[t * D + j];",
+                              "double term = p[t] * (double)vsb[t] * (double)kb[t * D + j];"),
+    "attn_group_map": ("int64_t hk = h / G;", "int64_t hk = h % Hkv;"),
+    "attn_last_token_dropped": ("for (int64_t t = 0; t < L; t++) {\n                double dot = 0.0, adot = 0.0;",
+                                "for (int64_t t = 0; t + 1 < L; t++) {\n                double dot = 0.0, adot = 0.0;"),
+    "attn_no_max_shift": ("p[t] = exp(p[t] - m);", "p[t] = exp(p[t]);"),
+    "attn_unnormalized": ("            for (int64_t t = 0; t < L; t++)\n                p[t] /= l;\n", ""),
+    "attn_key_row_stride": ("double term = (double)qv[j] * (double)kb[t * D + j];",
+                            "double term = (double)qv[j] * (double)kb[(t * D + j * 7) % (L * D)];"),
     "q8_abs_dropped": ("float a = fabsf(x[j]);\n        if (a > amax) amax = a;",
                        "float a = x[j];\n        if (a > amax) amax = a;"),
 }
