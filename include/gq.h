@@ -85,9 +85,10 @@ const char *gq_status_string(gq_status status); /* static text, never NULL */
 const char *gq_last_error_message(void);
 
 /* Sticky device-side status of the current device: GQ_ERR_TIMEOUT if a kernel
- * gave up a bounded wait since the last call, else GQ_OK; reading clears it and,
- * after a timeout, re-zeroes the workspace counters of the device.
- * Synchronizes the current device first. */
+ * gave up a bounded wait since the last call, else GQ_ERR_INVALID_ARG if a
+ * length or position read on the device was out of range (the INT8 KV-cache
+ * calls), else GQ_OK; reading clears it and, after a timeout, re-zeroes the
+ * workspace counters of the device.  Synchronizes the current device first. */
 gq_status gq_last_error(void);
 
 /* ---- buffer sizes --------------------------------------------------------- */
@@ -340,6 +341,58 @@ gq_status gq_mul_mat_q4_0_f32_noalloc(const void *q4_repacked, const float *src1
  * every earlier kernel in the stream has finished.  Process-wide. */
 gq_status gq_set_static_weights(int enable);
 int gq_get_static_weights(void);
+
+/* ---- INT8 KV cache and the decode attention over it -------------------------------
+ *
+ * xFasterTransformer (arXiv 2407.07304), "2.2 Effective KV cache Optimization":
+ * the KV cache is stored as INT8 with its own scale for each token and each head,
+ * and after the first token attention is a pair of memory-bound GEMVs whose INT8
+ * operand is widened to FP32 before the multiply-add.  Section "2.1 LLM
+ * Optimization" (SlimAttention) fixes the order for a query row: all its scores,
+ * the softmax over them, then their product with the values.
+ *
+ * Scale (the page does not give its formula; this library reads it like Q8_0's):
+ * for the D values x[0..D-1] of one token and one head, s = amax / 127 in f32,
+ * kept as f32; q_j = roundf(x_j / s) (IEEE f32 division, ties away from zero),
+ * or 0 when s == 0.  The cached value is q_j * s.
+ *
+ * Layouts (row-major, last index contiguous; all DEVICE pointers, 16-byte aligned):
+ *   cache codes  int8  [B][Hkv][Tcap][D]   (one array for K, one for V)
+ *   cache scales float [B][Hkv][Tcap]
+ *   queries      float [B][Hq][D], Hq = G * Hkv; query head h reads KV head h / G
+ *   lens, pos    int32 [B]
+ *   output       float [B][Hq][D]
+ * Sizes: D is 64 or 128; G is 1, 2, 4 or 8; B, Hkv, Tcap positive with
+ * B * Hkv * Tcap * D < 2^40 and Tcap < 2^30.  Other sizes: GQ_ERR_INVALID_ARG. */
+
+/* Quantizes `rows` rows of D f32 values x [rows][D] into codes q [rows][D] and
+ * scales scale [rows] (for example a prefill's K or V, laid out as the cache). */
+gq_status gq_kv_quantize_i8(const float *x, int8_t *q, float *scale, int64_t rows, int64_t D,
+                            cudaStream_t stream);
+
+/* Appends one token per sequence: row (b, h) of x [B][Hkv][D] is quantized into
+ * position pos[b] of the cache (codes [B][Hkv][Tcap][D], scales [B][Hkv][Tcap]).
+ * pos is read on the device; a pos[b] outside [0, Tcap) skips that sequence and
+ * makes the next gq_last_error() return GQ_ERR_INVALID_ARG. */
+gq_status gq_kv_append_i8(const float *x, int8_t *q, float *scale, const int32_t *pos,
+                          int64_t B, int64_t Hkv, int64_t Tcap, int64_t D, cudaStream_t stream);
+
+/* Decode attention of one query row per (sequence, query head) over the INT8 cache:
+ * for query head h of sequence b, over the tokens t < lens[b] of KV head h / G,
+ *     score_t = softmax_scale * ks_t * sum_j q_j * k_tj
+ *     out_j   = sum_t softmax(score)_t * vs_t * v_tj
+ * with f32 arithmetic (INT8 widened exactly to f32) and a softmax that subtracts
+ * the row's maximum.  lens[b] == 0 gives a zero row.  lens is read on the
+ * device: a value outside [0, Tcap] is taken as 0 and makes the next
+ * gq_last_error() return GQ_ERR_INVALID_ARG.  Long caches, or too few
+ * (sequence, KV head) pairs to fill the GPU, split a sequence's tokens over
+ * several CTAs whose parts are merged in a fixed order in the stream's
+ * workspace (grown on demand, as for the products; GQ_ERR_NO_MEMORY if that
+ * fails).  Results are deterministic. */
+gq_status gq_attn_decode_i8(const float *q, const int8_t *k, const float *k_scale,
+                            const int8_t *v, const float *v_scale, const int32_t *lens,
+                            float *out, int64_t B, int64_t Hq, int64_t Hkv, int64_t Tcap,
+                            int64_t D, float softmax_scale, cudaStream_t stream);
 
 /* ---- verification --------------------------------------------------------------- */
 

@@ -48,6 +48,9 @@ _S = ctypes.c_int
 
 # name -> (argtypes, restype); the signatures of include/gq.h
 SIGNATURES = {
+    "gq_kv_quantize_i8": ([_P, _P, _P, _I, _I, _P], _S),
+    "gq_kv_append_i8": ([_P, _P, _P, _P, _I, _I, _I, _I, _P], _S),
+    "gq_attn_decode_i8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P], _S),
     "gq_abi_version": ([], ctypes.c_int),
     "gq_status_string": ([_S], ctypes.c_char_p),
     "gq_last_error_message": ([], ctypes.c_char_p),
@@ -337,6 +340,22 @@ def gq_debug_block_dots_q4_0(q4_repacked, q8_blocks, sumi, M: int, N: int, K: in
                                           _stream(stream)), "gq_debug_block_dots_q4_0")
 
 
+def gq_kv_quantize_i8(x, q, scale, rows: int, D: int, stream=None) -> None:
+    _check(lib().gq_kv_quantize_i8(_ptr(x), _ptr(q), _ptr(scale), rows, D, _stream(stream)), "gq_kv_quantize_i8")
+
+
+def gq_kv_append_i8(x, q, scale, pos, B: int, Hkv: int, Tcap: int, D: int, stream=None) -> None:
+    _check(lib().gq_kv_append_i8(_ptr(x), _ptr(q), _ptr(scale), _ptr(pos), B, Hkv, Tcap, D, _stream(stream)),
+           "gq_kv_append_i8")
+
+
+def gq_attn_decode_i8(q, k, k_scale, v, v_scale, lens, out, B: int, Hq: int, Hkv: int, Tcap: int, D: int,
+                      softmax_scale: float, stream=None) -> None:
+    _check(lib().gq_attn_decode_i8(_ptr(q), _ptr(k), _ptr(k_scale), _ptr(v), _ptr(v_scale), _ptr(lens), _ptr(out),
+                                   B, Hq, Hkv, Tcap, D, float(softmax_scale), _stream(stream)),
+           "gq_attn_decode_i8")
+
+
 # ---------------------------------------------------------------------------
 # allocating helpers (torch tensors in, torch tensors out)
 # ---------------------------------------------------------------------------
@@ -513,4 +532,29 @@ def tune_dispatch(weights, N: int, K: int, kind: int = GQ_KIND_Q4_0,
         out["tc_us"].append(times[1])
     if install:
         gq_set_dispatch_profile(kind, N, K, out["M"], out["gemv_us"], out["tc_us"])
+    return out
+
+
+def kv_quantize_i8(x):
+    """f32 CUDA tensor [..., D] -> (int8 codes [..., D], f32 scales [...]), one scale per row of D."""
+    import torch
+    x = x.contiguous()
+    D = x.shape[-1]
+    q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    s = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    gq_kv_quantize_i8(x, q, s, x.numel() // D, D)
+    return q, s
+
+
+def attn_decode_i8(q, k, k_scale, v, v_scale, lens, softmax_scale=None, out=None):
+    """Decode attention over an INT8 cache: q f32 [B, Hq, D]; k, v int8 [B, Hkv, Tcap, D];
+    scales f32 [B, Hkv, Tcap]; lens int32 [B].  Returns f32 [B, Hq, D]."""
+    import torch
+    B, Hq, D = q.shape
+    Hkv, Tcap = k.shape[1], k.shape[2]
+    if softmax_scale is None:
+        softmax_scale = D ** -0.5
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    gq_attn_decode_i8(q, k, k_scale, v, v_scale, lens, out, B, Hq, Hkv, Tcap, D, softmax_scale)
     return out

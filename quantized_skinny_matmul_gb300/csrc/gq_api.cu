@@ -176,6 +176,7 @@ gq_status gq_last_error(void) {
         reset_workspace_counters();
         return fail(GQ_ERR_TIMEOUT, "a kernel gave up a bounded wait");
     }
+    if (word & STATUS_RANGE) return fail(GQ_ERR_INVALID_ARG, "a length or position read on the device was out of range");
     return ok();
 }
 
@@ -553,6 +554,73 @@ gq_status gq_debug_block_dots_q4_0(const void *q4_repacked, const void *q8_block
     GQ_TRY(check_ptr(sumi, "sumi"));
     GQ_TRY(check_device());
     GQ_TRY(launch_block_dots_q4_0(q4_repacked, q8_blocks, sumi, M, N, K, stream));
+    return ok();
+}
+
+}  // extern "C"
+
+// ---- INT8 KV cache ------------------------------------------------------------------
+
+namespace {
+gq_status check_kv(int64_t B, int64_t Hkv, int64_t Tcap, int64_t D) {
+    if (B <= 0 || Hkv <= 0 || Tcap <= 0)
+        return fail(GQ_ERR_INVALID_ARG, "sizes must be positive (B=%lld Hkv=%lld Tcap=%lld)", (long long)B,
+                    (long long)Hkv, (long long)Tcap);
+    if (D != 64 && D != 128) return fail(GQ_ERR_INVALID_ARG, "head size D must be 64 or 128 (got %lld)", (long long)D);
+    if (Tcap >= (1LL << 30) || B >= (1LL << 30) || Hkv >= (1LL << 30) || B * Hkv >= (1LL << 31) ||
+        (double)B * (double)Hkv * (double)Tcap * (double)D >= 1099511627776.0)
+        return fail(GQ_ERR_INVALID_ARG, "sizes too large (B=%lld Hkv=%lld Tcap=%lld D=%lld)", (long long)B,
+                    (long long)Hkv, (long long)Tcap, (long long)D);
+    return GQ_OK;
+}
+}  // namespace
+
+extern "C" {
+
+gq_status gq_kv_quantize_i8(const float *x, int8_t *q, float *scale, int64_t rows, int64_t D, cudaStream_t stream) {
+    if (rows <= 0 || rows >= (1LL << 34))
+        return fail(GQ_ERR_INVALID_ARG, "rows must be in [1, 2^34) (got %lld)", (long long)rows);
+    GQ_TRY(check_kv(1, 1, 1, D));
+    GQ_TRY(check_ptr(x, "x"));
+    GQ_TRY(check_ptr(q, "q"));
+    GQ_TRY(check_ptr(scale, "scale"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_kv_quantize_i8(x, q, scale, rows, D, stream));
+    return ok();
+}
+
+gq_status gq_kv_append_i8(const float *x, int8_t *q, float *scale, const int32_t *pos, int64_t B, int64_t Hkv,
+                          int64_t Tcap, int64_t D, cudaStream_t stream) {
+    GQ_TRY(check_kv(B, Hkv, Tcap, D));
+    GQ_TRY(check_ptr(x, "x"));
+    GQ_TRY(check_ptr(q, "q"));
+    GQ_TRY(check_ptr(scale, "scale"));
+    GQ_TRY(check_ptr(pos, "pos"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_kv_append_i8(x, q, scale, pos, B, Hkv, Tcap, D, stream));
+    return ok();
+}
+
+gq_status gq_attn_decode_i8(const float *q, const int8_t *k, const float *k_scale, const int8_t *v,
+                            const float *v_scale, const int32_t *lens, float *out, int64_t B, int64_t Hq,
+                            int64_t Hkv, int64_t Tcap, int64_t D, float softmax_scale, cudaStream_t stream) {
+    GQ_TRY(check_kv(B, Hkv, Tcap, D));
+    if (Hq <= 0 || Hq % Hkv != 0)
+        return fail(GQ_ERR_INVALID_ARG, "Hq=%lld is not a positive multiple of Hkv=%lld", (long long)Hq,
+                    (long long)Hkv);
+    const int64_t G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(GQ_ERR_INVALID_ARG, "query heads per KV head must be 1, 2, 4 or 8 (got %lld)", (long long)G);
+    if (!std::isfinite(softmax_scale)) return fail(GQ_ERR_INVALID_ARG, "softmax_scale is not finite");
+    GQ_TRY(check_ptr(q, "q"));
+    GQ_TRY(check_ptr(k, "k"));
+    GQ_TRY(check_ptr(k_scale, "k_scale"));
+    GQ_TRY(check_ptr(v, "v"));
+    GQ_TRY(check_ptr(v_scale, "v_scale"));
+    GQ_TRY(check_ptr(lens, "lens"));
+    GQ_TRY(check_ptr(out, "out"));
+    GQ_TRY(check_device());
+    GQ_TRY(launch_attn_decode_i8(q, k, k_scale, v, v_scale, lens, out, B, Hq, Hkv, Tcap, D, softmax_scale, stream));
     return ok();
 }
 

@@ -25,6 +25,7 @@ constexpr int TILE_SCALE_OFFSET = 1024;
 // Kernels with bounded waits receive the address of the device's sticky
 // status word (owned by gq_api.cu, read and cleared by gq_last_error).
 constexpr unsigned int STATUS_TIMEOUT = 1u;
+constexpr unsigned int STATUS_RANGE = 2u;     // a length or position read on the device was out of range
 __device__ __forceinline__ void flag_timeout(unsigned int *status) { atomicOr(status, STATUS_TIMEOUT); }
 
 // ---------------------------------------------------------------------------

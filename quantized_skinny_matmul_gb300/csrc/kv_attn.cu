@@ -1,0 +1,622 @@
+// kv_attn.cu -- the INT8 KV cache and the decode attention that reads it.
+//
+// xFasterTransformer (arXiv 2407.07304), "2.2 Effective KV cache Optimization":
+// after the first token, attention over the cache is a pair of GEMVs bound by
+// memory bandwidth; the cache is stored as INT8 with one scale for each token and
+// each head, and the INT8 operand is widened to FP32 before the multiply-add.
+// Section "2.1 LLM Optimization" (SlimAttention) gives the order for one query
+// row: the whole row of scores, then the softmax over it, then its product with
+// the values.  The scale's formula is not given; it is read like Q8_0's:
+// s = amax / 127 (f32, kept as f32), q = roundf(x / s) (IEEE division).
+//
+// Layouts: codes int8 [B][Hkv][Tcap][D] (a head's tokens are contiguous, so one
+// (sequence, head) pair streams as one run of bytes), scales f32 [B][Hkv][Tcap],
+// queries f32 [B][Hq][D] with Hq = G * Hkv (query head h reads KV head h / G),
+// lens int32 [B], output f32 [B][Hq][D].
+//
+// The decode kernel takes one (sequence, KV head, token range) per CTA.  A
+// producer warp streams the range's K rows and then its V rows through a ring of
+// 8 KB shared-memory slots with bulk copies (the cache is read once: L2
+// evict-first); four consumer warps take whole slots in turn:
+//   scores  each lane widens 16 int8 of a token to f32 (a byte placed in the
+//           mantissa of 2^23 and the offset subtracted: exact, no conversion
+//           instruction), multiplies them with the matching query values in
+//           packed f32x2 FMAs, and the lanes of a token add their partials; the
+//           score, times the token's scale and the softmax scale in base-2
+//           units, goes to a shared-memory row of scores;
+//   softmax the consumer warps take the row's maximum, replace each score by
+//           exp2(score - max) times the token's value scale, and add the
+//           exponentials (the denominator), in a fixed order;
+//   values  each lane widens 16 (8 when G = 8) int8 of a token's value row and
+//           accumulates weight x value into registers; lanes and then warps are
+//           added in a fixed order and divided by the denominator.
+// A range longer than the shared-memory row of scores holds, or a grid too small
+// to fill the GPU, splits a sequence's tokens over several CTAs; each writes its
+// unnormalised output with its maximum and denominator, and a second kernel merges
+// the parts in order.  Every result is deterministic.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gq_common.cuh"
+#include "gq_internal.h"
+
+namespace gq {
+namespace {
+
+constexpr int AT_CHUNK = 8192;                 // bytes per ring slot
+constexpr int AT_SLOTS = 8;
+constexpr int AT_WARPS = 4;                    // consumer warps
+constexpr int AT_THREADS = (AT_WARPS + 1) * 32;
+constexpr int AT_CONSUMERS = AT_WARPS * 32;
+constexpr size_t AT_SMEM_MAX = 113 * 1024;     // two CTAs per SM
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr uint32_t MAGIC = 0x4B000000u;        // 2^23 as f32 bits
+constexpr float MAGIC_OFFSET = 8388736.0f;     // 2^23 + 128
+
+#define KV_TRY(expr)                  \
+    do {                              \
+        gq_status _st = (expr);       \
+        if (_st != GQ_OK) return _st; \
+    } while (0)
+
+struct AttnParams {
+    const float *q;
+    const int8_t *k, *v;
+    const float *ks, *vs;
+    const int32_t *lens;
+    float *out;
+    float *part;                // [B][Hq][S][D + 2] when S > 1
+    unsigned int *status;
+    int Hkv, Tcap, S, TR;
+    float c2;                   // softmax scale times log2(e)
+};
+
+struct AttnLayout {
+    size_t bars, qs, ring, ksc, vsc, sc, wred, total;
+};
+
+template <int D, int G>
+__host__ __device__ constexpr size_t attn_fixed_bytes() {
+    return 128 + (size_t)G * D * 4 + (size_t)AT_SLOTS * AT_CHUNK + 2 * AT_WARPS * G * 4 + 128;
+}
+
+template <int D, int G>
+__host__ __device__ AttnLayout attn_layout(int TR) {
+    AttnLayout L{};
+    L.bars = 0;                                          // full[AT_SLOTS], empty[AT_SLOTS]
+    L.qs = 128;                                          // the G query rows, f32
+    L.ring = L.qs + (size_t)G * D * 4;                   // 128-byte aligned (D * 4 is)
+    L.ksc = L.ring + (size_t)AT_SLOTS * AT_CHUNK;        // key scale x c2, per token
+    L.vsc = L.ksc + (size_t)TR * 4;                      // value scale, per token
+    L.sc = L.vsc + (size_t)TR * 4;                       // scores [TR][G]
+    L.wred = L.sc + (size_t)TR * G * 4;                  // per-warp maxima and sums [2][W][G]
+    L.total = L.wred + 2 * AT_WARPS * G * 4;
+    return L;
+}
+
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(AT_CONSUMERS) : "memory");
+}
+
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// The four int8 of a word as f32 pairs (bytes 0, 1) and (2, 3).  With u = k + 128 the
+// biased byte, the f32 whose bits are 0x4B0000uu is 2^23 + u exactly, and subtracting
+// 2^23 + 128 is exact too.
+__device__ __forceinline__ void widen4(uint32_t w, uint64_t &p01, uint64_t &p23) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint64_t off = pack2(-MAGIC_OFFSET, -MAGIC_OFFSET);
+    // result bytes, low to high: byte i of u, then bytes 0, 1 and 3 of MAGIC (0x00, 0x00, 0x4B)
+    p01 = add2(pack2(__uint_as_float(__byte_perm(u, MAGIC, 0x7540)), __uint_as_float(__byte_perm(u, MAGIC, 0x7541))), off);
+    p23 = add2(pack2(__uint_as_float(__byte_perm(u, MAGIC, 0x7542)), __uint_as_float(__byte_perm(u, MAGIC, 0x7543))), off);
+}
+
+// Sums v[0..HG) over the LPT lanes of a token (xor masks LPT/2 .. 1).  While a lane
+// holds more than one head, each exchange halves them: the lane with the mask bit set
+// keeps the upper half.  On return v[0] is the full sum of head (lane % LPT) / (LPT / HG).
+template <int HG, int LPT>
+__device__ __forceinline__ float reduce_heads(float (&v)[HG], int lane) {
+    static_assert(HG <= LPT, "more heads than lanes per token");
+    int nh = HG;
+#pragma unroll
+    for (int m = LPT / 2; m >= 1; m >>= 1) {
+        if (nh > 1) {
+            const int half = nh / 2;
+            const bool up = (lane & m) != 0;
+#pragma unroll
+            for (int i = 0; i < HG / 2; i++) {
+                if (i < half) {
+                    const float send = up ? v[i] : v[i + half];
+                    const float keep = up ? v[i + half] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                }
+            }
+            nh = half;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+        }
+    }
+    return v[0];
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(AT_THREADS, 2) attn_decode_i8_kernel(const AttnParams p) {
+    constexpr int CT = AT_CHUNK / D;       // tokens per slot
+    constexpr int LPT = D / 16;            // score phase: lanes per token, 16 bytes each
+    constexpr int TPW = 32 / LPT;          // tokens per warp step
+    constexpr int HG = G < 4 ? G : 4;      // heads per pass of the score phase
+    constexpr int VB = G >= 8 ? 8 : 16;    // value phase: bytes per lane
+    constexpr int LPV = D / VB;
+    constexpr int TPV = 32 / LPV;
+    static_assert(D % 16 == 0 && 32 % LPT == 0 && 32 % LPV == 0, "head size");
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    const AttnLayout L = attn_layout<D, G>(p.TR);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + AT_SLOTS;
+    float *qs = reinterpret_cast<float *>(smem + L.qs);
+    float *ksc = reinterpret_cast<float *>(smem + L.ksc);
+    float *vsc = reinterpret_cast<float *>(smem + L.vsc);
+    float *sc = reinterpret_cast<float *>(smem + L.sc);
+    float *wmax = reinterpret_cast<float *>(smem + L.wred);
+    float *wsum = wmax + AT_WARPS * G;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int z = blockIdx.x % p.S, bh = blockIdx.x / p.S;   // bh = b * Hkv + hk
+    const int b = bh / p.Hkv, hk = bh % p.Hkv;
+    const int Hq = p.Hkv * G;
+
+    pdl_launch_dependents();
+    pdl_wait();   // the cache, the queries and the lengths may come from the grid in front
+
+    int len = p.lens[b];
+    if (len < 0 || len > p.Tcap) {
+        if (threadIdx.x == 0) atomicOr(p.status, STATUS_RANGE);
+        len = 0;
+    }
+    const int t0 = z * p.TR;
+    const int nt = max(0, min(len, t0 + p.TR) - t0);
+    const size_t orow = ((size_t)b * Hq + (size_t)hk * G) * D;   // first output row of this CTA
+
+    if (nt == 0) {   // an empty range: a zero output, or an empty part
+        for (int i = threadIdx.x; i < G * D; i += AT_THREADS) {
+            if (p.S == 1) {
+                p.out[orow + i] = 0.0f;
+            } else {
+                const int g = i / D, d = i % D;
+                float *pp = p.part + (((size_t)b * Hq + (size_t)hk * G + g) * p.S + z) * (D + 2);
+                pp[d] = 0.0f;
+                if (d == 0) {
+                    pp[D] = -INFINITY;
+                    pp[D + 1] = 0.0f;
+                }
+            }
+        }
+        return;
+    }
+    const int nc = (nt + CT - 1) / CT;   // slots per phase
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < AT_SLOTS; s++) {
+            mbar_init(smem_addr(full + s), 1);
+            mbar_init(smem_addr(empty + s), 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- producer
+    if (warp == AT_WARPS) {
+        if (lane != 0) return;
+        const size_t row0 = (size_t)bh * p.Tcap + t0;
+        const int8_t *kbase = p.k + row0 * D, *vbase = p.v + row0 * D;
+        const uint64_t policy = l2_evict_first_policy();
+        int issued = 0;
+        for (int i = 0; i < 2 * nc; i++) {
+            const int slot = i % AT_SLOTS;
+            if (i >= AT_SLOTS && !mbar_wait(smem_addr(empty + slot), (uint32_t)(((i / AT_SLOTS) - 1) & 1), p.status))
+                break;
+            const int c = i < nc ? i : i - nc;
+            const uint32_t bytes = (uint32_t)(min(CT, nt - c * CT) * D);
+            mbar_arrive_expect_tx(smem_addr(full + slot), bytes);
+            bulk_g2s_hint(smem_addr(smem + L.ring + (size_t)slot * AT_CHUNK), (i < nc ? kbase : vbase) + (size_t)c * CT * D,
+                          bytes, smem_addr(full + slot), policy);
+            issued = i + 1;
+        }
+        // Stay until every copy issued has landed, so that the CTA never ends with a bulk
+        // copy in flight (the last copy into each slot completes that slot's last phase).
+        for (int i = max(0, issued - AT_SLOTS); i < issued; i++)
+            mbar_wait(smem_addr(full + i % AT_SLOTS), (uint32_t)((i / AT_SLOTS) & 1), p.status);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int ctid = threadIdx.x;   // 0 .. AT_CONSUMERS - 1
+    {
+        const float *qg = p.q + orow;   // the G query rows of KV head hk are contiguous
+        for (int i = ctid; i < G * D; i += AT_CONSUMERS) qs[i] = qg[i];
+        const size_t srow = (size_t)bh * p.Tcap + t0;
+        for (int i = ctid; i < nt; i += AT_CONSUMERS) {
+            ksc[i] = p.ks[srow + i] * p.c2;
+            vsc[i] = p.vs[srow + i];
+        }
+    }
+    consumer_sync();
+
+    const uint8_t *ring = smem + L.ring;
+    bool failed = false;
+    auto wait_slot = [&](int i) {
+        const bool ok = mbar_wait(smem_addr(full + i % AT_SLOTS), (uint32_t)((i / AT_SLOTS) & 1), p.status);
+        failed |= !__all_sync(0xffffffffu, ok);
+    };
+    auto release_slot = [&](int i) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(empty + i % AT_SLOTS));
+    };
+
+    // ---- scores: slot c of the key phase goes to warp c % AT_WARPS
+    const int sl = lane % LPT;   // this lane's 16-byte column of a token row
+    for (int c = warp; c < nc; c += AT_WARPS) {
+        wait_slot(c);
+        if (!failed) {
+            const uint8_t *chunk = ring + (size_t)(c % AT_SLOTS) * AT_CHUNK;
+            const int ntok = min(CT, nt - c * CT);
+#pragma unroll 1
+            for (int pass = 0; pass < G / HG; pass++) {
+                uint64_t qv[HG][8];
+#pragma unroll
+                for (int h = 0; h < HG; h++) {
+                    const float *qrow = qs + (pass * HG + h) * D + sl * 16;
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const float4 f = *reinterpret_cast<const float4 *>(qrow + 4 * j);
+                        qv[h][2 * j] = pack2(f.x, f.y);
+                        qv[h][2 * j + 1] = pack2(f.z, f.w);
+                    }
+                }
+#pragma unroll 2
+                for (int it = 0; it < ntok; it += TPW) {
+                    const int tok = it + lane / LPT;
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (tok < ntok) w = lds128(chunk + (size_t)tok * D + sl * 16);
+                    uint64_t kf[8];
+                    widen4(w.x, kf[0], kf[1]);
+                    widen4(w.y, kf[2], kf[3]);
+                    widen4(w.z, kf[4], kf[5]);
+                    widen4(w.w, kf[6], kf[7]);
+                    float part[HG];
+#pragma unroll
+                    for (int h = 0; h < HG; h++) {
+                        uint64_t a = fma2(qv[h][0], kf[0], 0ull);
+#pragma unroll
+                        for (int j = 1; j < 8; j++) a = fma2(qv[h][j], kf[j], a);
+                        float lo, hi;
+                        unpack2(a, lo, hi);
+                        part[h] = lo + hi;
+                    }
+                    const float s = reduce_heads<HG, LPT>(part, lane);
+                    if (tok < ntok && (sl % (LPT / HG)) == 0) {
+                        const int t = c * CT + tok, h = pass * HG + sl / (LPT / HG);
+                        sc[t * G + h] = s * ksc[t];
+                    }
+                }
+            }
+        }
+        release_slot(c);
+    }
+    consumer_sync();
+
+    // ---- softmax over the row: thread ctid takes entries ctid, ctid + 128, ... (head ctid % G)
+    const int gh = ctid % G;
+    {
+        float mx = -INFINITY;
+        for (int i = ctid; i < nt * G; i += AT_CONSUMERS) mx = fmaxf(mx, sc[i]);
+#pragma unroll
+        for (int m = 16; m >= G; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        if (lane < G) wmax[warp * G + lane] = mx;
+        consumer_sync();
+        float M = wmax[gh];
+#pragma unroll
+        for (int w = 1; w < AT_WARPS; w++) M = fmaxf(M, wmax[w * G + gh]);
+        float l = 0.0f;
+        for (int i = ctid; i < nt * G; i += AT_CONSUMERS) {
+            const float e = exp2f(sc[i] - M);
+            l += e;
+            sc[i] = e * vsc[i / G];
+        }
+#pragma unroll
+        for (int m = 16; m >= G; m >>= 1) l += __shfl_xor_sync(0xffffffffu, l, m);
+        if (lane < G) wsum[warp * G + lane] = l;
+    }
+    consumer_sync();
+
+    // ---- values: slot nc + c goes to warp c % AT_WARPS
+    uint64_t acc[G][VB / 2];
+#pragma unroll
+    for (int g = 0; g < G; g++)
+#pragma unroll
+        for (int j = 0; j < VB / 2; j++) acc[g][j] = 0ull;
+    const int vl = lane % LPV;
+    for (int c = warp; c < nc; c += AT_WARPS) {
+        wait_slot(nc + c);
+        if (!failed) {
+            const uint8_t *chunk = ring + (size_t)((nc + c) % AT_SLOTS) * AT_CHUNK;
+            const int ntok = min(CT, nt - c * CT);
+#pragma unroll 2
+            for (int it = 0; it < ntok; it += TPV) {
+                const int tok = it + lane / LPV;
+                const bool live = tok < ntok;
+                uint32_t wv[VB / 4];
+                if constexpr (VB == 16) {
+                    const uint4 w = live ? lds128(chunk + (size_t)tok * D + vl * 16) : make_uint4(0u, 0u, 0u, 0u);
+                    wv[0] = w.x;
+                    wv[1] = w.y;
+                    wv[2] = w.z;
+                    wv[3] = w.w;
+                } else {
+                    const uint2 w = live ? *reinterpret_cast<const uint2 *>(chunk + (size_t)tok * D + vl * 8)
+                                         : make_uint2(0u, 0u);
+                    wv[0] = w.x;
+                    wv[1] = w.y;
+                }
+                uint64_t vf[VB / 2];
+#pragma unroll
+                for (int j = 0; j < VB / 4; j++) widen4(wv[j], vf[2 * j], vf[2 * j + 1]);
+                const int t = c * CT + (live ? tok : 0);
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    const float wt = live ? sc[t * G + g] : 0.0f;
+                    const uint64_t w2 = pack2(wt, wt);
+#pragma unroll
+                    for (int j = 0; j < VB / 2; j++) acc[g][j] = fma2(w2, vf[j], acc[g][j]);
+                }
+            }
+        }
+        release_slot(nc + c);
+    }
+
+    // ---- add the token lanes of each warp, then the warps (in order), and scale
+#pragma unroll
+    for (int m = LPV; m < 32; m <<= 1)
+#pragma unroll
+        for (int g = 0; g < G; g++)
+#pragma unroll
+            for (int j = 0; j < VB / 2; j++) {
+                float lo, hi;
+                unpack2(acc[g][j], lo, hi);
+                lo += __shfl_xor_sync(0xffffffffu, lo, m);
+                hi += __shfl_xor_sync(0xffffffffu, hi, m);
+                acc[g][j] = pack2(lo, hi);
+            }
+    consumer_sync();   // every warp is done with the ring: it holds the per-warp sums now
+    float *red = reinterpret_cast<float *>(smem + L.ring);   // [W][G][D]
+    if (lane < LPV) {
+#pragma unroll
+        for (int g = 0; g < G; g++)
+#pragma unroll
+            for (int j = 0; j < VB / 2; j++) {
+                float lo, hi;
+                unpack2(acc[g][j], lo, hi);
+                red[((size_t)warp * G + g) * D + vl * VB + 2 * j] = lo;
+                red[((size_t)warp * G + g) * D + vl * VB + 2 * j + 1] = hi;
+            }
+    }
+    consumer_sync();
+    for (int i = ctid; i < G * D; i += AT_CONSUMERS) {
+        const int g = i / D, d = i % D;
+        float o = red[(size_t)g * D + d];
+#pragma unroll
+        for (int w = 1; w < AT_WARPS; w++) o += red[((size_t)w * G + g) * D + d];
+        float l = wsum[g], M = wmax[g];
+#pragma unroll
+        for (int w = 1; w < AT_WARPS; w++) {
+            l += wsum[w * G + g];
+            M = fmaxf(M, wmax[w * G + g]);
+        }
+        if (p.S == 1) {
+            p.out[orow + i] = o / l;
+        } else {
+            float *pp = p.part + (((size_t)b * Hq + (size_t)hk * G + g) * p.S + z) * (D + 2);
+            pp[d] = o;
+            if (d == 0) {
+                pp[D] = M;
+                pp[D + 1] = l;
+            }
+        }
+    }
+}
+
+// Merges the S parts of each output row in order: with M the largest part maximum,
+// out = sum_z 2^(m_z - M) o_z / sum_z 2^(m_z - M) l_z.  One CTA per row, one thread per column.
+__global__ void attn_merge_kernel(const float *part, float *out, int S, int D) {
+    pdl_wait();
+    const float *pp = part + (size_t)blockIdx.x * S * (D + 2);
+    const int d = threadIdx.x;
+    if (d >= D) return;
+    float M = -INFINITY;
+    for (int z = 0; z < S; z++) M = fmaxf(M, pp[(size_t)z * (D + 2) + D]);
+    float o = 0.0f, l = 0.0f;
+    if (M != -INFINITY) {
+        for (int z = 0; z < S; z++) {
+            const float *pz = pp + (size_t)z * (D + 2);
+            const float a = exp2f(pz[D] - M);
+            o += a * pz[d];
+            l += a * pz[D + 1];
+        }
+    }
+    out[(size_t)blockIdx.x * D + d] = l > 0.0f ? o / l : 0.0f;
+}
+
+// One warp per row of D values: the row's f32 scale amax / 127 and its int8 codes.
+__device__ __forceinline__ void quantize_row(const float *x, int8_t *q, float *scale, int D, int lane) {
+    float amax = 0.0f;
+    for (int j = 4 * lane; j < D; j += 128) {
+        const float4 v = *reinterpret_cast<const float4 *>(x + j);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    const float s = amax / 127.0f;
+    auto code = [&](float v) -> int {
+        if (s == 0.0f) return 0;
+        const int c = (int)roundf(v / s);
+        return c < -127 ? -127 : (c > 127 ? 127 : c);
+    };
+    for (int j = 4 * lane; j < D; j += 128) {
+        const float4 v = *reinterpret_cast<const float4 *>(x + j);
+        *reinterpret_cast<uint32_t *>(q + j) = pack_bytes(code(v.x), code(v.y), code(v.z), code(v.w));
+    }
+    if (lane == 0) *scale = s;
+}
+
+__global__ void kv_quantize_i8_kernel(const float *x, int8_t *q, float *scale, int64_t rows, int D) {
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    pdl_wait();
+    pdl_launch_dependents();
+    if (r >= rows) return;
+    quantize_row(x + r * D, q + r * D, scale + r, D, threadIdx.x & 31);
+}
+
+// Row (b, h) of x [B][Hkv][D] goes to position pos[b] of the cache [B][Hkv][Tcap][D].
+__global__ void kv_append_i8_kernel(const float *x, int8_t *q, float *scale, const int32_t *pos, int64_t rows,
+                                    int Hkv, int Tcap, int D, unsigned int *status) {
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    pdl_wait();
+    pdl_launch_dependents();
+    if (r >= rows) return;
+    const int t = pos[r / Hkv];
+    if (t < 0 || t >= Tcap) {
+        if ((threadIdx.x & 31) == 0) atomicOr(status, STATUS_RANGE);
+        return;
+    }
+    const int64_t cr = r * Tcap + t;
+    quantize_row(x + r * D, q + cr * D, scale + cr, D, threadIdx.x & 31);
+}
+
+gq_status pdl_launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void **args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return check_cuda(cudaLaunchKernelExC(&cfg, fn, args), "INT8 KV-cache kernel launch");
+}
+
+template <int D, int G>
+gq_status launch_attn_dg(const AttnParams &base, int64_t B, int64_t Tcap, cudaStream_t s) {
+    constexpr int CT = AT_CHUNK / D;
+    auto kernel = attn_decode_i8_kernel<D, G>;
+    // tokens per CTA: what the shared-memory row of scores holds, and few enough that
+    // (sequence, KV head, range) work items fill the GPU twice over
+    const int64_t per_token = 4 * (2 + G);
+    const int64_t room = (int64_t)(AT_SMEM_MAX - attn_fixed_bytes<D, G>());
+    const int64_t tr_max = std::max<int64_t>(CT, room / per_token / CT * CT);
+    const int64_t items = B * base.Hkv;
+    const int64_t want = (2 * (int64_t)sm_count() + items - 1) / items;
+    int64_t S = std::max<int64_t>((Tcap + tr_max - 1) / tr_max, std::min<int64_t>(want, (Tcap + CT - 1) / CT));
+    int64_t TR = ((Tcap + S - 1) / S + CT - 1) / CT * CT;
+    TR = std::min(TR, tr_max);
+    S = (Tcap + TR - 1) / TR;
+    if (items * S > INT32_MAX) return fail(GQ_ERR_INVALID_ARG, "attention grid too large");
+    AttnParams p = base;
+    p.S = (int)S;
+    p.TR = (int)TR;
+    float *out = p.out;
+    if (S > 1) {
+        Workspace ws{};
+        KV_TRY(get_workspace(s, 0, (size_t)B * base.Hkv * G * S * (D + 2) * sizeof(float), &ws));
+        p.part = reinterpret_cast<float *>(ws.data);
+    }
+    const size_t smem = attn_layout<D, G>((int)TR).total;
+    KV_TRY(check_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                               "attention shared-memory attribute"));
+    void *args[] = {(void *)&p};
+    KV_TRY(pdl_launch((const void *)kernel, dim3((unsigned)(items * S)), dim3(AT_THREADS), smem, s, args));
+    if (S > 1) {
+        const float *part = p.part;
+        int Si = (int)S, Di = D;
+        void *margs[] = {(void *)&part, (void *)&out, (void *)&Si, (void *)&Di};
+        KV_TRY(pdl_launch((const void *)attn_merge_kernel, dim3((unsigned)(B * base.Hkv * G)), dim3(D), 0, s,
+                                   margs));
+    }
+    return GQ_OK;
+}
+
+template <int D>
+gq_status launch_attn_d(const AttnParams &p, int64_t B, int64_t G, int64_t Tcap, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_attn_dg<D, 1>(p, B, Tcap, s);
+        case 2: return launch_attn_dg<D, 2>(p, B, Tcap, s);
+        case 4: return launch_attn_dg<D, 4>(p, B, Tcap, s);
+        case 8: return launch_attn_dg<D, 8>(p, B, Tcap, s);
+    }
+    return fail(GQ_ERR_INVALID_ARG, "query heads per KV head must be 1, 2, 4 or 8 (got %lld)", (long long)G);
+}
+
+}  // namespace
+
+gq_status launch_attn_decode_i8(const float *q, const int8_t *k, const float *ks, const int8_t *v, const float *vs,
+                                const int32_t *lens, float *out, int64_t B, int64_t Hq, int64_t Hkv, int64_t Tcap,
+                                int64_t D, float softmax_scale, cudaStream_t s) {
+    AttnParams p{};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.ks = ks;
+    p.vs = vs;
+    p.lens = lens;
+    p.out = out;
+    p.status = device_status_word();
+    if (!p.status) return fail(GQ_ERR_CUDA, "device status word unavailable");
+    p.Hkv = (int)Hkv;
+    p.Tcap = (int)Tcap;
+    p.c2 = softmax_scale * LOG2E;
+    const int64_t G = Hq / Hkv;
+    if (D == 64) return launch_attn_d<64>(p, B, G, Tcap, s);
+    return launch_attn_d<128>(p, B, G, Tcap, s);
+}
+
+gq_status launch_kv_quantize_i8(const float *x, int8_t *q, float *scale, int64_t rows, int64_t D, cudaStream_t s) {
+    const int64_t blocks = (rows + 7) / 8;
+    int Di = (int)D;
+    void *args[] = {(void *)&x, (void *)&q, (void *)&scale, (void *)&rows, (void *)&Di};
+    return pdl_launch((const void *)kv_quantize_i8_kernel, dim3((unsigned)blocks), dim3(256), 0, s, args);
+}
+
+gq_status launch_kv_append_i8(const float *x, int8_t *q, float *scale, const int32_t *pos, int64_t B, int64_t Hkv,
+                              int64_t Tcap, int64_t D, cudaStream_t s) {
+    unsigned int *status = device_status_word();
+    if (!status) return fail(GQ_ERR_CUDA, "device status word unavailable");
+    int64_t rows = B * Hkv;
+    const int64_t blocks = (rows + 7) / 8;
+    int Hi = (int)Hkv, Ti = (int)Tcap, Di = (int)D;
+    void *args[] = {(void *)&x, (void *)&q, (void *)&scale, (void *)&pos, (void *)&rows,
+                    (void *)&Hi, (void *)&Ti, (void *)&Di, (void *)&status};
+    return pdl_launch((const void *)kv_append_i8_kernel, dim3((unsigned)blocks), dim3(256), 0, s, args);
+}
+
+}  // namespace gq

@@ -136,3 +136,46 @@ def edge_activations(seed: int, M: int, K: int) -> np.ndarray:
             elif kind == 3:
                 blk *= np.float32(50.0)
     return x
+
+
+# ---------------------------------------------------------------------------
+# INT8 KV-cache decode attention (xFasterTransformer, "2.2 Effective KV cache
+# Optimization": Llama2-7B with 32 heads of 128, batch 256, 1024 input and 1024
+# output tokens).  Keys and values ~ N(0, 1), keys with a per-channel spread
+# exp(0.5 N(0, 1)) drawn once per head (a few wide channels, as keys have);
+# queries ~ N(0, 1).  Lengths: "full" = Tcap for every sequence; "mix" = uniform
+# in [1, Tcap]; the tests add their own edge lengths.
+# ---------------------------------------------------------------------------
+KV_LLAMA2_7B = {"B": 256, "Hq": 32, "Hkv": 32, "Tcap": 2048, "D": 128}
+
+
+def kv_lengths(seed: int, B: int, Tcap: int, mode: str = "full") -> np.ndarray:
+    if mode == "full":
+        return np.full(B, Tcap, np.int32)
+    gen = np.random.default_rng(seed)
+    return gen.integers(1, Tcap + 1, size=B).astype(np.int32)
+
+
+def kv_problem(seed: int, B: int, Hq: int, Hkv: int, Tcap: int, D: int):
+    """(q f32 [B, Hq, D], k f32 [B, Hkv, Tcap, D], v f32 [B, Hkv, Tcap, D])."""
+    gen = np.random.default_rng(seed)
+    chan = np.exp(np.float32(0.5) * gen.standard_normal((1, Hkv, 1, D), dtype=np.float32))
+    k = gen.standard_normal((B, Hkv, Tcap, D), dtype=np.float32) * chan
+    v = gen.standard_normal((B, Hkv, Tcap, D), dtype=np.float32)
+    q = gen.standard_normal((B, Hq, D), dtype=np.float32)
+    return q, k, v
+
+
+def kv_codes_device(seed: int, B: int, Hkv: int, Tcap: int, D: int, device):
+    """Random INT8 cache contents drawn on the device (for sizes the host should not
+    generate): codes uniform in [-127, 127] and scales exp(0.3 N(0, 1)) / 42, for K and V.
+    Returns (k, k_scale, v, v_scale) torch tensors."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    shape = (B, Hkv, Tcap, D)
+    k = torch.randint(-127, 128, shape, generator=g, device=device, dtype=torch.int8)
+    v = torch.randint(-127, 128, shape, generator=g, device=device, dtype=torch.int8)
+    ks = torch.exp(0.3 * torch.randn(shape[:3], generator=g, device=device)) / 42.0
+    vs = torch.exp(0.3 * torch.randn(shape[:3], generator=g, device=device)) / 42.0
+    return k, ks.float().contiguous(), v, vs.float().contiguous()

@@ -201,3 +201,34 @@ def test_dispatch_takes_the_tiles_when_the_gemv_needs_several_slices(lib):
             assert gq.gq_choose_path(Q, N, K, M) == gq.GQ_PATH_GEMV, (N, K, M)
         assert gq.gq_choose_path(Q, N, K, 17) == gq.GQ_PATH_TC
     assert gq.gq_choose_path(Q, 64, 100000, 1) == gq.GQ_PATH_GEMV
+
+
+def test_argument_checks_kv_cache(lib):
+    """The INT8 KV-cache entry points reject bad sizes, head counts and pointers before
+    touching the GPU."""
+    a = lib.gq_attn_decode_i8
+    ok_args = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 4, 64, 128, 0.1, None)
+    for i, bad in ((9, 6), (9, 12), (9, 40), (10, 0), (8, 3)):    # Hq not G * Hkv with G in 1, 2, 4, 8
+        args = list(ok_args)
+        args[i if i != 10 else 10] = bad
+        assert a(*args) == gq.GQ_ERR_INVALID_ARG, (i, bad)
+    for D in (32, 96, 256):
+        args = list(ok_args)
+        args[11] = D
+        assert a(*args) == gq.GQ_ERR_INVALID_ARG
+    for j in range(7):
+        args = list(ok_args)
+        args[j] = 0
+        assert a(*args) == gq.GQ_ERR_INVALID_ARG
+        args[j] = ODD
+        assert a(*args) == gq.GQ_ERR_MISALIGNED
+    args = list(ok_args)
+    args[12] = float("inf")
+    assert a(*args) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_kv_quantize_i8(FAKE, FAKE, FAKE, 0, 128, None) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_kv_quantize_i8(FAKE, FAKE, FAKE, 4, 48, None) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_kv_quantize_i8(FAKE, FAKE, ODD, 4, 64, None) == gq.GQ_ERR_MISALIGNED
+    assert lib.gq_kv_append_i8(FAKE, FAKE, FAKE, 0, 2, 4, 64, 128, None) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_kv_append_i8(FAKE, FAKE, FAKE, FAKE, 2, 4, 0, 128, None) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_kv_append_i8(FAKE, ODD, FAKE, FAKE, 2, 4, 64, 128, None) == gq.GQ_ERR_MISALIGNED
+    assert lib.gq_last_error_message()
