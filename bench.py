@@ -419,10 +419,56 @@ def run_ours(args, rank, world, local):
         print(json.dumps(out), flush=True)
 
 
+def attn_bytes(lens, Hq, Hkv, D):
+    """Algorithmic bytes of one decode attention over the INT8 cache: the K and V codes and
+    scales of the valid tokens, the queries, the outputs and the lengths."""
+    tokens = int(sum(int(t) for t in lens))
+    B = len(lens)
+    return tokens * Hkv * (2 * D + 8) + B * Hq * D * 8 + 4 * B
+
+
+def attn_case(b, B, Hq, Hkv, Tcap, D, lens_mode, seed):
+    import numpy as np
+    from quantized_skinny_matmul_gb300 import synth
+    torch = b.torch
+    k, ks, v, vs = synth.kv_codes_device(seed, B, Hkv, Tcap, D, b.dev)
+    q = torch.randn((B, Hq, D), generator=b.gen(seed + 1), device=b.dev, dtype=torch.float32)
+    lens_h = synth.kv_lengths(seed + 2, B, Tcap, lens_mode)
+    lens = torch.from_numpy(np.ascontiguousarray(lens_h)).to(b.dev)
+    out = torch.empty((B, Hq, D), device=b.dev)
+    return (q, k, ks, v, vs, lens, out), lens_h
+
+
+def attn_extras(b, hbm_peak):
+    """The INT8 KV-cache decode attention on the Llama2-7B layer of the KV-cache page (batch
+    256, 32 heads of 128, 1024 + 1024 tokens): 4.4 GB per launch, far above L2."""
+    from quantized_skinny_matmul_gb300 import synth
+    gq = b.gq
+    cfg = synth.KV_LLAMA2_7B
+    B, Hq, Hkv, Tcap, D = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["Tcap"], cfg["D"]
+    res = {}
+    for mode in ("full", "mix"):
+        (q, k, ks, v, vs, lens, out), lens_h = attn_case(b, B, Hq, Hkv, Tcap, D, mode, 90)
+        fn = lambda: gq.gq_attn_decode_i8(q, k, ks, v, vs, lens, out, B, Hq, Hkv, Tcap, D, D ** -0.5,
+                                          stream=b.stream)
+        t = b.time_launches([fn], min_seconds=0.2, max_graph=20)
+        nbytes = attn_bytes(lens_h, Hq, Hkv, D)
+        gbs = nbytes / t / 1e9
+        res[f"llama2_7b_b{B}_t{Tcap}_{mode}"] = {
+            "us": round(t * 1e6, 1), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4),
+            "algorithmic_bytes": nbytes, "tokens": int(lens_h.sum())}
+        del q, k, ks, v, vs, lens, out
+    b.torch.cuda.empty_cache()
+    res["workload"] = (f"decode attention over an INT8 KV cache, B={B} Hq={Hq} Hkv={Hkv} D={D}, "
+                       f"Tcap={Tcap}; lens full or uniform in [1, {Tcap}]")
+    return res
+
+
 def extras(b, weights, C, hbm_peak, bf16_peak, bf16_sustained, args):
     import torch
     gq = b.gq
     res = {}
+    res["attn_decode_i8"] = attn_extras(b, hbm_peak)
     # F16 weights, same shapes, M = 1
     f16_set = sum(2 * N * K for N, K in SHAPES)
     C16 = b.copies_for(f16_set)
@@ -644,11 +690,21 @@ def cpu_baseline(seconds: float):
 
 
 def run_profile(spec: str):
-    """A few plain launches of one product, for ncu: KIND:M:N:K with KIND q4_0 | q4_1 | q5_0 | q8_0 | f16 | f16r | q4_0_tc | f16_tc."""
+    """A few plain launches of one product, for ncu: KIND:M:N:K with KIND q4_0 | q4_1 | q5_0 | q8_0 | f16 | f16r |
+    q4_0_tc | f16_tc; or attn_i8:B:Hq:Hkv:Tcap:D for the INT8 KV-cache decode attention (all lengths Tcap)."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
     import quantized_skinny_matmul_gb300 as gq
+    if spec.startswith("attn_i8:"):
+        B, Hq, Hkv, Tcap, D = (int(v) for v in spec.split(":")[1:])
+        b = GpuBench(0)
+        (q, k, ks, v, vs, lens, out), _ = attn_case(b, B, Hq, Hkv, Tcap, D, "full", 90)
+        for _ in range(5):
+            gq.gq_attn_decode_i8(q, k, ks, v, vs, lens, out, B, Hq, Hkv, Tcap, D, D ** -0.5)
+        torch.cuda.synchronize()
+        print(f"profile {spec}: 5 launches done")
+        return
     kind, M, N, K = spec.split(":")
     M, N, K = int(M), int(N), int(K)
     b = GpuBench(0)

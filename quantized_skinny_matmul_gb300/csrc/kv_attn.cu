@@ -16,8 +16,8 @@
 //
 // The decode kernel takes one (sequence, KV head, token range) per CTA.  A
 // producer warp streams the range's K rows and then its V rows through a ring of
-// 8 KB shared-memory slots with bulk copies (the cache is read once: L2
-// evict-first); four consumer warps take whole slots in turn:
+// shared-memory slots with bulk copies (the cache is read once: L2 evict-first);
+// the consumer warps take whole slots in turn:
 //   scores  each lane widens 16 int8 of a token to f32 (a byte placed in the
 //           mantissa of 2^23 and the offset subtracted: exact, no conversion
 //           instruction), multiplies them with the matching query values in
@@ -35,6 +35,7 @@
 // unnormalised output with its maximum and denominator, and a second kernel merges
 // the parts in order.  Every result is deterministic.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -45,11 +46,19 @@
 namespace gq {
 namespace {
 
-constexpr int AT_CHUNK = 8192;                 // bytes per ring slot
-constexpr int AT_SLOTS = 8;
-constexpr int AT_WARPS = 4;                    // consumer warps
-constexpr int AT_THREADS = (AT_WARPS + 1) * 32;
-constexpr int AT_CONSUMERS = AT_WARPS * 32;
+// The ring and the consumer warps.  With one or two query heads per KV head a consumer
+// does little arithmetic per byte, so eight consumer warps on 4 KB slots keep enough
+// bytes in flight; with four or eight, four warps (their registers hold G accumulators)
+// on 8 KB slots.  SLOTS is a multiple of W: the warp that takes a slot's chunk also
+// takes the next chunk in that slot.
+template <int G>
+struct AtCfg {
+    static constexpr int W = G <= 2 ? 8 : 4;                 // consumer warps
+    static constexpr int CHUNK = G <= 2 ? 4096 : 8192;       // bytes per ring slot
+    static constexpr int SLOTS = G <= 2 ? 16 : 8;
+    static constexpr int THREADS = (W + 1) * 32;
+    static constexpr int CONSUMERS = W * 32;
+};
 constexpr size_t AT_SMEM_MAX = 113 * 1024;     // two CTAs per SM
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint32_t MAGIC = 0x4B000000u;        // 2^23 as f32 bits
@@ -79,25 +88,28 @@ struct AttnLayout {
 
 template <int D, int G>
 __host__ __device__ constexpr size_t attn_fixed_bytes() {
-    return 128 + (size_t)G * D * 4 + (size_t)AT_SLOTS * AT_CHUNK + 2 * AT_WARPS * G * 4 + 128;
+    using C = AtCfg<G>;
+    return 256 + (size_t)G * D * 4 + (size_t)C::SLOTS * C::CHUNK + 2 * C::W * G * 4 + 128;
 }
 
 template <int D, int G>
 __host__ __device__ AttnLayout attn_layout(int TR) {
+    using C = AtCfg<G>;
     AttnLayout L{};
-    L.bars = 0;                                          // full[AT_SLOTS], empty[AT_SLOTS]
-    L.qs = 128;                                          // the G query rows, f32
+    L.bars = 0;                                          // full[SLOTS], empty[SLOTS]
+    L.qs = 256;                                          // the G query rows, f32
     L.ring = L.qs + (size_t)G * D * 4;                   // 128-byte aligned (D * 4 is)
-    L.ksc = L.ring + (size_t)AT_SLOTS * AT_CHUNK;        // key scale x c2, per token
+    L.ksc = L.ring + (size_t)C::SLOTS * C::CHUNK;        // key scale x c2, per token
     L.vsc = L.ksc + (size_t)TR * 4;                      // value scale, per token
     L.sc = L.vsc + (size_t)TR * 4;                       // scores [TR][G]
     L.wred = L.sc + (size_t)TR * G * 4;                  // per-warp maxima and sums [2][W][G]
-    L.total = L.wred + 2 * AT_WARPS * G * 4;
+    L.total = L.wred + 2 * C::W * G * 4;
     return L;
 }
 
+template <int N>
 __device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;" ::"r"(AT_CONSUMERS) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
@@ -159,8 +171,10 @@ __device__ __forceinline__ float reduce_heads(float (&v)[HG], int lane) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(AT_THREADS, 2) attn_decode_i8_kernel(const AttnParams p) {
-    constexpr int CT = AT_CHUNK / D;       // tokens per slot
+__global__ void __launch_bounds__(AtCfg<G>::THREADS, 2) attn_decode_i8_kernel(const AttnParams p) {
+    constexpr int W = AtCfg<G>::W, SLOTS = AtCfg<G>::SLOTS, CHUNK = AtCfg<G>::CHUNK;
+    constexpr int THREADS = AtCfg<G>::THREADS, CONSUMERS = AtCfg<G>::CONSUMERS;
+    constexpr int CT = CHUNK / D;          // tokens per slot
     constexpr int LPT = D / 16;            // score phase: lanes per token, 16 bytes each
     constexpr int TPW = 32 / LPT;          // tokens per warp step
     constexpr int HG = G < 4 ? G : 4;      // heads per pass of the score phase
@@ -172,13 +186,13 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_decode_i8_kernel(const Att
     extern __shared__ __align__(128) uint8_t smem[];
     const AttnLayout L = attn_layout<D, G>(p.TR);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *empty = full + AT_SLOTS;
+    uint64_t *empty = full + SLOTS;
     float *qs = reinterpret_cast<float *>(smem + L.qs);
     float *ksc = reinterpret_cast<float *>(smem + L.ksc);
     float *vsc = reinterpret_cast<float *>(smem + L.vsc);
     float *sc = reinterpret_cast<float *>(smem + L.sc);
     float *wmax = reinterpret_cast<float *>(smem + L.wred);
-    float *wsum = wmax + AT_WARPS * G;
+    float *wsum = wmax + W * G;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int z = blockIdx.x % p.S, bh = blockIdx.x / p.S;   // bh = b * Hkv + hk
@@ -198,7 +212,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_decode_i8_kernel(const Att
     const size_t orow = ((size_t)b * Hq + (size_t)hk * G) * D;   // first output row of this CTA
 
     if (nt == 0) {   // an empty range: a zero output, or an empty part
-        for (int i = threadIdx.x; i < G * D; i += AT_THREADS) {
+        for (int i = threadIdx.x; i < G * D; i += THREADS) {
             if (p.S == 1) {
                 p.out[orow + i] = 0.0f;
             } else {
@@ -216,7 +230,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_decode_i8_kernel(const Att
     const int nc = (nt + CT - 1) / CT;   // slots per phase
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < AT_SLOTS; s++) {
+        for (int s = 0; s < SLOTS; s++) {
             mbar_init(smem_addr(full + s), 1);
             mbar_init(smem_addr(empty + s), 1);
         }
@@ -225,60 +239,88 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_decode_i8_kernel(const Att
     __syncthreads();
 
     // ---------------------------------------------------------------- producer
-    if (warp == AT_WARPS) {
+    if (warp == W) {
         if (lane != 0) return;
         const size_t row0 = (size_t)bh * p.Tcap + t0;
         const int8_t *kbase = p.k + row0 * D, *vbase = p.v + row0 * D;
         const uint64_t policy = l2_evict_first_policy();
         int issued = 0;
         for (int i = 0; i < 2 * nc; i++) {
-            const int slot = i % AT_SLOTS;
-            if (i >= AT_SLOTS && !mbar_wait(smem_addr(empty + slot), (uint32_t)(((i / AT_SLOTS) - 1) & 1), p.status))
+            const int slot = i % SLOTS;
+            if (i >= SLOTS && !mbar_wait(smem_addr(empty + slot), (uint32_t)(((i / SLOTS) - 1) & 1), p.status))
                 break;
             const int c = i < nc ? i : i - nc;
             const uint32_t bytes = (uint32_t)(min(CT, nt - c * CT) * D);
             mbar_arrive_expect_tx(smem_addr(full + slot), bytes);
-            bulk_g2s_hint(smem_addr(smem + L.ring + (size_t)slot * AT_CHUNK), (i < nc ? kbase : vbase) + (size_t)c * CT * D,
+            bulk_g2s_hint(smem_addr(smem + L.ring + (size_t)slot * CHUNK), (i < nc ? kbase : vbase) + (size_t)c * CT * D,
                           bytes, smem_addr(full + slot), policy);
             issued = i + 1;
         }
         // Stay until every copy issued has landed, so that the CTA never ends with a bulk
         // copy in flight (the last copy into each slot completes that slot's last phase).
-        for (int i = max(0, issued - AT_SLOTS); i < issued; i++)
-            mbar_wait(smem_addr(full + i % AT_SLOTS), (uint32_t)((i / AT_SLOTS) & 1), p.status);
+        for (int i = max(0, issued - SLOTS); i < issued; i++)
+            mbar_wait(smem_addr(full + i % SLOTS), (uint32_t)((i / SLOTS) & 1), p.status);
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    const int ctid = threadIdx.x;   // 0 .. AT_CONSUMERS - 1
+    const int ctid = threadIdx.x;   // 0 .. CONSUMERS - 1
     {
+        // staging in batches of SB loads per thread, all issued before any is stored, so that
+        // the batch costs one memory latency (the producer streams keys meanwhile)
+        constexpr int SB = 8;
         const float *qg = p.q + orow;   // the G query rows of KV head hk are contiguous
-        for (int i = ctid; i < G * D; i += AT_CONSUMERS) qs[i] = qg[i];
-        const size_t srow = (size_t)bh * p.Tcap + t0;
-        for (int i = ctid; i < nt; i += AT_CONSUMERS) {
-            ksc[i] = p.ks[srow + i] * p.c2;
-            vsc[i] = p.vs[srow + i];
+        for (int i0 = 0; i0 < G * D; i0 += SB * CONSUMERS) {
+            float a[SB];
+#pragma unroll
+            for (int j = 0; j < SB; j++) {
+                const int i = i0 + j * CONSUMERS + ctid;
+                a[j] = i < G * D ? __ldg(qg + i) : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < SB; j++) {
+                const int i = i0 + j * CONSUMERS + ctid;
+                if (i < G * D) qs[i] = a[j];
+            }
+        }
+        const float *ksg = p.ks + (size_t)bh * p.Tcap + t0, *vsg = p.vs + (size_t)bh * p.Tcap + t0;
+        for (int i0 = 0; i0 < nt; i0 += SB * CONSUMERS) {
+            float a[SB], c[SB];
+#pragma unroll
+            for (int j = 0; j < SB; j++) {
+                const int i = i0 + j * CONSUMERS + ctid;
+                a[j] = i < nt ? __ldg(ksg + i) : 0.0f;
+                c[j] = i < nt ? __ldg(vsg + i) : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < SB; j++) {
+                const int i = i0 + j * CONSUMERS + ctid;
+                if (i < nt) {
+                    ksc[i] = a[j] * p.c2;
+                    vsc[i] = c[j];
+                }
+            }
         }
     }
-    consumer_sync();
+    consumer_sync<CONSUMERS>();
 
     const uint8_t *ring = smem + L.ring;
     bool failed = false;
     auto wait_slot = [&](int i) {
-        const bool ok = mbar_wait(smem_addr(full + i % AT_SLOTS), (uint32_t)((i / AT_SLOTS) & 1), p.status);
+        const bool ok = mbar_wait(smem_addr(full + i % SLOTS), (uint32_t)((i / SLOTS) & 1), p.status);
         failed |= !__all_sync(0xffffffffu, ok);
     };
     auto release_slot = [&](int i) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(empty + i % AT_SLOTS));
+        if (lane == 0) mbar_arrive(smem_addr(empty + i % SLOTS));
     };
 
-    // ---- scores: slot c of the key phase goes to warp c % AT_WARPS
+    // ---- scores: slot c of the key phase goes to warp c % W
     const int sl = lane % LPT;   // this lane's 16-byte column of a token row
-    for (int c = warp; c < nc; c += AT_WARPS) {
+    for (int c = warp; c < nc; c += W) {
         wait_slot(c);
         if (!failed) {
-            const uint8_t *chunk = ring + (size_t)(c % AT_SLOTS) * AT_CHUNK;
+            const uint8_t *chunk = ring + (size_t)(c % SLOTS) * CHUNK;
             const int ntok = min(CT, nt - c * CT);
 #pragma unroll 1
             for (int pass = 0; pass < G / HG; pass++) {
@@ -323,22 +365,22 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_decode_i8_kernel(const Att
         }
         release_slot(c);
     }
-    consumer_sync();
+    consumer_sync<CONSUMERS>();
 
     // ---- softmax over the row: thread ctid takes entries ctid, ctid + 128, ... (head ctid % G)
     const int gh = ctid % G;
     {
         float mx = -INFINITY;
-        for (int i = ctid; i < nt * G; i += AT_CONSUMERS) mx = fmaxf(mx, sc[i]);
+        for (int i = ctid; i < nt * G; i += CONSUMERS) mx = fmaxf(mx, sc[i]);
 #pragma unroll
         for (int m = 16; m >= G; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
         if (lane < G) wmax[warp * G + lane] = mx;
-        consumer_sync();
+        consumer_sync<CONSUMERS>();
         float M = wmax[gh];
 #pragma unroll
-        for (int w = 1; w < AT_WARPS; w++) M = fmaxf(M, wmax[w * G + gh]);
+        for (int w = 1; w < W; w++) M = fmaxf(M, wmax[w * G + gh]);
         float l = 0.0f;
-        for (int i = ctid; i < nt * G; i += AT_CONSUMERS) {
+        for (int i = ctid; i < nt * G; i += CONSUMERS) {
             const float e = exp2f(sc[i] - M);
             l += e;
             sc[i] = e * vsc[i / G];
@@ -347,19 +389,19 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_decode_i8_kernel(const Att
         for (int m = 16; m >= G; m >>= 1) l += __shfl_xor_sync(0xffffffffu, l, m);
         if (lane < G) wsum[warp * G + lane] = l;
     }
-    consumer_sync();
+    consumer_sync<CONSUMERS>();
 
-    // ---- values: slot nc + c goes to warp c % AT_WARPS
+    // ---- values: slot nc + c goes to warp c % W
     uint64_t acc[G][VB / 2];
 #pragma unroll
     for (int g = 0; g < G; g++)
 #pragma unroll
         for (int j = 0; j < VB / 2; j++) acc[g][j] = 0ull;
     const int vl = lane % LPV;
-    for (int c = warp; c < nc; c += AT_WARPS) {
+    for (int c = warp; c < nc; c += W) {
         wait_slot(nc + c);
         if (!failed) {
-            const uint8_t *chunk = ring + (size_t)((nc + c) % AT_SLOTS) * AT_CHUNK;
+            const uint8_t *chunk = ring + (size_t)((nc + c) % SLOTS) * CHUNK;
             const int ntok = min(CT, nt - c * CT);
 #pragma unroll 2
             for (int it = 0; it < ntok; it += TPV) {
@@ -407,7 +449,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_decode_i8_kernel(const Att
                 hi += __shfl_xor_sync(0xffffffffu, hi, m);
                 acc[g][j] = pack2(lo, hi);
             }
-    consumer_sync();   // every warp is done with the ring: it holds the per-warp sums now
+    consumer_sync<CONSUMERS>();   // every warp is done with the ring: it holds the per-warp sums now
     float *red = reinterpret_cast<float *>(smem + L.ring);   // [W][G][D]
     if (lane < LPV) {
 #pragma unroll
@@ -420,15 +462,15 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_decode_i8_kernel(const Att
                 red[((size_t)warp * G + g) * D + vl * VB + 2 * j + 1] = hi;
             }
     }
-    consumer_sync();
-    for (int i = ctid; i < G * D; i += AT_CONSUMERS) {
+    consumer_sync<CONSUMERS>();
+    for (int i = ctid; i < G * D; i += CONSUMERS) {
         const int g = i / D, d = i % D;
         float o = red[(size_t)g * D + d];
 #pragma unroll
-        for (int w = 1; w < AT_WARPS; w++) o += red[((size_t)w * G + g) * D + d];
+        for (int w = 1; w < W; w++) o += red[((size_t)w * G + g) * D + d];
         float l = wsum[g], M = wmax[g];
 #pragma unroll
-        for (int w = 1; w < AT_WARPS; w++) {
+        for (int w = 1; w < W; w++) {
             l += wsum[w * G + g];
             M = fmaxf(M, wmax[w * G + g]);
         }
@@ -528,7 +570,7 @@ gq_status pdl_launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStr
 
 template <int D, int G>
 gq_status launch_attn_dg(const AttnParams &base, int64_t B, int64_t Tcap, cudaStream_t s) {
-    constexpr int CT = AT_CHUNK / D;
+    constexpr int CT = AtCfg<G>::CHUNK / D;
     auto kernel = attn_decode_i8_kernel<D, G>;
     // tokens per CTA: what the shared-memory row of scores holds, and few enough that
     // (sequence, KV head, range) work items fill the GPU twice over
@@ -552,10 +594,18 @@ gq_status launch_attn_dg(const AttnParams &base, int64_t B, int64_t Tcap, cudaSt
         p.part = reinterpret_cast<float *>(ws.data);
     }
     const size_t smem = attn_layout<D, G>((int)TR).total;
-    KV_TRY(check_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-                               "attention shared-memory attribute"));
+    if (smem > AT_SMEM_MAX) return fail(GQ_ERR_INVALID_ARG, "attention layout of %zu bytes", smem);
+    static std::atomic<bool> smem_set[64];   // per device: the opt-in to AT_SMEM_MAX bytes
+    int dev = 0;
+    KV_TRY(check_cuda(cudaGetDevice(&dev), "cudaGetDevice"));
+    if (dev < 0 || dev >= 64) return fail(GQ_ERR_UNSUPPORTED_DEVICE, "device index %d", dev);
+    if (!smem_set[dev].load(std::memory_order_acquire)) {
+        KV_TRY(check_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AT_SMEM_MAX),
+                          "attention shared-memory attribute"));
+        smem_set[dev].store(true, std::memory_order_release);
+    }
     void *args[] = {(void *)&p};
-    KV_TRY(pdl_launch((const void *)kernel, dim3((unsigned)(items * S)), dim3(AT_THREADS), smem, s, args));
+    KV_TRY(pdl_launch((const void *)kernel, dim3((unsigned)(items * S)), dim3(AtCfg<G>::THREADS), smem, s, args));
     if (S > 1) {
         const float *part = p.part;
         int Si = (int)S, Di = D;
