@@ -404,6 +404,14 @@ gq_status gq_debug_block_dots_q4_0(const void *q4_repacked, const void *q8_block
                                    int32_t *sumi, int64_t M, int64_t N, int64_t K,
                                    cudaStream_t stream);
 
+/* The failure path of the bounded in-kernel waits, for tests: launches one warp that
+ * waits, `limit` polls at most (1 .. 2^22), on an mbarrier that nothing completes and
+ * that no copy signals, so the wait gives up and the kernel returns.  The next
+ * gq_last_error() then returns GQ_ERR_TIMEOUT (and clears it); nothing else is
+ * touched, and the products that follow on the device run as before.  Not a product
+ * entry point. */
+gq_status gq_debug_wait_timeout(uint32_t limit, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

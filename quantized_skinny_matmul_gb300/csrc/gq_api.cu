@@ -559,6 +559,36 @@ gq_status gq_debug_block_dots_q4_0(const void *q4_repacked, const void *q8_block
 
 }  // extern "C"
 
+// ---- the wait-timeout probe (verification) --------------------------------------------
+
+namespace gq {
+// One warp waits, with the given poll limit, on an mbarrier that nothing arrives on and
+// no copy signals: phase 0 never completes, so every wait gives up, records the timeout
+// in the device status word and returns; the kernel then invalidates the barrier and ends.
+__global__ void wait_probe_kernel(unsigned int *status, uint32_t limit) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    mbar_wait(smem_addr(&bar), 0u, status, limit);
+    __syncthreads();
+    if (threadIdx.x == 0) asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_addr(&bar)) : "memory");
+}
+}  // namespace gq
+
+extern "C" gq_status gq_debug_wait_timeout(uint32_t limit, cudaStream_t stream) {
+    if (limit == 0 || limit > WAIT_LIMIT)
+        return fail(GQ_ERR_INVALID_ARG, "limit must be in [1, %u] (got %u)", WAIT_LIMIT, limit);
+    GQ_TRY(check_device());
+    unsigned int *status = device_status_word();
+    if (!status) return fail(GQ_ERR_CUDA, "device status word unavailable");
+    wait_probe_kernel<<<1, 32, 0, stream>>>(status, limit);
+    GQ_TRY(check_cuda(cudaGetLastError(), "wait probe launch"));
+    return ok();
+}
+
 // ---- INT8 KV cache ------------------------------------------------------------------
 
 namespace {

@@ -408,10 +408,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity; gives up after WAIT_LIMIT polls,
-// records the timeout in the device status word and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int *status) {
-    for (uint32_t i = 0; i < WAIT_LIMIT; i++)
+// Waits for the phase with the given parity; gives up after `limit` polls, records the
+// timeout in the device status word and returns false.  The product kernels use the
+// fixed WAIT_LIMIT: a shorter limit inside a pipeline would let a consumer give up on a
+// copy that is still landing.  The wait-timeout probe passes its own limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int *status,
+                                          uint32_t limit = WAIT_LIMIT) {
+    for (uint32_t i = 0; i < limit; i++)
         if (mbar_try_wait(bar, parity)) return true;
     flag_timeout(status);
     return false;

@@ -114,6 +114,8 @@ def test_argument_checks_other_entries(lib):
     assert lib.gq_debug_block_dots_q4_0(FAKE, FAKE, ODD, 1, 16, 64, None) == gq.GQ_ERR_MISALIGNED
     assert lib.gq_mul_mat_q4_0_f32_path(FAKE, FAKE, FAKE, 1, 64, 64, 7, None) == gq.GQ_ERR_INVALID_ARG
     assert lib.gq_set_m_threshold(-1) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_debug_wait_timeout(0, None) == gq.GQ_ERR_INVALID_ARG
+    assert lib.gq_debug_wait_timeout((1 << 22) + 1, None) == gq.GQ_ERR_INVALID_ARG
     assert lib.gq_set_m_threshold(16) == gq.GQ_OK and lib.gq_get_m_threshold() == 16
 
 
