@@ -339,6 +339,10 @@ def run_ours(args, rank, world, local):
         dist.barrier()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(b.stream):
+        # untimed pre-roll: the start event then waits behind W warm-up steps, long enough for
+        # the host to submit the timed graphs, so the host latency of the first graph launch is
+        # not inside the timed region (it would be ~3 % of a 20-step region)
+        warm_plan[0].replay()
         start.record(b.stream)
         for g in timed_plan:              # exactly K timed steps
             g.replay()
@@ -394,6 +398,8 @@ def run_ours(args, rank, world, local):
         "config": {"workload": "7B-shaped single-token decode matvecs, Q4_0 [4096,4096]+[11008,4096]+[4096,11008], M=1",
                    "M": M, "shapes_NxK": [list(s) for s in SHAPES], "weight_copies": C,
                    "l2_defeat": f"{C} rotating weight copies, {C * set_bytes / 2**20:.0f} MiB > 4x L2",
+                   "timing": "CUDA events around CUDA-graph replays of exactly K steps; the start event "
+                             "follows an untimed replay of warm-up steps on the same stream",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
@@ -407,6 +413,10 @@ def run_ours(args, rank, world, local):
                        "kernel": "gemv_m1_q4_0_kernel<16>", "launches": launches_per_step * args.steps,
                        "algorithmic_bytes_per_launch": round(bytes_per_step / launches_per_step)}
 
+    # the integer-ALU ceiling of the same kernel: a dp4a throughput probe on this GPU, and the
+    # dp4a rate the timed step needed (8 dp4a per 32-weight block: one block dot)
+    out["roofline"]["alu"] = dp4a_roofline(b, sum(N * K // 32 * 8 for N, K in SHAPES) * args.steps / t)
+
     if rank == 0 and world == 1:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
 
@@ -417,6 +427,29 @@ def run_ours(args, rank, world, local):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def dp4a_roofline(b, needed_per_s):
+    """dp4a/s of a throughput probe (8 independent chains per thread, 8 CTAs of 256 per SM),
+    and the fraction of it that `needed_per_s` dp4a/s is."""
+    torch, gq = b.torch, b.gq
+    blocks = 8 * b.props.multi_processor_count
+    sink = torch.empty(blocks * 256, dtype=torch.int32, device=b.dev)
+    iters = 20000
+    with torch.cuda.stream(b.stream):
+        for _ in range(2):
+            gq.gq_debug_dp4a_probe(iters, sink, blocks, stream=b.stream)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(b.stream)
+        for _ in range(5):
+            gq.gq_debug_dp4a_probe(iters, sink, blocks, stream=b.stream)
+        end.record(b.stream)
+    end.synchronize()
+    t = start.elapsed_time(end) / 1e3 / 5
+    peak = blocks * 256 * 8 * iters / t
+    return {"bound": "alu", "unit": "dp4a/s", "peak": float(f"{peak:.4g}"), "needed": float(f"{needed_per_s:.4g}"),
+            "frac": round(needed_per_s / peak, 4),
+            "peak_source": "measured: dp4a probe, 8 independent chains per thread, 8 x 256 threads per SM"}
 
 
 def attn_bytes(lens, Hq, Hkv, D):

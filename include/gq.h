@@ -404,6 +404,11 @@ gq_status gq_debug_block_dots_q4_0(const void *q4_repacked, const void *q8_block
                                    int32_t *sumi, int64_t M, int64_t N, int64_t K,
                                    cudaStream_t stream);
 
+/* dp4a throughput probe, for the benchmark's ALU roofline: `blocks` CTAs of 256 threads,
+ * each thread 8 * iters independent dp4a (int8 x4 dot with int32 accumulate); writes one
+ * int per thread to sink [blocks * 256].  Not a product entry point. */
+gq_status gq_debug_dp4a_probe(int64_t iters, int *sink, int64_t blocks, cudaStream_t stream);
+
 /* The failure path of the bounded in-kernel waits, for tests: launches one warp that
  * waits, `limit` polls at most (1 .. 2^22), on an mbarrier that nothing completes and
  * that no copy signals, so the wait gives up and the kernel returns.  The next

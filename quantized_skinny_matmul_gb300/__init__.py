@@ -49,6 +49,7 @@ _S = ctypes.c_int
 # name -> (argtypes, restype); the signatures of include/gq.h
 SIGNATURES = {
     "gq_debug_wait_timeout": ([ctypes.c_uint32, _P], _S),
+    "gq_debug_dp4a_probe": ([_I, _P, _I, _P], _S),
     "gq_kv_quantize_i8": ([_P, _P, _P, _I, _I, _P], _S),
     "gq_kv_append_i8": ([_P, _P, _P, _P, _I, _I, _I, _I, _P], _S),
     "gq_attn_decode_i8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P], _S),
@@ -343,6 +344,10 @@ def gq_debug_block_dots_q4_0(q4_repacked, q8_blocks, sumi, M: int, N: int, K: in
 
 def gq_debug_wait_timeout(limit: int, stream=None) -> None:
     _check(lib().gq_debug_wait_timeout(limit, _stream(stream)), "gq_debug_wait_timeout")
+
+
+def gq_debug_dp4a_probe(iters: int, sink, blocks: int, stream=None) -> None:
+    _check(lib().gq_debug_dp4a_probe(iters, _ptr(sink), blocks, _stream(stream)), "gq_debug_dp4a_probe")
 
 
 def gq_kv_quantize_i8(x, q, scale, rows: int, D: int, stream=None) -> None:

@@ -578,6 +578,35 @@ __global__ void wait_probe_kernel(unsigned int *status, uint32_t limit) {
 }
 }  // namespace gq
 
+namespace gq {
+// dp4a throughput probe: every thread runs `iters` rounds of 8 independent dp4a chains and
+// stores one sum (so that nothing is optimized away).  8 * iters dp4a per thread.
+__global__ void dp4a_probe_kernel(int64_t iters, int *sink) {
+    int a[8];
+    const int x = (int)threadIdx.x * 0x01010101, y = (int)blockIdx.x | 0x03050709;
+#pragma unroll
+    for (int j = 0; j < 8; j++) a[j] = j;
+    for (int64_t i = 0; i < iters; i++) {
+#pragma unroll
+        for (int j = 0; j < 8; j++) a[j] = __dp4a(x + j, y, a[j]);
+    }
+    int t = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) t += a[j];
+    sink[(size_t)blockIdx.x * blockDim.x + threadIdx.x] = t;
+}
+}  // namespace gq
+
+extern "C" gq_status gq_debug_dp4a_probe(int64_t iters, int *sink, int64_t blocks, cudaStream_t stream) {
+    if (iters <= 0 || blocks <= 0 || blocks > (1LL << 20))
+        return fail(GQ_ERR_INVALID_ARG, "iters and blocks must be positive (blocks <= 2^20)");
+    GQ_TRY(check_ptr(sink, "sink"));
+    GQ_TRY(check_device());
+    dp4a_probe_kernel<<<(unsigned)blocks, 256, 0, stream>>>(iters, sink);
+    GQ_TRY(check_cuda(cudaGetLastError(), "dp4a probe launch"));
+    return ok();
+}
+
 extern "C" gq_status gq_debug_wait_timeout(uint32_t limit, cudaStream_t stream) {
     if (limit == 0 || limit > WAIT_LIMIT)
         return fail(GQ_ERR_INVALID_ARG, "limit must be in [1, %u] (got %u)", WAIT_LIMIT, limit);

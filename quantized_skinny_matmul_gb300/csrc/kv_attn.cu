@@ -107,6 +107,27 @@ __host__ __device__ AttnLayout attn_layout(int TR) {
     return L;
 }
 
+// Shared-memory accesses with the state space explicit (a generic access to shared memory
+// costs an address-space check and waits on the long scoreboard).
+__device__ __forceinline__ uint4 sh_ld128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 sh_ld64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float sh_ldf(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sh_stf(uint32_t a, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
 template <int N>
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
@@ -304,7 +325,8 @@ __global__ void __launch_bounds__(AtCfg<G>::THREADS, 2) attn_decode_i8_kernel(co
     }
     consumer_sync<CONSUMERS>();
 
-    const uint8_t *ring = smem + L.ring;
+    const uint32_t ring_a = smem_addr(smem + L.ring), sc_a = smem_addr(sc), ksc_a = smem_addr(ksc),
+                   qs_a = smem_addr(qs);
     bool failed = false;
     auto wait_slot = [&](int i) {
         const bool ok = mbar_wait(smem_addr(full + i % SLOTS), (uint32_t)((i / SLOTS) & 1), p.status);
@@ -320,26 +342,26 @@ __global__ void __launch_bounds__(AtCfg<G>::THREADS, 2) attn_decode_i8_kernel(co
     for (int c = warp; c < nc; c += W) {
         wait_slot(c);
         if (!failed) {
-            const uint8_t *chunk = ring + (size_t)(c % SLOTS) * CHUNK;
+            const uint32_t chunk = ring_a + (uint32_t)((c % SLOTS) * CHUNK);
             const int ntok = min(CT, nt - c * CT);
 #pragma unroll 1
             for (int pass = 0; pass < G / HG; pass++) {
                 uint64_t qv[HG][8];
 #pragma unroll
                 for (int h = 0; h < HG; h++) {
-                    const float *qrow = qs + (pass * HG + h) * D + sl * 16;
+                    const uint32_t qrow = qs_a + (uint32_t)(((pass * HG + h) * D + sl * 16) * 4);
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
-                        const float4 f = *reinterpret_cast<const float4 *>(qrow + 4 * j);
-                        qv[h][2 * j] = pack2(f.x, f.y);
-                        qv[h][2 * j + 1] = pack2(f.z, f.w);
+                        const uint4 f = sh_ld128(qrow + 16 * j);
+                        qv[h][2 * j] = pack2(__uint_as_float(f.x), __uint_as_float(f.y));
+                        qv[h][2 * j + 1] = pack2(__uint_as_float(f.z), __uint_as_float(f.w));
                     }
                 }
-#pragma unroll 2
+#pragma unroll 4
                 for (int it = 0; it < ntok; it += TPW) {
                     const int tok = it + lane / LPT;
                     uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                    if (tok < ntok) w = lds128(chunk + (size_t)tok * D + sl * 16);
+                    if (tok < ntok) w = sh_ld128(chunk + (uint32_t)(tok * D + sl * 16));
                     uint64_t kf[8];
                     widen4(w.x, kf[0], kf[1]);
                     widen4(w.y, kf[2], kf[3]);
@@ -358,7 +380,7 @@ __global__ void __launch_bounds__(AtCfg<G>::THREADS, 2) attn_decode_i8_kernel(co
                     const float s = reduce_heads<HG, LPT>(part, lane);
                     if (tok < ntok && (sl % (LPT / HG)) == 0) {
                         const int t = c * CT + tok, h = pass * HG + sl / (LPT / HG);
-                        sc[t * G + h] = s * ksc[t];
+                        sh_stf(sc_a + 4u * (uint32_t)(t * G + h), s * sh_ldf(ksc_a + 4u * (uint32_t)t));
                     }
                 }
             }
@@ -401,22 +423,21 @@ __global__ void __launch_bounds__(AtCfg<G>::THREADS, 2) attn_decode_i8_kernel(co
     for (int c = warp; c < nc; c += W) {
         wait_slot(nc + c);
         if (!failed) {
-            const uint8_t *chunk = ring + (size_t)((nc + c) % SLOTS) * CHUNK;
+            const uint32_t chunk = ring_a + (uint32_t)(((nc + c) % SLOTS) * CHUNK);
             const int ntok = min(CT, nt - c * CT);
-#pragma unroll 2
+#pragma unroll 4
             for (int it = 0; it < ntok; it += TPV) {
                 const int tok = it + lane / LPV;
                 const bool live = tok < ntok;
                 uint32_t wv[VB / 4];
                 if constexpr (VB == 16) {
-                    const uint4 w = live ? lds128(chunk + (size_t)tok * D + vl * 16) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 w = live ? sh_ld128(chunk + (uint32_t)(tok * D + vl * 16)) : make_uint4(0u, 0u, 0u, 0u);
                     wv[0] = w.x;
                     wv[1] = w.y;
                     wv[2] = w.z;
                     wv[3] = w.w;
                 } else {
-                    const uint2 w = live ? *reinterpret_cast<const uint2 *>(chunk + (size_t)tok * D + vl * 8)
-                                         : make_uint2(0u, 0u);
+                    const uint2 w = live ? sh_ld64(chunk + (uint32_t)(tok * D + vl * 8)) : make_uint2(0u, 0u);
                     wv[0] = w.x;
                     wv[1] = w.y;
                 }
@@ -426,7 +447,7 @@ __global__ void __launch_bounds__(AtCfg<G>::THREADS, 2) attn_decode_i8_kernel(co
                 const int t = c * CT + (live ? tok : 0);
 #pragma unroll
                 for (int g = 0; g < G; g++) {
-                    const float wt = live ? sc[t * G + g] : 0.0f;
+                    const float wt = live ? sh_ldf(sc_a + 4u * (uint32_t)(t * G + g)) : 0.0f;
                     const uint64_t w2 = pack2(wt, wt);
 #pragma unroll
                     for (int j = 0; j < VB / 2; j++) acc[g][j] = fma2(w2, vf[j], acc[g][j]);
