@@ -92,6 +92,10 @@ gq_status launch_kv_append_i8(const float *x, int8_t *q, float *scale, const int
 gq_status launch_attn_decode_i8(const float *q, const int8_t *k, const float *ks, const int8_t *v, const float *vs,
                                 const int32_t *lens, float *out, int64_t B, int64_t Hq, int64_t Hkv, int64_t Tcap,
                                 int64_t D, float softmax_scale, cudaStream_t s);
+// A 2D tensor map (`map` points to a 64-byte-aligned CUtensorMap) over `rows` rows of 128
+// bytes at `base`: boxes of 128 bytes x box_rows rows, 128-byte swizzle, rows past the end
+// read as zeros.
+gq_status byte_rows_map(void *map, const void *base, int64_t rows, int box_rows);
 gq_status launch_block_dots_q4_0(const void *rep, const void *q8, int32_t *sumi, int64_t M,
                                  int64_t N, int64_t K, cudaStream_t s);
 

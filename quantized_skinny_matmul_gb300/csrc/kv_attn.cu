@@ -38,6 +38,8 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "gq_common.cuh"
@@ -508,6 +510,464 @@ __global__ void __launch_bounds__(AtCfg<G>::THREADS, 2) attn_decode_i8_kernel(co
     }
 }
 
+// ---------------------------------------------------------------------------
+// The same attention on the tensor cores (D = 128).  With G query rows per KV head the two
+// products are [G x D] . [D x T] and [G x T] . [T x D]: G multiply-adds per cached byte, which
+// the FP32 lanes cannot issue at the memory rate once G reaches about four.  Here both run as
+// m16n8k16 fp16 MMAs with f32 accumulation:
+//   * the int8 codes become exact fp16 values (the byte, biased by 128, in the mantissa of
+//     1024, then 1152 subtracted);
+//   * the query (scores) and the softmax weights (values) are f32 values split into two fp16
+//     terms, hi = fp16(x) and lo = fp16(x - hi), after a power-of-two scaling that puts the
+//     largest in [2^14, 2^15): hi + lo carries x to within 2^-22 of its magnitude, and each
+//     fp16 x fp16 product is exact, so the products keep f32 accuracy;
+//   * the cache comes in through 2D tensor copies with the 128-byte swizzle (16-byte chunk c of
+//     row r lands at chunk c ^ (r mod 8)), which keeps the fragment loads free of bank
+//     conflicts.
+// Scores: MMA rows are 16 tokens, columns (head, hi / lo) pairs; the k order inside each 16
+// steps is permuted the same way for both operands (lane t takes the 16 bytes of chunk 2t + h
+// of its two rows).  Values: MMA rows are 16 of the 128 value positions, columns (head,
+// hi / lo) pairs, k the 16 tokens of a step; the hi and lo columns of a head sit in one lane.
+template <int G>
+struct AmCfg {
+    static constexpr int D = 128;
+    static constexpr int W = G <= 2 ? 8 : 4;          // consumer warps
+    static constexpr int CT = 32;                      // tokens per slot
+    static constexpr int CHUNK = CT * D;               // 4 KB
+    static constexpr int SLOTS = 16;                   // a multiple of W
+    static constexpr int THREADS = (W + 1) * 32;
+    static constexpr int CONSUMERS = W * 32;
+    static constexpr int NN = G <= 4 ? 1 : 2;          // column tiles of the score MMA
+    static constexpr int ROWS = 2 * G;                 // (head, hi / lo) rows of the value MMA
+};
+
+struct AmLayout {
+    size_t bars, ring, qf, hsc, ksc, vsc, sc, sp, wred, total;
+    int trp;   // f16 entries per row of sp (TR padded so that rows start in different banks)
+};
+
+template <int G>
+__host__ __device__ AmLayout am_layout(int TR) {
+    using C = AmCfg<G>;
+    AmLayout L{};
+    L.trp = TR + 8;
+    L.bars = 0;                                                 // full[16], empty[16]
+    L.ring = 1024;                                              // 1024-byte aligned slots (swizzle)
+    L.qf = L.ring + (size_t)C::SLOTS * C::CHUNK;                // the query split: [2G][128] fp16
+    L.hsc = L.qf + (size_t)C::ROWS * C::D * 2;                  // per head: 1 / its scaling
+    L.ksc = L.hsc + 64;                                         // key scale x c2, per token
+    L.vsc = L.ksc + (size_t)TR * 4;                             // value scale, per token
+    L.sc = L.vsc + (size_t)TR * 4;                              // scores [TR][G]
+    L.sp = L.sc + (size_t)TR * G * 4;                           // weights [2G][trp] fp16
+    L.wred = L.sp + (((size_t)C::ROWS * L.trp * 2 + 15) & ~(size_t)15);   // [W][G] max and sum, [W] value max
+    L.total = L.wred + (2 * C::W * G + C::W + 4) * 4;
+    return L;
+}
+
+template <int G>
+__host__ __device__ constexpr size_t am_fixed_bytes() {
+    using C = AmCfg<G>;
+    return 1024 + (size_t)C::SLOTS * C::CHUNK + (size_t)C::ROWS * C::D * 2 + 64 + (size_t)C::ROWS * 8 * 2 + 16 +
+           (2 * C::W * G + C::W + 4) * 4 + 1024;   // + the alignment of the dynamic base
+}
+
+__device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap *map, int row, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void sh_sth(uint32_t a, __half v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(__half_as_ushort(v)) : "memory");
+}
+
+__device__ __forceinline__ uint32_t sh_ld32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// The four int8 of a word as two exact fp16 pairs: bytes (0, 1) and (2, 3).
+__device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t &p01, uint32_t &p23) {
+    const uint32_t u = w ^ 0x80808080u;
+    const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+    uint32_t a = __byte_perm(u, 0x64646464u, 0x4140), b = __byte_perm(u, 0x64646464u, 0x4342);
+    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), off), hb = __hsub2(*reinterpret_cast<__half2 *>(&b), off);
+    p01 = *reinterpret_cast<uint32_t *>(&ha);
+    p23 = *reinterpret_cast<uint32_t *>(&hb);
+}
+
+// Byte j of x and byte j of y as one exact fp16 pair (x_j, y_j), for j = 0 .. 3 of the two words.
+__device__ __forceinline__ void i8x4_pairs_to_f16x2(uint32_t x, uint32_t y, uint32_t (&o)[4]) {
+    const uint32_t ux = x ^ 0x80808080u, uy = y ^ 0x80808080u;
+    const uint32_t i01 = __byte_perm(ux, uy, 0x5140), i23 = __byte_perm(ux, uy, 0x7362);   // x0 y0 x1 y1, x2 y2 x3 y3
+    const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    uint32_t t[4] = {__byte_perm(i01, 0x64646464u, 0x4140), __byte_perm(i01, 0x64646464u, 0x4342),
+                     __byte_perm(i23, 0x64646464u, 0x4140), __byte_perm(i23, 0x64646464u, 0x4342)};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        __half2 h = __hsub2(*reinterpret_cast<__half2 *>(&t[i]), off);
+        o[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
+    attn_mma_i8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                       const AttnParams p) {
+    using C = AmCfg<G>;
+    constexpr int D = C::D, W = C::W, CT = C::CT, CHUNK = C::CHUNK, SLOTS = C::SLOTS, NN = C::NN;
+    constexpr int THREADS = C::THREADS, CONSUMERS = C::CONSUMERS, ROWS = C::ROWS;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const AmLayout L = am_layout<G>(p.TR);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + SLOTS;
+    float *hsc = reinterpret_cast<float *>(smem + L.hsc);
+    float *ksc = reinterpret_cast<float *>(smem + L.ksc);
+    float *vsc = reinterpret_cast<float *>(smem + L.vsc);
+    float *sc = reinterpret_cast<float *>(smem + L.sc);
+    __half *sp = reinterpret_cast<__half *>(smem + L.sp);
+    float *wmax = reinterpret_cast<float *>(smem + L.wred);
+    float *wsum = wmax + W * G;
+    float *wvmax = wsum + W * G;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int z = blockIdx.x % p.S, bh = blockIdx.x / p.S;   // bh = b * Hkv + hk
+    const int b = bh / p.Hkv, hk = bh % p.Hkv;
+    const int Hq = p.Hkv * G;
+
+    pdl_launch_dependents();
+    pdl_wait();   // the cache, the queries and the lengths may come from the grid in front
+
+    int len = p.lens[b];
+    if (len < 0 || len > p.Tcap) {
+        if (threadIdx.x == 0) atomicOr(p.status, STATUS_RANGE);
+        len = 0;
+    }
+    const int t0 = z * p.TR;
+    const int nt = max(0, min(len, t0 + p.TR) - t0);
+    const size_t orow = ((size_t)b * Hq + (size_t)hk * G) * D;
+
+    if (nt == 0) {   // an empty range: a zero output, or an empty part
+        for (int i = threadIdx.x; i < G * D; i += THREADS) {
+            if (p.S == 1) {
+                p.out[orow + i] = 0.0f;
+            } else {
+                const int g = i / D, d = i % D;
+                float *pp = p.part + (((size_t)b * Hq + (size_t)hk * G + g) * p.S + z) * (D + 2);
+                pp[d] = 0.0f;
+                if (d == 0) {
+                    pp[D] = -INFINITY;
+                    pp[D + 1] = 0.0f;
+                }
+            }
+        }
+        return;
+    }
+    const int nc = (nt + CT - 1) / CT;   // slots per phase
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SLOTS; s++) {
+            mbar_init(smem_addr(full + s), 1);
+            mbar_init(smem_addr(empty + s), 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- producer
+    if (warp == W) {
+        if (lane != 0) return;
+        const int row0 = bh * p.Tcap + t0;   // first cache row of the range (rows of 128 bytes)
+        const uint64_t policy = l2_evict_first_policy();
+        int issued = 0;
+        for (int i = 0; i < 2 * nc; i++) {
+            const int slot = i % SLOTS;
+            if (i >= SLOTS && !mbar_wait(smem_addr(empty + slot), (uint32_t)(((i / SLOTS) - 1) & 1), p.status)) break;
+            const int c = i < nc ? i : i - nc;
+            // a whole box every time: rows past the range belong to the next range or lie past the
+            // tensor (read as zeros); their scores are not stored and their weights are zero
+            mbar_arrive_expect_tx(smem_addr(full + slot), (uint32_t)CHUNK);
+            tma_rows(smem_addr(smem + L.ring + (size_t)slot * CHUNK), i < nc ? &kmap : &vmap, row0 + c * CT,
+                     smem_addr(full + slot), policy);
+            issued = i + 1;
+        }
+        // stay until every copy issued has landed: the CTA never ends with a copy in flight
+        for (int i = max(0, issued - SLOTS); i < issued; i++)
+            mbar_wait(smem_addr(full + i % SLOTS), (uint32_t)((i / SLOTS) & 1), p.status);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int ctid = threadIdx.x;
+    const uint32_t qf_a = smem_addr(smem + L.qf), sp_a = smem_addr(sp), ring_a = smem_addr(smem + L.ring),
+                   sc_a = smem_addr(sc), ksc_a = smem_addr(ksc), vsc_a = smem_addr(vsc), hsc_a = smem_addr(hsc);
+    {
+        // the query rows, scaled by a power of two per head and split into fp16 hi / lo
+        for (int g = warp; g < G; g += W) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(p.q + orow + (size_t)g * D) + lane);
+            float am = absmax4(v);
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, m));
+            int ex = 0;
+            if (am > 0.0f) frexpf(am, &ex);                      // am = f 2^ex, f in [0.5, 1)
+            const float scale = am > 0.0f ? ldexpf(1.0f, 15 - ex) : 1.0f;
+            const float xs[4] = {v.x * scale, v.y * scale, v.z * scale, v.w * scale};
+            __half hi[4], lo[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                hi[i] = __float2half_rn(xs[i]);
+                lo[i] = __float2half_rn(xs[i] - __half2float(hi[i]));
+            }
+            __half *qh = reinterpret_cast<__half *>(smem + L.qf) + (2 * g) * D + 4 * lane;
+            __half *ql = qh + D;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                qh[i] = hi[i];
+                ql[i] = lo[i];
+            }
+            if (lane == 0) hsc[g] = am > 0.0f ? ldexpf(1.0f, ex - 15) : 1.0f;
+        }
+        // the token scales, in batches of SB loads per thread issued before any is stored
+        constexpr int SB = 8;
+        const float *ksg = p.ks + (size_t)bh * p.Tcap + t0, *vsg = p.vs + (size_t)bh * p.Tcap + t0;
+        float vmax = 0.0f;
+        for (int i0 = 0; i0 < nt; i0 += SB * CONSUMERS) {
+            float a[SB], c[SB];
+#pragma unroll
+            for (int j = 0; j < SB; j++) {
+                const int i = i0 + j * CONSUMERS + ctid;
+                a[j] = i < nt ? __ldg(ksg + i) : 0.0f;
+                c[j] = i < nt ? __ldg(vsg + i) : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < SB; j++) {
+                const int i = i0 + j * CONSUMERS + ctid;
+                if (i < nt) {
+                    ksc[i] = a[j] * p.c2;
+                    vsc[i] = c[j];
+                    vmax = fmaxf(vmax, fabsf(c[j]));
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, m));
+        if (lane == 0) wvmax[warp] = vmax;
+    }
+    consumer_sync<CONSUMERS>();
+
+    const int g8 = lane >> 2, t = lane & 3;   // m16n8k16 fragment coordinates
+    bool failed = false;
+    auto wait_slot = [&](int i) {
+        const bool ok = mbar_wait(smem_addr(full + i % SLOTS), (uint32_t)((i / SLOTS) & 1), p.status);
+        failed |= !__all_sync(0xffffffffu, ok);
+    };
+    auto release_slot = [&](int i) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(empty + i % SLOTS));
+    };
+
+    // ---- scores.  B fragments of the query split: column n = 8 nn + g8 is row n of qf (head n / 2,
+    // hi for even n, lo for odd); k-step (h, s) takes positions 16 (2t + h) + 4s + {0, 1} and {2, 3}.
+    uint32_t qb[NN][2][4][2];
+#pragma unroll
+    for (int nn = 0; nn < NN; nn++)
+#pragma unroll
+        for (int h = 0; h < 2; h++)
+#pragma unroll
+            for (int s = 0; s < 4; s++) {
+                const int n = 8 * nn + g8, d0 = 16 * (2 * t + h) + 4 * s;
+                const bool live = n < ROWS;
+                qb[nn][h][s][0] = live ? sh_ld32(qf_a + (uint32_t)((n * D + d0) * 2)) : 0u;
+                qb[nn][h][s][1] = live ? sh_ld32(qf_a + (uint32_t)((n * D + d0 + 2) * 2)) : 0u;
+            }
+    for (int c = warp; c < nc; c += W) {
+        wait_slot(c);
+        if (!failed) {
+            const uint32_t chunk = ring_a + (uint32_t)((c % SLOTS) * CHUNK);
+            const int ntok = min(CT, nt - c * CT);
+#pragma unroll
+            for (int mt = 0; mt < CT / 16; mt++) {
+                if (16 * mt >= ntok) break;
+                float acc[NN][4];
+#pragma unroll
+                for (int nn = 0; nn < NN; nn++) acc[nn][0] = acc[nn][1] = acc[nn][2] = acc[nn][3] = 0.0f;
+                const int ra = 16 * mt + g8;   // rows ra and ra + 8 of the slot: both are g8 mod 8
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const uint32_t ch = (uint32_t)(((2 * t + h) ^ g8) * 16);
+                    const uint4 wa = sh_ld128(chunk + (uint32_t)(ra * D) + ch);
+                    const uint4 wb = sh_ld128(chunk + (uint32_t)((ra + 8) * D) + ch);
+                    const uint32_t av[4] = {wa.x, wa.y, wa.z, wa.w}, bv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                    for (int s = 0; s < 4; s++) {
+                        uint32_t a0, a2, a1, a3;
+                        i8x4_to_f16x2(av[s], a0, a2);
+                        i8x4_to_f16x2(bv[s], a1, a3);
+#pragma unroll
+                        for (int nn = 0; nn < NN; nn++)
+                            mma_f16_16x8x16(acc[nn], a0, a1, a2, a3, qb[nn][h][s][0], qb[nn][h][s][1]);
+                    }
+                }
+#pragma unroll
+                for (int nn = 0; nn < NN; nn++) {
+                    const int head = 4 * nn + t;   // columns 2t, 2t + 1 of tile nn: (head, hi), (head, lo)
+                    if (head < G) {
+                        const int ta = c * CT + ra;
+                        const float hs = sh_ldf(hsc_a + 4u * (uint32_t)head);
+                        if (ra < ntok)
+                            sh_stf(sc_a + 4u * (uint32_t)(ta * G + head),
+                                   (acc[nn][0] + acc[nn][1]) * hs * sh_ldf(ksc_a + 4u * (uint32_t)ta));
+                        if (ra + 8 < ntok)
+                            sh_stf(sc_a + 4u * (uint32_t)((ta + 8) * G + head),
+                                   (acc[nn][2] + acc[nn][3]) * hs * sh_ldf(ksc_a + 4u * (uint32_t)(ta + 8)));
+                    }
+                }
+            }
+        }
+        release_slot(c);
+    }
+    consumer_sync<CONSUMERS>();
+
+    // ---- softmax over the row (thread ctid takes entries ctid, ctid + CONSUMERS, ...: head ctid % G)
+    const int gh = ctid % G;
+    float vscale;   // weights are scaled by this power of two so that the largest is below 2^15
+    {
+        float vm = wvmax[0];
+#pragma unroll
+        for (int w = 1; w < W; w++) vm = fmaxf(vm, wvmax[w]);
+        int ex = 0;
+        if (vm > 0.0f) frexpf(vm, &ex);
+        vscale = vm > 0.0f ? ldexpf(1.0f, 14 - ex) : 1.0f;   // e vs vscale < 2^15 (e <= 1)
+        float mx = -INFINITY;
+        for (int i = ctid; i < nt * G; i += CONSUMERS) mx = fmaxf(mx, sh_ldf(sc_a + 4u * (uint32_t)i));
+#pragma unroll
+        for (int m = 16; m >= G; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        if (lane < G) wmax[warp * G + lane] = mx;
+        consumer_sync<CONSUMERS>();
+        float M = wmax[gh];
+#pragma unroll
+        for (int w = 1; w < W; w++) M = fmaxf(M, wmax[w * G + gh]);
+        float l = 0.0f;
+        const uint32_t sp_hi = sp_a + (uint32_t)((2 * gh) * L.trp * 2), sp_lo = sp_hi + (uint32_t)(L.trp * 2);
+        for (int i = ctid; i < nt * G; i += CONSUMERS) {
+            const int tok = i / G;
+            const float e = exp2f(sh_ldf(sc_a + 4u * (uint32_t)i) - M);
+            l += e;
+            const float wv = e * sh_ldf(vsc_a + 4u * (uint32_t)tok) * vscale;
+            const __half hi = __float2half_rn(wv);
+            sh_sth(sp_hi + 2u * (uint32_t)tok, hi);
+            sh_sth(sp_lo + 2u * (uint32_t)tok, __float2half_rn(wv - __half2float(hi)));
+        }
+        // the tokens of the last 16-token step past the range weigh nothing
+        const int pad = ((nt + 15) & ~15) - nt;
+        for (int i = ctid; i < ROWS * pad; i += CONSUMERS) sp[(i / pad) * L.trp + nt + i % pad] = __float2half_rn(0.0f);
+#pragma unroll
+        for (int m = 16; m >= G; m >>= 1) l += __shfl_xor_sync(0xffffffffu, l, m);
+        if (lane < G) wsum[warp * G + lane] = l;
+    }
+    consumer_sync<CONSUMERS>();
+
+    // ---- values: D[position][column] = sum_t V[t][position] P[column][t], the MMA rows being
+    // 16 value positions (row g8 of row tile m is position 16 g8 + 2m, row g8 + 8 the next one:
+    // the 16 bytes a lane loads from each token row serve its rows of all 8 row tiles), the
+    // columns (head, hi / lo) pairs, k the 16 tokens of a step.
+    constexpr int NV = G <= 4 ? 1 : 2;   // column tiles of the value MMA
+    float acc[8][NV][4];
+#pragma unroll
+    for (int m = 0; m < 8; m++)
+#pragma unroll
+        for (int nv = 0; nv < NV; nv++) acc[m][nv][0] = acc[m][nv][1] = acc[m][nv][2] = acc[m][nv][3] = 0.0f;
+    for (int c = warp; c < nc; c += W) {
+        wait_slot(nc + c);
+        if (!failed) {
+            const uint32_t chunk = ring_a + (uint32_t)(((nc + c) % SLOTS) * CHUNK);
+            const int ntok = min(CT, nt - c * CT);
+#pragma unroll
+            for (int mt = 0; mt < CT / 16; mt++) {
+                if (16 * mt >= ntok) break;
+                const int tk = c * CT + 16 * mt;   // first token of the step in the range
+                // B: the weights of column n = 8 nv + g8 (sp row n) at tokens 2t, 2t + 1 and 2t + 8, 2t + 9
+                uint32_t pb[NV][2];
+#pragma unroll
+                for (int nv = 0; nv < NV; nv++) {
+                    const int n = 8 * nv + g8;
+                    const uint32_t a = sp_a + (uint32_t)((n * L.trp + tk + 2 * t) * 2);
+                    pb[nv][0] = n < ROWS ? sh_ld32(a) : 0u;
+                    pb[nv][1] = n < ROWS ? sh_ld32(a + 16) : 0u;
+                }
+                // A: positions 16 g8 .. 16 g8 + 15 (chunk g8) of slot rows r, r + 1, r + 8, r + 9
+                const int r = 16 * mt + 2 * t;
+                const uint4 v0 = sh_ld128(chunk + (uint32_t)(r * D) + (uint32_t)((g8 ^ (r & 7)) * 16));
+                const uint4 v1 = sh_ld128(chunk + (uint32_t)((r + 1) * D) + (uint32_t)((g8 ^ ((r + 1) & 7)) * 16));
+                const uint4 v8 = sh_ld128(chunk + (uint32_t)((r + 8) * D) + (uint32_t)((g8 ^ ((r + 8) & 7)) * 16));
+                const uint4 v9 = sh_ld128(chunk + (uint32_t)((r + 9) * D) + (uint32_t)((g8 ^ ((r + 9) & 7)) * 16));
+                const uint32_t x0[4] = {v0.x, v0.y, v0.z, v0.w}, x1[4] = {v1.x, v1.y, v1.z, v1.w};
+                const uint32_t x8[4] = {v8.x, v8.y, v8.z, v8.w}, x9[4] = {v9.x, v9.y, v9.z, v9.w};
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    uint32_t p01[4], p89[4];   // byte 4q + i of tokens (r, r + 1) and (r + 8, r + 9)
+                    i8x4_pairs_to_f16x2(x0[q], x1[q], p01);
+                    i8x4_pairs_to_f16x2(x8[q], x9[q], p89);
+#pragma unroll
+                    for (int i2 = 0; i2 < 2; i2++) {
+                        const int m = 2 * q + i2;   // row tile: positions 16 g8 + 2m (row g8), + 1 (row g8 + 8)
+#pragma unroll
+                        for (int nv = 0; nv < NV; nv++)
+                            mma_f16_16x8x16(acc[m][nv], p01[2 * i2], p01[2 * i2 + 1], p89[2 * i2], p89[2 * i2 + 1],
+                                            pb[nv][0], pb[nv][1]);
+                    }
+                }
+            }
+        }
+        release_slot(nc + c);
+    }
+
+    // ---- hi + lo (columns 2t and 2t + 1 of this lane), then the warps in order, then scale
+    consumer_sync<CONSUMERS>();   // every warp is done with the ring: it holds the per-warp sums now
+    float *red = reinterpret_cast<float *>(smem + L.ring);   // [W][G][D]
+#pragma unroll
+    for (int nv = 0; nv < NV; nv++) {
+        const int head = 4 * nv + t;
+        if (head < G) {
+            const uint32_t o = smem_addr(red) + 4u * (uint32_t)((warp * G + head) * D + 16 * g8);
+#pragma unroll
+            for (int m = 0; m < 8; m++) {
+                sh_stf(o + 8u * m, acc[m][nv][0] + acc[m][nv][1]);
+                sh_stf(o + 8u * m + 4u, acc[m][nv][2] + acc[m][nv][3]);
+            }
+        }
+    }
+    consumer_sync<CONSUMERS>();
+    const float inv_vscale = 1.0f / vscale;   // a power of two: exact
+    for (int i = ctid; i < G * D; i += CONSUMERS) {
+        const int g = i / D, d = i % D;
+        float o = red[(size_t)g * D + d];
+#pragma unroll
+        for (int w = 1; w < W; w++) o += red[((size_t)w * G + g) * D + d];
+        o *= inv_vscale;
+        float l = wsum[g], M = wmax[g];
+#pragma unroll
+        for (int w = 1; w < W; w++) {
+            l += wsum[w * G + g];
+            M = fmaxf(M, wmax[w * G + g]);
+        }
+        if (p.S == 1) {
+            p.out[orow + i] = o / l;
+        } else {
+            float *pp = p.part + (((size_t)b * Hq + (size_t)hk * G + g) * p.S + z) * (D + 2);
+            pp[d] = o;
+            if (d == 0) {
+                pp[D] = M;
+                pp[D + 1] = l;
+            }
+        }
+    }
+}
+
 // Merges the S parts of each output row in order: with M the largest part maximum,
 // out = sum_z 2^(m_z - M) o_z / sum_z 2^(m_z - M) l_z.  One CTA per row, one thread per column.
 __global__ void attn_merge_kernel(const float *part, float *out, int S, int D) {
@@ -637,6 +1097,66 @@ gq_status launch_attn_dg(const AttnParams &base, int64_t B, int64_t Tcap, cudaSt
     return GQ_OK;
 }
 
+template <int G>
+gq_status launch_attn_mma(const AttnParams &base, int64_t B, int64_t Tcap, cudaStream_t s) {
+    using C = AmCfg<G>;
+    constexpr int CT = C::CT;
+    auto kernel = attn_mma_i8_kernel<G>;
+    const int64_t per_token = 8 + 8 * G;
+    const int64_t room = (int64_t)AT_SMEM_MAX - (int64_t)am_fixed_bytes<G>();
+    const int64_t tr_max = std::max<int64_t>(CT, room / per_token / CT * CT);
+    const int64_t items = B * base.Hkv;
+    const int64_t want = (2 * (int64_t)sm_count() + items - 1) / items;
+    int64_t S = std::max<int64_t>((Tcap + tr_max - 1) / tr_max, std::min<int64_t>(want, (Tcap + CT - 1) / CT));
+    int64_t TR = ((Tcap + S - 1) / S + CT - 1) / CT * CT;
+    TR = std::min(TR, tr_max);
+    S = (Tcap + TR - 1) / TR;
+    if (items * S > INT32_MAX) return fail(GQ_ERR_INVALID_ARG, "attention grid too large");
+    AttnParams p = base;
+    p.S = (int)S;
+    p.TR = (int)TR;
+    float *out = p.out;
+    if (S > 1) {
+        Workspace ws{};
+        KV_TRY(get_workspace(s, 0, (size_t)B * base.Hkv * G * S * (C::D + 2) * sizeof(float), &ws));
+        p.part = reinterpret_cast<float *>(ws.data);
+    }
+    const size_t smem = am_layout<G>((int)TR).total + 1024;   // + the alignment of the dynamic base
+    if (smem > AT_SMEM_MAX + 1024) return fail(GQ_ERR_INVALID_ARG, "attention layout of %zu bytes", smem);
+    static std::atomic<bool> smem_set[64];
+    int dev = 0;
+    KV_TRY(check_cuda(cudaGetDevice(&dev), "cudaGetDevice"));
+    if (dev < 0 || dev >= 64) return fail(GQ_ERR_UNSUPPORTED_DEVICE, "device index %d", dev);
+    if (!smem_set[dev].load(std::memory_order_acquire)) {
+        KV_TRY(check_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(AT_SMEM_MAX + 1024)),
+                          "attention shared-memory attribute"));
+        smem_set[dev].store(true, std::memory_order_release);
+    }
+    alignas(64) CUtensorMap kmap, vmap;
+    const int64_t rows = B * base.Hkv * Tcap;
+    KV_TRY(byte_rows_map(&kmap, base.k, rows, CT));
+    KV_TRY(byte_rows_map(&vmap, base.v, rows, CT));
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(items * S));
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    KV_TRY(check_cuda(cudaLaunchKernelEx(&cfg, kernel, kmap, vmap, p), "attention (tensor cores) launch"));
+    if (S > 1) {
+        const float *part = p.part;
+        int Si = (int)S, Di = C::D;
+        void *margs[] = {(void *)&part, (void *)&out, (void *)&Si, (void *)&Di};
+        KV_TRY(pdl_launch((const void *)attn_merge_kernel, dim3((unsigned)(B * base.Hkv * G)), dim3(C::D), 0, s, margs));
+    }
+    return GQ_OK;
+}
+
 template <int D>
 gq_status launch_attn_d(const AttnParams &p, int64_t B, int64_t G, int64_t Tcap, cudaStream_t s) {
     switch (G) {
@@ -668,6 +1188,17 @@ gq_status launch_attn_decode_i8(const float *q, const int8_t *k, const float *ks
     p.c2 = softmax_scale * LOG2E;
     const int64_t G = Hq / Hkv;
     if (D == 64) return launch_attn_d<64>(p, B, G, Tcap, s);
+    // D = 128: the tensor-core kernel (its tensor maps address at most 2^32 - 1 rows), unless
+    // GQ_ATTN_FP32 asks for the FP32 one (a test and tuning switch)
+    const char *e = getenv("GQ_ATTN_FP32");
+    if (B * Hkv * Tcap <= 0xFFFFFFFFLL && !(e && *e && atoi(e) != 0)) {
+        switch (G) {
+            case 1: return launch_attn_mma<1>(p, B, Tcap, s);
+            case 2: return launch_attn_mma<2>(p, B, Tcap, s);
+            case 4: return launch_attn_mma<4>(p, B, Tcap, s);
+            case 8: return launch_attn_mma<8>(p, B, Tcap, s);
+        }
+    }
     return launch_attn_d<128>(p, B, G, Tcap, s);
 }
 

@@ -664,4 +664,20 @@ gq_status launch_tc_f16(const void *w16, const float *x, float *dst, int64_t M, 
     return launch_tc_common(false, w16, x, dst, M, N, K, s);
 }
 
+gq_status byte_rows_map(void *map, const void *base, int64_t rows, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    gq_status st = encoder(&enc);
+    if (st != GQ_OK) return st;
+    if (rows <= 0 || rows > 0xFFFFFFFFLL) return fail(GQ_ERR_INVALID_ARG, "tensor map of %lld rows", (long long)rows);
+    const cuuint64_t dims[2] = {128u, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {128u};
+    const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(reinterpret_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base),
+                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GQ_ERR_CUDA, "cuTensorMapEncodeTiled (byte rows) failed (%d)", (int)r);
+    return GQ_OK;
+}
+
 }  // namespace gq

@@ -10,17 +10,22 @@ f32 scale per token and head; decode attention widens them to f32.
 * The attention output is f32 arithmetic against the oracle's f64.  Bound per
   output element j, with u = 2^-24, S the largest |score| bound of the row
   (oracle's S) and E_j = sum_t p_t |vs_t v_tj| (oracle's E):
-    - a score is a dot of D terms split over lanes (at most 8 products and a sum
-      per f32 pair, a tree over the lanes of a token, the pair's halves), times the
-      key scale and the softmax scale in base 2: at most 15 roundings of terms
-      bounded by S, and 2 more for the subtraction of the maximum;
+    - a score is a dot of D terms: on the FP32 path split over lanes (at most 8
+      products and a sum per f32 pair, a tree over the lanes of a token); on the
+      tensor cores (D = 128) 8 MMA steps of 16 exact fp16 products each, with the
+      query carried as two fp16 terms to within 4u of each element, accumulated in
+      f32 (counted at 2u per step, in case the accumulation truncates); then the key
+      scale and the softmax scale in base 2: at most 15 roundings of terms bounded by
+      S on either path, and 2 more for the subtraction of the maximum;
     - exp2f is within 2 ulp (4u relative);
     - so every exponential, and hence the numerator and the denominator, is off by
       at most (34 S + 4) u relative, and p_t by twice that;
-    - the denominator and the output are sums in f32 of at most T / 128 + 9 and
-      T / 16 + 9 sequential roundings (lanes, then warps), plus the division and,
-      for split ranges, the merge (a few more roundings and one exp2f per part).
-  Taken together and doubled: |out_j - oracle_j| <= 2 (70 S + T / 8 + 64) u E_j.
+    - the denominator is a sum in f32 of at most T / 128 + 9 sequential roundings;
+      the output sums T / 4 tokens per warp at most (each tensor-core step adds 16
+      exact products of the two-term weights, again counted at 2u), then the warps,
+      the division and, for split ranges, the merge (a few more roundings and one
+      exp2f per part).
+  Taken together and doubled: |out_j - oracle_j| <= 2 (70 S + T / 2 + 64) u E_j.
 """
 import math
 
@@ -67,7 +72,7 @@ def edge_rows(seed, rows, D):
 
 
 def attn_tolerance(E, S, T):
-    return 2.0 * (70.0 * S[..., None] + T / 8.0 + 64.0) * U * E + 1e-30
+    return 2.0 * (70.0 * S[..., None] + T / 2.0 + 64.0) * U * E + 1e-30
 
 
 def assert_attention(got, want, E, S, T, what=""):
@@ -144,6 +149,13 @@ def test_attention_parity(oracle, B, Hq, Hkv, Tcap, D, lens):
         assert np.all(got[b] == 0)
     again = host(gq.attn_decode_i8(dev(qf), k, ks, v, vs, dev(lens), c))
     assert np.array_equal(again.view(np.uint32), got.view(np.uint32)), "not deterministic"
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tcap,D,lens", [CASES[0], CASES[2], CASES[3], CASES[6]])
+def test_attention_parity_fp32_kernel(oracle, monkeypatch, B, Hq, Hkv, Tcap, D, lens):
+    """The FP32 kernel, which serves D = 64, forced for D = 128 (GQ_ATTN_FP32), on the same cases."""
+    monkeypatch.setenv("GQ_ATTN_FP32", "1")
+    test_attention_parity(oracle, B, Hq, Hkv, Tcap, D, lens)
 
 
 def test_attention_dominant_score_and_zero_scale(oracle):
