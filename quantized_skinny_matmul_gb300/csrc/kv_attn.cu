@@ -539,27 +539,33 @@ struct AmCfg {
     static constexpr int CONSUMERS = W * 32;
     static constexpr int NN = G <= 4 ? 1 : 2;          // column tiles of the score MMA
     static constexpr int ROWS = 2 * G;                 // (head, hi / lo) rows of the value MMA
+    // eight heads: the weights replace the scores in place ([token][head] pairs of fp16), which
+    // halves the shared memory per token and so the number of CTAs a sequence is split over;
+    // fewer heads: the weights go to rows of their own ([2G][token] fp16), one 32-bit load per
+    // pair of tokens in the value steps
+    static constexpr bool INPLACE = G >= 8;
+    static constexpr int PER_TOKEN = 8 + 4 * G + (INPLACE ? 0 : 4 * G);   // shared bytes per token
 };
 
 struct AmLayout {
     size_t bars, ring, qf, hsc, ksc, vsc, sc, sp, wred, total;
-    int trp;   // f16 entries per row of sp (TR padded so that rows start in different banks)
+    int trp;   // fp16 entries per row of sp: TR padded so that the rows start in different banks
 };
 
 template <int G>
 __host__ __device__ AmLayout am_layout(int TR) {
     using C = AmCfg<G>;
     AmLayout L{};
-    L.trp = TR + 8;
     L.bars = 0;                                                 // full[16], empty[16]
     L.ring = 1024;                                              // 1024-byte aligned slots (swizzle)
     L.qf = L.ring + (size_t)C::SLOTS * C::CHUNK;                // the query split: [2G][128] fp16
     L.hsc = L.qf + (size_t)C::ROWS * C::D * 2;                  // per head: 1 / its scaling
     L.ksc = L.hsc + 64;                                         // key scale x c2, per token
     L.vsc = L.ksc + (size_t)TR * 4;                             // value scale, per token
-    L.sc = L.vsc + (size_t)TR * 4;                              // scores [TR][G]
-    L.sp = L.sc + (size_t)TR * G * 4;                           // weights [2G][trp] fp16
-    L.wred = L.sp + (((size_t)C::ROWS * L.trp * 2 + 15) & ~(size_t)15);   // [W][G] max and sum, [W] value max
+    L.sc = L.vsc + (size_t)TR * 4;                              // scores [TR][G] f32 (then weights, in place)
+    L.trp = TR + 8;
+    L.sp = L.sc + (size_t)TR * G * 4;                           // weights [2G][trp] fp16 (not in place)
+    L.wred = L.sp + (C::INPLACE ? 0 : (((size_t)C::ROWS * L.trp * 2 + 15) & ~(size_t)15));   // [W][G] max, sum; [W]
     L.total = L.wred + (2 * C::W * G + C::W + 4) * 4;
     return L;
 }
@@ -567,8 +573,9 @@ __host__ __device__ AmLayout am_layout(int TR) {
 template <int G>
 __host__ __device__ constexpr size_t am_fixed_bytes() {
     using C = AmCfg<G>;
-    return 1024 + (size_t)C::SLOTS * C::CHUNK + (size_t)C::ROWS * C::D * 2 + 64 + (size_t)C::ROWS * 8 * 2 + 16 +
-           (2 * C::W * G + C::W + 4) * 4 + 1024;   // + the alignment of the dynamic base
+    return 1024 + (size_t)C::SLOTS * C::CHUNK + (size_t)C::ROWS * C::D * 2 + 64 +
+           (C::INPLACE ? 0 : (size_t)C::ROWS * 8 * 2 + 16) + (2 * C::W * G + C::W + 4) * 4 +
+           1024;   // + the alignment of the dynamic base
 }
 
 __device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap *map, int row, uint32_t bar, uint64_t policy) {
@@ -581,6 +588,12 @@ __device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap *map, i
 
 __device__ __forceinline__ void sh_sth(uint32_t a, __half v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(__half_as_ushort(v)) : "memory");
+}
+
+__device__ __forceinline__ uint32_t sh_ldu16(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
 }
 
 __device__ __forceinline__ uint32_t sh_ld32(uint32_t a) {
@@ -629,7 +642,6 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
     float *ksc = reinterpret_cast<float *>(smem + L.ksc);
     float *vsc = reinterpret_cast<float *>(smem + L.vsc);
     float *sc = reinterpret_cast<float *>(smem + L.sc);
-    __half *sp = reinterpret_cast<__half *>(smem + L.sp);
     float *wmax = reinterpret_cast<float *>(smem + L.wred);
     float *wsum = wmax + W * G;
     float *wvmax = wsum + W * G;
@@ -703,7 +715,7 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
 
     // ---------------------------------------------------------------- consumers
     const int ctid = threadIdx.x;
-    const uint32_t qf_a = smem_addr(smem + L.qf), sp_a = smem_addr(sp), ring_a = smem_addr(smem + L.ring),
+    const uint32_t qf_a = smem_addr(smem + L.qf), ring_a = smem_addr(smem + L.ring), sp_a = smem_addr(smem + L.sp),
                    sc_a = smem_addr(sc), ksc_a = smem_addr(ksc), vsc_a = smem_addr(vsc), hsc_a = smem_addr(hsc);
     {
         // the query rows, scaled by a power of two per head and split into fp16 hi / lo
@@ -852,19 +864,31 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
 #pragma unroll
         for (int w = 1; w < W; w++) M = fmaxf(M, wmax[w * G + gh]);
         float l = 0.0f;
+        // each entry (token, head) becomes its weight as two fp16 terms: in place (the thread that
+        // reads an entry is the one that writes it), or into rows 2 head (hi) and 2 head + 1 (lo)
         const uint32_t sp_hi = sp_a + (uint32_t)((2 * gh) * L.trp * 2), sp_lo = sp_hi + (uint32_t)(L.trp * 2);
         for (int i = ctid; i < nt * G; i += CONSUMERS) {
             const int tok = i / G;
             const float e = exp2f(sh_ldf(sc_a + 4u * (uint32_t)i) - M);
             l += e;
             const float wv = e * sh_ldf(vsc_a + 4u * (uint32_t)tok) * vscale;
-            const __half hi = __float2half_rn(wv);
-            sh_sth(sp_hi + 2u * (uint32_t)tok, hi);
-            sh_sth(sp_lo + 2u * (uint32_t)tok, __float2half_rn(wv - __half2float(hi)));
+            const __half hi = __float2half_rn(wv), lo = __float2half_rn(wv - __half2float(hi));
+            if constexpr (C::INPLACE) {
+                sh_stf(sc_a + 4u * (uint32_t)i,
+                       __uint_as_float((uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16)));
+            } else {
+                sh_sth(sp_hi + 2u * (uint32_t)tok, hi);
+                sh_sth(sp_lo + 2u * (uint32_t)tok, lo);
+            }
         }
         // the tokens of the last 16-token step past the range weigh nothing
         const int pad = ((nt + 15) & ~15) - nt;
-        for (int i = ctid; i < ROWS * pad; i += CONSUMERS) sp[(i / pad) * L.trp + nt + i % pad] = __float2half_rn(0.0f);
+        if constexpr (C::INPLACE) {
+            for (int i = nt * G + ctid; i < (nt + pad) * G; i += CONSUMERS) sh_stf(sc_a + 4u * (uint32_t)i, 0.0f);
+        } else {
+            for (int i = ctid; i < ROWS * pad; i += CONSUMERS)
+                sh_sth(sp_a + 2u * (uint32_t)((i / pad) * L.trp + nt + i % pad), __float2half_rn(0.0f));
+        }
 #pragma unroll
         for (int m = 16; m >= G; m >>= 1) l += __shfl_xor_sync(0xffffffffu, l, m);
         if (lane < G) wsum[warp * G + lane] = l;
@@ -890,14 +914,24 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
             for (int mt = 0; mt < CT / 16; mt++) {
                 if (16 * mt >= ntok) break;
                 const int tk = c * CT + 16 * mt;   // first token of the step in the range
-                // B: the weights of column n = 8 nv + g8 (sp row n) at tokens 2t, 2t + 1 and 2t + 8, 2t + 9
+                // B: the weights of column n = 8 nv + g8 (head n / 2, hi for even n, lo for odd) at tokens
+                // 2t, 2t + 1 and 2t + 8, 2t + 9: the fp16 at byte 2 (n % 2) of entry (token, head)
                 uint32_t pb[NV][2];
 #pragma unroll
                 for (int nv = 0; nv < NV; nv++) {
                     const int n = 8 * nv + g8;
-                    const uint32_t a = sp_a + (uint32_t)((n * L.trp + tk + 2 * t) * 2);
-                    pb[nv][0] = n < ROWS ? sh_ld32(a) : 0u;
-                    pb[nv][1] = n < ROWS ? sh_ld32(a + 16) : 0u;
+                    if (n >= ROWS) {
+                        pb[nv][0] = pb[nv][1] = 0u;
+                    } else if constexpr (C::INPLACE) {
+                        const uint32_t a = sc_a + (uint32_t)(((tk + 2 * t) * G + (n >> 1)) * 4 + (n & 1) * 2);
+                        const uint32_t rowb = (uint32_t)(G * 4);   // bytes per token
+                        pb[nv][0] = sh_ldu16(a) | (sh_ldu16(a + rowb) << 16);
+                        pb[nv][1] = sh_ldu16(a + 8 * rowb) | (sh_ldu16(a + 9 * rowb) << 16);
+                    } else {
+                        const uint32_t a = sp_a + (uint32_t)((n * L.trp + tk + 2 * t) * 2);
+                        pb[nv][0] = sh_ld32(a);
+                        pb[nv][1] = sh_ld32(a + 16);
+                    }
                 }
                 // A: positions 16 g8 .. 16 g8 + 15 (chunk g8) of slot rows r, r + 1, r + 8, r + 9
                 const int r = 16 * mt + 2 * t;
@@ -1102,7 +1136,7 @@ gq_status launch_attn_mma(const AttnParams &base, int64_t B, int64_t Tcap, cudaS
     using C = AmCfg<G>;
     constexpr int CT = C::CT;
     auto kernel = attn_mma_i8_kernel<G>;
-    const int64_t per_token = 8 + 8 * G;
+    const int64_t per_token = C::PER_TOKEN;
     const int64_t room = (int64_t)AT_SMEM_MAX - (int64_t)am_fixed_bytes<G>();
     const int64_t tr_max = std::max<int64_t>(CT, room / per_token / CT * CT);
     const int64_t items = B * base.Hkv;
