@@ -491,9 +491,20 @@ def attn_extras(b, hbm_peak):
             "us": round(t * 1e6, 1), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4),
             "algorithmic_bytes": nbytes, "tokens": int(lens_h.sum())}
         del q, k, ks, v, vs, lens, out
+    # grouped queries (G = Hq / Hkv = 4 and 8) and one long sequence, full lengths
+    for name, (B2, Hq2, Hkv2, T2) in (("g4_b64_t4096", (64, 32, 8, 4096)), ("g8_b128_t2048", (128, 32, 4, 2048)),
+                                      ("g4_b1_t32768", (1, 32, 8, 32768))):
+        (q, k, ks, v, vs, lens, out), lens_h = attn_case(b, B2, Hq2, Hkv2, T2, D, "full", 91)
+        fn = lambda: gq.gq_attn_decode_i8(q, k, ks, v, vs, lens, out, B2, Hq2, Hkv2, T2, D, D ** -0.5,
+                                          stream=b.stream)
+        t = b.time_launches([fn], min_seconds=0.2, max_graph=50)
+        nbytes = attn_bytes(lens_h, Hq2, Hkv2, D)
+        res[name] = {"us": round(t * 1e6, 1), "GB/s": round(nbytes / t / 1e9, 1),
+                     "frac_of_hbm": round(nbytes / t / 1e9 / hbm_peak, 4), "B": B2, "Hq": Hq2, "Hkv": Hkv2, "Tcap": T2}
+        del q, k, ks, v, vs, lens, out
     b.torch.cuda.empty_cache()
     res["workload"] = (f"decode attention over an INT8 KV cache, B={B} Hq={Hq} Hkv={Hkv} D={D}, "
-                       f"Tcap={Tcap}; lens full or uniform in [1, {Tcap}]")
+                       f"Tcap={Tcap}; lens full or uniform in [1, {Tcap}]; then grouped-query and long-context cases")
     return res
 
 
