@@ -63,7 +63,8 @@ typedef enum gq_status {
     GQ_ERR_UNSUPPORTED_DEVICE = 3, /* the current device is not sm_103 */
     GQ_ERR_CUDA = 4,               /* a CUDA runtime call or a launch failed */
     GQ_ERR_TIMEOUT = 5,            /* a bounded in-kernel wait gave up (gq_last_error) */
-    GQ_ERR_NO_MEMORY = 6           /* the stream-ordered workspace could not be allocated */
+    GQ_ERR_NO_MEMORY = 6,          /* the stream-ordered workspace could not be allocated */
+    GQ_ERR_DEVICE_CHECK = 7        /* a bounds check of a GQ_DEBUG build failed (gq_last_error) */
 } gq_status;
 
 /* Which kernel family serves a product. */
@@ -85,9 +86,11 @@ const char *gq_status_string(gq_status status); /* static text, never NULL */
 const char *gq_last_error_message(void);
 
 /* Sticky device-side status of the current device: GQ_ERR_TIMEOUT if a kernel
- * gave up a bounded wait since the last call, else GQ_ERR_INVALID_ARG if a
- * length or position read on the device was out of range (the INT8 KV-cache
- * calls), else GQ_OK; reading clears it and, after a timeout, re-zeroes the
+ * gave up a bounded wait since the last call, else GQ_ERR_DEVICE_CHECK if a
+ * bounds check of a GQ_DEBUG build failed (a library bug; those builds check the
+ * indices the kernels derive from their arguments and never trap), else
+ * GQ_ERR_INVALID_ARG if a length or position read on the device was out of range
+ * (the INT8 KV-cache calls), else GQ_OK; reading clears it and, after a timeout, re-zeroes the
  * workspace counters of the device.  Synchronizes the current device first. */
 gq_status gq_last_error(void);
 

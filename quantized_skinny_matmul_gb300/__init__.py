@@ -18,7 +18,8 @@ import os
 import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_lib", "libgq.so")
+# GQ_LIBRARY may name another build of the same ABI (the GQ_DEBUG build, _lib/libgq_debug.so)
+LIB_PATH = os.environ.get("GQ_LIBRARY") or os.path.join(_PKG, "_lib", "libgq.so")
 
 GQ_OK = 0
 GQ_ERR_INVALID_ARG = 1
@@ -27,6 +28,7 @@ GQ_ERR_UNSUPPORTED_DEVICE = 3
 GQ_ERR_CUDA = 4
 GQ_ERR_TIMEOUT = 5
 GQ_ERR_NO_MEMORY = 6
+GQ_ERR_DEVICE_CHECK = 7
 
 GQ_PATH_AUTO = 0
 GQ_PATH_GEMV = 1

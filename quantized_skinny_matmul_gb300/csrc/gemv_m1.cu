@@ -147,6 +147,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 2) gemv_m1_q4_0_kernel(const M1
             if (k >= p.slots && !mbar_wait(smem_addr(empty + slot), (uint32_t)(((k / p.slots) - 1) & 1), p.status))
                 break;
             chunk_at(k, src, bytes);
+            GQ_DCHECK(g0 + k / nc < p.N16 && (k % nc) * M1_TILES + (int)(bytes / TILE_BYTES) <= p.NT &&
+                          bytes <= (uint32_t)M1_CHUNK,
+                      p.status);
             mbar_arrive_expect_tx(smem_addr(full + slot), bytes);
             bulk_g2s_hint(smem_addr(smem + L.ring + (size_t)slot * M1_CHUNK), src, bytes, smem_addr(full + slot),
                           policy);
@@ -209,6 +212,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 2) gemv_m1_q4_0_kernel(const M1
     auto tile_dot = [&](const uint32_t chunk_a, const int u, const int ti, float (&a)[2]) {
         const uint32_t tile_a = chunk_a + ti * TILE_BYTES;
         const int blk = 4 * (u + ti) + jb;
+        GQ_DCHECK(ti < M1_TILES && blk < 4 * p.NT, p.status);
         const uint4 a0 = m1_lds128(codes_a + blk * QK), a1 = m1_lds128(codes_a + blk * QK + 16);
         const uint32_t sc = m1_lds32(scales_a + 4 * blk);
         const uint4 q0 = m1_lds128(tile_a + (jb * 16 + r0) * 16);

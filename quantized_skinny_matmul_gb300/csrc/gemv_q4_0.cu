@@ -605,7 +605,8 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
             if (!failed) failed = !mbar_wait(smem_addr(full + slot), phase, p.status);
             // the tile at position ti of the chunk, into the accumulators of position tw
             auto tile_dot = [&](const int tw, const int ti) {
-                const int tl = u + ti;                         // tile index within the slice
+                const int tl = u + ti;
+                GQ_DCHECK(tl < p.NT && ti < CHUNK_TILES, p.status);                         // tile index within the slice
                 const uint8_t *tile = ring + (size_t)slot * CB + ti * TB;
                 const uint2 d4w = *reinterpret_cast<const uint2 *>(tile + SCALES + n * 8);
                 const uint2 m4w = Q41W ? *reinterpret_cast<const uint2 *>(tile + Q41_TILE_MIN_OFFSET + n * 8) : d4w;
@@ -654,6 +655,7 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
             // f32 result is the exact block dot sumi.
             auto tile_mma = [&](const int tw, const int ti) {
                 const int tl = u + ti;
+                GQ_DCHECK(tl < p.NT && ti < CHUNK_TILES, p.status);
                 const uint8_t *tile = ring + (size_t)slot * CB + ti * TB;
                 const uint2 s0 = *reinterpret_cast<const uint2 *>(tile + SCALES + fg * 8);
                 const uint2 s1 = *reinterpret_cast<const uint2 *>(tile + SCALES + (fg + 8) * 8);
@@ -739,6 +741,7 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
             // those of a second, so the two MMAs add the 32 products of the tile.
             auto tile_f16 = [&](const int tw, const int ti) {
                 const int tl = u + ti;
+                GQ_DCHECK(tl < p.NT && ti < CHUNK_TILES, p.status);
                 const uint8_t *tile = ring + (size_t)slot * CB + ti * TB;
                 const uint4 wa = lds128(tile + fg * 64 + 16 * ft);
                 const uint4 wb = lds128(tile + (fg + 8) * 64 + 16 * ft);

@@ -160,6 +160,7 @@ const char *gq_status_string(gq_status s) {
         case GQ_ERR_CUDA: return "CUDA error";
         case GQ_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
         case GQ_ERR_NO_MEMORY: return "workspace allocation failed";
+        case GQ_ERR_DEVICE_CHECK: return "a device-side bounds check failed";
     }
     return "unknown status";
 }
@@ -176,6 +177,7 @@ gq_status gq_last_error(void) {
         reset_workspace_counters();
         return fail(GQ_ERR_TIMEOUT, "a kernel gave up a bounded wait");
     }
+    if (word & STATUS_CHECK) return fail(GQ_ERR_DEVICE_CHECK, "a device-side bounds check (GQ_DEBUG build) failed");
     if (word & STATUS_RANGE) return fail(GQ_ERR_INVALID_ARG, "a length or position read on the device was out of range");
     return ok();
 }

@@ -26,6 +26,20 @@ constexpr int TILE_SCALE_OFFSET = 1024;
 // status word (owned by gq_api.cu, read and cleared by gq_last_error).
 constexpr unsigned int STATUS_TIMEOUT = 1u;
 constexpr unsigned int STATUS_RANGE = 2u;     // a length or position read on the device was out of range
+constexpr unsigned int STATUS_CHECK = 4u;     // a GQ_DEBUG bounds check failed
+
+// GQ_DEBUG builds (see _build.py) check the indices the kernels derive from their arguments and
+// record a failure in the device status word; they never trap.  Other builds compile the checks out.
+#ifdef GQ_DEBUG
+#define GQ_DCHECK(cond, status)                                      \
+    do {                                                             \
+        if (!(cond)) atomicOr((status), ::gq::STATUS_CHECK);         \
+    } while (0)
+#else
+#define GQ_DCHECK(cond, status) \
+    do {                        \
+    } while (0)
+#endif
 __device__ __forceinline__ void flag_timeout(unsigned int *status) { atomicOr(status, STATUS_TIMEOUT); }
 
 // ---------------------------------------------------------------------------

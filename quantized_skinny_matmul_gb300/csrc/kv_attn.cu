@@ -251,6 +251,7 @@ __global__ void __launch_bounds__(AtCfg<G>::THREADS, 2) attn_decode_i8_kernel(co
         return;
     }
     const int nc = (nt + CT - 1) / CT;   // slots per phase
+    GQ_DCHECK(nt <= p.TR && t0 + nt <= p.Tcap, p.status);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SLOTS; s++) {
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(AtCfg<G>::THREADS, 2) attn_decode_i8_kernel(co
                 break;
             const int c = i < nc ? i : i - nc;
             const uint32_t bytes = (uint32_t)(min(CT, nt - c * CT) * D);
+            GQ_DCHECK(c * CT < nt && bytes <= (uint32_t)CHUNK, p.status);
             mbar_arrive_expect_tx(smem_addr(full + slot), bytes);
             bulk_g2s_hint(smem_addr(smem + L.ring + (size_t)slot * CHUNK), (i < nc ? kbase : vbase) + (size_t)c * CT * D,
                           bytes, smem_addr(full + slot), policy);
@@ -346,6 +348,7 @@ __global__ void __launch_bounds__(AtCfg<G>::THREADS, 2) attn_decode_i8_kernel(co
         if (!failed) {
             const uint32_t chunk = ring_a + (uint32_t)((c % SLOTS) * CHUNK);
             const int ntok = min(CT, nt - c * CT);
+            GQ_DCHECK(ntok > 0 && c * CT + ntok <= nt, p.status);
 #pragma unroll 1
             for (int pass = 0; pass < G / HG; pass++) {
                 uint64_t qv[HG][8];
@@ -680,6 +683,7 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
         return;
     }
     const int nc = (nt + CT - 1) / CT;   // slots per phase
+    GQ_DCHECK(nt <= p.TR && t0 + nt <= p.Tcap, p.status);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SLOTS; s++) {
@@ -700,6 +704,7 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
             const int slot = i % SLOTS;
             if (i >= SLOTS && !mbar_wait(smem_addr(empty + slot), (uint32_t)(((i / SLOTS) - 1) & 1), p.status)) break;
             const int c = i < nc ? i : i - nc;
+            GQ_DCHECK(c * CT < nt && t0 + c * CT < p.Tcap, p.status);
             // a whole box every time: rows past the range belong to the next range or lie past the
             // tensor (read as zeros); their scores are not stored and their weights are zero
             mbar_arrive_expect_tx(smem_addr(full + slot), (uint32_t)CHUNK);
@@ -801,6 +806,7 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
         if (!failed) {
             const uint32_t chunk = ring_a + (uint32_t)((c % SLOTS) * CHUNK);
             const int ntok = min(CT, nt - c * CT);
+            GQ_DCHECK(ntok > 0 && c * CT + ntok <= nt, p.status);
 #pragma unroll
             for (int mt = 0; mt < CT / 16; mt++) {
                 if (16 * mt >= ntok) break;
@@ -914,6 +920,7 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
             for (int mt = 0; mt < CT / 16; mt++) {
                 if (16 * mt >= ntok) break;
                 const int tk = c * CT + 16 * mt;   // first token of the step in the range
+                GQ_DCHECK(tk + 16 <= ((nt + 15) & ~15) && tk + 16 <= p.TR, p.status);
                 // B: the weights of column n = 8 nv + g8 (head n / 2, hi for even n, lo for odd) at tokens
                 // 2t, 2t + 1 and 2t + 8, 2t + 9: the fp16 at byte 2 (n % 2) of entry (token, head)
                 uint32_t pb[NV][2];

@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // the eight row groups' tiles of column step kt: one box of 8 x 1152 bytes
                     // (row groups past the matrix are filled with zeros: weight 0 after conversion)
                     const int rs = kt % RAW;
+                    GQ_DCHECK(kt0 + kt < p.NT && n0 / 16 < p.N16, p.status);
                     if (kt >= RAW) wait_or_fail(bar(RAW_EMPTY + rs), (uint32_t)((kt / RAW - 1) & 1), failed, p.status);
                     if (failed) break;
                     mbar_arrive_expect_tx(bar(RAW_FULL + rs), (uint32_t)RAW_STAGE);
@@ -320,6 +321,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int rs = kt % RAW, st = kt % ST;
                 wait_or_fail(bar(RAW_FULL + rs), (uint32_t)((kt / RAW) & 1), failed, p.status);
                 if (kt >= ST) wait_or_fail(bar(EMPTY + st), (uint32_t)((kt / ST - 1) & 1), failed, p.status);
+                GQ_DCHECK(gi < RAW_ROWGROUPS && rr < 16 && h < 2, p.status);
                 if (!failed) {
                     const uint8_t *tile = smem + L::raw + rs * RAW_STAGE + gi * TILE_BYTES;
                     uint8_t *a_stage = smem + L::a + st * A_STAGE;

@@ -3,6 +3,8 @@ include/gq.h declares, and rejects bad arguments before launching anything."""
 import ctypes
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -44,7 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_strings(lib):
     assert gq.gq_abi_version() == 1
-    for s in range(7):
+    for s in range(8):
         assert lib.gq_status_string(s)
     assert lib.gq_status_string(99) == b"unknown status"
 
@@ -234,3 +236,18 @@ def test_argument_checks_kv_cache(lib):
     assert lib.gq_kv_append_i8(FAKE, FAKE, FAKE, FAKE, 2, 4, 0, 128, None) == gq.GQ_ERR_INVALID_ARG
     assert lib.gq_kv_append_i8(FAKE, ODD, FAKE, FAKE, 2, 4, 64, 128, None) == gq.GQ_ERR_MISALIGNED
     assert lib.gq_last_error_message()
+
+
+def test_debug_build_and_library_override(tmp_path):
+    """The GQ_DEBUG build compiles (nvcc here, no GPU) into its own library, and the binding
+    loads the library GQ_LIBRARY names."""
+    from quantized_skinny_matmul_gb300 import _build
+    path = _build.build(debug=True)
+    assert path.endswith("libgq_debug.so") and os.path.exists(path) and path != _build.LIB_PATH
+    code = ("import quantized_skinny_matmul_gb300 as gq; print(gq.LIB_PATH); "
+            "print(gq.gq_abi_version()); print(gq.lib().gq_status_string(gq.GQ_ERR_DEVICE_CHECK).decode())")
+    res = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, GQ_LIBRARY=path), cwd=ROOT,
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr
+    lines = res.stdout.split("\n")
+    assert lines[0] == path and lines[1] == "1" and "bounds check" in lines[2]
