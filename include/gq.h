@@ -365,7 +365,8 @@ int gq_get_static_weights(void);
  *   queries      float [B][Hq][D], Hq = G * Hkv; query head h reads KV head h / G
  *   lens, pos    int32 [B]
  *   output       float [B][Hq][D]
- * Sizes: D is 64 or 128; G is 1, 2, 4 or 8; B, Hkv, Tcap positive with
+ * Sizes: D is 64 or 128; G is 1 to 8 for D = 128, and 1, 2, 4 or 8 for D = 64;
+ * B, Hkv, Tcap positive with
  * B * Hkv * Tcap * D < 2^40 and Tcap < 2^30.  Other sizes: GQ_ERR_INVALID_ARG. */
 
 /* Quantizes `rows` rows of D f32 values x [rows][D] into codes q [rows][D] and

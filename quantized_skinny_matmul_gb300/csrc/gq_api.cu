@@ -670,8 +670,9 @@ gq_status gq_attn_decode_i8(const float *q, const int8_t *k, const float *k_scal
         return fail(GQ_ERR_INVALID_ARG, "Hq=%lld is not a positive multiple of Hkv=%lld", (long long)Hq,
                     (long long)Hkv);
     const int64_t G = Hq / Hkv;
-    if (G != 1 && G != 2 && G != 4 && G != 8)
-        return fail(GQ_ERR_INVALID_ARG, "query heads per KV head must be 1, 2, 4 or 8 (got %lld)", (long long)G);
+    if (D == 128 ? (G < 1 || G > 8) : (G != 1 && G != 2 && G != 4 && G != 8))
+        return fail(GQ_ERR_INVALID_ARG, "query heads per KV head must be 1 .. 8 (D = 128) or 1, 2, 4, 8 (D = 64); got %lld",
+                    (long long)G);
     if (!std::isfinite(softmax_scale)) return fail(GQ_ERR_INVALID_ARG, "softmax_scale is not finite");
     GQ_TRY(check_ptr(q, "q"));
     GQ_TRY(check_ptr(k, "k"));

@@ -85,7 +85,8 @@ gq_status launch_tc_q4_0(const void *rep, const float *x, float *dst, int64_t M,
 gq_status launch_tc_f16(const void *w16, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
                         cudaStream_t s);
 // INT8 KV cache: rows of D values to codes and f32 scales; one token per sequence into
-// the cache at pos[b]; the decode attention over the cache (D 64 or 128, Hq / Hkv 1, 2, 4, 8).
+// the cache at pos[b]; the decode attention over the cache (D 128 with Hq / Hkv 1 .. 8, or D 64
+// with Hq / Hkv 1, 2, 4, 8).
 gq_status launch_kv_quantize_i8(const float *x, int8_t *q, float *scale, int64_t rows, int64_t D, cudaStream_t s);
 gq_status launch_kv_append_i8(const float *x, int8_t *q, float *scale, const int32_t *pos, int64_t B, int64_t Hkv,
                               int64_t Tcap, int64_t D, cudaStream_t s);

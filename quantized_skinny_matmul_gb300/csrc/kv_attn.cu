@@ -540,13 +540,13 @@ struct AmCfg {
     static constexpr int SLOTS = 16;                   // a multiple of W
     static constexpr int THREADS = (W + 1) * 32;
     static constexpr int CONSUMERS = W * 32;
-    static constexpr int NN = G <= 4 ? 1 : 2;          // column tiles of the score MMA
+    static constexpr int NN = G <= 4 ? 1 : 2;          // column tiles of the score MMA (2G columns)
     static constexpr int ROWS = 2 * G;                 // (head, hi / lo) rows of the value MMA
-    // eight heads: the weights replace the scores in place ([token][head] pairs of fp16), which
-    // halves the shared memory per token and so the number of CTAs a sequence is split over;
-    // fewer heads: the weights go to rows of their own ([2G][token] fp16), one 32-bit load per
-    // pair of tokens in the value steps
-    static constexpr bool INPLACE = G >= 8;
+    // five to eight heads: the weights replace the scores in place ([token][head] pairs of fp16),
+    // which halves the shared memory per token and so the number of CTAs a sequence is split
+    // over; fewer heads: the weights go to rows of their own ([2G][token] fp16), one 32-bit load
+    // per pair of tokens in the value steps
+    static constexpr bool INPLACE = G > 4;
     static constexpr int PER_TOKEN = 8 + 4 * G + (INPLACE ? 0 : 4 * G);   // shared bytes per token
 };
 
@@ -850,7 +850,7 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
     }
     consumer_sync<CONSUMERS>();
 
-    // ---- softmax over the row (thread ctid takes entries ctid, ctid + CONSUMERS, ...: head ctid % G)
+    // ---- softmax over the row, per head
     const int gh = ctid % G;
     float vscale;   // weights are scaled by this power of two so that the largest is below 2^15
     {
@@ -860,31 +860,77 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
         int ex = 0;
         if (vm > 0.0f) frexpf(vm, &ex);
         vscale = vm > 0.0f ? ldexpf(1.0f, 14 - ex) : 1.0f;   // e vs vscale < 2^15 (e <= 1)
-        float mx = -INFINITY;
-        for (int i = ctid; i < nt * G; i += CONSUMERS) mx = fmaxf(mx, sh_ldf(sc_a + 4u * (uint32_t)i));
-#pragma unroll
-        for (int m = 16; m >= G; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-        if (lane < G) wmax[warp * G + lane] = mx;
-        consumer_sync<CONSUMERS>();
-        float M = wmax[gh];
-#pragma unroll
-        for (int w = 1; w < W; w++) M = fmaxf(M, wmax[w * G + gh]);
-        float l = 0.0f;
         // each entry (token, head) becomes its weight as two fp16 terms: in place (the thread that
         // reads an entry is the one that writes it), or into rows 2 head (hi) and 2 head + 1 (lo)
-        const uint32_t sp_hi = sp_a + (uint32_t)((2 * gh) * L.trp * 2), sp_lo = sp_hi + (uint32_t)(L.trp * 2);
-        for (int i = ctid; i < nt * G; i += CONSUMERS) {
-            const int tok = i / G;
-            const float e = exp2f(sh_ldf(sc_a + 4u * (uint32_t)i) - M);
-            l += e;
-            const float wv = e * sh_ldf(vsc_a + 4u * (uint32_t)tok) * vscale;
+        auto put = [&](int i, int tok, int g, float wv) {
             const __half hi = __float2half_rn(wv), lo = __float2half_rn(wv - __half2float(hi));
             if constexpr (C::INPLACE) {
                 sh_stf(sc_a + 4u * (uint32_t)i,
                        __uint_as_float((uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16)));
             } else {
-                sh_sth(sp_hi + 2u * (uint32_t)tok, hi);
-                sh_sth(sp_lo + 2u * (uint32_t)tok, lo);
+                sh_sth(sp_a + 2u * (uint32_t)((2 * g) * L.trp + tok), hi);
+                sh_sth(sp_a + 2u * (uint32_t)((2 * g + 1) * L.trp + tok), lo);
+            }
+        };
+        if constexpr (32 % G == 0) {
+            // entries ctid, ctid + CONSUMERS, ... all belong to head ctid % G
+            float mx = -INFINITY;
+            for (int i = ctid; i < nt * G; i += CONSUMERS) mx = fmaxf(mx, sh_ldf(sc_a + 4u * (uint32_t)i));
+#pragma unroll
+            for (int m = 16; m >= G; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+            if (lane < G) wmax[warp * G + lane] = mx;
+            consumer_sync<CONSUMERS>();
+            float M = wmax[gh];
+#pragma unroll
+            for (int w = 1; w < W; w++) M = fmaxf(M, wmax[w * G + gh]);
+            float l = 0.0f;
+            for (int i = ctid; i < nt * G; i += CONSUMERS) {
+                const int tok = i / G;
+                const float e = exp2f(sh_ldf(sc_a + 4u * (uint32_t)i) - M);
+                l += e;
+                put(i, tok, gh, e * sh_ldf(vsc_a + 4u * (uint32_t)tok) * vscale);
+            }
+#pragma unroll
+            for (int m = 16; m >= G; m >>= 1) l += __shfl_xor_sync(0xffffffffu, l, m);
+            if (lane < G) wsum[warp * G + lane] = l;
+        } else {
+            // other head counts: each thread takes whole tokens (all G heads of each)
+            float mx[G], l[G];
+#pragma unroll
+            for (int g = 0; g < G; g++) mx[g] = -INFINITY;
+            for (int tok = ctid; tok < nt; tok += CONSUMERS)
+#pragma unroll
+                for (int g = 0; g < G; g++) mx[g] = fmaxf(mx[g], sh_ldf(sc_a + 4u * (uint32_t)(tok * G + g)));
+#pragma unroll
+            for (int g = 0; g < G; g++) {
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], m));
+                if (lane == 0) wmax[warp * G + g] = mx[g];
+            }
+            consumer_sync<CONSUMERS>();
+#pragma unroll
+            for (int g = 0; g < G; g++) {
+                float M = wmax[g];
+#pragma unroll
+                for (int w = 1; w < W; w++) M = fmaxf(M, wmax[w * G + g]);
+                mx[g] = M;
+                l[g] = 0.0f;
+            }
+            for (int tok = ctid; tok < nt; tok += CONSUMERS) {
+                const float vsv = sh_ldf(vsc_a + 4u * (uint32_t)tok) * vscale;
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    const int i = tok * G + g;
+                    const float e = exp2f(sh_ldf(sc_a + 4u * (uint32_t)i) - mx[g]);
+                    l[g] += e;
+                    put(i, tok, g, e * vsv);
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < G; g++) {
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], m);
+                if (lane == 0) wsum[warp * G + g] = l[g];
             }
         }
         // the tokens of the last 16-token step past the range weigh nothing
@@ -895,9 +941,6 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
             for (int i = ctid; i < ROWS * pad; i += CONSUMERS)
                 sh_sth(sp_a + 2u * (uint32_t)((i / pad) * L.trp + nt + i % pad), __float2half_rn(0.0f));
         }
-#pragma unroll
-        for (int m = 16; m >= G; m >>= 1) l += __shfl_xor_sync(0xffffffffu, l, m);
-        if (lane < G) wsum[warp * G + lane] = l;
     }
     consumer_sync<CONSUMERS>();
 
@@ -1232,14 +1275,22 @@ gq_status launch_attn_decode_i8(const float *q, const int8_t *k, const float *ks
     // D = 128: the tensor-core kernel (its tensor maps address at most 2^32 - 1 rows), unless
     // GQ_ATTN_FP32 asks for the FP32 one (a test and tuning switch)
     const char *e = getenv("GQ_ATTN_FP32");
-    if (B * Hkv * Tcap <= 0xFFFFFFFFLL && !(e && *e && atoi(e) != 0)) {
+    const bool fp32_g = G == 1 || G == 2 || G == 4 || G == 8;   // the group sizes the FP32 kernel takes
+    if (B * Hkv * Tcap <= 0xFFFFFFFFLL && !(fp32_g && e && *e && atoi(e) != 0)) {
         switch (G) {
             case 1: return launch_attn_mma<1>(p, B, Tcap, s);
             case 2: return launch_attn_mma<2>(p, B, Tcap, s);
+            case 3: return launch_attn_mma<3>(p, B, Tcap, s);
             case 4: return launch_attn_mma<4>(p, B, Tcap, s);
+            case 5: return launch_attn_mma<5>(p, B, Tcap, s);
+            case 6: return launch_attn_mma<6>(p, B, Tcap, s);
+            case 7: return launch_attn_mma<7>(p, B, Tcap, s);
             case 8: return launch_attn_mma<8>(p, B, Tcap, s);
         }
     }
+    if (!fp32_g)
+        return fail(GQ_ERR_INVALID_ARG, "%lld query heads per KV head need the tensor-core kernel (at most 2^32 - 1 "
+                    "cache rows)", (long long)G);
     return launch_attn_d<128>(p, B, G, Tcap, s);
 }
 

@@ -212,10 +212,14 @@ def test_argument_checks_kv_cache(lib):
     touching the GPU."""
     a = lib.gq_attn_decode_i8
     ok_args = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 4, 64, 128, 0.1, None)
-    for i, bad in ((9, 6), (9, 12), (9, 40), (10, 0), (8, 3)):    # Hq not G * Hkv with G in 1, 2, 4, 8
+    for i, bad in ((9, 6), (9, 12), (9, 40), (10, 0), (8, 3), (8, 36)):   # Hq not G * Hkv, G in 1 .. 8
         args = list(ok_args)
-        args[i if i != 10 else 10] = bad
+        args[i] = bad
         assert a(*args) == gq.GQ_ERR_INVALID_ARG, (i, bad)
+    for Hq, D in ((12, 64), (20, 64), (24, 64)):   # G = 3, 5, 6: the tensor-core kernel only (D = 128)
+        args = list(ok_args)
+        args[8], args[11] = Hq, D
+        assert a(*args) == gq.GQ_ERR_INVALID_ARG, (Hq, D)
     for D in (32, 96, 256):
         args = list(ok_args)
         args[11] = D

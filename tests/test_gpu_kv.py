@@ -113,8 +113,8 @@ def test_kv_append_writes_one_position_per_sequence(oracle):
         assert np.all(hq[b][:, rest] == 7) and np.all(hs[b][:, rest] == 2.5)
 
 
-# (B, Hq, Hkv, Tcap, D, lens): ragged and empty sequences, every group size, both head
-# sizes, lengths across several 8 KB slots with a ragged last one, and few (sequence,
+# (B, Hq, Hkv, Tcap, D, lens): ragged and empty sequences, every group size (1 .. 8 for D = 128),
+# both head sizes, lengths across several 8 KB slots with a ragged last one, and few (sequence,
 # head) pairs with long caches (split over CTAs and merged)
 CASES = [
     (2, 8, 8, 300, 128, [300, 77]),
@@ -126,6 +126,10 @@ CASES = [
     (6, 4, 2, 1031, 128, "mix"),
     (1, 8, 8, 40000, 128, [40000]),
     (2, 2, 1, 9000, 64, [1, 9000]),
+    (3, 12, 4, 600, 128, [600, 333, 17]),      # G = 3
+    (2, 28, 4, 2100, 128, [2100, 1500]),       # G = 7 (28 query heads on 4 KV heads)
+    (2, 10, 2, 800, 128, "mix"),               # G = 5
+    (1, 24, 4, 3000, 128, [2999]),             # G = 6
 ]
 
 
