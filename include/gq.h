@@ -153,18 +153,20 @@ gq_status gq_mul_mat_f16_f32(const void *src0_f16, const float *src1, float *dst
                              int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /* The Q4_0 product of gq_mul_mat_q4_0_f32 with src1 ([M][K] f32) and dst ([M][N]
- * f32) in HOST memory.  The call enqueues on `stream` a copy of src1 to a device
- * staging buffer, the product, and a copy of dst back to the host, and returns;
- * dst_host holds the result once the stream has reached that point
+ * f32) in HOST memory.  The call enqueues on `stream` the transfer of src1 to a
+ * device staging buffer, the product, and the transfer of dst back to the host,
+ * and returns; dst_host holds the result once the stream has reached that point
  * (cudaStreamSynchronize).  src1_host and dst_host are plain host pointers with
- * no alignment rule; page-locked memory (cudaHostAlloc, cudaHostRegister) keeps
- * the copies asynchronous, pageable memory makes them synchronous for the host,
- * as cudaMemcpyAsync does.  (Reading src1 in place through the device mapping of
- * page-locked memory was slower: every CTA reads all of src1 across the host
- * link.)  The staging buffer belongs to the stream and grows like the workspace
- * (GQ_ERR_NO_MEMORY while the stream is captured); calls on one stream use it in
- * stream order.  Results equal gq_mul_mat_q4_0_f32's bit for bit.  (An interface
- * of this library: one call per decode step from host data.) */
+ * no alignment rule.  Page-locked memory that the device maps (cudaHostAlloc,
+ * cudaHostRegister with mapping; 16-byte aligned) is moved by the kernels
+ * themselves: a small kernel stages src1 and the product stores dst straight into
+ * host memory, with no copy-engine transfer.  Other host memory is copied with
+ * cudaMemcpyAsync (synchronous for the host when it is pageable).  (Reading src1
+ * in place in the product was slower: every CTA would read all of src1 across the
+ * host link.)  The staging buffer belongs to the stream and grows like the
+ * workspace (GQ_ERR_NO_MEMORY while the stream is captured); calls on one stream
+ * use it in stream order.  Results equal gq_mul_mat_q4_0_f32's bit for bit.  (An
+ * interface of this library: one call per decode step from host data.) */
 gq_status gq_mul_mat_q4_0_f32_host(const void *q4_repacked, const float *src1_host, float *dst_host,
                                    int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 

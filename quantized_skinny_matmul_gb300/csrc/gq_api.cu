@@ -382,6 +382,34 @@ gq_status gq_mul_mat_q4_0_f32(const void *q4_repacked, const float *src1, float 
     return gq_mul_mat_q4_0_f32_path(q4_repacked, src1, dst, M, N, K, GQ_PATH_AUTO, stream);
 }
 
+}  // extern "C"
+
+namespace gq {
+namespace {
+// The device address of page-locked host memory mapped into the device's address space, or
+// nullptr (pageable memory, or memory this device cannot address).
+void *mapped_host(const void *p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();   // clear the error of an unknown pointer
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+}  // namespace
+
+// Copies n float4 from mapped host memory into device memory, after every earlier grid in the
+// stream (the previous product may still read the destination).
+__global__ void host_stage_kernel(const float4 *__restrict__ src, float4 *__restrict__ dst, int64_t n) {
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+}  // namespace gq
+
+extern "C" {
+
 gq_status gq_mul_mat_q4_0_f32_host(const void *q4_repacked, const float *src1_host, float *dst_host, int64_t M,
                                    int64_t N, int64_t K, cudaStream_t stream) {
     GQ_TRY(check_sizes(M, N, K));
@@ -391,15 +419,38 @@ gq_status gq_mul_mat_q4_0_f32_host(const void *q4_repacked, const float *src1_ho
     GQ_TRY(check_device());
     const size_t xb = (size_t)M * (size_t)K * sizeof(float), ob = (size_t)M * (size_t)N * sizeof(float);
     const size_t xs = (xb + 255) / 256 * 256;
+    // Page-locked buffers that the device addresses are read and written by the kernels
+    // themselves: a small kernel stages src1 (no copy engine), and the product stores dst into
+    // host memory. Other host memory goes through copies on the stream.
+    void *hx = mapped_host(src1_host), *hd = mapped_host(dst_host);
+    const bool stage_x = hx != nullptr && aligned16(hx), direct_dst = hd != nullptr && aligned16(hd);
     uint8_t *stage = nullptr;
-    GQ_TRY(get_staging(stream, xs + ob, &stage));
-    float *dx = reinterpret_cast<float *>(stage), *dd = reinterpret_cast<float *>(stage + xs);
-    GQ_TRY(check_cuda(cudaMemcpyAsync(dx, src1_host, xb, cudaMemcpyHostToDevice, stream), "src1 copy to the device"));
+    GQ_TRY(get_staging(stream, xs + (direct_dst ? 0 : ob), &stage));
+    float *dx = reinterpret_cast<float *>(stage), *dd = direct_dst ? static_cast<float *>(hd)
+                                                                   : reinterpret_cast<float *>(stage + xs);
+    if (stage_x) {
+        const int64_t n4 = (int64_t)(xb / 16);   // K is a multiple of 32: whole float4
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)std::min<int64_t>((n4 + 255) / 256, 64));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        GQ_TRY(check_cuda(cudaLaunchKernelEx(&cfg, host_stage_kernel, static_cast<const float4 *>(hx),
+                                             reinterpret_cast<float4 *>(dx), n4),
+                          "src1 staging kernel"));
+    } else {
+        GQ_TRY(check_cuda(cudaMemcpyAsync(dx, src1_host, xb, cudaMemcpyHostToDevice, stream), "src1 copy to the device"));
+    }
     if (resolve(GQ_PATH_AUTO, GQ_KIND_Q4_0, M, N, K) == GQ_PATH_TC)
         GQ_TRY(launch_tc_q4_0(q4_repacked, dx, dd, M, N, K, stream));
     else
         GQ_TRY(launch_gemv_q4_0(q4_repacked, dx, dd, M, N, K, stream));
-    GQ_TRY(check_cuda(cudaMemcpyAsync(dst_host, dd, ob, cudaMemcpyDeviceToHost, stream), "dst copy to the host"));
+    if (!direct_dst)
+        GQ_TRY(check_cuda(cudaMemcpyAsync(dst_host, dd, ob, cudaMemcpyDeviceToHost, stream), "dst copy to the host"));
     return ok();
 }
 

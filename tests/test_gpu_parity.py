@@ -232,7 +232,8 @@ def test_full_size_sampled(oracle, M, N, K):
     assert_within(dst16[ms, ns], ref16, T16, what="f16 full size")
 
 
-@pytest.mark.parametrize("M,N,K,pinned", [(1, 4096, 4096, True), (5, 300, 1024, False), (40, 77, 352, True)])
+@pytest.mark.parametrize("M,N,K,pinned", [(1, 4096, 4096, True), (5, 300, 1024, False), (40, 77, 352, True),
+                                         (16, 500, 11008, True), (1, 11008, 4096, False)])
 def test_host_pointer_entry_equals_device_entry(M, N, K, pinned):
     """gq_mul_mat_q4_0_f32_host (src1 and dst in host memory) gives the device entry's
     result bit for bit, with page-locked and with pageable host buffers."""
@@ -247,6 +248,24 @@ def test_host_pointer_entry_equals_device_entry(M, N, K, pinned):
     gq.gq_mul_mat_q4_0_f32_host(rep, hx, hd, M, N, K, s)
     s.synchronize()
     assert np.array_equal(hd.numpy(), want)
+
+
+def test_host_entry_back_to_back_calls():
+    """Three host-entry calls in a row on one stream, with one synchronization at the end: the
+    staging of each call's src1 waits for the product before it, and each dst is its own."""
+    N, K = 4096, 4096
+    w = synth.weights(80, N, K)
+    rep = gq.repack_q4_0(gq.quantize_q4_0(dev(w)), N, K)
+    xs = [synth.activations(81 + i, 1, K) for i in range(3)]
+    wants = [host(gq.mul_mat_q4_0_f32(rep, dev(x), N)) for x in xs]
+    hxs = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in xs]
+    hds = [torch.full((1, N), float("nan")).pin_memory() for _ in xs]
+    s = torch.cuda.current_stream()
+    for hx, hd in zip(hxs, hds):
+        gq.gq_mul_mat_q4_0_f32_host(rep, hx, hd, 1, N, K, s)
+    s.synchronize()
+    for hd, want in zip(hds, wants):
+        assert np.array_equal(hd.numpy(), want)
 
 
 def test_concatenated_rows_equal_separate_products(oracle):
