@@ -240,3 +240,42 @@ def test_attention_full_size_sampled(oracle, lens_mode):
     want, E, S, T = sampled_rows(oracle, q, k, ks, v, vs, lens, Hq // Hkv, c, picks)
     got = np.stack([host(out[b, h]) for b, h in picks])
     assert_attention(got, want, E, S, T, f"full size, lens {lens_mode}")
+
+
+def test_attention_shares_the_stream_workspace(oracle):
+    """A split sequence keeps its parts in the stream's workspace, which the products use
+    too: attention launches interleaved with Q4_0 products on one stream, and replays of a
+    captured attention launch, give the same bits every time."""
+    B, Hq, Hkv, Tcap, D = 8, 32, 8, 3000, 128
+    qf, kf, vf = synth.kv_problem(21, B, Hq, Hkv, Tcap, D)
+    lens = synth.kv_lengths(21, B, Tcap, "mix")
+    c = 1.0 / math.sqrt(D)
+    gen = np.random.default_rng(22)
+    N, K, M = 4096, 11008, 2
+    w = dev(gen.standard_normal((N, K)).astype(np.float32))
+    x = dev(gen.standard_normal((M, K)).astype(np.float32))
+    rp = gq.repack_q4_0(gq.quantize_q4_0(w), N, K)
+    y_ref = gq.mul_mat_q4_0_f32(rp, x, N)   # on the default stream: its own workspace
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        q, L = dev(qf), dev(lens)
+        k, ks = gq.kv_quantize_i8(dev(kf))
+        v, vs = gq.kv_quantize_i8(dev(vf))
+        ref = gq.attn_decode_i8(q, k, ks, v, vs, L, c)
+        for _ in range(3):
+            y = gq.mul_mat_q4_0_f32(rp, x, N)
+            got = gq.attn_decode_i8(q, k, ks, v, vs, L, c)
+            assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32))
+            assert torch.equal(got.view(torch.int32), ref.view(torch.int32))
+        out = torch.zeros_like(ref)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            gq.attn_decode_i8(q, k, ks, v, vs, L, c, out=out)
+        for _ in range(3):
+            out.zero_()
+            g.replay()
+            assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+    s.synchronize()
+    want, E, S = oracle.attn_decode_i8(qf, host(k), host(ks), host(v), host(vs), lens, c)
+    assert_attention(host(ref), want, E, S, int(lens.max()))
