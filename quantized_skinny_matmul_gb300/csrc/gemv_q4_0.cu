@@ -31,7 +31,8 @@
 //    the CTA's tiles through a ring of shared-memory chunks with bulk (TMA)
 //    copies and keep L2 prefetches ahead of it; with static weights they start
 //    before the wait on the grids in front.  8 or 16 consumer warps take the
-//    tiles of each chunk by position: up to four rows, eight dp4a per block on
+//    tiles of each chunk by position (two tiles, or one, per warp): up to four
+//    rows, eight dp4a per block on
 //    the unpacked nibbles and the codes (exact int32) scaled by d4 * d8; eight
 //    rows and more, two m16n8k16 fp16 MMAs per block whose f32 result is the
 //    exact block dot (the codes and (q - 8) are exact in fp16).  At the end of
@@ -50,13 +51,15 @@ namespace {
 constexpr int CHUNK_TILES = 16;                    // tiles per chunk = tile positions
 constexpr int PRODUCERS = 2;                       // producer warps (bulk-copy issue rate is per warp)
 
-// CTA shapes: 8 consumer warps (with no fix-up warp, two CTAs per SM, so the next
-// product's CTA streams its weights beside this one) or 16 (one CTA per SM, for
-// the ALU work of several activation rows).  A consumer warp keeps one
-// accumulator per tile position of a chunk, and the row-group sum adds the 16
-// positions in order: every output is the same sum, in the same order, for both
-// shapes.  A scheduler holds 16 K registers: five warps of 96 (16 + 2 + 2 warps,
-// one CTA) or, twice over, five of 88 (8 + 2 + 0 warps, two CTAs).
+// CTA shapes: 8 consumer warps (one row, with no fix-up warp: two CTAs per SM, so
+// the next product's CTA streams its weights beside this one; five rows and more
+// of Q4_0 weights: one CTA per SM, 128 registers, two tiles of each chunk per warp)
+// or 16 (one CTA per SM, for the dp4a work of two to four rows and the other
+// formats).  A consumer warp keeps one accumulator per tile position of a chunk,
+// and the row-group sum adds the 16 positions in order: every output is the same
+// sum, in the same order, for both shapes.  A scheduler holds 16 K registers: five
+// warps of 96 (16 + 2 + 2 warps, one CTA), twice over five of 88 (8 + 2 + 0 warps,
+// two CTAs), or three of 128 (8 + 2 + 1 warps, one CTA).
 template <int CWT, int FIXW = (CWT == 8 ? 1 : 2)>
 struct Shape {
     static constexpr int CW = CWT;                          // consumer warps
@@ -880,7 +883,8 @@ Plan plan(int N16, int NT, int M, bool f16 = false) {
 // shared memory, so that the CTAs of the next product in the stream are resident
 // and stream their weights while this product finishes; with several K slices it
 // keeps one fix-up warp and runs one CTA per SM.  The 16-warp shape (20 warps)
-// runs one CTA per SM at 96 registers.
+// runs one CTA per SM at 96 registers, the 8-warp shape of several Q4_0 rows one
+// at 128.
 struct Variant {
     int mt, cw, regs;
     int wf;
@@ -905,14 +909,20 @@ const Variant VARIANTS[] = {
     variant<1, 8, 88, WF_Q5, 0>(),   variant<1, 8, 88, WF_Q5, 1>(),   variant<2, 16, 96, WF_Q5, 2>(),
     variant<4, 16, 96, WF_Q5, 2>(),  variant<8, 16, 96, WF_Q5, 2>(),  variant<16, 16, 96, WF_Q5, 2>(),
     variant<1, 8, 88, WF_Q41, 0>(),  variant<1, 8, 88, WF_Q41, 1>(),  variant<2, 16, 96, WF_Q41, 2>(),
-    variant<4, 16, 96, WF_Q41, 2>(), variant<8, 16, 96, WF_Q41, 2>(), variant<16, 16, 96, WF_Q41, 2>()};
+    variant<4, 16, 96, WF_Q41, 2>(), variant<8, 16, 96, WF_Q41, 2>(), variant<16, 16, 96, WF_Q41, 2>(),
+    variant<8, 8, 128, WF_Q4, 0>(),  variant<8, 8, 128, WF_Q4, 1>(),  variant<16, 8, 128, WF_Q4, 0>(),
+    variant<16, 8, 128, WF_Q4, 1>()};
 constexpr int N_VARIANTS = sizeof(VARIANTS) / sizeof(VARIANTS[0]);
 static_assert(N_VARIANTS <= MAX_VARIANTS, "one shared-memory flag per variant");
 
-// One activation row: 8 consumer warps.  More rows: 16 warps for the ALU work.
-int consumer_warps_for(int M) { return M == 1 ? 8 : 16; }
+// Consumer warps and register cap.  One activation row: 8 warps at 88 registers (two CTAs per
+// SM).  Two to four rows (dp4a): 16 warps at 96.  Five rows and more of Q4_0 weights (MMA block
+// dots): 8 warps at 128 registers, each taking two tiles of a chunk; measured 13-16 % faster
+// than 16 warps at M = 8 on the 7B decode shapes and 2-5 % at M = 16.  The other formats keep
+// 16 warps for several rows.
+int consumer_warps_for(int M, int wf) { return M == 1 || (wf == WF_Q4 && M >= 5) ? 8 : 16; }
 
-int regs_for(int cw) { return cw == 16 ? 96 : 88; }
+int regs_for(int cw, int M) { return cw == 16 ? 96 : M > 1 ? 128 : 88; }
 
 const Variant *variant_for(int mt, int cw, int regs, int wf, int fixw) {
     for (int i = 0; i < N_VARIANTS; i++)
@@ -994,7 +1004,7 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
         const bool seq = q.S > 1 && (f16 || MT > 1);
         p.seq_slice = -1;
         if (seq) p.Gs = std::max(1, std::min(sm_count(), p.N16));
-        const int cw = f16 ? (MT == 8 ? 8 : 16) : consumer_warps_for(p.M);
+        const int cw = f16 ? (MT == 8 ? 8 : 16) : consumer_warps_for(p.M, wf);
         const int consumers = cw == 8 ? Shape<8>::CONSUMERS : Shape<16>::CONSUMERS;
         const int fused_loads = cw == 8 ? Shape<8>::FUSED_LOADS : Shape<16>::FUSED_LOADS;
         // fuse INIT when each consumer thread loads a few float4 (F16: always)
@@ -1004,7 +1014,7 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
                       ? 1
                       : 0;
         const int fixw = cw == 16 ? 2 : q.S == 1 ? 0 : 1;   // one K slice: no shared row group
-        const Variant *kvp = variant_for(MT, cw, regs_for(cw), wf, fixw);
+        const Variant *kvp = variant_for(MT, cw, f16 ? 88 : regs_for(cw, p.M), wf, fixw);
         if (!kvp) return fail(GQ_ERR_INVALID_ARG, "gemv: no kernel for M=%d", p.M);
         const Variant &kv = *kvp;
         // behind INIT (which waited for every earlier grid) the weights are final; otherwise only
@@ -1024,7 +1034,10 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
         // least): two CTAs per SM without fix-up warps; with one, a half ring measured faster than
         // a full one.  F16 and Q8_0 tiles (more bytes per weight; 34 KB Q8_0 chunks would leave
         // two slots in half the shared memory) keep a full ring.
-        p.slots = kv.cw == 8 && (wf == WF_Q4 || wf == WF_Q5 || wf == WF_Q41) ? slots_for(SMEM_HALF - 1024) : 0;
+        // (The 128-register shape of several rows never fits twice in an SM's registers.)
+        p.slots = kv.cw == 8 && kv.regs == 88 && (wf == WF_Q4 || wf == WF_Q5 || wf == WF_Q41)
+                      ? slots_for(SMEM_HALF - 1024)
+                      : 0;
         if (p.slots < MIN_SLOTS_HALF) p.slots = slots_for(SMEM_LIMIT - 1024);
         const int slots_env = env_int("GQ_GEMV_SLOTS", 0);   // tuning: ring slots, up to what fits
         if (slots_env > 0) p.slots = std::min(slots_env, slots_for(SMEM_LIMIT - 1024));
