@@ -52,10 +52,9 @@ constexpr int CHUNK_TILES = 16;                    // tiles per chunk = tile pos
 constexpr int PRODUCERS = 2;                       // producer warps (bulk-copy issue rate is per warp)
 
 // CTA shapes: 8 consumer warps (one row, with no fix-up warp: two CTAs per SM, so
-// the next product's CTA streams its weights beside this one; five rows and more
-// of Q4_0 weights: one CTA per SM, 128 registers, two tiles of each chunk per warp)
-// or 16 (one CTA per SM, for the dp4a work of two to four rows and the other
-// formats).  A consumer warp keeps one accumulator per tile position of a chunk,
+// the next product's CTA streams its weights beside this one; several rows of a
+// block format: one CTA per SM, 128 registers, two tiles of each chunk per warp) or
+// 16 (one CTA per SM: F16 tiles of more than 8 rows).  A consumer warp keeps one accumulator per tile position of a chunk,
 // and the row-group sum adds the 16 positions in order: every output is the same
 // sum, in the same order, for both shapes.  A scheduler holds 16 K registers: five
 // warps of 96 (16 + 2 + 2 warps, one CTA), twice over five of 88 (8 + 2 + 0 warps,
@@ -878,13 +877,14 @@ Plan plan(int N16, int NT, int M, bool f16 = false) {
 }
 
 // Instantiated kernels: activation rows per tile (MT), consumer warps (CW), the
-// register cap and the fix-up warps.  The 8-warp shape without fix-up warps (one
-// K slice: no row group is shared) runs two CTAs per SM, each with half of the
-// shared memory, so that the CTAs of the next product in the stream are resident
-// and stream their weights while this product finishes; with several K slices it
-// keeps one fix-up warp and runs one CTA per SM.  The 16-warp shape (20 warps)
-// runs one CTA per SM at 96 registers, the 8-warp shape of several Q4_0 rows one
-// at 128.
+// register cap and the fix-up warps.  The one-row 8-warp shape without fix-up
+// warps (one K slice: no row group is shared) runs two CTAs per SM, each with half
+// of the shared memory, so that the CTAs of the next product in the stream are
+// resident and stream their weights while this product finishes; with several K
+// slices in its one launch it keeps one fix-up warp and runs one CTA per SM.
+// Several rows take one launch per K slice and never share a row group.  The
+// 16-warp shape (20 warps) runs one CTA per SM at 96 registers, the 8-warp shape
+// of several rows of a block format one at 128.
 struct Variant {
     int mt, cw, regs;
     int wf;
@@ -901,28 +901,27 @@ constexpr Variant variant() {
 }
 
 const Variant VARIANTS[] = {
-    variant<1, 8, 88, WF_Q4, 0>(),   variant<1, 8, 88, WF_Q4, 1>(),   variant<2, 16, 96, WF_Q4, 2>(),
-    variant<4, 16, 96, WF_Q4, 2>(),  variant<8, 16, 96, WF_Q4, 2>(),  variant<16, 16, 96, WF_Q4, 2>(),
-    variant<8, 8, 88, WF_F16, 0>(),  variant<8, 8, 88, WF_F16, 1>(),  variant<16, 16, 96, WF_F16, 2>(),
-    variant<1, 8, 88, WF_Q8, 0>(),   variant<1, 8, 88, WF_Q8, 1>(),   variant<2, 16, 96, WF_Q8, 2>(),
-    variant<4, 16, 96, WF_Q8, 2>(),  variant<8, 16, 96, WF_Q8, 2>(),  variant<16, 16, 96, WF_Q8, 2>(),
-    variant<1, 8, 88, WF_Q5, 0>(),   variant<1, 8, 88, WF_Q5, 1>(),   variant<2, 16, 96, WF_Q5, 2>(),
-    variant<4, 16, 96, WF_Q5, 2>(),  variant<8, 16, 96, WF_Q5, 2>(),  variant<16, 16, 96, WF_Q5, 2>(),
-    variant<1, 8, 88, WF_Q41, 0>(),  variant<1, 8, 88, WF_Q41, 1>(),  variant<2, 16, 96, WF_Q41, 2>(),
-    variant<4, 16, 96, WF_Q41, 2>(), variant<8, 16, 96, WF_Q41, 2>(), variant<16, 16, 96, WF_Q41, 2>(),
-    variant<8, 8, 128, WF_Q4, 0>(),  variant<8, 8, 128, WF_Q4, 1>(),  variant<16, 8, 128, WF_Q4, 0>(),
-    variant<16, 8, 128, WF_Q4, 1>()};
+    variant<1, 8, 88, WF_Q4, 0>(),    variant<1, 8, 88, WF_Q4, 1>(),    variant<2, 8, 128, WF_Q4, 0>(),
+    variant<4, 8, 128, WF_Q4, 0>(),   variant<8, 8, 128, WF_Q4, 0>(),   variant<16, 8, 128, WF_Q4, 0>(),
+    variant<8, 8, 88, WF_F16, 0>(),   variant<16, 16, 96, WF_F16, 2>(),
+    variant<1, 8, 88, WF_Q8, 0>(),    variant<1, 8, 88, WF_Q8, 1>(),    variant<2, 8, 128, WF_Q8, 0>(),
+    variant<4, 8, 128, WF_Q8, 0>(),   variant<8, 8, 128, WF_Q8, 0>(),   variant<16, 8, 128, WF_Q8, 0>(),
+    variant<1, 8, 88, WF_Q5, 0>(),    variant<1, 8, 88, WF_Q5, 1>(),    variant<2, 8, 128, WF_Q5, 0>(),
+    variant<4, 8, 128, WF_Q5, 0>(),   variant<8, 8, 128, WF_Q5, 0>(),   variant<16, 8, 128, WF_Q5, 0>(),
+    variant<1, 8, 88, WF_Q41, 0>(),   variant<1, 8, 88, WF_Q41, 1>(),   variant<2, 8, 128, WF_Q41, 0>(),
+    variant<4, 8, 128, WF_Q41, 0>(),  variant<8, 8, 128, WF_Q41, 0>(),  variant<16, 8, 128, WF_Q41, 0>()};
 constexpr int N_VARIANTS = sizeof(VARIANTS) / sizeof(VARIANTS[0]);
 static_assert(N_VARIANTS <= MAX_VARIANTS, "one shared-memory flag per variant");
 
-// Consumer warps and register cap.  One activation row: 8 warps at 88 registers (two CTAs per
-// SM).  Two to four rows (dp4a): 16 warps at 96.  Five rows and more of Q4_0 weights (MMA block
-// dots): 8 warps at 128 registers, each taking two tiles of a chunk; measured 13-16 % faster
-// than 16 warps at M = 8 on the 7B decode shapes and 2-5 % at M = 16.  The other formats keep
-// 16 warps for several rows.
-int consumer_warps_for(int M, int wf) { return M == 1 || (wf == WF_Q4 && M >= 5) ? 8 : 16; }
+// Consumer warps and register cap.  Block formats: 8 warps, at 88 registers for one activation
+// row (two CTAs per SM) and at 128 for several (each warp taking two tiles of a chunk).  Against
+// 16 warps at 96 registers, several Q4_0 rows measured 2-16 % faster at M = 2 (where the 8-warp
+// shape also takes the separate INIT at K = 11008), 4-11 % at M = 4, 13-16 % at M = 8 and 2-5 %
+// at M = 16 on the 7B decode shapes; Q5_0 and Q4_1 at [11008, 4096] 2-17 %; Q8_0 3-5 % from M = 4
+// (2.5 % slower at M = 2).  F16 tiles: 8 warps at 88 registers for up to 8 rows, 16 at 96 above.
+int consumer_warps_for(int M, int wf) { return wf == WF_F16 ? (M <= 8 ? 8 : 16) : 8; }
 
-int regs_for(int cw, int M) { return cw == 16 ? 96 : M > 1 ? 128 : 88; }
+int regs_for(int cw, int M, int wf) { return cw == 16 ? 96 : M > 1 && wf != WF_F16 ? 128 : 88; }
 
 const Variant *variant_for(int mt, int cw, int regs, int wf, int fixw) {
     for (int i = 0; i < N_VARIANTS; i++)
@@ -1004,7 +1003,7 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
         const bool seq = q.S > 1 && (f16 || MT > 1);
         p.seq_slice = -1;
         if (seq) p.Gs = std::max(1, std::min(sm_count(), p.N16));
-        const int cw = f16 ? (MT == 8 ? 8 : 16) : consumer_warps_for(p.M, wf);
+        const int cw = consumer_warps_for(f16 ? MT : p.M, wf);
         const int consumers = cw == 8 ? Shape<8>::CONSUMERS : Shape<16>::CONSUMERS;
         const int fused_loads = cw == 8 ? Shape<8>::FUSED_LOADS : Shape<16>::FUSED_LOADS;
         // fuse INIT when each consumer thread loads a few float4 (F16: always)
@@ -1013,8 +1012,10 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
                           (int64_t)p.M * p.ntmax * 32 <= (int64_t)consumers * fused_loads * FUSED_ROUNDS
                       ? 1
                       : 0;
-        const int fixw = cw == 16 ? 2 : q.S == 1 ? 0 : 1;   // one K slice: no shared row group
-        const Variant *kvp = variant_for(MT, cw, f16 ? 88 : regs_for(cw, p.M), wf, fixw);
+        // one K slice, or one launch per slice: no shared row group, no fix-up warp (the 16-warp
+        // shape has its two either way)
+        const int fixw = cw == 16 ? 2 : q.S == 1 || seq ? 0 : 1;
+        const Variant *kvp = variant_for(MT, cw, regs_for(cw, p.M, wf), wf, fixw);
         if (!kvp) return fail(GQ_ERR_INVALID_ARG, "gemv: no kernel for M=%d", p.M);
         const Variant &kv = *kvp;
         // behind INIT (which waited for every earlier grid) the weights are final; otherwise only
