@@ -148,7 +148,11 @@ gq_status gq_mul_mat_q4_0_f32(const void *q4_repacked, const float *src1, float 
 
 /* dst[M][N] = src1[M][K] . src0[N][K]^T with F16 weights src0 (IEEE binary16,
  * row-major).  Activations are rounded to fp16 for the tensor instructions and
- * the sums are accumulated in f32 (relative error <= 2e-3 of sum |terms|). */
+ * the sums are accumulated in f32 (relative error <= 2e-3 of sum |terms|).  On
+ * the GEMV path (M <= threshold) tensor copies read the row-major weights as
+ * 16 x 32 tiles, the unit of gq_mul_mat_f16r_f32, whose kernel it shares.  Uses
+ * the stream's workspace (see gq_reserve_workspace); results do not depend on
+ * timing. */
 gq_status gq_mul_mat_f16_f32(const void *src0_f16, const float *src1, float *dst,
                              int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 

@@ -39,6 +39,8 @@
 //    a row group the positions' partials are added in shared memory in a fixed
 //    order (DeepSpeed-Inference notes, III.C.2: make the partials of one
 //    output contiguous and reduce them in one pass).
+#include <cuda.h>
+
 #include <algorithm>
 #include <atomic>
 
@@ -87,9 +89,12 @@ constexpr int Q5_TILE_BYTES = Q5_TILE_SCALE_OFFSET + 16 * TILE_BLOCKS * 2;
 constexpr int Q41_TILE_MIN_OFFSET = TILE_SCALE_OFFSET + 16 * TILE_BLOCKS * 2;
 constexpr int Q41_TILE_BYTES = Q41_TILE_MIN_OFFSET + 16 * TILE_BLOCKS * 2;
 // weight formats of the kernel
-enum : int { WF_Q4 = 0, WF_F16 = 1, WF_Q8 = 2, WF_Q5 = 3, WF_Q41 = 4 };
+// (WF_F16RM: F16 weights as stored, row-major [N][K]; a 3D tensor copy lands 16 of their
+// 16 x 32 tiles in the layout of the repacked F16 tiles, so the kernel is the repacked one's)
+enum : int { WF_Q4 = 0, WF_F16 = 1, WF_Q8 = 2, WF_Q5 = 3, WF_Q41 = 4, WF_F16RM = 5 };
+__host__ __device__ constexpr bool is_f16(int wf) { return wf == WF_F16 || wf == WF_F16RM; }
 __host__ __device__ constexpr int tile_bytes(int wf) {
-    return wf == WF_F16  ? F16_TILE_BYTES
+    return is_f16(wf)    ? F16_TILE_BYTES
            : wf == WF_Q8 ? Q8_TILE_BYTES
            : wf == WF_Q5 ? Q5_TILE_BYTES
            : wf == WF_Q41 ? Q41_TILE_BYTES
@@ -130,6 +135,7 @@ struct Image {
 };
 
 struct Params {
+    CUtensorMap wmap;        // row-major F16 weights: dims {32, N, K / 32}, box {32, 16, 16} (one chunk)
     const uint8_t *w;        // repacked Q4_0
     const float *x;          // [M][K]
     float *dst;              // [M][N]
@@ -152,7 +158,7 @@ struct Params {
 struct Layout {
     size_t bars, ring, act, red, total;
     __host__ __device__ Layout(int MT, int M, int ntmax, int slots, int maxfix, int wf = WF_Q4) {
-        const Image im(M, ntmax, wf == WF_F16);   // Q8_0 weights use the Q4_0 image
+        const Image im(M, ntmax, is_f16(wf));   // Q8_0 weights use the Q4_0 image
         bars = 0;                                         // full[slots], empty[slots], act, fix[maxfix]
         ring = align_up((size_t)(2 * slots + 1 + maxfix) * 8, 128);
         act = ring + (size_t)slots * chunk_bytes(wf);
@@ -273,12 +279,32 @@ __global__ void __launch_bounds__(256) wdata_kernel(const Params p) {
     }
 }
 
+// 3D tensor copy of one box into shared memory (completion on an mbarrier, L2 cache hint), and
+// its L2 prefetch.  Coordinates are element indices; the innermost one is 0 here (x * 2 bytes
+// aligned to 16).
+__device__ __forceinline__ void tensor3d_g2s_hint(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                                  uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tensor3d_prefetch_l2(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // COMPUTE
 // ---------------------------------------------------------------------------
 template <int MT, int CWT, int REGS, int WF, int FIXW>
-__global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) gemv_q4_0_kernel(const Params p) {
-    constexpr bool F16W = WF == WF_F16, Q8W = WF == WF_Q8, Q5W = WF == WF_Q5, Q41W = WF == WF_Q41;
+__global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS)
+    gemv_q4_0_kernel(const __grid_constant__ Params p) {
+    constexpr bool F16W = is_f16(WF), RMW = WF == WF_F16RM, Q8W = WF == WF_Q8, Q5W = WF == WF_Q5, Q41W = WF == WF_Q41;
     constexpr int TB = tile_bytes(WF), CB = chunk_bytes(WF);
     // fp16 scales in a Q4_0 / Q5_0 / Q8_0 tile
     constexpr int SCALES = Q8W ? Q8_TILE_SCALE_OFFSET : Q5W ? Q5_TILE_SCALE_OFFSET : TILE_SCALE_OFFSET;
@@ -330,16 +356,20 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
     // not declared static.
     if (warp >= PRODUCER_WARP && warp < PRODUCER_WARP + PRODUCERS) {
         const int pw = warp - PRODUCER_WARP;
-        // chunk k of this CTA's sequence: source and size; false past the last chunk
-        auto chunk_at = [&](int k, const uint8_t *&src, uint32_t &bytes) -> bool {
+        // chunk k of this CTA's sequence: source and size (row group g, first tile column t of the
+        // slice); false past the last chunk
+        auto chunk_at = [&](int k, const uint8_t *&src, uint32_t &bytes, int &g, int &t) -> bool {
             for (int j = 0; j < seg.n; j++) {
-                int g, u0, u1;
+                int u0, u1;
                 seg.get(j, g, u0, u1);
                 const int n = (u1 - u0 + CHUNK_TILES - 1) / CHUNK_TILES;
                 if (k < n) {
                     const int u = u0 + k * CHUNK_TILES;
-                    src = p.w + ((size_t)g * p.NT + ts0 + u) * TB;
-                    bytes = (uint32_t)(min(CHUNK_TILES, u1 - u) * TB);
+                    t = ts0 + u;
+                    src = p.w + ((size_t)g * p.NT + t) * TB;
+                    // row-major F16: the whole box, whose tiles past the row group's end are those
+                    // of the next K slice (unused) or lie past K (zeros)
+                    bytes = RMW ? (uint32_t)CB : (uint32_t)(min(CHUNK_TILES, u1 - u) * TB);
                     return true;
                 }
                 k -= n;
@@ -350,7 +380,11 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
         auto prefetch_to = [&](int kend) {
             const uint8_t *src;
             uint32_t bytes;
-            for (; kp < kend && chunk_at(kp, src, bytes); kp += PRODUCERS) bulk_prefetch_l2(src, bytes);
+            int g, t;
+            for (; kp < kend && chunk_at(kp, src, bytes, g, t); kp += PRODUCERS) {
+                if constexpr (RMW) tensor3d_prefetch_l2(&p.wmap, 0, 16 * g, t);
+                else bulk_prefetch_l2(src, bytes);
+            }
         };
         if (!p.early) {
             if (lane == 0) prefetch_to(p.pf);
@@ -360,13 +394,18 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS) g
             const uint64_t policy = l2_evict_first_policy();   // every weight byte is read once
             const uint8_t *src;
             uint32_t bytes;
-            for (int k = pw; chunk_at(k, src, bytes); k += PRODUCERS) {
+            int g, t;
+            for (int k = pw; chunk_at(k, src, bytes, g, t); k += PRODUCERS) {
                 const int slot = k % p.slots;
                 if (k >= p.slots &&
                     !mbar_wait(smem_addr(empty + slot), (uint32_t)(((k / p.slots) - 1) & 1), p.status))
                     break;
                 mbar_arrive_expect_tx(smem_addr(full + slot), bytes);
-                bulk_g2s_hint(smem_addr(ring + (size_t)slot * CB), src, bytes, smem_addr(full + slot), policy);
+                if constexpr (RMW)
+                    tensor3d_g2s_hint(smem_addr(ring + (size_t)slot * CB), &p.wmap, 0, 16 * g, t, smem_addr(full + slot),
+                                      policy);
+                else
+                    bulk_g2s_hint(smem_addr(ring + (size_t)slot * CB), src, bytes, smem_addr(full + slot), policy);
                 prefetch_to(k + p.pf);
             }
         }
@@ -904,6 +943,7 @@ const Variant VARIANTS[] = {
     variant<1, 8, 88, WF_Q4, 0>(),    variant<1, 8, 88, WF_Q4, 1>(),    variant<2, 8, 128, WF_Q4, 0>(),
     variant<4, 8, 128, WF_Q4, 0>(),   variant<8, 8, 128, WF_Q4, 0>(),   variant<16, 8, 128, WF_Q4, 0>(),
     variant<8, 8, 88, WF_F16, 0>(),   variant<16, 16, 96, WF_F16, 2>(),
+    variant<8, 8, 88, WF_F16RM, 0>(), variant<16, 16, 96, WF_F16RM, 2>(),
     variant<1, 8, 88, WF_Q8, 0>(),    variant<1, 8, 88, WF_Q8, 1>(),    variant<2, 8, 128, WF_Q8, 0>(),
     variant<4, 8, 128, WF_Q8, 0>(),   variant<8, 8, 128, WF_Q8, 0>(),   variant<16, 8, 128, WF_Q8, 0>(),
     variant<1, 8, 88, WF_Q5, 0>(),    variant<1, 8, 88, WF_Q5, 1>(),    variant<2, 8, 128, WF_Q5, 0>(),
@@ -919,9 +959,9 @@ static_assert(N_VARIANTS <= MAX_VARIANTS, "one shared-memory flag per variant");
 // shape also takes the separate INIT at K = 11008), 4-11 % at M = 4, 13-16 % at M = 8 and 2-5 %
 // at M = 16 on the 7B decode shapes; Q5_0 and Q4_1 at [11008, 4096] 2-17 %; Q8_0 3-5 % from M = 4
 // (2.5 % slower at M = 2).  F16 tiles: 8 warps at 88 registers for up to 8 rows, 16 at 96 above.
-int consumer_warps_for(int M, int wf) { return wf == WF_F16 ? (M <= 8 ? 8 : 16) : 8; }
+int consumer_warps_for(int M, int wf) { return is_f16(wf) ? (M <= 8 ? 8 : 16) : 8; }
 
-int regs_for(int cw, int M, int wf) { return cw == 16 ? 96 : M > 1 && wf != WF_F16 ? 128 : 88; }
+int regs_for(int cw, int M, int wf) { return cw == 16 ? 96 : M > 1 && !is_f16(wf) ? 128 : 88; }
 
 const Variant *variant_for(int mt, int cw, int regs, int wf, int fixw) {
     for (int i = 0; i < N_VARIANTS; i++)
@@ -934,7 +974,7 @@ const Variant *variant_for(int mt, int cw, int regs, int wf, int fixw) {
 }  // namespace
 
 void gemv_workspace(int wf, int64_t N, int64_t K, size_t *counter_bytes, size_t *data_bytes) {
-    const bool f16 = wf == WF_F16;
+    const bool f16 = is_f16(wf);
     const int N16 = (int)((N + 15) / 16);
     const int NT = f16 ? (int)(K / F16_TILE_COLS) : (int)((K + TILE_COLS - 1) / TILE_COLS);
     size_t db = 0;
@@ -966,7 +1006,7 @@ namespace {
 
 gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
                            const Workspace &ws, cudaStream_t s) {
-    const bool f16 = wf == WF_F16;
+    const bool f16 = is_f16(wf);
     Params p{};
     p.w = (const uint8_t *)rep;
     p.status = device_status_word();
@@ -978,6 +1018,10 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
     p.NT = f16 ? (int)(K / F16_TILE_COLS) : (int)((K + TILE_COLS - 1) / TILE_COLS);
 
     gq_status st = GQ_OK;
+    if (wf == WF_F16RM) {
+        st = f16_tile_map(&p.wmap, rep, N, K);
+        if (st != GQ_OK) return st;
+    }
     p.cnt = reinterpret_cast<unsigned int *>(ws.counters);
 
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
@@ -1095,6 +1139,16 @@ gq_status launch_gemv_f16r(const void *rep, const float *x, float *dst, int64_t 
     gq_status st = get_workspace(s, cb, db, &ws);
     if (st != GQ_OK) return st;
     return launch_gemv_with(WF_F16, rep, x, dst, M, N, K, ws, s);
+}
+
+gq_status launch_gemv_f16_rowmajor(const void *w16, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                                   cudaStream_t s) {
+    size_t cb, db;
+    gemv_f16r_workspace(N, K, &cb, &db);
+    Workspace ws;
+    gq_status st = get_workspace(s, cb, db, &ws);
+    if (st != GQ_OK) return st;
+    return launch_gemv_with(WF_F16RM, w16, x, dst, M, N, K, ws, s);
 }
 
 gq_status launch_gemv_q4_0(const void *rep, const float *x, float *dst, int64_t M, int64_t N, int64_t K,

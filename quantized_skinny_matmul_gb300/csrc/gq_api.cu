@@ -373,7 +373,7 @@ gq_status gq_mul_mat_f16_f32_path(const void *src0_f16, const float *src1, float
     if (resolve(path, GQ_KIND_F16, M, N, K) == GQ_PATH_TC)
         GQ_TRY(launch_tc_f16(src0_f16, src1, dst, M, N, K, stream));
     else
-        GQ_TRY(launch_gemv_f16(src0_f16, src1, dst, M, N, K, stream));
+        GQ_TRY(launch_gemv_f16_rowmajor(src0_f16, src1, dst, M, N, K, stream));
     return ok();
 }
 

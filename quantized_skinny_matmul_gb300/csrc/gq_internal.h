@@ -56,8 +56,6 @@ gq_status launch_gemv_q4_0_with(const void *rep, const float *x, float *dst, int
 // [N][K], and its launch.
 bool gemv_m1_supported(int64_t N, int64_t K);
 gq_status launch_gemv_m1_q4_0(const void *rep, const float *x, float *dst, int64_t N, int64_t K, cudaStream_t s);
-gq_status launch_gemv_f16(const void *w16, const float *x, float *dst, int64_t M, int64_t N,
-                          int64_t K, cudaStream_t s);
 // F16 weights repacked into 16 x 32 tiles: the repack, and the GEMV on them (the Q4_0
 // GEMV's pipeline with fp16 MMAs on the tiles as stored).
 gq_status launch_repack_f16(const void *w16, void *rep, int64_t N, int64_t K, cudaStream_t s);
@@ -97,6 +95,14 @@ gq_status launch_attn_decode_i8(const float *q, const int8_t *k, const float *ks
 // bytes at `base`: boxes of 128 bytes x box_rows rows, 128-byte swizzle, rows past the end
 // read as zeros.
 gq_status byte_rows_map(void *map, const void *base, int64_t rows, int box_rows);
+// A 3D tensor map (`map` as above) over row-major F16 weights [N][K] (K a multiple of 32):
+// dimensions {32 columns, N rows, K / 32 tile columns}, boxes {32, 16, 16}: one box is 16
+// consecutive 16 x 32 tiles of a row group, each stored as 16 rows of 64 bytes, one tile after
+// the other (the repacked F16 layout).  Rows past N and columns past K read as zeros.
+gq_status f16_tile_map(void *map, const void *base, int64_t N, int64_t K);
+// The F16 product over row-major weights through the GEMV pipeline of the repacked tiles.
+gq_status launch_gemv_f16_rowmajor(const void *w16, const float *x, float *dst, int64_t M, int64_t N, int64_t K,
+                                   cudaStream_t s);
 gq_status launch_block_dots_q4_0(const void *rep, const void *q8, int32_t *sumi, int64_t M,
                                  int64_t N, int64_t K, cudaStream_t s);
 

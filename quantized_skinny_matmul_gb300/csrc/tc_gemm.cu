@@ -666,6 +666,26 @@ gq_status launch_tc_f16(const void *w16, const float *x, float *dst, int64_t M, 
     return launch_tc_common(false, w16, x, dst, M, N, K, s);
 }
 
+constexpr int F16_TILE_COLS_RM = 32;
+
+gq_status f16_tile_map(void *map, const void *base, int64_t N, int64_t K) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    gq_status st = encoder(&enc);
+    if (st != GQ_OK) return st;
+    if (N <= 0 || N > 0xFFFFFFFFLL || K <= 0 || K % F16_TILE_COLS_RM)
+        return fail(GQ_ERR_INVALID_ARG, "row-major F16 tensor map of %lld x %lld", (long long)N, (long long)K);
+    // element (column c of tile column t, row n) at base + 2 (n K + 32 t + c)
+    const cuuint64_t dims[3] = {(cuuint64_t)F16_TILE_COLS_RM, (cuuint64_t)N, (cuuint64_t)(K / F16_TILE_COLS_RM)};
+    const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)F16_TILE_COLS_RM * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)F16_TILE_COLS_RM, 16u, 16u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = enc(reinterpret_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base),
+                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GQ_ERR_CUDA, "cuTensorMapEncodeTiled (row-major F16 tiles) failed (%d)", (int)r);
+    return GQ_OK;
+}
+
 gq_status byte_rows_map(void *map, const void *base, int64_t rows, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     gq_status st = encoder(&enc);
