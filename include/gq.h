@@ -294,7 +294,11 @@ gq_status gq_mul_mat_f16_f32_path(const void *src0_f16, const float *src1, float
  * narrow kernel serves products of at most 16 rows, the tiles the rest).  Q4_0
  * products of 2 .. threshold rows whose activation image needs several K slices
  * (one GEMV launch per slice, for example 9 to 16 rows at K = 11008) take the
- * tiles, which split K within one launch.
+ * tiles, which split K within one launch.  F16 products take the GEMV only when
+ * N < 64 x the number of SMs and M * K * 2 <= 64 KiB (the fp16 activations);
+ * otherwise the tiles, which read fp16 weights straight into the tensor cores
+ * and measured faster there (for example [11008, 4096] at every M, [4096, 11008]
+ * from 3 rows, [4096, 4096] from 9).
  * Process-wide; GQ_ERR_INVALID_ARG if t < 0.  The environment variable
  * GQ_M_THRESHOLD, read when the library loads, replaces the default when it
  * holds a non-negative decimal integer (other values are ignored). */

@@ -306,6 +306,11 @@ static gq_path choose_path(int kind, int64_t N, int64_t K, int64_t M) {
     }
     if (M > g_m_threshold.load()) return GQ_PATH_TC;
     if (kind == GQ_KIND_Q4_0 && M > 1 && gemv_q4_0_slices(N, K, M) > 1) return GQ_PATH_TC;
+    // F16: the tiles stream fp16 weights into the MMAs with nothing to convert, and measured faster
+    // than the GEMV once their grid has enough row tiles (N >= 64 per SM: [11008, 4096] at every M)
+    // or once the GEMV's fp16 image of the activations passes 64 KiB ([4096, 11008] from 3 rows,
+    // [4096, 4096] from 9)
+    if (kind == GQ_KIND_F16 && (N >= 64 * (int64_t)sm_count() || M * K * 2 > 64 * 1024)) return GQ_PATH_TC;
     return GQ_PATH_GEMV;
 }
 

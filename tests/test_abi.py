@@ -207,6 +207,24 @@ def test_dispatch_takes_the_tiles_when_the_gemv_needs_several_slices(lib):
     assert gq.gq_choose_path(Q, 64, 100000, 1) == gq.GQ_PATH_GEMV
 
 
+def test_dispatch_f16_takes_the_tiles_for_large_grids_or_images(lib):
+    """Without a profile, F16 products take the GEMV only for fewer than 64 weight rows per SM
+    and at most 64 KiB of fp16 activations (no GPU involved: the SM count then defaults to 148)."""
+    gq.gq_clear_dispatch_profiles()
+    F = gq.GQ_KIND_F16
+    for M in (1, 4, 16):
+        assert gq.gq_choose_path(F, 11008, 4096, M) == gq.GQ_PATH_TC, M
+    for M in (1, 2):
+        assert gq.gq_choose_path(F, 4096, 11008, M) == gq.GQ_PATH_GEMV, M
+    for M in (3, 8, 16):
+        assert gq.gq_choose_path(F, 4096, 11008, M) == gq.GQ_PATH_TC, M
+    for M in (1, 8):
+        assert gq.gq_choose_path(F, 4096, 4096, M) == gq.GQ_PATH_GEMV, M
+    for M in (9, 16, 17):
+        assert gq.gq_choose_path(F, 4096, 4096, M) == gq.GQ_PATH_TC, M
+    assert gq.gq_choose_path(F, 4096, 40000, 1) == gq.GQ_PATH_TC
+
+
 def test_argument_checks_kv_cache(lib):
     """The INT8 KV-cache entry points reject bad sizes, head counts and pointers before
     touching the GPU."""
