@@ -155,6 +155,11 @@ struct Params {
                              // (one launch per slice); slices after the first add into dst
 };
 
+// Buffers of row-group partials: four for tiles of up to 4 rows (the partials of two row groups
+// are added after one barrier: 2-4 % faster at M = 2 and 4 on the 7B decode shapes), two above
+// (one barrier per row group; four buffers cost a ring slot at M = 8 and measured 5 % slower).
+__host__ __device__ constexpr int red_buffers(int MT) { return MT <= 4 ? 4 : 2; }
+
 struct Layout {
     size_t bars, ring, act, red, total;
     __host__ __device__ Layout(int MT, int M, int ntmax, int slots, int maxfix, int wf = WF_Q4) {
@@ -163,7 +168,7 @@ struct Layout {
         ring = align_up((size_t)(2 * slots + 1 + maxfix) * 8, 128);
         act = ring + (size_t)slots * chunk_bytes(wf);
         red = act + im.bytes;
-        total = red + 2 * (size_t)CHUNK_TILES * 16 * MT * 4;   // two buffers: row groups alternate
+        total = red + (size_t)red_buffers(MT) * CHUNK_TILES * 16 * MT * 4;   // row groups rotate over them
     }
 };
 
@@ -638,6 +643,8 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS)
 
     int slot = 0;
     uint32_t phase = 0;
+    constexpr int NRB = red_buffers(MT), BATCH = NRB / 2;   // row groups added after one barrier
+    int pend = 0, gprev = 0;   // row groups written but not yet added (0 .. BATCH - 1); the last one's g
     for (int j = 0; j < seg.n; j++) {
         int g, u0, u1;
         seg.get(j, g, u0, u1);
@@ -819,10 +826,12 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS)
         }
 
         // ---- row group g of this slice is complete: add the partials of the 16 tile positions.
-        // Row groups alternate between two buffers: the threads that add row group j's
-        // partials are done before they reach the barrier of row group j + 1, which every
-        // writer of row group j + 2 has passed, so one barrier per row group suffices.
-        float *redb = red + (j & 1) * CHUNK_TILES * outs;
+        // Row group j's partials go to buffer j % NRB.  After a barrier the consumer threads add
+        // those of the row groups written since the last one (at most BATCH; a row group shared
+        // with another CTA is added at once, for the fix-up).  Before a buffer is written again,
+        // every row group that used it has been added: the threads that add a batch do so before
+        // they reach the next barrier, which the writers of the batch after next have passed.
+        float *redb = red + (j % NRB) * CHUNK_TILES * outs;
         if constexpr (MMA) {
 #pragma unroll
             for (int tw = 0; tw < TPW; tw++)
@@ -845,23 +854,34 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS)
                     acc[tw][m] = 0.0f;
                 }
         }
+        const bool shared_rg = j < seg.nshared;
+        if (!shared_rg && pend + 1 < BATCH && j + 1 < seg.n && j + 1 >= seg.nshared) {
+            pend++;                                    // added with the next row group
+            gprev = g;
+            continue;
+        }
         consumers_sync<CONSUMERS>();
-        if (tid < outs) {
+        const int nb = pend + 1;                       // row groups j - pend .. j
+        for (int t = tid; t < nb * outs; t += CONSUMERS) {
+            const int k = t / outs, o = t % outs, jj = j - pend + k;
+            const int gg = k == pend ? g : gprev;      // BATCH <= 2: an earlier row group is the previous one
+            const float *rbuf = red + (jj % NRB) * CHUNK_TILES * outs;
             float v = 0.0f;
 #pragma unroll
-            for (int pos = 0; pos < CHUNK_TILES; pos++) v += redb[pos * outs + tid];
-            if (j < seg.nshared) {                     // this CTA's part of a shared row group
-                const int slot_i = ci == owner(T, p.Gs, g * nts) ? 0 : 1;
-                p.part[(((size_t)g * p.S + s) * 2 + slot_i) * PART_STRIDE + tid] = v;
+            for (int pos = 0; pos < CHUNK_TILES; pos++) v += rbuf[pos * outs + o];
+            if (shared_rg) {                           // this CTA's part of a shared row group
+                const int slot_i = ci == owner(T, p.Gs, gg * nts) ? 0 : 1;
+                p.part[(((size_t)gg * p.S + s) * 2 + slot_i) * PART_STRIDE + o] = v;
             } else {
-                const int m = tid / 16, row = 16 * g + tid % 16;
+                const int m = o / 16, row = 16 * gg + o % 16;
                 if (m < p.M && row < p.N) {   // a later slice's launch adds to the earlier ones' sum
-                    float *o = p.dst + (size_t)m * p.N + row;
-                    *o = seq_slice > 0 ? *o + v : v;
+                    float *dp = p.dst + (size_t)m * p.N + row;
+                    *dp = seq_slice > 0 ? *dp + v : v;
                 }
             }
         }
-        if (j < seg.nshared) {                         // the partial is written: the fix-up may read it
+        pend = 0;
+        if (shared_rg) {                               // the partial is written: the fix-up may read it
             consumers_sync<CONSUMERS>();
             if (tid == 0) mbar_arrive(smem_addr(fixbar + j));
         }
