@@ -1054,12 +1054,13 @@ __global__ void __launch_bounds__(AmCfg<G>::THREADS, 2)
 
 // Merges the S parts of each output row in order: with M the largest part maximum,
 // out = sum_z 2^(m_z - M) o_z / sum_z 2^(m_z - M) l_z, both sums over z in increasing order.
-// One CTA per row, one thread per column.  Two forms with the same result: a thread walks the
-// parts one by one (few parts), or (many parts: a long cache split over many CTAs) the maxima,
-// weights and sums of MERGE_CHUNK parts at a time are read in parallel into shared memory and a
-// thread keeps MERGE_BATCH value loads in flight, so that no chain of dependent loads runs over
-// all the parts (at S = 38 the merge went from about 8 to about 5 us).
-constexpr int MERGE_CHUNK = 256, MERGE_BATCH = 8, MERGE_WIDE_FROM = 16;
+// One CTA per row.  Two forms: one thread per column walks the parts one by one (few parts);
+// or (many parts: a long cache split over many CTAs) the maxima, weights and sums of MERGE_CHUNK
+// parts at a time are read in parallel into shared memory, and MERGE_GROUPS groups of one thread
+// per column each add every MERGE_GROUPS-th part (MERGE_BATCH value loads in flight per thread),
+// then the groups are added in order, so that no chain of dependent loads runs over all the
+// parts.  Both orders are fixed: results are deterministic.
+constexpr int MERGE_CHUNK = 256, MERGE_BATCH = 8, MERGE_WIDE_FROM = 16, MERGE_GROUPS = 4;
 
 __global__ void attn_merge_kernel(const float *part, float *out, int S, int D) {
     pdl_wait();
@@ -1081,47 +1082,60 @@ __global__ void attn_merge_kernel(const float *part, float *out, int S, int D) {
 }
 
 __global__ void attn_merge_wide_kernel(const float *part, float *out, int S, int D) {
-    __shared__ float sa[MERGE_CHUNK], sl[MERGE_CHUNK], sred[32];
+    __shared__ float sa[MERGE_CHUNK], sl[MERGE_CHUNK], sred[32], so[MERGE_GROUPS][128];
     pdl_wait();
     const float *pp = part + (size_t)blockIdx.x * S * (D + 2);
-    const int d = threadIdx.x, lane = d & 31, wid = d >> 5, nw = (blockDim.x + 31) >> 5;
-    // M: every thread takes the parts d, d + D, ...; then the warps, then the CTA
+    const int tid = threadIdx.x, d = tid % D, grp = tid / D;   // MERGE_GROUPS groups of D threads
+    const int lane = tid & 31, wid = tid >> 5, nw = (int)(blockDim.x >> 5);
+    // M: every thread takes the parts tid, tid + blockDim.x, ...; then the warps, then the CTA
     float M = -INFINITY;
-    for (int z = d; z < S; z += blockDim.x) M = fmaxf(M, pp[(size_t)z * (D + 2) + D]);
+    for (int z = tid; z < S; z += blockDim.x) M = fmaxf(M, pp[(size_t)z * (D + 2) + D]);
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
     if (lane == 0) sred[wid] = M;
     __syncthreads();
     M = sred[0];
     for (int w = 1; w < nw; w++) M = fmaxf(M, sred[w]);
+    if (M == -INFINITY) {   // every part is empty
+        if (grp == 0) out[(size_t)blockIdx.x * D + d] = 0.0f;
+        return;
+    }
     float o = 0.0f, l = 0.0f;
-    if (M != -INFINITY) {
-        for (int z0 = 0; z0 < S; z0 += MERGE_CHUNK) {
-            const int nz = min(MERGE_CHUNK, S - z0);
-            __syncthreads();   // the previous chunk's weights are no longer read
-            for (int i = d; i < nz; i += blockDim.x) {
-                const float *pz = pp + (size_t)(z0 + i) * (D + 2);
-                sa[i] = exp2f(pz[D] - M);
-                sl[i] = pz[D + 1];
+    for (int z0 = 0; z0 < S; z0 += MERGE_CHUNK) {
+        const int nz = min(MERGE_CHUNK, S - z0);
+        __syncthreads();   // the previous chunk's weights are no longer read (and sred, M, by all)
+        for (int i = tid; i < nz; i += blockDim.x) {
+            const float *pz = pp + (size_t)(z0 + i) * (D + 2);
+            sa[i] = exp2f(pz[D] - M);
+            sl[i] = pz[D + 1];
+        }
+        __syncthreads();
+        if (tid == 0)
+            for (int i = 0; i < nz; i++) l += sa[i] * sl[i];
+        // group grp adds the parts grp, grp + MERGE_GROUPS, ... of the chunk, in increasing order
+        for (int i0 = grp; i0 < nz; i0 += MERGE_GROUPS * MERGE_BATCH) {
+            float v[MERGE_BATCH];
+#pragma unroll
+            for (int jj = 0; jj < MERGE_BATCH; jj++) {
+                const int i = i0 + jj * MERGE_GROUPS;
+                v[jj] = i < nz ? pp[(size_t)(z0 + i) * (D + 2) + d] : 0.0f;
             }
-            __syncthreads();
-            if (d == 0)
-                for (int i = 0; i < nz; i++) l += sa[i] * sl[i];
-            for (int i0 = 0; i0 < nz; i0 += MERGE_BATCH) {
-                float v[MERGE_BATCH];
 #pragma unroll
-                for (int j = 0; j < MERGE_BATCH; j++)
-                    v[j] = i0 + j < nz ? pp[(size_t)(z0 + i0 + j) * (D + 2) + d] : 0.0f;
-#pragma unroll
-                for (int j = 0; j < MERGE_BATCH; j++)
-                    if (i0 + j < nz) o += sa[i0 + j] * v[j];
+            for (int jj = 0; jj < MERGE_BATCH; jj++) {
+                const int i = i0 + jj * MERGE_GROUPS;
+                if (i < nz) o += sa[i] * v[jj];
             }
         }
-        if (d == 0) sred[0] = l;   // every thread has read sred[0] (M) before the chunks' barriers
-        __syncthreads();
-        l = sred[0];
     }
-    out[(size_t)blockIdx.x * D + d] = l > 0.0f ? o / l : 0.0f;
+    so[grp][d] = o;
+    if (tid == 0) sred[0] = l;
+    __syncthreads();
+    if (grp == 0) {   // the groups in order
+        float t = so[0][d];
+        for (int q = 1; q < MERGE_GROUPS; q++) t += so[q][d];
+        const float lt = sred[0];
+        out[(size_t)blockIdx.x * D + d] = lt > 0.0f ? t / lt : 0.0f;
+    }
 }
 
 // One warp per row of D values: the row's f32 scale amax / 127 and its int8 codes.
@@ -1227,7 +1241,7 @@ gq_status launch_attn_dg(const AttnParams &base, int64_t B, int64_t Tcap, cudaSt
         int Si = (int)S, Di = D;
         void *margs[] = {(void *)&part, (void *)&out, (void *)&Si, (void *)&Di};
         KV_TRY(pdl_launch(S >= MERGE_WIDE_FROM ? (const void *)attn_merge_wide_kernel : (const void *)attn_merge_kernel,
-                          dim3((unsigned)(B * base.Hkv * G)), dim3(D), 0, s,
+                          dim3((unsigned)(B * base.Hkv * G)), dim3(S >= MERGE_WIDE_FROM ? D * MERGE_GROUPS : D), 0, s,
                                    margs));
     }
     return GQ_OK;
@@ -1289,7 +1303,8 @@ gq_status launch_attn_mma(const AttnParams &base, int64_t B, int64_t Tcap, cudaS
         int Si = (int)S, Di = C::D;
         void *margs[] = {(void *)&part, (void *)&out, (void *)&Si, (void *)&Di};
         KV_TRY(pdl_launch(S >= MERGE_WIDE_FROM ? (const void *)attn_merge_wide_kernel : (const void *)attn_merge_kernel,
-                          dim3((unsigned)(B * base.Hkv * G)), dim3(C::D), 0, s, margs));
+                          dim3((unsigned)(B * base.Hkv * G)), dim3(S >= MERGE_WIDE_FROM ? C::D * MERGE_GROUPS : C::D), 0,
+                          s, margs));
     }
     return GQ_OK;
 }
