@@ -93,8 +93,10 @@ constexpr int Q41_TILE_BYTES = Q41_TILE_MIN_OFFSET + 16 * TILE_BLOCKS * 2;
 // 16 x 32 tiles in the layout of the repacked F16 tiles, so the kernel is the repacked one's)
 enum : int { WF_Q4 = 0, WF_F16 = 1, WF_Q8 = 2, WF_Q5 = 3, WF_Q41 = 4, WF_F16RM = 5 };
 __host__ __device__ constexpr bool is_f16(int wf) { return wf == WF_F16 || wf == WF_F16RM; }
+// (tile_bytes and Layout spell the F16 test out: the kernels build their Layout from a wf argument,
+// and with the call to is_f16 there the one-row 88-register kernels spilled and ran 5-10 % slower)
 __host__ __device__ constexpr int tile_bytes(int wf) {
-    return is_f16(wf)    ? F16_TILE_BYTES
+    return wf == WF_F16 || wf == WF_F16RM ? F16_TILE_BYTES
            : wf == WF_Q8 ? Q8_TILE_BYTES
            : wf == WF_Q5 ? Q5_TILE_BYTES
            : wf == WF_Q41 ? Q41_TILE_BYTES
@@ -134,8 +136,19 @@ struct Image {
     }
 };
 
+// The tensor map of row-major F16 weights (dims {32, N, K / 32}, box {32, 16, 16}: one chunk),
+// a kernel parameter of its own: in the parameters of every kernel, its 128 bytes made the
+// 88-register one-row kernels spill (and run 5-7 % slower), so the other kernels take a byte.
+template <bool RM>
+struct Wmap {
+    unsigned char unused;
+};
+template <>
+struct Wmap<true> {
+    CUtensorMap map;
+};
+
 struct Params {
-    CUtensorMap wmap;        // row-major F16 weights: dims {32, N, K / 32}, box {32, 16, 16} (one chunk)
     const uint8_t *w;        // repacked Q4_0
     const float *x;          // [M][K]
     float *dst;              // [M][N]
@@ -155,15 +168,16 @@ struct Params {
                              // (one launch per slice); slices after the first add into dst
 };
 
-// Buffers of row-group partials: four for tiles of up to 4 rows (the partials of two row groups
-// are added after one barrier: 2-4 % faster at M = 2 and 4 on the 7B decode shapes), two above
-// (one barrier per row group; four buffers cost a ring slot at M = 8 and measured 5 % slower).
-__host__ __device__ constexpr int red_buffers(int MT) { return MT <= 4 ? 4 : 2; }
+// Buffers of row-group partials: four for tiles of 2 to 4 rows (the partials of two row groups
+// are added after one barrier: 2-4 % faster at M = 2 and 4 on the 7B decode shapes), two otherwise
+// (one barrier per row group; four buffers cost a ring slot at M = 8 and measured 5 % slower, and
+// the 88-register one-row shape spilled and lost 5-7 % with them).
+__host__ __device__ constexpr int red_buffers(int MT) { return MT >= 2 && MT <= 4 ? 4 : 2; }
 
 struct Layout {
     size_t bars, ring, act, red, total;
     __host__ __device__ Layout(int MT, int M, int ntmax, int slots, int maxfix, int wf = WF_Q4) {
-        const Image im(M, ntmax, is_f16(wf));   // Q8_0 weights use the Q4_0 image
+        const Image im(M, ntmax, wf == WF_F16 || wf == WF_F16RM);   // Q8_0 weights use the Q4_0 image
         bars = 0;                                         // full[slots], empty[slots], act, fix[maxfix]
         ring = align_up((size_t)(2 * slots + 1 + maxfix) * 8, 128);
         act = ring + (size_t)slots * chunk_bytes(wf);
@@ -308,7 +322,7 @@ __device__ __forceinline__ void tensor3d_prefetch_l2(const CUtensorMap *map, int
 // ---------------------------------------------------------------------------
 template <int MT, int CWT, int REGS, int WF, int FIXW>
 __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS)
-    gemv_q4_0_kernel(const __grid_constant__ Params p) {
+    gemv_q4_0_kernel(const Params p, const __grid_constant__ Wmap<WF == WF_F16RM> wm) {
     constexpr bool F16W = is_f16(WF), RMW = WF == WF_F16RM, Q8W = WF == WF_Q8, Q5W = WF == WF_Q5, Q41W = WF == WF_Q41;
     constexpr int TB = tile_bytes(WF), CB = chunk_bytes(WF);
     // fp16 scales in a Q4_0 / Q5_0 / Q8_0 tile
@@ -387,7 +401,7 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS)
             uint32_t bytes;
             int g, t;
             for (; kp < kend && chunk_at(kp, src, bytes, g, t); kp += PRODUCERS) {
-                if constexpr (RMW) tensor3d_prefetch_l2(&p.wmap, 0, 16 * g, t);
+                if constexpr (RMW) tensor3d_prefetch_l2(&wm.map, 0, 16 * g, t);
                 else bulk_prefetch_l2(src, bytes);
             }
         };
@@ -407,7 +421,7 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS)
                     break;
                 mbar_arrive_expect_tx(smem_addr(full + slot), bytes);
                 if constexpr (RMW)
-                    tensor3d_g2s_hint(smem_addr(ring + (size_t)slot * CB), &p.wmap, 0, 16 * g, t, smem_addr(full + slot),
+                    tensor3d_g2s_hint(smem_addr(ring + (size_t)slot * CB), &wm.map, 0, 16 * g, t, smem_addr(full + slot),
                                       policy);
                 else
                     bulk_g2s_hint(smem_addr(ring + (size_t)slot * CB), src, bytes, smem_addr(full + slot), policy);
@@ -855,6 +869,29 @@ __global__ void __launch_bounds__(Shape<CWT, FIXW>::THREADS) __maxnreg__(REGS)
                 }
         }
         const bool shared_rg = j < seg.nshared;
+        if constexpr (BATCH == 1) {   // one row group per barrier
+            consumers_sync<CONSUMERS>();
+            if (tid < outs) {
+                float v = 0.0f;
+#pragma unroll
+                for (int pos = 0; pos < CHUNK_TILES; pos++) v += redb[pos * outs + tid];
+                if (shared_rg) {                       // this CTA's part of a shared row group
+                    const int slot_i = ci == owner(T, p.Gs, g * nts) ? 0 : 1;
+                    p.part[(((size_t)g * p.S + s) * 2 + slot_i) * PART_STRIDE + tid] = v;
+                } else {
+                    const int m = tid / 16, row = 16 * g + tid % 16;
+                    if (m < p.M && row < p.N) {   // a later slice's launch adds to the earlier ones' sum
+                        float *dp = p.dst + (size_t)m * p.N + row;
+                        *dp = seq_slice > 0 ? *dp + v : v;
+                    }
+                }
+            }
+            if (shared_rg) {                           // the partial is written: the fix-up may read it
+                consumers_sync<CONSUMERS>();
+                if (tid == 0) mbar_arrive(smem_addr(fixbar + j));
+            }
+            continue;
+        }
         if (!shared_rg && pend + 1 < BATCH && j + 1 < seg.n && j + 1 >= seg.nshared) {
             pend++;                                    // added with the next row group
             gprev = g;
@@ -949,14 +986,14 @@ struct Variant {
     int wf;
     int fixw;
     int consumers, threads, fused_loads;
-    void (*kernel)(Params);
+    const void *kernel;   // gemv_q4_0_kernel<...>(Params, Wmap<wf == WF_F16RM>)
 };
 
 template <int MT, int CW, int REGS, int WF, int FIXW>
-constexpr Variant variant() {
+Variant variant() {
     using SH = Shape<CW, FIXW>;
     return {MT, CW, REGS, WF, FIXW, SH::CONSUMERS, SH::THREADS, SH::FUSED_LOADS,
-            gemv_q4_0_kernel<MT, CW, REGS, WF, FIXW>};
+            reinterpret_cast<const void *>(gemv_q4_0_kernel<MT, CW, REGS, WF, FIXW>)};
 }
 
 const Variant VARIANTS[] = {
@@ -1038,8 +1075,10 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
     p.NT = f16 ? (int)(K / F16_TILE_COLS) : (int)((K + TILE_COLS - 1) / TILE_COLS);
 
     gq_status st = GQ_OK;
+    Wmap<true> wmap{};       // row-major F16 only
+    Wmap<false> no_wmap{};
     if (wf == WF_F16RM) {
-        st = f16_tile_map(&p.wmap, rep, N, K);
+        st = f16_tile_map(&wmap.map, rep, N, K);
         if (st != GQ_OK) return st;
     }
     p.cnt = reinterpret_cast<unsigned int *>(ws.counters);
@@ -1137,7 +1176,8 @@ gq_status launch_gemv_with(int wf, const void *rep, const float *x, float *dst, 
         cfg.dynamicSmemBytes = smem;
         for (int sl = 0; sl < (seq ? p.S : 1); sl++) {
             if (seq) p.seq_slice = sl;
-            st = check_cuda(cudaLaunchKernelEx(&cfg, kv.kernel, p), "gemv launch");
+            void *args[] = {(void *)&p, wf == WF_F16RM ? (void *)&wmap : (void *)&no_wmap};
+            st = check_cuda(cudaLaunchKernelExC(&cfg, kv.kernel, args), "gemv launch");
             if (st != GQ_OK) return st;
         }
     }
